@@ -1,0 +1,193 @@
+"""gather_radix_select_gb300 -- batched row-wise top-k and flat row gather on GB300.
+
+Python face of the C ABI in ``include/sel.h`` (libsel.so, built in-tree for
+sm_103a by ``gather_radix_select_gb300.build``).  PyTorch supplies device
+memory and the current CUDA stream; every step of the computation runs in
+the library's kernels.  There is no CPU fallback: without the built library
+every call raises ``RuntimeError``.
+
+API shape after "Speed up PyTorch TopK with DeepSelect" ("Basic TopK usage",
+"Returning indices only", "Handling stride alignment", "Using an existing
+index buffer", "Working with variable-length rows") and, for the gather,
+the MindSpore hyper-parallel pull request "perf/gather-index-select".
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _native
+from ._native import SelError, SEL_MAX_K
+
+__all__ = ["topk", "gather_rows", "topk_gather", "stride_requirement", "max_cols", "SelError", "SEL_MAX_K",
+           "library_path"]
+
+_DTYPES = {torch.float32: _native.SEL_F32, torch.bfloat16: _native.SEL_BF16}
+_IDX = {torch.int32: _native.SEL_I32, torch.int64: _native.SEL_I64}
+
+
+def library_path() -> str:
+    return _native.library_path()
+
+
+def stride_requirement() -> tuple[int, int]:
+    """(input_alignment, output_alignment) in bytes, as in ``get_stride_requirement()``."""
+    a, b = ctypes.c_int(), ctypes.c_int()
+    _native.check(_native.load().sel_stride_requirement(ctypes.byref(a), ctypes.byref(b)), "sel_stride_requirement")
+    return a.value, b.value
+
+
+def max_cols(dtype: torch.dtype = torch.float32) -> int:
+    """Widest row ``topk`` accepts for ``dtype`` on the current device."""
+    return int(_native.load().sel_max_cols(_DTYPES[dtype]))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device, stream):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _padded_rows(rows: int, k: int, dtype: torch.dtype, device) -> torch.Tensor:
+    """[rows, k] view of a buffer whose row stride is a multiple of the output alignment."""
+    _, out_align = stride_requirement()
+    es = torch.empty((), dtype=dtype).element_size()
+    per = max(1, out_align // es)
+    stride = (k + per - 1) // per * per
+    return torch.empty((rows, stride), dtype=dtype, device=device)[:, :k]
+
+
+def _check_x(x: torch.Tensor):
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (batch_size, vocab_size)")
+    if x.dtype not in _DTYPES:
+        raise TypeError("x must be torch.float32 or torch.bfloat16")
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    if x.size(1) > 1 and x.stride(1) != 1:
+        raise ValueError("the last dimension of x must be contiguous")
+
+
+def _check_end(end, rows, device):
+    if end is None:
+        return None
+    if end.dtype != torch.int32 or end.dim() != 1 or end.numel() != rows or not end.is_cuda or not end.is_contiguous():
+        raise ValueError("end must be a contiguous int32 CUDA tensor with one entry per row")
+    if end.device != device:
+        raise ValueError("end must be on x's device")
+    return end
+
+
+def _row_stride(x):
+    return x.stride(0) if x.size(0) > 1 else max(x.stride(0), x.size(1))
+
+
+def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_index: bool = False,
+         indices_type: torch.dtype = torch.int32, return_value: bool = True,
+         output_idx: torch.Tensor | None = None, nan_flag: torch.Tensor | None = None,
+         err_flag: torch.Tensor | None = None, stream=None):
+    """Row-wise top-k of a 2-D CUDA tensor (largest values; ties: smaller index).
+
+    Returns ``(values, indices)``; ``values`` is None when ``return_value``
+    is False.  Rows shorter than k (per ``end``) are filled with index -1 and
+    value -inf.  Outputs may be non-contiguous (row strides padded to the
+    output alignment).  ``nan_flag`` / ``err_flag`` are optional caller-zeroed
+    int32 CUDA tensors the kernel ORs / writes into.
+    """
+    _check_x(x)
+    rows, cols = x.shape
+    dev = x.device
+    end = _check_end(end, rows, dev)
+    if indices_type not in _IDX:
+        raise TypeError("indices_type must be torch.int32 or torch.int64")
+    if output_idx is None:
+        idx = _padded_rows(rows, k, indices_type, dev)
+    else:
+        idx = output_idx
+        if idx.dtype != indices_type or idx.dim() != 2 or idx.shape[0] != rows or idx.shape[1] < k \
+                or (rows > 1 and idx.stride(1) != 1) or idx.device != dev:
+            raise ValueError("output_idx must be a [rows, >=k] %s tensor on x's device" % indices_type)
+    val = _padded_rows(rows, k, x.dtype, dev) if return_value else None
+    with torch.cuda.device(dev):
+        st = _native.load().sel_topk(
+            _ptr(x), _DTYPES[x.dtype], rows, cols, _row_stride(x), _ptr(end), int(k), int(bool(sorted_index)),
+            _IDX[indices_type], int(bool(return_value)), _ptr(idx), idx.stride(0) if rows > 1 else max(idx.stride(0), k),
+            _ptr(val), 0 if val is None else (val.stride(0) if rows > 1 else max(val.stride(0), k)),
+            _ptr(nan_flag), _ptr(err_flag), _stream(dev, stream))
+    _native.check(st, "sel_topk")
+    return val, idx[:, :k] if output_idx is not None else idx
+
+
+def _key_strides(key):
+    if key.dim() != 3 or key.dtype != torch.bfloat16 or not key.is_cuda:
+        raise ValueError("key must be a 3-D bf16 CUDA tensor [b, comp_len, d]")
+    if key.size(2) > 1 and key.stride(2) != 1:
+        raise ValueError("key rows must be contiguous in their last dimension")
+    return key.stride(0), key.stride(1)
+
+
+def gather_rows(key: torch.Tensor, idx: torch.Tensor, *, out: torch.Tensor | None = None,
+                err_flag: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[r, j, :] = key[r // (rows // b), max(idx[r, j], 0), :] as one flat-index gather.
+
+    key: bf16 [b, comp_len, d] (rows may be strided); idx: int32/int64 [rows, n]
+    with rows a multiple of b.  A position >= comp_len yields a zero row and
+    sets ``err_flag``.
+    """
+    kbs, krs = _key_strides(key)
+    b, comp_len, d = key.shape
+    if idx.dim() != 2 or idx.dtype not in _IDX or idx.device != key.device:
+        raise ValueError("idx must be a 2-D int32/int64 tensor on key's device")
+    if idx.size(1) > 1 and idx.stride(1) != 1:
+        raise ValueError("idx rows must be contiguous")
+    rows, n = idx.shape
+    if out is None:
+        out = torch.empty((rows, n, d), dtype=torch.bfloat16, device=key.device)
+    elif out.shape != (rows, n, d) or not out.is_contiguous() or out.dtype != torch.bfloat16:
+        raise ValueError("out must be a contiguous bf16 [rows, n, d] tensor")
+    with torch.cuda.device(key.device):
+        st = _native.load().sel_gather_rows(
+            _ptr(key), b, comp_len, d, kbs, krs, _ptr(idx), _IDX[idx.dtype], rows, n,
+            idx.stride(0) if rows > 1 else max(idx.stride(0), n), _ptr(out), _ptr(err_flag),
+            _stream(key.device, stream))
+    _native.check(st, "sel_gather_rows")
+    return out
+
+
+def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, end: torch.Tensor | None = None,
+                sorted_index: bool = False, indices_type: torch.dtype = torch.int32, return_value: bool = False,
+                return_indices: bool = True, gather_out: torch.Tensor | None = None,
+                nan_flag: torch.Tensor | None = None, err_flag: torch.Tensor | None = None, stream=None):
+    """``topk`` then ``gather_rows`` of the first ``n_gather`` selected columns, in one launch.
+
+    Returns ``(values, indices, gathered)`` with ``gathered`` bf16
+    [rows, n_gather, d]; values / indices are None when not requested.
+    """
+    _check_x(x)
+    rows, cols = x.shape
+    dev = x.device
+    end = _check_end(end, rows, dev)
+    kbs, krs = _key_strides(key)
+    b, comp_len, d = key.shape
+    if key.device != dev:
+        raise ValueError("key must be on x's device")
+    idx = _padded_rows(rows, k, indices_type, dev) if return_indices else None
+    val = _padded_rows(rows, k, x.dtype, dev) if return_value else None
+    if gather_out is None:
+        gather_out = torch.empty((rows, n_gather, d), dtype=torch.bfloat16, device=dev)
+    elif gather_out.shape != (rows, n_gather, d) or not gather_out.is_contiguous():
+        raise ValueError("gather_out must be a contiguous bf16 [rows, n_gather, d] tensor")
+    with torch.cuda.device(dev):
+        st = _native.load().sel_topk_gather(
+            _ptr(x), _DTYPES[x.dtype], rows, cols, _row_stride(x), _ptr(end), int(k), int(bool(sorted_index)),
+            _IDX[indices_type], int(bool(return_value)),
+            _ptr(idx), 0 if idx is None else (idx.stride(0) if rows > 1 else max(idx.stride(0), k)),
+            _ptr(val), 0 if val is None else (val.stride(0) if rows > 1 else max(val.stride(0), k)),
+            _ptr(key), b, comp_len, d, kbs, krs, int(n_gather), _ptr(gather_out),
+            _ptr(nan_flag), _ptr(err_flag), _stream(dev, stream))
+    _native.check(st, "sel_topk_gather")
+    return val, idx, gather_out

@@ -1,0 +1,75 @@
+// sel_internal.h -- argument blocks and launcher declarations shared by the
+// C-ABI layer (api.cu) and the kernels (topk.cu, gather.cu).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace sel {
+
+constexpr int kThreads = 512;       // threads per CTA of the selection kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxLevels = 4;       // radix passes (digits) at most
+constexpr int kMaxChunks = 16;      // bulk-copy chunks per CTA slice
+constexpr uint32_t kChunkBytes = 16384;
+constexpr int kMaxCluster = 16;     // CTAs splitting one row (non-portable above 8)
+constexpr int kGatherThreads = 256;
+
+// Everything one selection launch needs; passed by value (kernel parameter space).
+struct TopkArgs {
+    const void *x;            // [rows, stride] elements (fp32 or bf16 bits)
+    int64_t rows, cols, stride;
+    const int32_t *row_end;   // nullable
+    int32_t k;
+    int32_t idx_i64;          // 0: int32 indices, 1: int64
+    int32_t want_values;
+    void *out_idx;            // nullable only in the fused launch
+    int64_t out_idx_stride;
+    void *out_val;            // nullable
+    int64_t out_val_stride;
+    int32_t *nan_flag;        // nullable
+    int32_t *err_flag;        // nullable
+    int64_t slice;            // elements of a row per CTA (multiple of 64)
+    int32_t nlevels;          // digits from the most significant end
+    int32_t bits[kMaxLevels];
+    int32_t hist_bins;        // 1 << max(bits)
+    uint32_t smem_buf_bytes;  // bytes reserved for the staged slice
+    uint32_t smem_hist_off;   // offset of the local histogram
+    uint32_t smem_merge_off;  // offset of the per-level merged histograms (cluster only)
+    uint32_t smem_glist_off;  // offset of the gather position list (fused only)
+    // fused gather (ignored unless the gather variant is launched)
+    const uint16_t *key;
+    int64_t comp_len, d, key_batch_stride, key_row_stride, rows_per_batch;
+    int64_t n_gather;
+    uint16_t *gather_out;     // [rows, n_gather, d]
+};
+
+struct GatherArgs {
+    const uint16_t *key;
+    int64_t comp_len, d, key_batch_stride, key_row_stride;
+    const void *idx;
+    int32_t idx_i64;
+    int64_t rows, n, idx_row_stride, rows_per_batch;
+    uint16_t *out;
+    int32_t *err_flag;
+    int64_t pairs_per_cta;    // (row, position) pairs handled by one CTA
+    int32_t ctas_per_row;
+};
+
+// dtype: 0 fp32, 1 bf16.  cluster: CTAs per row (1 = no cluster).  gather: fused variant.
+cudaError_t launch_topk(int dtype, bool gather, int cluster, size_t smem_bytes, const TopkArgs &a,
+                        cudaStream_t stream);
+
+// Max dynamic shared memory a selection CTA may use on the current device.
+size_t topk_smem_limit();
+
+// Number of clusters of `cluster` CTAs with `smem_bytes` each that can be co-resident (0 = cannot launch).
+int topk_max_active_clusters(int dtype, bool gather, int cluster, size_t smem_bytes);
+
+cudaError_t launch_gather(const GatherArgs &a, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace sel

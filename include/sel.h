@@ -1,0 +1,150 @@
+/*
+ * sel.h -- C ABI of libsel: batched row-wise top-k selection and the flat
+ * row gather of the selected key rows, on one GB300 (sm_103a).
+ *
+ * Operations and the passages that define them:
+ *
+ *   sel_topk          "Speed up PyTorch TopK with DeepSelect" (tutorial):
+ *                     "Basic TopK usage" (2-D input, contiguous last dim,
+ *                     values in x's dtype, int32/int64 indices, sorted_index
+ *                     = ascending indices per row), "Returning indices only"
+ *                     (return_value=False), "Working with variable-length
+ *                     rows" (per-row exclusive end, fills for rows shorter
+ *                     than k), "NaN handling" (rows with valid length <= k are
+ *                     not checked), "Supported workloads" (k <= 4096).
+ *   sel_stride_requirement
+ *                     same tutorial, "Handling stride alignment" (input and
+ *                     output row-stride alignment in bytes).
+ *   sel_gather_rows   MindSpore hyper-parallel pull request
+ *                     "perf/gather-index-select", description: the gather
+ *                     key[batch, position] done as one index_select over the
+ *                     batch-flattened key at batch * comp_len + position,
+ *                     with clamped ("safe") positions.
+ *   sel_topk_gather   the two above in one launch: the selection's index list
+ *                     feeds the gather without a round trip through memory.
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no device or host memory on any call.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  No call synchronises.
+ *   - The return value is a sel_status.  Argument errors are found on the
+ *     host before anything is launched.  Findings made on the device are
+ *     written to caller-owned int32 flags: `nan_flag` is OR-ed with 1 when a
+ *     checked row holds a NaN; `err_flag` receives a nonzero sel_status
+ *     (first writer wins) when a device wait timed out or a gather position
+ *     was out of range.  Both flags are optional (NULL) and must be zeroed by
+ *     the caller.  Nothing traps.
+ *   - Element strides are in ELEMENTS, not bytes.
+ *   - Reads stay inside [0, row_end) of each input row; padding columns and
+ *     pad rows are never read.
+ *
+ * Readings of the tutorial where it is silent (stated once here):
+ *   - "top-k" keeps the LARGEST values; among equal values the smaller
+ *     column index wins; -0.0 and +0.0 are equal.
+ *   - Index fill is -1; value fill is -inf (fp32 0xFF800000, bf16 0xFF80).
+ *     Valid entries come first, fills last.
+ *   - Without sorted_index the order of a row's k entries is unspecified
+ *     (this implementation happens to return them in ascending index order).
+ *   - A NaN is not trapped: it sets *nan_flag and the selection of that row
+ *     is unspecified (but only in-range indices are written).
+ */
+#ifndef SEL_H_
+#define SEL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SEL_API __attribute__((visibility("default")))
+#else
+#define SEL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SEL_OK = 0,
+    SEL_EINVAL = 1,       /* bad argument (k, sizes, null pointer, gather position) */
+    SEL_EALIGN = 2,       /* a pointer or row stride breaks the alignment rule */
+    SEL_EUNSUPPORTED = 3, /* dtype / width outside what the kernels handle */
+    SEL_ECUDA = 4,        /* a CUDA runtime call failed (launch, attribute query) */
+    SEL_ETIMEOUT = 5      /* (device flag only) a bounded device wait ran out */
+} sel_status;
+
+enum { SEL_F32 = 0, SEL_BF16 = 1 };  /* input element type */
+enum { SEL_I32 = 0, SEL_I64 = 1 };   /* index element type */
+
+#define SEL_MAX_K 4096
+
+/* Alignment contract ("Handling stride alignment").  *in_align_bytes: the
+ * input base pointer and the input row stride in bytes must be multiples of
+ * it (rows are staged into shared memory by bulk copies).  *out_align_bytes:
+ * every output base pointer and output row stride in bytes must be multiples
+ * of it, so outputs of small k come with padded (non-contiguous) rows.
+ * Either pointer may be NULL.  Always returns SEL_OK. */
+SEL_API int sel_stride_requirement(int *in_align_bytes, int *out_align_bytes);
+
+/* Row-wise top-k.
+ *   x           [rows, stride] elements of `dtype` (SEL_F32 | SEL_BF16); the first
+ *               `cols` of each row are data.  Needs stride >= cols.
+ *   row_end     int32 [rows] exclusive end per row, clamped on the device to
+ *               [0, cols]; NULL means cols for every row.
+ *   k           1..SEL_MAX_K.  k > cols is allowed (every row is then short).
+ *   sorted_index  nonzero: each row's indices ascending (values follow).
+ *   idx_dtype   SEL_I32 | SEL_I64.
+ *   out_idx     [rows, out_idx_stride] of idx_dtype; columns [0, k) written.
+ *   out_val     [rows, out_val_stride] of `dtype`, or NULL when want_values == 0.
+ *   nan_flag, err_flag   optional device int32 flags (see above).
+ * Errors: SEL_EINVAL (k out of range, negative sizes, stride < cols, output
+ * strides < k, null required pointer, bad enum), SEL_EALIGN, SEL_EUNSUPPORTED
+ * (a row wider than the widest supported split: see sel_max_cols),
+ * SEL_ECUDA (launch failure).  rows == 0 returns SEL_OK without a launch. */
+SEL_API int sel_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride,
+             const int32_t *row_end, int k, int sorted_index, int idx_dtype, int want_values,
+             void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride,
+             int32_t *nan_flag, int32_t *err_flag, void *stream);
+
+/* Largest `cols` sel_topk accepts for `dtype` on the current device (a row is
+ * split over at most one thread-block cluster whose shared memory holds it). */
+SEL_API int64_t sel_max_cols(int dtype);
+
+/* Flat row gather:  out[r, j, :] = key[b_r, max(idx[r, j], 0), :],
+ * b_r = r / (rows / b).
+ *   key         bf16 element (bb, p, e) at bb*key_batch_stride + p*key_row_stride + e;
+ *               rows of the key may be strided (non-contiguous key).
+ *   idx         idx_dtype element (r, j) at r*idx_row_stride + j.
+ *   rows        a multiple of b (rows are batch-major).
+ *   out         bf16 [rows, n, d] contiguous.
+ * A negative position reads position 0; a position >= comp_len writes a zero
+ * row and sets *err_flag = SEL_EINVAL.  Alignment: key, out and the key
+ * strides must make every key row and out row start on 16 bytes, and
+ * d*2 must be a multiple of 16 (else SEL_EALIGN). */
+SEL_API int sel_gather_rows(const void *key, int64_t b, int64_t comp_len, int64_t d,
+                    int64_t key_batch_stride, int64_t key_row_stride,
+                    const void *idx, int idx_dtype, int64_t rows, int64_t n, int64_t idx_row_stride,
+                    void *out, int32_t *err_flag, void *stream);
+
+/* sel_topk followed by sel_gather_rows of the first n_gather output columns
+ * (n_gather <= k), in one launch.  The top-k arguments are those of
+ * sel_topk (out_idx may be NULL when the indices themselves are not needed);
+ * the gather arguments are those of sel_gather_rows with idx taken from the
+ * selection.  Fill positions (-1) of short rows gather position 0, as in
+ * sel_gather_rows. */
+SEL_API int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride,
+                    const int32_t *row_end, int k, int sorted_index, int idx_dtype, int want_values,
+                    void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride,
+                    const void *key, int64_t b, int64_t comp_len, int64_t d,
+                    int64_t key_batch_stride, int64_t key_row_stride, int64_t n_gather,
+                    void *gather_out, int32_t *nan_flag, int32_t *err_flag, void *stream);
+
+/* Static message for a sel_status value. */
+SEL_API const char *sel_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SEL_H_ */

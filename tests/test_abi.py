@@ -1,0 +1,116 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+include/sel.h declares, and rejects bad arguments on the host before any
+CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gather_radix_select_gb300 import _native
+    return _native.load(build_if_missing=True)
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "sel.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sel_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_symbols() == sorted(["sel_gather_rows", "sel_max_cols", "sel_stride_requirement",
+                                         "sel_strerror", "sel_topk", "sel_topk_gather"])
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from gather_radix_select_gb300 import _native
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in _native.SIGNATURES, name
+
+
+def test_stride_requirement_and_messages(lib):
+    a, b = ctypes.c_int(), ctypes.c_int()
+    assert lib.sel_stride_requirement(ctypes.byref(a), ctypes.byref(b)) == 0
+    assert (a.value, b.value) == (16, 16)
+    assert lib.sel_stride_requirement(None, None) == 0
+    for st in range(6):
+        assert lib.sel_strerror(st)
+    assert lib.sel_strerror(99) == b"unknown status"
+
+
+FAKE = 0x10000  # never dereferenced: every call below is rejected on the host
+
+
+def topk(lib, x=FAKE, dtype=0, rows=4, cols=64, stride=64, k=8, idx_dtype=0, want_values=0, out_idx=FAKE,
+         out_idx_stride=8, out_val=None, out_val_stride=0):
+    return lib.sel_topk(x, dtype, rows, cols, stride, None, k, 0, idx_dtype, want_values, out_idx, out_idx_stride,
+                        out_val, out_val_stride, None, None, None)
+
+
+def test_topk_rejections(lib):
+    EINVAL, EALIGN = 1, 2
+    assert topk(lib, k=0) == EINVAL
+    assert topk(lib, k=4097) == EINVAL
+    assert topk(lib, dtype=7) == EINVAL
+    assert topk(lib, idx_dtype=3) == EINVAL
+    assert topk(lib, stride=63) == EINVAL
+    assert topk(lib, rows=-1) == EINVAL
+    assert topk(lib, out_idx=None) == EINVAL
+    assert topk(lib, out_idx_stride=4) == EINVAL
+    assert topk(lib, want_values=1) == EINVAL          # no value buffer
+    assert topk(lib, x=FAKE + 8) == EALIGN              # base not on 16 bytes
+    assert topk(lib, cols=65, stride=65) == EALIGN      # 260-byte rows
+    assert topk(lib, dtype=1, cols=60, stride=60) == EALIGN
+    assert topk(lib, out_idx_stride=9) == EALIGN        # 36-byte output rows
+    assert topk(lib, rows=0) == 0                       # nothing to do, no launch
+
+
+def test_gather_rejections(lib):
+    EINVAL, EALIGN = 1, 2
+    def g(key=FAKE, b=1, comp_len=10, d=64, kbs=640, krs=64, idx=FAKE, idx_dtype=0, rows=4, n=3, irs=3, out=FAKE):
+        return lib.sel_gather_rows(key, b, comp_len, d, kbs, krs, idx, idx_dtype, rows, n, irs, out, None, None)
+    assert g(d=12, krs=12, kbs=120) == EALIGN
+    assert g(rows=5, b=2) == EINVAL
+    assert g(idx=None) == EINVAL
+    assert g(idx_dtype=2) == EINVAL
+    assert g(krs=32) == EINVAL  # row stride < d
+    assert g(key=FAKE + 2) == EALIGN
+    assert g(rows=0) == 0 and g(n=0) == 0
+
+
+def test_fused_rejections(lib):
+    r = lib.sel_topk_gather(FAKE, 0, 4, 64, 64, None, 8, 0, 0, 0, None, 0, None, 0,
+                            FAKE, 1, 64, 64, 64 * 64, 64, 9, FAKE, None, None, None)
+    assert r == 1  # n_gather > k
+    r = lib.sel_topk_gather(FAKE, 0, 4, 64, 64, None, 8, 0, 0, 0, None, 0, None, 0,
+                            FAKE, 3, 64, 64, 64 * 64, 64, 8, FAKE, None, None, None)
+    assert r == 1  # rows not a multiple of b
+
+
+def test_product_has_no_cpu_path():
+    """The package imports no oracle code and fails loudly without its library."""
+    import gather_radix_select_gb300 as g
+    from gather_radix_select_gb300 import _native
+    pkg = os.path.dirname(g.__file__)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "oracle/" not in text, f
+    saved = _native._lib
+    real = _native.library_path
+    try:
+        _native._lib = None
+        _native.library_path = lambda: "/nonexistent/libsel.so"
+        with pytest.raises(RuntimeError):
+            _native.load()
+    finally:
+        _native.library_path = real
+        _native._lib = saved
