@@ -1,0 +1,478 @@
+"""Benchmark: batched row-wise top-k + flat row gather on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one pass of the whole path over one batch of the workload: the
+fused top-k + gather launch (sel_topk_gather) for the gather workloads, the
+top-k launch (sel_topk) for the others.  Inputs are seeded synthetic data of
+the workload's shape (no dataset), resident in HBM before timing starts; L2
+is flushed (a 256 MiB write) before every timed step and the flush is not
+timed.  Each step is timed with CUDA events on the launching stream.
+
+Prints ONE JSON line on rank 0.  The default workload is the bf16 indexer
+top-k + gather on scores[4096, 2048]; the line also carries per-workload
+numbers for all five named workloads (`per_workload`).
+
+--impl reference times the CPU oracle (the plain full-sort definition) on a
+bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic as syn  # noqa: E402
+
+METRIC = "top-k effective HBM GB/s (fraction of GB300 peak) and rows/s per config, 1 GPU"
+DEFAULT_WORKLOAD = "indexer_bf16_4096x2048_causal_k512_gather"
+FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes (what the method must move; re-reads are not counted)
+# ----------------------------------------------------------------------------
+
+def valid_lengths(w) -> np.ndarray:
+    if w["row_end"] is None:
+        return np.full(w["rows"], w["cols"], dtype=np.int64)
+    return np.clip(w["row_end"].astype(np.int64), 0, w["cols"])
+
+
+def topk_bytes(w) -> int:
+    """Read every valid element of rows with n > k, write k indices (and k values) per row."""
+    e = syn.elem_bytes(w["dtype"])
+    ib = 8 if w["idx_dtype"] == "i64" else 4
+    n = valid_lengths(w)
+    read = int(n[n > w["k"]].sum()) * e
+    write = w["rows"] * w["k"] * (ib + (e if w["want_values"] else 0))
+    return read + write
+
+
+def gather_bytes(w, fused: bool) -> int:
+    """Unique key rows read at least once + gathered rows written (+ the index read when not fused)."""
+    if w.get("key") is None:
+        return 0
+    key_bytes = w["b"] * w["comp_len"] * w["d"] * 2
+    out = w["rows"] * w["n_gather"] * w["d"] * 2
+    idx_read = 0 if fused else w["rows"] * w["n_gather"] * 4
+    return key_bytes + out + idx_read
+
+
+def step_bytes(w) -> int:
+    return topk_bytes(w) + gather_bytes(w, fused=True)
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+class Runner:
+    """Device-resident inputs/outputs of one workload and the call that is timed."""
+
+    def __init__(self, w, dev):
+        import torch
+
+        import gather_radix_select_gb300 as g
+
+        self.g, self.torch, self.w, self.dev = g, torch, w, dev
+        if w["dtype"] == "f32":
+            self.x = torch.from_numpy(w["x"].view(np.int32)).view(torch.float32).to(dev)
+        else:
+            self.x = torch.from_numpy(w["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+        self.x = self.x[:, :w["cols"]]
+        self.end = None if w["row_end"] is None else torch.from_numpy(w["row_end"]).to(dev)
+        self.idx_t = torch.int64 if w["idx_dtype"] == "i64" else torch.int32
+        self.key = None
+        if w.get("key") is not None:
+            self.key = torch.from_numpy(w["key"].view(np.int16)).view(torch.bfloat16).to(dev)
+            self.gout = torch.empty((w["rows"], w["n_gather"], w["d"]), dtype=torch.bfloat16, device=dev)
+        self.nan = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.launches_per_step = 1
+
+    def step(self):
+        w = self.w
+        if self.key is not None:
+            return self.g.topk_gather(self.x, w["k"], self.key, w["n_gather"], end=self.end,
+                                      sorted_index=w["sorted_index"], indices_type=self.idx_t,
+                                      return_value=w["want_values"], gather_out=self.gout,
+                                      nan_flag=self.nan, err_flag=self.err)
+        return self.g.topk(self.x, w["k"], end=self.end, sorted_index=w["sorted_index"], indices_type=self.idx_t,
+                           return_value=w["want_values"], nan_flag=self.nan, err_flag=self.err)
+
+
+def time_steps(runner, steps, warmup, flush):
+    """Per-step CUDA-event times (ms) with an untimed L2 flush before each step."""
+    torch = runner.torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        runner.step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        runner.step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def e2e_measure(w, dev, steps, warmup):
+    """Same step through the public API with host buffers: pinned H2D of the inputs,
+    the call, D2H of every output, all inside the timed region."""
+    import torch
+
+    import gather_radix_select_gb300 as g
+
+    tdt = torch.float32 if w["dtype"] == "f32" else torch.bfloat16
+    host_x = torch.from_numpy(w["x"].view(np.int32 if w["dtype"] == "f32" else np.int16)).view(tdt).pin_memory()
+    host_end = None if w["row_end"] is None else torch.from_numpy(w["row_end"]).pin_memory()
+    host_key = None
+    if w.get("key") is not None:
+        host_key = torch.from_numpy(w["key"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    idx_t = torch.int64 if w["idx_dtype"] == "i64" else torch.int32
+    x = torch.empty(host_x.shape, dtype=tdt, device=dev)
+    end = None if host_end is None else torch.empty(host_end.shape, dtype=torch.int32, device=dev)
+    key = None if host_key is None else torch.empty(host_key.shape, dtype=torch.bfloat16, device=dev)
+    outs_host = None
+    h2d = host_x.numel() * host_x.element_size() + (0 if host_end is None else host_end.numel() * 4) + \
+        (0 if host_key is None else host_key.numel() * 2)
+
+    def one():
+        nonlocal outs_host
+        x.copy_(host_x, non_blocking=True)
+        if end is not None:
+            end.copy_(host_end, non_blocking=True)
+        if key is not None:
+            key.copy_(host_key, non_blocking=True)
+        xv = x[:, :w["cols"]]
+        if key is not None:
+            vals, idx, gout = g.topk_gather(xv, w["k"], key, w["n_gather"], end=end, sorted_index=w["sorted_index"],
+                                            indices_type=idx_t, return_value=w["want_values"])
+            outs = [t for t in (vals, idx, gout) if t is not None]
+        else:
+            vals, idx = g.topk(xv, w["k"], end=end, sorted_index=w["sorted_index"], indices_type=idx_t,
+                               return_value=w["want_values"])
+            outs = [t for t in (vals, idx) if t is not None]
+        if outs_host is None:
+            outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        for hdst, t in zip(outs_host, outs):
+            hdst.copy_(t, non_blocking=True)
+        return outs
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        outs = one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    return ms, h2d, d2h
+
+
+def gpu_arm(args):
+    import torch
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = syn.workload(args.workload)
+    runner = Runner(w, dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    peak, peak_kind = measured_peaks()
+
+    # the timed region: K steps, barrier + synchronize on both sides, clocks sampled meanwhile
+    for _ in range(args.warmup):
+        flush.zero_()
+        runner.step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t0 = time.perf_counter()
+    times = time_steps(runner, args.steps, 0, flush)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    if dist:
+        dist.barrier()
+    ms_step = sum(times) / len(times)
+    ms_max = ms_step
+    if dist:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    nbytes = step_bytes(w)
+    value = nbytes * world / (ms_max * 1e-3) / 1e9
+    err_flag = int(runner.err.item())
+
+    result = None
+    if rank == 0:
+        kernel_ms = statistics.median(times)
+        achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+        e2e_ms, h2d, d2h = e2e_measure(w, dev, max(2, min(args.steps, 10)), 2)
+        per = per_workload(args, dev, flush, peak) if not args.no_per_workload else None
+        cpu = cpu_baseline(args.workload)
+        kname = "topk_kernel<bf16,gather>" if w.get("key") is not None else "topk_kernel"
+        result = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_max, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": w["dtype"],
+            "data": "synthetic (seeded; shapes of the workload, no dataset)",
+            "config": {"workload": args.workload, "description": w["description"], "rows": w["rows"],
+                       "cols": w["cols"], "k": w["k"], "algorithmic_bytes_per_step": nbytes,
+                       "rows_per_s": round(w["rows"] * world / (ms_max * 1e-3), 1),
+                       "l2": "flushed before every timed step (256 MiB write, untimed)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": kname,
+                         "peak_kind": peak_kind},
+            "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": args.steps * runner.launches_per_step,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "wall_s_timed_region": round(wall, 4),
+            "device_err_flag": err_flag,
+            "per_workload": per,
+        }
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def per_workload(args, dev, flush, peak):
+    """Every named workload, a few L2-flushed reps each (median)."""
+    import torch
+
+    out = {}
+    for name in syn.WORKLOADS:
+        w = syn.workload(name)
+        r = Runner(w, dev)
+        times = time_steps(r, 10, 3, flush)
+        ms = statistics.median(times)
+        nb = step_bytes(w)
+        tb = topk_bytes(w)
+        out[name] = {"ms": round(ms, 5), "rows_per_s": round(w["rows"] / (ms * 1e-3), 1),
+                     "gbs": round(nb / (ms * 1e-3) / 1e9, 2), "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
+                     "bytes": nb, "topk_bytes": tb, "fused_gather": w.get("key") is not None}
+        if w.get("key") is not None:
+            # the top-k alone on the same workload
+            w2 = dict(w)
+            w2["key"] = None
+            r2 = Runner(w2, dev)
+            t2 = statistics.median(time_steps(r2, 10, 3, flush))
+            out[name]["topk_only_ms"] = round(t2, 5)
+            out[name]["topk_only_gbs"] = round(tb / (t2 * 1e-3) / 1e9, 2)
+        del r
+        torch.cuda.empty_cache()
+    return out
+
+
+# ----------------------------------------------------------------------------
+# CPU arm: the oracle as it stands, on a bounded sample
+# ----------------------------------------------------------------------------
+
+def oracle_step(w, rows_sel):
+    import oracle
+
+    s = syn.row_subset(w, rows_sel)
+    t0 = time.perf_counter()
+    idx, _, _ = oracle.topk(s["x"], w["dtype"], w["k"], row_end=s["row_end"], sorted_index=w["sorted_index"],
+                            cols=w["cols"])
+    if w.get("key") is not None:
+        # gather of the sampled rows, batch by batch (the oracle's own batch rule per block)
+        rpb = w["rows_per_batch"]
+        for bb in range(w["b"]):
+            m = (rows_sel // rpb) == bb
+            if m.any():
+                oracle.gather_rows(np.ascontiguousarray(w["key"][bb:bb + 1]), idx[m][:, :w["n_gather"]], 1)
+    return time.perf_counter() - t0
+
+
+def sample_bytes(w, rows_sel):
+    s = syn.row_subset(w, rows_sel)
+    s["key"] = w.get("key")
+    if s["key"] is not None:
+        s["b"], s["comp_len"], s["d"], s["n_gather"] = w["b"], w["comp_len"], w["d"], w["n_gather"]
+    return topk_bytes(s) + (gather_bytes(s, fused=True) if s["key"] is not None else 0)
+
+
+def cpu_baseline(name, budget_s=10.0):
+    w = syn.workload(name)
+    R = w["rows"]
+    # start with a small sample, grow until one pass takes >= ~1 s, then repeat within the budget
+    n = min(R, 64)
+    while True:
+        rows_sel = np.linspace(0, R - 1, n).astype(np.int64)
+        dt = oracle_step(w, rows_sel)
+        if dt >= 1.0 or n >= R:
+            break
+        n = min(R, n * 4)
+    total, reps = dt, 1
+    while total < budget_s and reps < 20:
+        total += oracle_step(w, rows_sel)
+        reps += 1
+    per = total / reps
+    nb = sample_bytes(w, rows_sel)
+    return {"value": round(nb / per / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of %d rows (evenly spaced), %d passes, %.2f s per pass; single-threaded C full sort "
+                      "per row%s" % (len(rows_sel), R, reps, per, " + triple-loop gather" if w.get("key") is not None
+                                     else ""),
+            "rows_per_s": round(len(rows_sel) / per, 1)}
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    w = syn.workload(args.workload)
+    R = w["rows"]
+    # each step: a bounded sample of the workload's rows on the oracle
+    n = min(R, 64)
+    while True:
+        rows_sel = np.linspace(0, R - 1, n).astype(np.int64)
+        dt = oracle_step(w, rows_sel)
+        if dt >= 0.5 or n >= R:
+            break
+        n = min(R, n * 4)
+    for _ in range(args.warmup):
+        oracle_step(w, rows_sel)
+    times = [oracle_step(w, rows_sel) for _ in range(args.steps)]
+    per = sum(times) / len(times)
+    nb = sample_bytes(w, rows_sel)
+    value = nb / per / 1e9
+    sample = "%d of %d rows per step (evenly spaced); single-threaded C full sort per row" % (len(rows_sel), R)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic (seeded)",
+            "config": {"workload": args.workload, "rows": w["rows"], "cols": w["cols"], "k": w["k"]},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(syn.WORKLOADS))
+    ap.add_argument("--no-per-workload", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    res = reference_arm(args) if args.impl == "reference" else gpu_arm(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

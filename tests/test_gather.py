@@ -135,7 +135,11 @@ def test_fused_small_cases_match_separate():
                                         ("bf16", 9, 500, 600, 300, 3)):
         v = rng.standard_normal((rows, cols)).astype(np.float32)
         bits = syn.f32_to_bits(v) if dtype == "f32" else syn.f32_to_bf16_bits(v)
-        x = to_torch(bits, dtype)
+        e = syn.elem_bytes(dtype)
+        stride = (cols * e + 15) // 16 * 16 // e
+        padded = np.zeros((rows, stride), dtype=bits.dtype)
+        padded[:, :cols] = bits
+        x = to_torch(padded, dtype)[:, :cols]  # row stride padded to 16 bytes
         end = torch.from_numpy(rng.integers(0, cols + 1, size=rows).astype(np.int32)).cuda()
         key = key_tensor(syn.f32_to_bf16_bits(rng.standard_normal((b, cols, 64)).astype(np.float32)))
         vals, idx = g.topk(x, k, end=end, sorted_index=True, return_value=True)
