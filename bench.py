@@ -303,7 +303,10 @@ def gpu_arm(args):
     err_flag = int(runner.err.item())
 
     result = None
-    if rank == 0:
+    if rank == 0 and args.profile:
+        result = {"profile_run": True, "workload": args.workload, "ms_per_step": round(ms_max, 5),
+                  "value": round(value, 2), "unit": "GB/s", "steps": args.steps, "warmup": args.warmup}
+    elif rank == 0:
         kernel_ms = statistics.median(times)
         achieved = nbytes / (kernel_ms * 1e-3) / 1e9
         e2e_ms, h2d, d2h = e2e_measure(w, dev, max(2, min(args.steps, 10)), 2)
@@ -466,6 +469,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(syn.WORKLOADS))
     ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="only the warm-up and timed steps of --workload (a short run for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -2,6 +2,7 @@
 // dispatch.  Host code only; every step of the computation runs in the
 // kernels of topk.cu and gather.cu.
 #include <cstdint>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -24,6 +25,7 @@ int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 struct Plan {
     int cluster = 1;
+    int threads = 256;
     size_t smem = 0;
     sel::TopkArgs layout{};  // slice, digit plan and shared-memory offsets
 };
@@ -53,44 +55,96 @@ void digit_plan(int dtype, int64_t cols, sel::TopkArgs &a)
     a.hist_bins = 1 << mb;
 }
 
-// Shared-memory layout of one CTA for a given slice; returns total bytes.
-size_t layout_for(int dtype, int cluster, int64_t slice, bool gather, int64_t n_gather, sel::TopkArgs &a)
+// Threads per selection CTA for a slice of `slice` elements.
+int threads_for(int64_t slice)
 {
+    if (slice <= 4096) return 128;
+    if (slice <= 16384) return 256;
+    return 512;
+}
+
+// Shared-memory layout of one CTA for a given slice; returns total bytes.
+size_t layout_for(int dtype, int cluster, int64_t slice, int k, bool gather, int64_t n_gather, sel::TopkArgs &a)
+{
+    const int64_t e = elem_bytes(dtype);
     a.slice = slice;
-    size_t off = static_cast<size_t>(round_up(slice * elem_bytes(dtype), 128));
+    size_t off = static_cast<size_t>(round_up(slice * e, 128));
     a.smem_buf_bytes = static_cast<uint32_t>(off);
     a.smem_hist_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(a.hist_bins) * 4;
     a.smem_merge_off = static_cast<uint32_t>(off);
     if (cluster > 1)
         for (int l = 0; l < a.nlevels; ++l) off += static_cast<size_t>(1u << a.bits[l]) * 4;
+    a.smem_mask_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(round_up(ceil_div(slice, 16 / e), 16));
+    // candidate list: keys whose top digit reaches the threshold bin (at most k - 1 above it plus the bin)
+    const int64_t cap = slice < static_cast<int64_t>(k) + 4096 ? slice : static_cast<int64_t>(k) + 4096;
+    a.list_cap = static_cast<int32_t>(cap);
+    a.smem_list_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(round_up(cap * 2, 16));
     a.smem_glist_off = static_cast<uint32_t>(off);
     if (gather) off += static_cast<size_t>(round_up(n_gather * 4, 16));
     return off;
 }
 
-int cached_max_clusters(int dtype, bool gather, int cluster, size_t smem)
+int cached_max_clusters(int dtype, int threads, bool gather, int cluster, size_t smem)
 {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int, int, size_t>, int> cache;
+    static std::map<std::tuple<int, int, int, int, int, size_t>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, dtype, gather ? 1 : 0, cluster, smem);
+    const auto key = std::make_tuple(dev, dtype, threads, gather ? 1 : 0, cluster, smem);
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    const int n = sel::topk_max_active_clusters(dtype, gather, cluster, smem);
+    const int n = sel::topk_max_active_clusters(dtype, threads, gather, cluster, smem);
     std::lock_guard<std::mutex> g(mu);
     cache[key] = n;
     return n;
 }
 
+// First-pass histogram flavour: SEL_HIST_AGG=1 selects warp-aggregated atomics
+// (__match_any_sync), anything else plain shared atomics (the default).
+int hist_agg()
+{
+    static const int v = [] {
+        const char *e = std::getenv("SEL_HIST_AGG");
+        return (e && e[0] == '1') ? 1 : 0;
+    }();
+    return v;
+}
+
+// Tries a cluster size: slice, threads, layout, and whether it can be scheduled.
+bool try_cluster(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, int64_t cs,
+                 size_t limit, Plan &p, bool &too_big)
+{
+    const int64_t e = elem_bytes(dtype);
+    const int64_t slice = round_up(ceil_div(cols > 0 ? cols : 1, cs), 64);
+    too_big = slice > sel::kMaxSlice || slice * e > static_cast<int64_t>(sel::kMaxChunks) * sel::kChunkBytes;
+    if (too_big) return false;
+    sel::TopkArgs a = p.layout;
+    const size_t smem = layout_for(dtype, static_cast<int>(cs), slice, k, gather, n_gather, a);
+    if (smem > limit) {
+        too_big = true;
+        return false;
+    }
+    if (rows * cs > 0x7fffffffLL) return false;
+    const int threads = threads_for(slice);
+    if (cached_max_clusters(dtype, threads, gather, static_cast<int>(cs), smem) <= 0) return false;
+    p.cluster = static_cast<int>(cs);
+    p.threads = threads;
+    p.smem = smem;
+    p.layout = a;
+    return true;
+}
+
 // Chooses CTAs per row (cluster), the slice each CTA stages and the digit plan.
-int make_plan(int dtype, int64_t rows, int64_t cols, bool gather, int64_t n_gather, Plan &p)
+int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, Plan &p)
 {
     digit_plan(dtype, cols, p.layout);
+    p.layout.agg = hist_agg();
     const size_t limit = sel::topk_smem_limit();
     const int sms = sel::device_sm_count();
     if (limit == 0 || sms == 0) return SEL_ECUDA;
@@ -106,32 +160,14 @@ int make_plan(int dtype, int64_t rows, int64_t cols, bool gather, int64_t n_gath
     }
     if (want > sel::kMaxCluster) want = sel::kMaxCluster;
     if (want < 1) want = 1;
+    bool too_big = false;
     // smallest cluster >= want whose slice fits in shared memory and can be scheduled
-    for (int64_t cs = want; cs <= sel::kMaxCluster; ++cs) {
-        const int64_t slice = round_up(ceil_div(cols > 0 ? cols : 1, cs), 64);
-        if (slice * e > static_cast<int64_t>(sel::kMaxChunks) * sel::kChunkBytes) continue;
-        sel::TopkArgs a = p.layout;
-        const size_t smem = layout_for(dtype, static_cast<int>(cs), slice, gather, n_gather, a);
-        if (smem > limit) continue;
-        if (static_cast<int64_t>(rows) * cs > 0x7fffffffLL) return SEL_EUNSUPPORTED;
-        if (cached_max_clusters(dtype, gather, static_cast<int>(cs), smem) <= 0) continue;
-        p.cluster = static_cast<int>(cs);
-        p.smem = smem;
-        p.layout = a;
-        return SEL_OK;
-    }
-    // a cluster larger than wanted could not be scheduled: try smaller ones that still fit
+    for (int64_t cs = want; cs <= sel::kMaxCluster; ++cs)
+        if (try_cluster(dtype, rows, cols, k, gather, n_gather, cs, limit, p, too_big)) return SEL_OK;
+    // a cluster that large could not be scheduled: try smaller ones that still fit
     for (int64_t cs = want - 1; cs >= 1; --cs) {
-        const int64_t slice = round_up(ceil_div(cols > 0 ? cols : 1, cs), 64);
-        if (slice * e > static_cast<int64_t>(sel::kMaxChunks) * sel::kChunkBytes) break;
-        sel::TopkArgs a = p.layout;
-        const size_t smem = layout_for(dtype, static_cast<int>(cs), slice, gather, n_gather, a);
-        if (smem > limit) break;
-        if (cached_max_clusters(dtype, gather, static_cast<int>(cs), smem) <= 0) continue;
-        p.cluster = static_cast<int>(cs);
-        p.smem = smem;
-        p.layout = a;
-        return SEL_OK;
+        if (try_cluster(dtype, rows, cols, k, gather, n_gather, cs, limit, p, too_big)) return SEL_OK;
+        if (too_big) break;
     }
     return SEL_EUNSUPPORTED;
 }
@@ -197,20 +233,27 @@ const char *sel_strerror(int status)
 int64_t sel_max_cols(int dtype)
 {
     if (dtype != SEL_F32 && dtype != SEL_BF16) return 0;
-    const int64_t e = elem_bytes(dtype);
     const size_t limit = sel::topk_smem_limit();
+    if (limit == 0) return 0;
     // widest row: the largest schedulable cluster with the largest slice that fits in shared memory
-    for (int cs = sel::kMaxCluster; cs >= 1; --cs) {
-        sel::TopkArgs a{};
-        digit_plan(dtype, 1 << 20, a);  // wide-row digit plan
-        const size_t fixed = layout_for(dtype, cs, 0, false, 0, a);
-        if (fixed >= limit) continue;
-        int64_t slice = static_cast<int64_t>(limit - fixed) / e / 64 * 64;
-        const int64_t cap = static_cast<int64_t>(sel::kMaxChunks) * sel::kChunkBytes / e;
-        if (slice > cap) slice = cap;
-        if (slice < 64) continue;
-        const size_t smem = layout_for(dtype, cs, slice, false, 0, a);
-        if (cached_max_clusters(dtype, false, cs, smem) > 0) return slice * cs;
+    for (int64_t cs = sel::kMaxCluster; cs >= 1; --cs) {
+        int64_t lo = 64, hi = sel::kMaxSlice;
+        Plan best;
+        bool found = false;
+        while (lo <= hi) {  // largest slice (multiple of 64) that fits and schedules, at k = SEL_MAX_K
+            const int64_t mid = (lo + hi) / 2 / 64 * 64;
+            Plan p;
+            digit_plan(dtype, mid * cs, p.layout);
+            bool too_big = false;
+            if (try_cluster(dtype, 1, mid * cs, SEL_MAX_K, false, 0, cs, limit, p, too_big) && p.cluster == cs) {
+                best = p;
+                found = true;
+                lo = mid + 64;
+            } else {
+                hi = mid - 64;
+            }
+        }
+        if (found) return best.layout.slice * cs;
     }
     return 0;
 }
@@ -224,7 +267,7 @@ int sel_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
                              out_val_stride, true);
     if (st != SEL_OK || rows == 0) return st;
     Plan p;
-    st = make_plan(dtype, rows, cols, false, 0, p);
+    st = make_plan(dtype, rows, cols, k, false, 0, p);
     if (st != SEL_OK) return st;
     sel::TopkArgs a = p.layout;
     a.x = x;
@@ -242,7 +285,7 @@ int sel_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
     a.nan_flag = nan_flag;
     a.err_flag = err_flag;
     a.rows_per_batch = 1;
-    return status_of(sel::launch_topk(dtype == SEL_F32 ? 0 : 1, false, p.cluster, p.smem, a,
+    return status_of(sel::launch_topk(dtype == SEL_F32 ? 0 : 1, p.threads, false, p.cluster, p.smem, a,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -290,7 +333,7 @@ int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_
         if (st != SEL_OK) return st;
     }
     Plan p;
-    st = make_plan(dtype, rows, cols, n_gather > 0, n_gather, p);
+    st = make_plan(dtype, rows, cols, k, n_gather > 0, n_gather, p);
     if (st != SEL_OK) return st;
     sel::TopkArgs a = p.layout;
     a.x = x;
@@ -315,7 +358,7 @@ int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_
     a.rows_per_batch = n_gather > 0 ? rows / b : 1;
     a.n_gather = n_gather;
     a.gather_out = static_cast<uint16_t *>(gather_out);
-    return status_of(sel::launch_topk(dtype == SEL_F32 ? 0 : 1, n_gather > 0, p.cluster, p.smem, a,
+    return status_of(sel::launch_topk(dtype == SEL_F32 ? 0 : 1, p.threads, n_gather > 0, p.cluster, p.smem, a,
                                       static_cast<cudaStream_t>(stream)));
 }
 

@@ -9,9 +9,8 @@
 
 namespace sel {
 
-constexpr int kThreads = 512;       // threads per CTA of the selection kernel
-constexpr int kWarps = kThreads / 32;
 constexpr int kMaxLevels = 4;       // radix passes (digits) at most
+constexpr int kMaxSlice = 65536;    // elements of a row staged by one CTA (list offsets are 16-bit)
 constexpr int kMaxChunks = 16;      // bulk-copy chunks per CTA slice
 constexpr uint32_t kChunkBytes = 16384;
 constexpr int kMaxCluster = 16;     // CTAs splitting one row (non-portable above 8)
@@ -38,7 +37,11 @@ struct TopkArgs {
     uint32_t smem_buf_bytes;  // bytes reserved for the staged slice
     uint32_t smem_hist_off;   // offset of the local histogram
     uint32_t smem_merge_off;  // offset of the per-level merged histograms (cluster only)
+    uint32_t smem_mask_off;   // offset of the per-vector candidate masks (one byte per 16-byte vector)
+    uint32_t smem_list_off;   // offset of the candidate list (16-bit offsets within the slice)
     uint32_t smem_glist_off;  // offset of the gather position list (fused only)
+    int32_t list_cap;         // capacity of the candidate list
+    int32_t agg;              // 1: first-pass histogram with warp-aggregated atomics
     // fused gather (ignored unless the gather variant is launched)
     const uint16_t *key;
     int64_t comp_len, d, key_batch_stride, key_row_stride, rows_per_batch;
@@ -58,15 +61,16 @@ struct GatherArgs {
     int32_t ctas_per_row;
 };
 
-// dtype: 0 fp32, 1 bf16.  cluster: CTAs per row (1 = no cluster).  gather: fused variant.
-cudaError_t launch_topk(int dtype, bool gather, int cluster, size_t smem_bytes, const TopkArgs &a,
+// dtype: 0 fp32, 1 bf16.  threads: 128 | 256 | 512.  cluster: CTAs per row (1 = no cluster).
+// gather: fused variant.
+cudaError_t launch_topk(int dtype, int threads, bool gather, int cluster, size_t smem_bytes, const TopkArgs &a,
                         cudaStream_t stream);
 
 // Max dynamic shared memory a selection CTA may use on the current device.
 size_t topk_smem_limit();
 
 // Number of clusters of `cluster` CTAs with `smem_bytes` each that can be co-resident (0 = cannot launch).
-int topk_max_active_clusters(int dtype, bool gather, int cluster, size_t smem_bytes);
+int topk_max_active_clusters(int dtype, int threads, bool gather, int cluster, size_t smem_bytes);
 
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t stream);
 

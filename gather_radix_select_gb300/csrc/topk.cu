@@ -110,11 +110,17 @@ __device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, int32
     }
 }
 
-// One shared atomicAdd per distinct digit per warp.  All 32 lanes must call.
-__device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t digit, bool valid, int lane)
+// Shared-memory histogram increment.  `agg`: warp-aggregated (one atomicAdd per
+// distinct digit per warp, via __match_any_sync; all 32 lanes must call), else
+// one plain shared atomicAdd per valid lane.
+__device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t digit, bool valid, int lane, bool agg)
 {
-    const unsigned peers = __match_any_sync(kFull, valid ? digit : 0xffffffffu);
-    if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+    if (agg) {
+        const unsigned peers = __match_any_sync(kFull, valid ? digit : 0xffffffffu);
+        if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
+    } else if (valid) {
+        atomicAdd(&hist[digit], 1u);
+    }
 }
 
 __device__ __forceinline__ uint32_t warp_exclusive_scan(uint32_t v, int lane, uint32_t &total)
@@ -136,33 +142,63 @@ __device__ __forceinline__ uint32_t take_from_ties(uint32_t need, uint32_t befor
     return count < left ? count : left;
 }
 
+// Exclusive prefix sum over the CTA (thread order); `total` gets the CTA sum.
+// Uses s_warp[NT/32]; contains two __syncthreads.
+template <int NT>
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s_warp, uint32_t &total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) s_warp[warp] = inc;
+    __syncthreads();
+    uint32_t before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        const uint32_t t = s_warp[w];
+        before += (w < warp) ? t : 0u;
+        tot += t;
+    }
+    __syncthreads();
+    total = tot;
+    return before + inc - v;
+}
+
 // Threshold digit of a histogram h[0, nb): the digit d with
 //   sum_{e > d} h[e] < need <= sum_{e >= d} h[e].
 // Result in out[0] = d, out[1] = sum_{e > d} h[e], out[2] = h[d].  All threads call.
-__device__ void find_threshold(const uint32_t *h, int nb, uint32_t need, uint32_t *out, uint32_t *wsum)
+template <int NT>
+__device__ void find_threshold(const uint32_t *h, int nb, uint32_t need, uint32_t *out, uint32_t *s_warp)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per = nb > kThreads ? nb / kThreads : 1;
+    const int tid = threadIdx.x;
+    const int per = nb > NT ? nb / NT : 1;
     const int lo = tid * per;
     uint32_t s = 0;
     if (lo < nb)
         for (int i = 0; i < per; ++i) s += h[lo + i];
-    uint32_t inc = s;  // becomes the sum over lanes >= lane
+    // exclusive scan in reversed thread order gives the count above this thread's bins
+    const int lane = tid & 31, warp = tid >> 5;
+    uint32_t inc = s;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const uint32_t y = __shfl_down_sync(kFull, inc, o);
         if (lane + o < 32) inc += y;
     }
-    if (lane == 0) wsum[warp] = inc;
+    if (lane == 0) s_warp[warp] = inc;
     __syncthreads();
     uint32_t above = inc - s;
-    for (int w = warp + 1; w < kWarps; ++w) above += wsum[w];
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) above += (w > warp) ? s_warp[w] : 0u;
     if (lo < nb && above < need && above + s >= need) {
         uint32_t acc = above;
         for (int i = per - 1; i >= 0; --i) {
             const uint32_t c = h[lo + i];
             if (acc + c >= need) {
-                out[0] = (uint32_t)(lo + i);
+                out[0] = static_cast<uint32_t>(lo + i);
                 out[1] = acc;
                 out[2] = c;
                 break;
@@ -191,48 +227,67 @@ __device__ __forceinline__ void store_val(const TopkArgs &a, int64_t row, int64_
 // Copies key rows for output positions [j0, j1) of `row`:
 //   gather_out[row, j, :] = key[row / rows_per_batch, max(col_j, 0), :]
 // col_j = glist[j - j0] when glist is given, else j for j < n_short and 0 beyond.
+template <int NT>
 __device__ void gather_rows_of(const TopkArgs &a, int64_t row, int64_t j0, int64_t j1, const int32_t *glist,
                                int64_t n_short)
 {
     const int vpr = static_cast<int>(a.d >> 3);  // 16-byte vectors per key row
     const int64_t bb = row / a.rows_per_batch;
     const uint16_t *kb = a.key + bb * a.key_batch_stride;
-    uint4 *ob = reinterpret_cast<uint4 *>(a.gather_out + row * a.n_gather * a.d);
+    uint4 *ob = reinterpret_cast<uint4 *>(a.gather_out + (row * a.n_gather + j0) * a.d);
     const int total = static_cast<int>(j1 - j0) * vpr;
-#pragma unroll 4
-    for (int t = threadIdx.x; t < total; t += kThreads) {
-        const int jj = t / vpr;
-        const int v = t - jj * vpr;
-        const int64_t j = j0 + jj;
-        int64_t p = glist ? static_cast<int64_t>(glist[jj]) : (j < n_short ? j : 0);
-        if (p < 0) p = 0;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (p < a.comp_len)
-            val = __ldg(reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + v);
-        else if (v == 0)
-            set_err(a.err_flag, kStatusInval);
-        __stcs(ob + j * vpr + v, val);
+    constexpr int U = 4;
+    for (int t0 = threadIdx.x; t0 < total; t0 += U * NT) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int t = t0 + u * NT;
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (t < total) {
+                const int jj = t / vpr;
+                const int64_t j = j0 + jj;
+                int64_t p = glist ? static_cast<int64_t>(glist[jj]) : (j < n_short ? j : 0);
+                if (p < 0) p = 0;
+                if (p < a.comp_len)
+                    v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + (t - jj * vpr));
+                else if (t - jj * vpr == 0)
+                    set_err(a.err_flag, kStatusInval);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int t = t0 + u * NT;
+            if (t < total) __stcs(ob + t, v[u]);
+        }
     }
 }
 
-template <typename E, bool CLUSTER, bool GATHER>
-__global__ void __launch_bounds__(kThreads, 2) topk_kernel(const TopkArgs a)
+template <int NT>
+struct MinBlocks {
+    static constexpr int value = NT >= 512 ? 2 : (NT >= 256 ? 4 : 8);
+};
+
+template <typename E, int NT, bool CLUSTER, bool GATHER>
+__global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const TopkArgs a)
 {
     using T = Elem<E>;
     constexpr int V = T::V;
+    constexpr int W = NT / 32;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t s_bar[kMaxChunks];
-    __shared__ uint32_t s_wsum[kWarps];
-    __shared__ uint32_t s_wgt[kWarps], s_weq[kWarps];
-    __shared__ uint32_t s_wsel_base[kWarps], s_weq_base[kWarps];
+    __shared__ uint32_t s_warp[W];
+    __shared__ uint32_t s_wgt[W], s_weq[W];
+    __shared__ uint32_t s_wsel_base[W], s_weq_base[W];
     __shared__ uint32_t s_thr[3];
     __shared__ uint32_t s_tot[2];       // this CTA's (greater, equal) counts; read by the cluster
     __shared__ uint32_t s_cta_sel[2];   // (selected before this CTA, selected by this CTA)
+    __shared__ uint32_t s_eq_before;    // keys of the threshold class before this CTA
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = CLUSTER ? cluster_rank() : 0u;
     const uint32_t csize = CLUSTER ? cluster_size() : 1u;
     const int64_t row = CLUSTER ? static_cast<int64_t>(cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
+    const bool agg = a.agg != 0;
 
     int64_t n = a.cols;
     if (a.row_end) {
@@ -247,13 +302,13 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const TopkArgs a)
         const int per = (k + static_cast<int>(csize) - 1) / static_cast<int>(csize);
         const int j0 = static_cast<int>(rank) * per;
         const int j1 = min(k, j0 + per);
-        for (int j = j0 + tid; j < j1; j += kThreads) {
+        for (int j = j0 + tid; j < j1; j += NT) {
             store_idx(a, row, j, j < n ? j : -1);
             if (a.want_values) store_val<E>(a, row, j, j < n ? xrow[j] : static_cast<E>(T::kFill));
         }
         if (GATHER) {
             const int64_t g1 = min(static_cast<int64_t>(j1), a.n_gather);
-            if (j0 < g1) gather_rows_of(a, row, j0, g1, nullptr, n);
+            if (j0 < g1) gather_rows_of<NT>(a, row, j0, g1, nullptr, n);
         }
         return;
     }
@@ -272,12 +327,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const TopkArgs a)
         for (int c = 0; c < nchunks; ++c) mbar_init(&s_bar[c], 1);
         fence_mbar_init();
     }
-    for (int i = tid; i < a.hist_bins; i += kThreads) hist[i] = 0u;
+    for (int i = tid; i < a.hist_bins; i += NT) hist[i] = 0u;
     if (CLUSTER) {
         uint32_t *m = reinterpret_cast<uint32_t *>(smem + a.smem_merge_off);
         int words = 0;
         for (int l = 0; l < a.nlevels; ++l) words += 1 << a.bits[l];
-        for (int i = tid; i < words; i += kThreads) m[i] = 0u;
+        for (int i = tid; i < words; i += NT) m[i] = 0u;
     }
     __syncthreads();
     if (tid == 0) {
@@ -299,16 +354,15 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const TopkArgs a)
         const uint32_t cb = min(kChunkBytes, bulk - static_cast<uint32_t>(c) * kChunkBytes);
         const int nv = static_cast<int>(cb >> 4);
         const uint4 *vb = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(c) * kChunkBytes);
-        for (int base = warp * 32; base < nv; base += kThreads) {
+        for (int base = warp * 32; base < nv; base += NT) {
             const int v = base + lane;
             const bool ok = v < nv;
-            const uint4 q = ok ? vb[v] : make_uint4(0u, 0u, 0u, 0u);
             E el[V];
-            T::unpack(q, el);
+            T::unpack(ok ? vb[v] : make_uint4(0u, 0u, 0u, 0u), el);
 #pragma unroll
             for (int t = 0; t < V; ++t) {
                 has_nan |= ok && T::is_nan(el[t]);
-                hist_add(hist, T::key(el[t]) >> sh0, ok, lane);
+                hist_add(hist, T::key(el[t]) >> sh0, ok, lane, agg);
             }
         }
     }
@@ -323,63 +377,187 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const TopkArgs a)
     }
     if (__syncthreads_or(has_nan) && tid == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
 
-    // --------------------------------------------------- radix levels
-    uint32_t prefix = 0;     // selection class: (key >> shift) == prefix
-    int shift = T::KB;
-    uint32_t need = static_cast<uint32_t>(k);
+    // histogram merge over the cluster (level l uses its own merge buffer) + threshold search
     uint32_t merge_off = a.smem_merge_off;
-    const int nvt = (len + V - 1) / V;
-    for (int l = 0; l < a.nlevels; ++l) {
-        const int bl = a.bits[l];
-        const int nsh = shift - bl;
-        const int nb = 1 << bl;
-        const uint32_t mask = static_cast<uint32_t>(nb - 1);
-        if (l > 0) {
-            const uint4 *vb = reinterpret_cast<const uint4 *>(buf);
-            for (int base = warp * 32; base < nvt; base += kThreads) {
-                const int v = base + lane;
-                const bool ok = v < nvt;
-                const uint4 q = ok ? vb[v] : make_uint4(0u, 0u, 0u, 0u);
-                E el[V];
-                T::unpack(q, el);
-#pragma unroll
-                for (int t = 0; t < V; ++t) {
-                    const uint32_t kk = T::key(el[t]);
-                    const bool m = ok && (v * V + t < len) && ((kk >> shift) == prefix);
-                    hist_add(hist, (kk >> nsh) & mask, m, lane);
-                }
-            }
-            __syncthreads();
-        }
+    auto resolve_level = [&](int nb, uint32_t need) {
         if (CLUSTER) {
             uint32_t *mrg = reinterpret_cast<uint32_t *>(smem + merge_off);
-            for (int i = tid; i < nb; i += kThreads) {
+            for (int i = tid; i < nb; i += NT) {
                 const uint32_t c = hist[i];
                 if (c) dsmem_add(map_to_rank(smem_addr(&mrg[i]), 0u), c);
             }
             cluster_sync();
-            for (int i = tid; i < nb; i += kThreads) hist[i] = dsmem_load(map_to_rank(smem_addr(&mrg[i]), 0u));
+            for (int i = tid; i < nb; i += NT) hist[i] = dsmem_load(map_to_rank(smem_addr(&mrg[i]), 0u));
             __syncthreads();
             merge_off += static_cast<uint32_t>(nb) * 4u;
         }
-        find_threshold(hist, nb, need, s_thr, s_wsum);
-        const uint32_t d = s_thr[0], above = s_thr[1], cnt = s_thr[2];
-        prefix = (l == 0) ? d : ((prefix << bl) | d);
+        find_threshold<NT>(hist, nb, need, s_thr, s_warp);
+    };
+
+    uint32_t prefix = 0;  // selection class: (key >> shift) == prefix
+    int shift;
+    uint32_t need = static_cast<uint32_t>(k);
+    const int nvt = (len + V - 1) / V;  // 16-byte vectors in the slice (last one may be partial)
+    const uint4 *vbuf = reinterpret_cast<const uint4 *>(buf);
+
+    resolve_level(1 << a.bits[0], need);
+    uint32_t cnt;
+    {
+        const uint32_t d = s_thr[0], above = s_thr[1];
+        cnt = s_thr[2];
+        prefix = d;
+        need -= above;
+        shift = sh0;
+        for (int i = tid; i < (1 << a.bits[0]); i += NT) hist[i] = 0u;
+        // keys with top digit >= d: the (index-ordered) candidate list holds them if it can
+        // (every CTA has the same merged counts, so the choice is the same cluster-wide)
+    }
+    const bool list_mode = (a.list_cap >= len) || ((static_cast<uint32_t>(k) - need) + cnt <= static_cast<uint32_t>(a.list_cap));
+    __syncthreads();
+
+    uint16_t *list = reinterpret_cast<uint16_t *>(smem + a.smem_list_off);
+    int L = 0;
+    if (list_mode) {
+        // ---- filter: one mask byte per 16-byte vector, bit t set when key digit >= d
+        uint8_t *masks = smem + a.smem_mask_off;
+        for (int base = warp * 32; base < nvt; base += NT) {
+            const int v = base + lane;
+            if (v < nvt) {
+                E el[V];
+                T::unpack(vbuf[v], el);
+                uint32_t m = 0;
+#pragma unroll
+                for (int t = 0; t < V; ++t)
+                    m |= static_cast<uint32_t>((v * V + t < len) && ((T::key(el[t]) >> shift) >= prefix)) << t;
+                masks[v] = static_cast<uint8_t>(m);
+            }
+        }
+        __syncthreads();
+        // ---- ordered list: each thread owns a contiguous run of vectors
+        const int q = (nvt + NT - 1) / NT;
+        const int v0 = min(nvt, tid * q), v1 = min(nvt, v0 + q);
+        uint32_t c = 0;
+        for (int v = v0; v < v1; ++v) c += __popc(static_cast<uint32_t>(masks[v]));
+        uint32_t tot;
+        uint32_t pos = block_exclusive_scan<NT>(c, s_warp, tot);
+        for (int v = v0; v < v1; ++v) {
+            uint32_t m = masks[v];
+            while (m) {
+                const int b = __ffs(m) - 1;
+                list[pos++] = static_cast<uint16_t>(v * V + b);
+                m &= m - 1u;
+            }
+        }
+        L = static_cast<int>(tot);
+        __syncthreads();
+    }
+
+    // ---------------------------------------------------- further levels
+    for (int l = 1; l < a.nlevels && cnt != need; ++l) {
+        const int bl = a.bits[l];
+        const int nsh = shift - bl;
+        const int nb = 1 << bl;
+        const uint32_t mask = static_cast<uint32_t>(nb - 1);
+        if (list_mode) {
+            for (int i = tid; i < L; i += NT) {
+                const uint32_t kk = T::key(buf[list[i]]);
+                if ((kk >> shift) == prefix) atomicAdd(&hist[(kk >> nsh) & mask], 1u);
+            }
+        } else {
+            for (int base = warp * 32; base < nvt; base += NT) {
+                const int v = base + lane;
+                if (v < nvt) {
+                    E el[V];
+                    T::unpack(vbuf[v], el);
+#pragma unroll
+                    for (int t = 0; t < V; ++t) {
+                        const uint32_t kk = T::key(el[t]);
+                        if ((v * V + t < len) && ((kk >> shift) == prefix)) atomicAdd(&hist[(kk >> nsh) & mask], 1u);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        resolve_level(nb, need);
+        const uint32_t d = s_thr[0], above = s_thr[1];
+        cnt = s_thr[2];
+        prefix = (prefix << bl) | d;
         need -= above;
         shift = nsh;
-        for (int i = tid; i < nb; i += kThreads) hist[i] = 0u;
+        for (int i = tid; i < nb; i += NT) hist[i] = 0u;
         __syncthreads();
-        if (cnt == need) break;  // every key of the threshold bin is selected
     }
     const uint32_t P = prefix;
     const int S = shift;
     const uint32_t E_need = need;  // keys of class P still to take, in column order
 
-    // ----------------------------------------------- count per warp segment
-    const int seg = ((len + kWarps - 1) / kWarps + 32 * V - 1) / (32 * V) * (32 * V);
-    const int w_lo = min(len, warp * seg);
-    const int w_hi = min(len, w_lo + seg);
-    {
+    // --------------------------------------------- ordered write of the k
+    int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
+    auto exchange_cta_totals = [&](uint32_t tg, uint32_t te) {
+        // (selected before this CTA, threshold-class keys before this CTA) over the cluster, in rank order
+        if (tid == 0) {
+            s_tot[0] = tg;
+            s_tot[1] = te;
+        }
+        if (CLUSTER)
+            cluster_sync();
+        else
+            __syncthreads();
+        if (tid == 0) {
+            uint32_t eqb = 0, selb = 0;
+            if constexpr (CLUSTER) {
+                for (uint32_t r = 0; r < rank; ++r) {
+                    const uint32_t g = dsmem_load(map_to_rank(smem_addr(&s_tot[0]), r));
+                    const uint32_t e = dsmem_load(map_to_rank(smem_addr(&s_tot[1]), r));
+                    selb += g + take_from_ties(E_need, eqb, e);
+                    eqb += e;
+                }
+            }
+            s_cta_sel[0] = selb;
+            s_cta_sel[1] = tg + take_from_ties(E_need, eqb, te);
+            s_eq_before = eqb;
+        }
+        __syncthreads();
+    };
+
+    if (list_mode) {
+        const int m = (L + NT - 1) / NT;
+        const int i0 = min(L, tid * m), i1 = min(L, i0 + m);
+        uint32_t g = 0, q = 0;
+        for (int i = i0; i < i1; ++i) {
+            const uint32_t c = T::key(buf[list[i]]) >> S;
+            g += c > P;
+            q += c == P;
+        }
+        uint32_t tg, tq;
+        (void)block_exclusive_scan<NT>(g, s_warp, tg);
+        const uint32_t qx = block_exclusive_scan<NT>(q, s_warp, tq);
+        exchange_cta_totals(tg, tq);
+        uint32_t r = s_eq_before + qx;
+        const uint32_t sel = g + take_from_ties(E_need, r, q);
+        uint32_t ts;
+        uint32_t pos = s_cta_sel[0] + block_exclusive_scan<NT>(sel, s_warp, ts);
+        const uint32_t cta_base = s_cta_sel[0];
+        for (int i = i0; i < i1; ++i) {
+            const int o = list[i];
+            const E e = buf[o];
+            const uint32_t c = T::key(e) >> S;
+            bool take = c > P;
+            if (c == P) take = (r++ < E_need);
+            if (take) {
+                const int64_t col = lo + o;
+                store_idx(a, row, pos, col);
+                if (a.want_values) store_val<E>(a, row, pos, e);
+                if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos - cta_base] = static_cast<int32_t>(col);
+                ++pos;
+            }
+        }
+    } else {
+        // full-slice fallback (threshold bin too large for the list): warp-segment counts, then an
+        // ordered write in which every warp walks its own contiguous segment
+        const int seg = ((len + W - 1) / W + 32 * V - 1) / (32 * V) * (32 * V);
+        const int w_lo = min(len, warp * seg);
+        const int w_hi = min(len, w_lo + seg);
         uint32_t gt = 0, eq = 0;
         for (int o = w_lo + lane * V; o < w_hi; o += 32 * V) {
             E el[V];
@@ -399,46 +577,23 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const TopkArgs a)
             s_wgt[warp] = gt;
             s_weq[warp] = eq;
         }
-    }
-    __syncthreads();
-    if (tid == 0) {
+        __syncthreads();
         uint32_t tg = 0, te = 0;
-        for (int w = 0; w < kWarps; ++w) {
+        for (int w = 0; w < W; ++w) {
             tg += s_wgt[w];
             te += s_weq[w];
         }
-        s_tot[0] = tg;
-        s_tot[1] = te;
-    }
-    if (CLUSTER)
-        cluster_sync();
-    else
-        __syncthreads();
-    if (tid == 0) {
-        uint32_t eqb = 0, selb = 0;
-        if constexpr (CLUSTER) {
-            for (uint32_t q = 0; q < rank; ++q) {
-                const uint32_t g = dsmem_load(map_to_rank(smem_addr(&s_tot[0]), q));
-                const uint32_t e = dsmem_load(map_to_rank(smem_addr(&s_tot[1]), q));
-                selb += g + take_from_ties(E_need, eqb, e);
-                eqb += e;
+        exchange_cta_totals(tg, te);
+        if (tid == 0) {
+            uint32_t ws = s_cta_sel[0], we = s_eq_before;
+            for (int w = 0; w < W; ++w) {
+                s_wsel_base[w] = ws;
+                s_weq_base[w] = we;
+                ws += s_wgt[w] + take_from_ties(E_need, we, s_weq[w]);
+                we += s_weq[w];
             }
         }
-        s_cta_sel[0] = selb;
-        uint32_t ws = selb, we = eqb;
-        for (int w = 0; w < kWarps; ++w) {
-            s_wsel_base[w] = ws;
-            s_weq_base[w] = we;
-            ws += s_wgt[w] + take_from_ties(E_need, we, s_weq[w]);
-            we += s_weq[w];
-        }
-        s_cta_sel[1] = ws - selb;
-    }
-    __syncthreads();
-
-    // --------------------------------------------- ordered write of the k
-    int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
-    {
+        __syncthreads();
         const uint32_t cta_base = s_cta_sel[0];
         uint32_t eq_run = s_weq_base[warp];
         uint32_t sel_run = s_wsel_base[warp];
@@ -475,7 +630,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const TopkArgs a)
                     const int64_t col = lo + o + t;
                     store_idx(a, row, pos, col);
                     if (a.want_values) store_val<E>(a, row, pos, el[t]);
-                    if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos - cta_base] = static_cast<int32_t>(col);
+                    if (GATHER && static_cast<int64_t>(pos) < a.n_gather)
+                        glist[pos - cta_base] = static_cast<int32_t>(col);
                     ++pos;
                 }
             }
@@ -489,15 +645,15 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const TopkArgs a)
         __syncthreads();
         const int64_t g0 = s_cta_sel[0];
         const int64_t g1 = min(g0 + static_cast<int64_t>(s_cta_sel[1]), a.n_gather);
-        if (g0 < g1) gather_rows_of(a, row, g0, g1, glist, 0);
+        if (g0 < g1) gather_rows_of<NT>(a, row, g0, g1, glist, 0);
     }
     if (CLUSTER) cluster_sync();  // keep this CTA's shared memory alive until the cluster is done with it
 }
 
-template <typename E, bool C, bool G>
+template <typename E, int NT, bool C, bool G>
 cudaError_t launch_variant(int cluster, size_t smem, const TopkArgs &a, cudaStream_t stream)
 {
-    auto kern = topk_kernel<E, C, G>;
+    auto kern = topk_kernel<E, NT, C, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (C && cluster > 8) {
@@ -506,7 +662,7 @@ cudaError_t launch_variant(int cluster, size_t smem, const TopkArgs &a, cudaStre
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.rows * (C ? cluster : 1)), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -521,22 +677,22 @@ cudaError_t launch_variant(int cluster, size_t smem, const TopkArgs &a, cudaStre
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <typename E, bool C, bool G>
+template <typename E, int NT, bool C, bool G>
 int max_clusters_variant(int cluster, size_t smem)
 {
-    auto kern = topk_kernel<E, C, G>;
+    auto kern = topk_kernel<E, NT, C, G>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
         return 0;
     if (!C) {
         int blocks = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, kThreads, smem) != cudaSuccess) return 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, NT, smem) != cudaSuccess) return 0;
         return blocks * device_sm_count();
     }
     if (cluster > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -553,36 +709,60 @@ int max_clusters_variant(int cluster, size_t smem)
     return n;
 }
 
-}  // namespace
-
-cudaError_t launch_topk(int dtype, bool gather, int cluster, size_t smem, const TopkArgs &a, cudaStream_t stream)
+// Dispatch over (dtype, threads, cluster?, gather?) to one of the 24 instantiations.
+template <typename E, int NT>
+cudaError_t launch_nt(bool gather, int cluster, size_t smem, const TopkArgs &a, cudaStream_t s)
 {
-    const bool c = cluster > 1;
-    if (dtype == 0) {
-        if (c) return gather ? launch_variant<uint32_t, true, true>(cluster, smem, a, stream)
-                             : launch_variant<uint32_t, true, false>(cluster, smem, a, stream);
-        return gather ? launch_variant<uint32_t, false, true>(1, smem, a, stream)
-                      : launch_variant<uint32_t, false, false>(1, smem, a, stream);
-    }
-    if (c) return gather ? launch_variant<uint16_t, true, true>(cluster, smem, a, stream)
-                         : launch_variant<uint16_t, true, false>(cluster, smem, a, stream);
-    return gather ? launch_variant<uint16_t, false, true>(1, smem, a, stream)
-                  : launch_variant<uint16_t, false, false>(1, smem, a, stream);
+    if (cluster > 1)
+        return gather ? launch_variant<E, NT, true, true>(cluster, smem, a, s)
+                      : launch_variant<E, NT, true, false>(cluster, smem, a, s);
+    return gather ? launch_variant<E, NT, false, true>(1, smem, a, s) : launch_variant<E, NT, false, false>(1, smem, a, s);
 }
 
-int topk_max_active_clusters(int dtype, bool gather, int cluster, size_t smem)
+template <typename E, int NT>
+int occupancy_nt(bool gather, int cluster, size_t smem)
 {
-    const bool c = cluster > 1;
-    if (dtype == 0) {
-        if (c) return gather ? max_clusters_variant<uint32_t, true, true>(cluster, smem)
-                             : max_clusters_variant<uint32_t, true, false>(cluster, smem);
-        return gather ? max_clusters_variant<uint32_t, false, true>(1, smem)
-                      : max_clusters_variant<uint32_t, false, false>(1, smem);
+    if (cluster > 1)
+        return gather ? max_clusters_variant<E, NT, true, true>(cluster, smem)
+                      : max_clusters_variant<E, NT, true, false>(cluster, smem);
+    return gather ? max_clusters_variant<E, NT, false, true>(1, smem) : max_clusters_variant<E, NT, false, false>(1, smem);
+}
+
+template <typename E>
+cudaError_t launch_e(int threads, bool gather, int cluster, size_t smem, const TopkArgs &a, cudaStream_t s)
+{
+    switch (threads) {
+    case 128: return launch_nt<E, 128>(gather, cluster, smem, a, s);
+    case 256: return launch_nt<E, 256>(gather, cluster, smem, a, s);
+    case 512: return launch_nt<E, 512>(gather, cluster, smem, a, s);
+    default: return cudaErrorInvalidValue;
     }
-    if (c) return gather ? max_clusters_variant<uint16_t, true, true>(cluster, smem)
-                         : max_clusters_variant<uint16_t, true, false>(cluster, smem);
-    return gather ? max_clusters_variant<uint16_t, false, true>(1, smem)
-                  : max_clusters_variant<uint16_t, false, false>(1, smem);
+}
+
+template <typename E>
+int occupancy_e(int threads, bool gather, int cluster, size_t smem)
+{
+    switch (threads) {
+    case 128: return occupancy_nt<E, 128>(gather, cluster, smem);
+    case 256: return occupancy_nt<E, 256>(gather, cluster, smem);
+    case 512: return occupancy_nt<E, 512>(gather, cluster, smem);
+    default: return 0;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_topk(int dtype, int threads, bool gather, int cluster, size_t smem, const TopkArgs &a,
+                        cudaStream_t stream)
+{
+    return dtype == 0 ? launch_e<uint32_t>(threads, gather, cluster, smem, a, stream)
+                      : launch_e<uint16_t>(threads, gather, cluster, smem, a, stream);
+}
+
+int topk_max_active_clusters(int dtype, int threads, bool gather, int cluster, size_t smem)
+{
+    return dtype == 0 ? occupancy_e<uint32_t>(threads, gather, cluster, smem)
+                      : occupancy_e<uint16_t>(threads, gather, cluster, smem);
 }
 
 size_t topk_smem_limit()

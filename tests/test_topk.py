@@ -168,6 +168,11 @@ EDGE = [
     ("bf16", 1, 262147, 64, "normal"),
     ("f32", 300, 1000, 64, "normal"),
     ("bf16", 700, 4100, 256, "two_level"),
+    # one CTA per row with a threshold bin too large for the candidate list: full-slice path
+    ("bf16", 320, 16384, 100, "equal"),
+    ("f32", 320, 9000, 64, "two_level"),
+    ("bf16", 320, 16384, 2048, "levels"),
+    ("f32", 310, 40000, 4096, "zeros_inf"),
 ]
 
 
