@@ -36,7 +36,7 @@ def sources() -> list[str]:
 
 
 def _deps() -> list[str]:
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if not f.startswith(".")]
     files.append(os.path.join(ROOT, "include", "sel.h"))
     return files
 

@@ -66,6 +66,12 @@ struct GatherArgs {
 cudaError_t launch_topk(int dtype, int threads, bool gather, int cluster, size_t smem_bytes, const TopkArgs &a,
                         cudaStream_t stream);
 
+// Per element type (topk_f32.cu / topk_bf16.cu).
+cudaError_t launch_topk_f32(int threads, bool gather, int cluster, size_t smem, const TopkArgs &a, cudaStream_t s);
+cudaError_t launch_topk_bf16(int threads, bool gather, int cluster, size_t smem, const TopkArgs &a, cudaStream_t s);
+int topk_occupancy_f32(int threads, bool gather, int cluster, size_t smem);
+int topk_occupancy_bf16(int threads, bool gather, int cluster, size_t smem);
+
 // Max dynamic shared memory a selection CTA may use on the current device.
 size_t topk_smem_limit();
 
