@@ -170,6 +170,14 @@ class Runner:
             self.gout = torch.empty((w["rows"], w["n_gather"], w["d"]), dtype=torch.bfloat16, device=dev)
         self.nan = torch.zeros(1, dtype=torch.int32, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        # outputs allocated once (rows padded to 16 bytes), so a step is the library call alone
+        k = w["k"]
+        ipad = (k + 3) // 4 * 4 if self.idx_t == torch.int32 else (k + 1) // 2 * 2
+        self.out_idx = torch.empty((w["rows"], ipad), dtype=self.idx_t, device=dev)
+        self.out_val = None
+        if w["want_values"]:
+            vpad = (k + 3) // 4 * 4 if w["dtype"] == "f32" else (k + 7) // 8 * 8
+            self.out_val = torch.empty((w["rows"], vpad), dtype=self.x.dtype, device=dev)
         self.launches_per_step = 1
 
     def step(self):
@@ -178,9 +186,11 @@ class Runner:
             return self.g.topk_gather(self.x, w["k"], self.key, w["n_gather"], end=self.end,
                                       sorted_index=w["sorted_index"], indices_type=self.idx_t,
                                       return_value=w["want_values"], gather_out=self.gout,
+                                      output_idx=self.out_idx, output_val=self.out_val,
                                       nan_flag=self.nan, err_flag=self.err)
         return self.g.topk(self.x, w["k"], end=self.end, sorted_index=w["sorted_index"], indices_type=self.idx_t,
-                           return_value=w["want_values"], nan_flag=self.nan, err_flag=self.err)
+                           return_value=w["want_values"], output_idx=self.out_idx, output_val=self.out_val,
+                           nan_flag=self.nan, err_flag=self.err)
 
 
 def time_steps(runner, steps, warmup, flush):

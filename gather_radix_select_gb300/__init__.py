@@ -31,11 +31,18 @@ def library_path() -> str:
     return _native.library_path()
 
 
+_ALIGN = None
+
+
 def stride_requirement() -> tuple[int, int]:
     """(input_alignment, output_alignment) in bytes, as in ``get_stride_requirement()``."""
-    a, b = ctypes.c_int(), ctypes.c_int()
-    _native.check(_native.load().sel_stride_requirement(ctypes.byref(a), ctypes.byref(b)), "sel_stride_requirement")
-    return a.value, b.value
+    global _ALIGN
+    if _ALIGN is None:
+        a, b = ctypes.c_int(), ctypes.c_int()
+        _native.check(_native.load().sel_stride_requirement(ctypes.byref(a), ctypes.byref(b)),
+                      "sel_stride_requirement")
+        _ALIGN = (a.value, b.value)
+    return _ALIGN
 
 
 def max_cols(dtype: torch.dtype = torch.float32) -> int:
@@ -88,15 +95,17 @@ def _row_stride(x):
 
 def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_index: bool = False,
          indices_type: torch.dtype = torch.int32, return_value: bool = True,
-         output_idx: torch.Tensor | None = None, nan_flag: torch.Tensor | None = None,
-         err_flag: torch.Tensor | None = None, stream=None):
+         output_idx: torch.Tensor | None = None, output_val: torch.Tensor | None = None,
+         nan_flag: torch.Tensor | None = None, err_flag: torch.Tensor | None = None, stream=None):
     """Row-wise top-k of a 2-D CUDA tensor (largest values; ties: smaller index).
 
     Returns ``(values, indices)``; ``values`` is None when ``return_value``
     is False.  Rows shorter than k (per ``end``) are filled with index -1 and
     value -inf.  Outputs may be non-contiguous (row strides padded to the
     output alignment).  ``nan_flag`` / ``err_flag`` are optional caller-zeroed
-    int32 CUDA tensors the kernel ORs / writes into.
+    int32 CUDA tensors the kernel ORs / writes into.  ``output_idx`` /
+    ``output_val`` are optional caller-owned [rows, >=k] buffers (row strides
+    a multiple of the output alignment); results go to their first k columns.
     """
     _check_x(x)
     rows, cols = x.shape
@@ -111,7 +120,15 @@ def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_ind
         if idx.dtype != indices_type or idx.dim() != 2 or idx.shape[0] != rows or idx.shape[1] < k \
                 or (rows > 1 and idx.stride(1) != 1) or idx.device != dev:
             raise ValueError("output_idx must be a [rows, >=k] %s tensor on x's device" % indices_type)
-    val = _padded_rows(rows, k, x.dtype, dev) if return_value else None
+    if not return_value:
+        val = None
+    elif output_val is None:
+        val = _padded_rows(rows, k, x.dtype, dev)
+    else:
+        val = output_val
+        if val.dtype != x.dtype or val.dim() != 2 or val.shape[0] != rows or val.shape[1] < k \
+                or (rows > 1 and val.stride(1) != 1) or val.device != dev:
+            raise ValueError("output_val must be a [rows, >=k] tensor of x's dtype on x's device")
     with torch.cuda.device(dev):
         st = _native.load().sel_topk(
             _ptr(x), _DTYPES[x.dtype], rows, cols, _row_stride(x), _ptr(end), int(k), int(bool(sorted_index)),
@@ -119,6 +136,8 @@ def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_ind
             _ptr(val), 0 if val is None else (val.stride(0) if rows > 1 else max(val.stride(0), k)),
             _ptr(nan_flag), _ptr(err_flag), _stream(dev, stream))
     _native.check(st, "sel_topk")
+    if output_val is not None and val is not None:
+        val = val[:, :k]
     return val, idx[:, :k] if output_idx is not None else idx
 
 
@@ -161,6 +180,7 @@ def gather_rows(key: torch.Tensor, idx: torch.Tensor, *, out: torch.Tensor | Non
 def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, end: torch.Tensor | None = None,
                 sorted_index: bool = False, indices_type: torch.dtype = torch.int32, return_value: bool = False,
                 return_indices: bool = True, gather_out: torch.Tensor | None = None,
+                output_idx: torch.Tensor | None = None, output_val: torch.Tensor | None = None,
                 nan_flag: torch.Tensor | None = None, err_flag: torch.Tensor | None = None, stream=None):
     """``topk`` then ``gather_rows`` of the first ``n_gather`` selected columns, in one launch.
 
@@ -175,8 +195,14 @@ def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, en
     b, comp_len, d = key.shape
     if key.device != dev:
         raise ValueError("key must be on x's device")
-    idx = _padded_rows(rows, k, indices_type, dev) if return_indices else None
-    val = _padded_rows(rows, k, x.dtype, dev) if return_value else None
+    if not return_indices:
+        idx = None
+    else:
+        idx = output_idx if output_idx is not None else _padded_rows(rows, k, indices_type, dev)
+    if not return_value:
+        val = None
+    else:
+        val = output_val if output_val is not None else _padded_rows(rows, k, x.dtype, dev)
     if gather_out is None:
         gather_out = torch.empty((rows, n_gather, d), dtype=torch.bfloat16, device=dev)
     elif gather_out.shape != (rows, n_gather, d) or not gather_out.is_contiguous():
@@ -190,4 +216,8 @@ def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, en
             _ptr(key), b, comp_len, d, kbs, krs, int(n_gather), _ptr(gather_out),
             _ptr(nan_flag), _ptr(err_flag), _stream(dev, stream))
     _native.check(st, "sel_topk_gather")
+    if idx is not None and output_idx is not None:
+        idx = idx[:, :k]
+    if val is not None and output_val is not None:
+        val = val[:, :k]
     return val, idx, gather_out

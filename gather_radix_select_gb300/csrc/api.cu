@@ -72,13 +72,13 @@ size_t layout_for(int dtype, int cluster, int64_t slice, int k, bool gather, int
     a.smem_buf_bytes = static_cast<uint32_t>(off);
     a.smem_hist_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(a.hist_bins) * 4;
-    a.smem_merge_off = static_cast<uint32_t>(off);
-    if (cluster > 1)
-        for (int l = 0; l < a.nlevels; ++l) off += static_cast<size_t>(1u << a.bits[l]) * 4;
     a.smem_mask_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(round_up(ceil_div(slice, 16 / e), 16));
-    // candidate list: keys whose top digit reaches the threshold bin (at most k - 1 above it plus the bin)
-    const int64_t cap = slice < static_cast<int64_t>(k) + 4096 ? slice : static_cast<int64_t>(k) + 4096;
+    // candidate list (16-bit offsets): this CTA's share of k with room for the threshold bin; a CTA
+    // whose candidates do not fit works on its whole staged slice instead
+    const int64_t share = cluster > 1 ? 2 * ceil_div(k, cluster) : static_cast<int64_t>(k);
+    const int64_t want = share + 2048;
+    const int64_t cap = slice < want ? slice : want;
     a.list_cap = static_cast<int32_t>(cap);
     a.smem_list_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(round_up(cap * 2, 16));
@@ -145,6 +145,8 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
 {
     digit_plan(dtype, cols, p.layout);
     p.layout.agg = hist_agg();
+    p.layout.sample_step = 8;
+    p.layout.sample_min_cols = 8192;
     const size_t limit = sel::topk_smem_limit();
     const int sms = sel::device_sm_count();
     if (limit == 0 || sms == 0) return SEL_ECUDA;
@@ -170,6 +172,30 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
         if (too_big) break;
     }
     return SEL_EUNSUPPORTED;
+}
+
+// make_plan behind a cache: the plan depends only on the device and the call's shape.
+int cached_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, Plan &p)
+{
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int64_t, int64_t, int, int64_t>, Plan> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SEL_ECUDA;
+    const auto key = std::make_tuple(dev, dtype, rows, cols, k, gather ? n_gather : -1);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            p = it->second;
+            return SEL_OK;
+        }
+    }
+    const int st = make_plan(dtype, rows, cols, k, gather, n_gather, p);
+    if (st != SEL_OK) return st;
+    std::lock_guard<std::mutex> g(mu);
+    if (cache.size() > 4096) cache.clear();
+    cache[key] = p;
+    return SEL_OK;
 }
 
 int check_topk_args(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride, int k, int idx_dtype,
@@ -267,7 +293,7 @@ int sel_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
                              out_val_stride, true);
     if (st != SEL_OK || rows == 0) return st;
     Plan p;
-    st = make_plan(dtype, rows, cols, k, false, 0, p);
+    st = cached_plan(dtype, rows, cols, k, false, 0, p);
     if (st != SEL_OK) return st;
     sel::TopkArgs a = p.layout;
     a.x = x;
@@ -333,7 +359,7 @@ int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_
         if (st != SEL_OK) return st;
     }
     Plan p;
-    st = make_plan(dtype, rows, cols, k, n_gather > 0, n_gather, p);
+    st = cached_plan(dtype, rows, cols, k, n_gather > 0, n_gather, p);
     if (st != SEL_OK) return st;
     sel::TopkArgs a = p.layout;
     a.x = x;

@@ -99,6 +99,11 @@ __device__ __forceinline__ void dsmem_add(uint32_t caddr, uint32_t v)
     asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void dsmem_store(uint32_t caddr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t dsmem_load(uint32_t caddr)
 {
     uint32_t v;

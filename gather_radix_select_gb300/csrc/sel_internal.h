@@ -36,12 +36,14 @@ struct TopkArgs {
     int32_t hist_bins;        // 1 << max(bits)
     uint32_t smem_buf_bytes;  // bytes reserved for the staged slice
     uint32_t smem_hist_off;   // offset of the local histogram
-    uint32_t smem_merge_off;  // offset of the per-level merged histograms (cluster only)
     uint32_t smem_mask_off;   // offset of the per-vector candidate masks (one byte per 16-byte vector)
     uint32_t smem_list_off;   // offset of the candidate list (16-bit offsets within the slice)
     uint32_t smem_glist_off;  // offset of the gather position list (fused only)
     int32_t list_cap;         // capacity of the candidate list
     int32_t agg;              // 1: first-pass histogram with warp-aggregated atomics
+    int32_t sample_step;      // > 1: the first digit's threshold is estimated from every
+                              //      sample_step-th 16-byte vector of the row
+    int32_t sample_min_cols;  // rows shorter than this use the exact first histogram
     // fused gather (ignored unless the gather variant is launched)
     const uint16_t *key;
     int64_t comp_len, d, key_batch_stride, key_row_stride, rows_per_batch;

@@ -280,8 +280,8 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
     __shared__ uint32_t s_warp[W];
     __shared__ uint32_t s_wgt[W], s_weq[W];
     __shared__ uint32_t s_wsel_base[W], s_weq_base[W];
-    __shared__ uint32_t s_thr[3];
-    __shared__ uint32_t s_tot[2];       // this CTA's (greater, equal) counts; read by the cluster
+    __shared__ uint32_t s_res[4];       // broadcast result of a histogram reduction
+    __shared__ uint32_t s_all_g[kMaxCluster], s_all_e[kMaxCluster];  // per-CTA counts, written by the cluster
     __shared__ uint32_t s_cta_sel[2];   // (selected before this CTA, selected by this CTA)
     __shared__ uint32_t s_eq_before;    // keys of the threshold class before this CTA
 
@@ -324,18 +324,15 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
     const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(E);
     const uint32_t bulk = bytes & ~15u;
     const int nchunks = static_cast<int>((bulk + kChunkBytes - 1) / kChunkBytes);
+    // sampled first digit: only every sample_step-th 16-byte vector feeds the first histogram
+    const bool sampled = a.sample_step > 1 && n >= 4LL * k && n >= static_cast<int64_t>(a.sample_min_cols);
+    const int step = sampled ? a.sample_step : 1;
 
     if (tid == 0) {
         for (int c = 0; c < nchunks; ++c) mbar_init(&s_bar[c], 1);
         fence_mbar_init();
     }
     for (int i = tid; i < a.hist_bins; i += NT) hist[i] = 0u;
-    if (CLUSTER) {
-        uint32_t *m = reinterpret_cast<uint32_t *>(smem + a.smem_merge_off);
-        int words = 0;
-        for (int l = 0; l < a.nlevels; ++l) words += 1 << a.bits[l];
-        for (int i = tid; i < words; i += NT) m[i] = 0u;
-    }
     __syncthreads();
     if (tid == 0) {
         const char *src = reinterpret_cast<const char *>(xrow + lo);
@@ -346,26 +343,23 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
                       &s_bar[c]);
         }
     }
-    if (CLUSTER) cluster_sync();  // all CTAs started and merge buffers zeroed before any remote access
+    if (CLUSTER) cluster_sync();  // every CTA of the cluster has started before any remote access
 
-    // ------------------------------- pass 1: top digit, while chunks land
+    // -------------- first-digit histogram (every step-th vector) while chunks land
     const int sh0 = T::KB - a.bits[0];
-    bool has_nan = false;
+    const int nb0 = 1 << a.bits[0];
     for (int c = 0; c < nchunks; ++c) {
         wait_phase(&s_bar[c], 0u, a.err_flag);
         const uint32_t cb = min(kChunkBytes, bulk - static_cast<uint32_t>(c) * kChunkBytes);
         const int nv = static_cast<int>(cb >> 4);
         const uint4 *vb = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(c) * kChunkBytes);
-        for (int base = warp * 32; base < nv; base += NT) {
-            const int v = base + lane;
+        for (int base = warp * 32; base * step < nv; base += NT) {
+            const int v = (base + lane) * step;
             const bool ok = v < nv;
             E el[V];
             T::unpack(ok ? vb[v] : make_uint4(0u, 0u, 0u, 0u), el);
 #pragma unroll
-            for (int t = 0; t < V; ++t) {
-                has_nan |= ok && T::is_nan(el[t]);
-                hist_add(hist, T::key(el[t]) >> sh0, ok, lane, agg);
-            }
+            for (int t = 0; t < V; ++t) hist_add(hist, T::key(el[t]) >> sh0, ok, lane, agg);
         }
     }
     {
@@ -373,55 +367,58 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
         if (tid < len - tail0) {  // < 16 bytes left over: plain loads
             const E e = xrow[lo + tail0 + tid];
             buf[tail0 + tid] = e;
-            has_nan |= T::is_nan(e);
-            atomicAdd(&hist[T::key(e) >> sh0], 1u);
+            if (!sampled) atomicAdd(&hist[T::key(e) >> sh0], 1u);
         }
     }
-    if (__syncthreads_or(has_nan) && tid == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
-
-    // histogram merge over the cluster (level l uses its own merge buffer) + threshold search
-    uint32_t merge_off = a.smem_merge_off;
-    auto resolve_level = [&](int nb, uint32_t need) {
-        if (CLUSTER) {
-            uint32_t *mrg = reinterpret_cast<uint32_t *>(smem + merge_off);
-            for (int i = tid; i < nb; i += NT) {
-                const uint32_t c = hist[i];
-                if (c) dsmem_add(map_to_rank(smem_addr(&mrg[i]), 0u), c);
-            }
-            cluster_sync();
-            for (int i = tid; i < nb; i += NT) hist[i] = dsmem_load(map_to_rank(smem_addr(&mrg[i]), 0u));
-            __syncthreads();
-            merge_off += static_cast<uint32_t>(nb) * 4u;
-        }
-        find_threshold<NT>(hist, nb, need, s_thr, s_warp);
-    };
-
-    uint32_t prefix = 0;  // selection class: (key >> shift) == prefix
-    int shift;
-    uint32_t need = static_cast<uint32_t>(k);
-    const int nvt = (len + V - 1) / V;  // 16-byte vectors in the slice (last one may be partial)
-    const uint4 *vbuf = reinterpret_cast<const uint4 *>(buf);
-
-    resolve_level(1 << a.bits[0], need);
-    uint32_t cnt;
-    {
-        const uint32_t d = s_thr[0], above = s_thr[1];
-        cnt = s_thr[2];
-        prefix = d;
-        need -= above;
-        shift = sh0;
-        for (int i = tid; i < (1 << a.bits[0]); i += NT) hist[i] = 0u;
-        // keys with top digit >= d: the (index-ordered) candidate list holds them if it can
-        // (every CTA has the same merged counts, so the choice is the same cluster-wide)
-    }
-    const bool list_mode = (a.list_cap >= len) || ((static_cast<uint32_t>(k) - need) + cnt <= static_cast<uint32_t>(a.list_cap));
     __syncthreads();
 
+    // Histogram reduction over the cluster: CTA 0's histogram is the merge target; CTA 0 evaluates
+    // `decide` on the total and stores s_res[0..3] into every CTA.  Leaves every local histogram zero.
+    auto reduce_decide = [&](int nb, auto &&decide) {
+        if constexpr (CLUSTER) {
+            if (rank != 0) {
+                for (int i = tid; i < nb; i += NT) {
+                    const uint32_t c = hist[i];
+                    if (c) {
+                        dsmem_add(map_to_rank(smem_addr(&hist[i]), 0u), c);
+                        hist[i] = 0u;
+                    }
+                }
+            }
+            cluster_sync();
+            if (rank == 0) {
+                decide(hist, nb);  // block-wide; ends with __syncthreads
+                for (int i = tid; i < nb; i += NT) hist[i] = 0u;
+                if (tid < static_cast<int>(csize)) {
+                    const uint32_t r = static_cast<uint32_t>(tid);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) dsmem_store(map_to_rank(smem_addr(&s_res[w]), r), s_res[w]);
+                }
+            }
+            cluster_sync();
+        } else {
+            decide(hist, nb);
+            for (int i = tid; i < nb; i += NT) hist[i] = 0u;
+            __syncthreads();
+        }
+    };
+    // exact threshold digit for `need` keys: s_res = {digit, count above it, count in it, 0}
+    auto exact_threshold = [&](uint32_t need) {
+        return [&, need](const uint32_t *h, int nb) {
+            find_threshold<NT>(h, nb, need, s_res, s_warp);
+            if (tid == 0) s_res[3] = 0u;
+        };
+    };
+
+    // ---- candidate filter: mask byte per vector (bit t: key >= tkey), NaN check, ordered list
     uint16_t *list = reinterpret_cast<uint16_t *>(smem + a.smem_list_off);
+    uint8_t *masks = smem + a.smem_mask_off;
+    const int nvt = (len + V - 1) / V;  // 16-byte vectors in the slice (last one may be partial)
+    const uint4 *vbuf = reinterpret_cast<const uint4 *>(buf);
     int L = 0;
-    if (list_mode) {
-        // ---- filter: one mask byte per 16-byte vector, bit t set when key digit >= d
-        uint8_t *masks = smem + a.smem_mask_off;
+    bool list_ok = false;
+    auto build_list = [&](uint32_t tkey) {
+        bool has_nan = false;
         for (int base = warp * 32; base < nvt; base += NT) {
             const int v = base + lane;
             if (v < nvt) {
@@ -429,30 +426,120 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
                 T::unpack(vbuf[v], el);
                 uint32_t m = 0;
 #pragma unroll
-                for (int t = 0; t < V; ++t)
-                    m |= static_cast<uint32_t>((v * V + t < len) && ((T::key(el[t]) >> shift) >= prefix)) << t;
+                for (int t = 0; t < V; ++t) {
+                    const bool in = v * V + t < len;
+                    has_nan |= in && T::is_nan(el[t]);
+                    m |= static_cast<uint32_t>(in && T::key(el[t]) >= tkey) << t;
+                }
                 masks[v] = static_cast<uint8_t>(m);
             }
         }
-        __syncthreads();
-        // ---- ordered list: each thread owns a contiguous run of vectors
+        if (__syncthreads_or(has_nan) && tid == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
         const int q = (nvt + NT - 1) / NT;
         const int v0 = min(nvt, tid * q), v1 = min(nvt, v0 + q);
         uint32_t c = 0;
         for (int v = v0; v < v1; ++v) c += __popc(static_cast<uint32_t>(masks[v]));
         uint32_t tot;
         uint32_t pos = block_exclusive_scan<NT>(c, s_warp, tot);
-        for (int v = v0; v < v1; ++v) {
-            uint32_t m = masks[v];
-            while (m) {
-                const int b = __ffs(m) - 1;
-                list[pos++] = static_cast<uint16_t>(v * V + b);
-                m &= m - 1u;
+        list_ok = tot <= static_cast<uint32_t>(a.list_cap);
+        if (list_ok) {
+            for (int v = v0; v < v1; ++v) {
+                uint32_t m = masks[v];
+                while (m) {
+                    const int b = __ffs(m) - 1;
+                    list[pos++] = static_cast<uint16_t>(v * V + b);
+                    m &= m - 1u;
+                }
             }
         }
-        L = static_cast<int>(tot);
+        L = list_ok ? static_cast<int>(tot) : 0;
         __syncthreads();
+    };
+    // histogram of the first digit over keys >= tkey (the list, or the whole slice when the list overflowed)
+    auto candidate_hist = [&](uint32_t tkey) {
+        if (list_ok) {
+            for (int i = tid; i < L; i += NT) atomicAdd(&hist[T::key(buf[list[i]]) >> sh0], 1u);
+        } else {
+            for (int base = warp * 32; base < nvt; base += NT) {
+                const int v = base + lane;
+                if (v < nvt) {
+                    E el[V];
+                    T::unpack(vbuf[v], el);
+#pragma unroll
+                    for (int t = 0; t < V; ++t) {
+                        const uint32_t kk = T::key(el[t]);
+                        if (v * V + t < len && kk >= tkey) atomicAdd(&hist[kk >> sh0], 1u);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    };
+
+    bool exact_done = false;
+    if (sampled) {
+        // threshold estimate from the sample: the highest digit that keeps, with a 4-sigma margin,
+        // at least k keys of the whole row at or above it
+        reduce_decide(nb0, [&](const uint32_t *h, int nb) {
+            uint32_t s = 0;
+            for (int i = tid; i < nb; i += NT) s += h[i];
+            s = __reduce_add_sync(kFull, s);
+            if (lane == 0) s_warp[warp] = s;
+            __syncthreads();
+            uint32_t total = 0;
+#pragma unroll
+            for (int w = 0; w < W; ++w) total += s_warp[w];
+            __syncthreads();
+            const float mu = static_cast<float>(k) * static_cast<float>(total) / static_cast<float>(n);
+            const float want = mu + 4.0f * sqrtf(mu) + 2.0f;
+            if (want >= static_cast<float>(total)) {
+                if (tid == 0) {
+                    s_res[0] = 0u;
+                    s_res[3] = 0u;
+                }
+                __syncthreads();
+            } else {
+                find_threshold<NT>(h, nb, static_cast<uint32_t>(want), s_res, s_warp);
+            }
+        });
+        const uint32_t tkey = s_res[0] << sh0;
+        build_list(tkey);
+        candidate_hist(tkey);
+        // exact first digit among the candidates; flag 1 when fewer than k keys reached the estimate
+        reduce_decide(nb0, [&](const uint32_t *h, int nb) {
+            uint32_t s = 0;
+            for (int i = tid; i < nb; i += NT) s += h[i];
+            s = __reduce_add_sync(kFull, s);
+            if (lane == 0) s_warp[warp] = s;
+            __syncthreads();
+            uint32_t total = 0;
+#pragma unroll
+            for (int w = 0; w < W; ++w) total += s_warp[w];
+            __syncthreads();
+            if (total < static_cast<uint32_t>(k)) {
+                if (tid == 0) s_res[3] = 1u;
+                __syncthreads();
+            } else {
+                find_threshold<NT>(h, nb, static_cast<uint32_t>(k), s_res, s_warp);
+                if (tid == 0) s_res[3] = 0u;
+                __syncthreads();
+            }
+        });
+        exact_done = s_res[3] == 0u;
+        if (!exact_done) {
+            // the estimate was too high: exact histogram of the whole slice, then the list again
+            list_ok = false;
+            candidate_hist(0u);
+        }
     }
+    if (!exact_done) {
+        reduce_decide(nb0, exact_threshold(static_cast<uint32_t>(k)));
+        build_list(s_res[0] << sh0);
+    }
+    uint32_t prefix = s_res[0];  // selection class: (key >> shift) == prefix
+    int shift = sh0;
+    uint32_t need = static_cast<uint32_t>(k) - s_res[1];
+    uint32_t cnt = s_res[2];
 
     // ---------------------------------------------------- further levels
     for (int l = 1; l < a.nlevels && cnt != need; ++l) {
@@ -460,7 +547,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
         const int nsh = shift - bl;
         const int nb = 1 << bl;
         const uint32_t mask = static_cast<uint32_t>(nb - 1);
-        if (list_mode) {
+        if (list_ok) {
             for (int i = tid; i < L; i += NT) {
                 const uint32_t kk = T::key(buf[list[i]]);
                 if ((kk >> shift) == prefix) atomicAdd(&hist[(kk >> nsh) & mask], 1u);
@@ -480,14 +567,11 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
             }
         }
         __syncthreads();
-        resolve_level(nb, need);
-        const uint32_t d = s_thr[0], above = s_thr[1];
-        cnt = s_thr[2];
-        prefix = (prefix << bl) | d;
-        need -= above;
+        reduce_decide(nb, exact_threshold(need));
+        prefix = (prefix << bl) | s_res[0];
+        need -= s_res[1];
+        cnt = s_res[2];
         shift = nsh;
-        for (int i = tid; i < nb; i += NT) hist[i] = 0u;
-        __syncthreads();
     }
     const uint32_t P = prefix;
     const int S = shift;
@@ -497,20 +581,22 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
     int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
     auto exchange_cta_totals = [&](uint32_t tg, uint32_t te) {
         // (selected before this CTA, threshold-class keys before this CTA) over the cluster, in rank order
-        if (tid == 0) {
-            s_tot[0] = tg;
-            s_tot[1] = te;
-        }
-        if (CLUSTER)
+        if constexpr (CLUSTER) {
+            // every CTA stores its two counts into slot `rank` of every CTA of the cluster
+            if (tid < static_cast<int>(csize)) {
+                const uint32_t r = static_cast<uint32_t>(tid);
+                dsmem_store(map_to_rank(smem_addr(&s_all_g[rank]), r), tg);
+                dsmem_store(map_to_rank(smem_addr(&s_all_e[rank]), r), te);
+            }
             cluster_sync();
-        else
+        } else {
             __syncthreads();
+        }
         if (tid == 0) {
             uint32_t eqb = 0, selb = 0;
             if constexpr (CLUSTER) {
                 for (uint32_t r = 0; r < rank; ++r) {
-                    const uint32_t g = dsmem_load(map_to_rank(smem_addr(&s_tot[0]), r));
-                    const uint32_t e = dsmem_load(map_to_rank(smem_addr(&s_tot[1]), r));
+                    const uint32_t g = s_all_g[r], e = s_all_e[r];
                     selb += g + take_from_ties(E_need, eqb, e);
                     eqb += e;
                 }
@@ -522,7 +608,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
         __syncthreads();
     };
 
-    if (list_mode) {
+    if (list_ok) {
         const int m = (L + NT - 1) / NT;
         const int i0 = min(L, tid * m), i1 = min(L, i0 + m);
         uint32_t g = 0, q = 0;
@@ -649,19 +735,41 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
         const int64_t g1 = min(g0 + static_cast<int64_t>(s_cta_sel[1]), a.n_gather);
         if (g0 < g1) gather_rows_of<NT>(a, row, g0, g1, glist, 0);
     }
-    if (CLUSTER) cluster_sync();  // keep this CTA's shared memory alive until the cluster is done with it
+    // no cluster barrier here: after the totals exchange no CTA touches another CTA's shared memory
+}
+
+// Raises the kernel's dynamic shared-memory limit (and allows clusters above 8) once per device;
+// later calls that need no more than what was set skip the driver call.
+template <typename E, int NT, bool C, bool G>
+cudaError_t prepare_variant(int cluster, size_t smem)
+{
+    constexpr int kMaxDevices = 64;
+    static int set_smem[kMaxDevices] = {};
+    static bool set_cluster[kMaxDevices] = {};
+    auto kern = topk_kernel<E, NT, C, G>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cacheable = dev >= 0 && dev < kMaxDevices;
+    if (!cacheable || set_smem[dev] < static_cast<int>(smem)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        if (cacheable) set_smem[dev] = static_cast<int>(smem);
+    }
+    if (C && cluster > 8 && (!cacheable || !set_cluster[dev])) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        if (cacheable) set_cluster[dev] = true;
+    }
+    return cudaSuccess;
 }
 
 template <typename E, int NT, bool C, bool G>
 cudaError_t launch_variant(int cluster, size_t smem, const TopkArgs &a, cudaStream_t stream)
 {
     auto kern = topk_kernel<E, NT, C, G>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = prepare_variant<E, NT, C, G>(cluster, smem);
     if (e != cudaSuccess) return e;
-    if (C && cluster > 8) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.rows * (C ? cluster : 1)), 1, 1);
     cfg.blockDim = dim3(NT, 1, 1);
@@ -683,15 +791,12 @@ template <typename E, int NT, bool C, bool G>
 int max_clusters_variant(int cluster, size_t smem)
 {
     auto kern = topk_kernel<E, NT, C, G>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-        return 0;
+    if (prepare_variant<E, NT, C, G>(cluster, smem) != cudaSuccess) return 0;
     if (!C) {
         int blocks = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, NT, smem) != cudaSuccess) return 0;
         return blocks * device_sm_count();
     }
-    if (cluster > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-        return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
     cfg.blockDim = dim3(NT, 1, 1);

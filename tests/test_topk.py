@@ -129,6 +129,12 @@ def make_case(dtype, rows, cols, k, kind, seed, stride=None, row_end=None, sorte
         v = np.tile(-np.arange(cols, dtype=np.float32), (rows, 1))
     elif kind == "zeros_inf":
         v = g.choice(np.array([0.0, -0.0, np.inf, -np.inf, 1.0, -1.0], np.float32), size=(rows, cols))
+    elif kind == "strided_large":
+        # large values only in every 8th 16-byte vector: a strided sample of the row overestimates
+        # the threshold, which must be caught and corrected
+        v = g.standard_normal((rows, cols)).astype(np.float32)
+        per_vec = 4 if dtype == "f32" else 8
+        v[:, (np.arange(cols) // per_vec) % 8 == 0] += 100.0
     elif kind == "levels":
         v = (g.integers(0, 64, size=(rows, cols)) * 2 - 63).astype(np.float32) / 16
     else:
@@ -173,6 +179,11 @@ EDGE = [
     ("f32", 320, 9000, 64, "two_level"),
     ("bf16", 320, 16384, 2048, "levels"),
     ("f32", 310, 40000, 4096, "zeros_inf"),
+    # sampled threshold estimate too high -> exact fallback
+    ("f32", 4, 16384, 4096, "strided_large"),
+    ("f32", 320, 16384, 4096, "strided_large"),
+    ("bf16", 320, 32768, 4096, "strided_large"),
+    ("bf16", 2, 262144, 4096, "strided_large"),
 ]
 
 
