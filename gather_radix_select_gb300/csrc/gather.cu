@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs
     }
     __syncthreads();
     const int vpr = static_cast<int>(a.d >> 3);  // 16-byte vectors per key row
+    const int vsh = (vpr & (vpr - 1)) == 0 ? __ffs(vpr) - 1 : -1;  // log2(vpr), or -1
     const uint16_t *kb = a.key + (row / a.rows_per_batch) * a.key_batch_stride;
     uint4 *ob = reinterpret_cast<uint4 *>(a.out + (row * a.n + j0) * a.d);
     const int total = np * vpr;
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs
             const int t = t0 + u * kGatherThreads;
             v[u] = make_uint4(0u, 0u, 0u, 0u);
             if (t < total) {
-                const int jj = t / vpr;
+                const int jj = vsh >= 0 ? (t >> vsh) : t / vpr;
                 const int64_t p = s_pos[jj];
                 if (p >= 0) v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + (t - jj * vpr));
             }

@@ -102,9 +102,10 @@ __device__ __forceinline__ void set_err(int32_t *flag, int32_t code)
 // a timeout in err_flag and lets the CTA run on (so cluster barriers stay matched).
 __device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, int32_t *err)
 {
-    if (mbar_try_wait(bar, parity)) return;
+    constexpr uint32_t kSuspendNs = 100000;  // each try sleeps in hardware for up to 0.1 ms
+    if (mbar_try_wait(bar, parity, kSuspendNs)) return;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait(bar, parity, kSuspendNs)) {
         if (clock64() - t0 > kWaitCycles) {
             set_err(err, kStatusTimeout);
             return;
@@ -234,6 +235,7 @@ __device__ void gather_rows_of(const TopkArgs &a, int64_t row, int64_t j0, int64
                                int64_t n_short)
 {
     const int vpr = static_cast<int>(a.d >> 3);  // 16-byte vectors per key row
+    const int vsh = (vpr & (vpr - 1)) == 0 ? __ffs(vpr) - 1 : -1;  // log2(vpr), or -1
     const int64_t bb = row / a.rows_per_batch;
     const uint16_t *kb = a.key + bb * a.key_batch_stride;
     uint4 *ob = reinterpret_cast<uint4 *>(a.gather_out + (row * a.n_gather + j0) * a.d);
@@ -246,7 +248,7 @@ __device__ void gather_rows_of(const TopkArgs &a, int64_t row, int64_t j0, int64
             const int t = t0 + u * NT;
             v[u] = make_uint4(0u, 0u, 0u, 0u);
             if (t < total) {
-                const int jj = t / vpr;
+                const int jj = vsh >= 0 ? (t >> vsh) : t / vpr;
                 const int64_t j = j0 + jj;
                 int64_t p = glist ? static_cast<int64_t>(glist[jj]) : (j < n_short ? j : 0);
                 if (p < 0) p = 0;
