@@ -20,8 +20,8 @@ import torch
 from . import _native
 from ._native import SelError, SEL_MAX_K
 
-__all__ = ["topk", "gather_rows", "topk_gather", "stride_requirement", "max_cols", "SelError", "SEL_MAX_K",
-           "library_path"]
+__all__ = ["topk", "gather_rows", "topk_gather", "stride_requirement", "max_cols", "workspace_size", "SelError",
+           "SEL_MAX_K", "library_path"]
 
 _DTYPES = {torch.float32: _native.SEL_F32, torch.bfloat16: _native.SEL_BF16}
 _IDX = {torch.int32: _native.SEL_I32, torch.int64: _native.SEL_I64}
@@ -57,6 +57,31 @@ def _ptr(t):
 def _stream(device, stream):
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return ctypes.c_void_p(s.cuda_stream)
+
+
+_WORKSPACES: dict = {}
+
+
+def workspace_size(dtype: torch.dtype, rows: int, cols: int, k: int, device=None) -> int:
+    """Scratch bytes a top-k call of this shape needs on ``device`` (0 for most shapes)."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return int(_native.load().sel_topk_workspace_size(_DTYPES[dtype], rows, cols, int(k)))
+
+
+def _workspace(nbytes: int, device, stream):
+    """A zero-filled scratch buffer of >= nbytes, cached per (device, stream).
+
+    Every completed call leaves the buffer's counters zero again, so it is
+    reused as is; calls on the same stream never overlap.
+    """
+    if nbytes == 0:
+        return None, 0
+    key = (device.index, stream.cuda_stream)
+    buf = _WORKSPACES.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _WORKSPACES[key] = buf
+    return buf, buf.numel()
 
 
 def _padded_rows(rows: int, k: int, dtype: torch.dtype, device) -> torch.Tensor:
@@ -96,7 +121,8 @@ def _row_stride(x):
 def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_index: bool = False,
          indices_type: torch.dtype = torch.int32, return_value: bool = True,
          output_idx: torch.Tensor | None = None, output_val: torch.Tensor | None = None,
-         nan_flag: torch.Tensor | None = None, err_flag: torch.Tensor | None = None, stream=None):
+         nan_flag: torch.Tensor | None = None, err_flag: torch.Tensor | None = None, stream=None,
+         workspace: torch.Tensor | None = None):
     """Row-wise top-k of a 2-D CUDA tensor (largest values; ties: smaller index).
 
     Returns ``(values, indices)``; ``values`` is None when ``return_value``
@@ -106,6 +132,8 @@ def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_ind
     int32 CUDA tensors the kernel ORs / writes into.  ``output_idx`` /
     ``output_val`` are optional caller-owned [rows, >=k] buffers (row strides
     a multiple of the output alignment); results go to their first k columns.
+    ``workspace`` (uint8 CUDA tensor, zero-filled before first use) is only
+    needed by a few wide rows; by default a cached buffer is used.
     """
     _check_x(x)
     rows, cols = x.shape
@@ -130,15 +158,27 @@ def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_ind
                 or (rows > 1 and val.stride(1) != 1) or val.device != dev:
             raise ValueError("output_val must be a [rows, >=k] tensor of x's dtype on x's device")
     with torch.cuda.device(dev):
-        st = _native.load().sel_topk(
+        lib = _native.load()
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        ws, ws_bytes = _ws_for(lib, workspace, x.dtype, rows, cols, k, dev, s)
+        st = lib.sel_topk(
             _ptr(x), _DTYPES[x.dtype], rows, cols, _row_stride(x), _ptr(end), int(k), int(bool(sorted_index)),
             _IDX[indices_type], int(bool(return_value)), _ptr(idx), idx.stride(0) if rows > 1 else max(idx.stride(0), k),
             _ptr(val), 0 if val is None else (val.stride(0) if rows > 1 else max(val.stride(0), k)),
-            _ptr(nan_flag), _ptr(err_flag), _stream(dev, stream))
+            _ptr(ws), ws_bytes, _ptr(nan_flag), _ptr(err_flag), ctypes.c_void_p(s.cuda_stream))
     _native.check(st, "sel_topk")
     if output_val is not None and val is not None:
         val = val[:, :k]
     return val, idx[:, :k] if output_idx is not None else idx
+
+
+def _ws_for(lib, workspace, dtype, rows, cols, k, dev, s):
+    need = int(lib.sel_topk_workspace_size(_DTYPES[dtype], rows, cols, int(k))) if rows > 0 else 0
+    if workspace is not None:
+        if workspace.dtype != torch.uint8 or not workspace.is_cuda or workspace.numel() < need:
+            raise ValueError("workspace must be a uint8 CUDA tensor of at least %d bytes" % need)
+        return workspace, workspace.numel()
+    return _workspace(need, dev, s)
 
 
 def _key_strides(key):
@@ -181,7 +221,8 @@ def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, en
                 sorted_index: bool = False, indices_type: torch.dtype = torch.int32, return_value: bool = False,
                 return_indices: bool = True, gather_out: torch.Tensor | None = None,
                 output_idx: torch.Tensor | None = None, output_val: torch.Tensor | None = None,
-                nan_flag: torch.Tensor | None = None, err_flag: torch.Tensor | None = None, stream=None):
+                nan_flag: torch.Tensor | None = None, err_flag: torch.Tensor | None = None, stream=None,
+                workspace: torch.Tensor | None = None):
     """``topk`` then ``gather_rows`` of the first ``n_gather`` selected columns, in one launch.
 
     Returns ``(values, indices, gathered)`` with ``gathered`` bf16
@@ -208,13 +249,16 @@ def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, en
     elif gather_out.shape != (rows, n_gather, d) or not gather_out.is_contiguous():
         raise ValueError("gather_out must be a contiguous bf16 [rows, n_gather, d] tensor")
     with torch.cuda.device(dev):
-        st = _native.load().sel_topk_gather(
+        lib = _native.load()
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        ws, ws_bytes = _ws_for(lib, workspace, x.dtype, rows, cols, k, dev, s)
+        st = lib.sel_topk_gather(
             _ptr(x), _DTYPES[x.dtype], rows, cols, _row_stride(x), _ptr(end), int(k), int(bool(sorted_index)),
             _IDX[indices_type], int(bool(return_value)),
             _ptr(idx), 0 if idx is None else (idx.stride(0) if rows > 1 else max(idx.stride(0), k)),
             _ptr(val), 0 if val is None else (val.stride(0) if rows > 1 else max(val.stride(0), k)),
             _ptr(key), b, comp_len, d, kbs, krs, int(n_gather), _ptr(gather_out),
-            _ptr(nan_flag), _ptr(err_flag), _stream(dev, stream))
+            _ptr(ws), ws_bytes, _ptr(nan_flag), _ptr(err_flag), ctypes.c_void_p(s.cuda_stream))
     _native.check(st, "sel_topk_gather")
     if idx is not None and output_idx is not None:
         idx = idx[:, :k]

@@ -21,14 +21,15 @@ _vp, _i64, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 SIGNATURES = {
     "sel_stride_requirement": (_int, [ctypes.POINTER(_int), ctypes.POINTER(_int)]),
     "sel_topk": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _int, _int, _int, _int,
-                        _vp, _i64, _vp, _i64, _vp, _vp, _vp]),
+                        _vp, _i64, _vp, _i64, _vp, ctypes.c_size_t, _vp, _vp, _vp]),
+    "sel_topk_workspace_size": (ctypes.c_size_t, [_int, _i64, _i64, _int]),
     "sel_max_cols": (_i64, [_int]),
     "sel_gather_rows": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _int, _i64, _i64, _i64,
                                _vp, _vp, _vp]),
     "sel_topk_gather": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _int, _int, _int, _int,
                                _vp, _i64, _vp, _i64,
                                _vp, _i64, _i64, _i64, _i64, _i64, _i64, _vp,
-                               _vp, _vp, _vp]),
+                               _vp, ctypes.c_size_t, _vp, _vp, _vp]),
     "sel_strerror": (ctypes.c_char_p, [_int]),
 }
 

@@ -2,6 +2,7 @@
 // dispatch.  Host code only; every step of the computation runs in the
 // kernels of topk.cu and gather.cu.
 #include <cstdint>
+#include <algorithm>
 #include <cstdlib>
 #include <map>
 #include <mutex>
@@ -14,8 +15,9 @@ namespace {
 
 constexpr int kInAlign = 16;   // bulk copies stage input rows: 16-byte rows
 constexpr int kOutAlign = 16;  // output rows start on 16 bytes
-constexpr int64_t kSliceTargetBytes = 64 * 1024;
-constexpr int64_t kSliceMinBytes = 8 * 1024;
+constexpr int64_t kSliceTargetBytes = 32 * 1024;  // split_kernel: bytes of a row per CTA
+constexpr int64_t kSliceMinBytes = 16 * 1024;     // ... at least, when splitting further for parallelism
+constexpr int64_t kSplitMinRowBytes = 64 * 1024;  // rows narrower than this never split
 
 int elem_bytes(int dtype) { return dtype == SEL_F32 ? 4 : 2; }
 int idx_bytes(int idx_dtype) { return idx_dtype == SEL_I64 ? 8 : 4; }
@@ -24,26 +26,23 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 struct Plan {
-    int cluster = 1;
+    int mode = sel::kModeRow;
     int threads = 256;
+    int64_t grid = 0;
     size_t smem = 0;
-    sel::TopkArgs layout{};  // slice, digit plan and shared-memory offsets
+    size_t ws_bytes = 0;
+    sel::TopkArgs layout{};  // digit plan, slice, parts, shared-memory offsets, workspace layout
 };
 
 void digit_plan(int dtype, int64_t cols, sel::TopkArgs &a)
 {
-    const bool small = cols <= 4096;  // small rows: 256-bin histograms are cheaper to clear and scan
+    const bool small = cols <= 4096;  // short bf16 rows: 256-bin histograms are cheaper to clear and scan
     if (dtype == SEL_F32) {
-        if (small) {
-            a.nlevels = 4;
-            a.bits[0] = a.bits[1] = a.bits[2] = a.bits[3] = 8;
-        } else {
-            a.nlevels = 3;
-            a.bits[0] = 11;
-            a.bits[1] = 11;
-            a.bits[2] = 10;
-            a.bits[3] = 0;
-        }
+        a.nlevels = 3;
+        a.bits[0] = 11;
+        a.bits[1] = 11;
+        a.bits[2] = 10;
+        a.bits[3] = 0;
     } else {
         a.nlevels = 2;
         a.bits[0] = small ? 8 : 11;
@@ -55,7 +54,7 @@ void digit_plan(int dtype, int64_t cols, sel::TopkArgs &a)
     a.hist_bins = 1 << mb;
 }
 
-// Threads per selection CTA for a slice of `slice` elements.
+// Threads per row_kernel CTA for a row of `slice` elements.
 int threads_for(int64_t slice)
 {
     if (slice <= 4096) return 128;
@@ -63,8 +62,9 @@ int threads_for(int64_t slice)
     return 512;
 }
 
-// Shared-memory layout of one CTA for a given slice; returns total bytes.
-size_t layout_for(int dtype, int cluster, int64_t slice, int k, bool gather, int64_t n_gather, sel::TopkArgs &a)
+// Shared-memory layout of one CTA staging `slice` elements with a candidate list of `cap`
+// entries; returns the total bytes.
+size_t layout_staged(int dtype, int64_t slice, int64_t cap, bool gather, int64_t n_gather, sel::TopkArgs &a)
 {
     const int64_t e = elem_bytes(dtype);
     a.slice = slice;
@@ -74,11 +74,6 @@ size_t layout_for(int dtype, int cluster, int64_t slice, int k, bool gather, int
     off += static_cast<size_t>(a.hist_bins) * 4;
     a.smem_mask_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(round_up(ceil_div(slice, 16 / e), 16));
-    // candidate list (16-bit offsets): this CTA's share of k with room for the threshold bin; a CTA
-    // whose candidates do not fit works on its whole staged slice instead
-    const int64_t share = cluster > 1 ? 2 * ceil_div(k, cluster) : static_cast<int64_t>(k);
-    const int64_t want = share + 2048;
-    const int64_t cap = slice < want ? slice : want;
     a.list_cap = static_cast<int32_t>(cap);
     a.smem_list_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(round_up(cap * 2, 16));
@@ -87,19 +82,45 @@ size_t layout_for(int dtype, int cluster, int64_t slice, int k, bool gather, int
     return off;
 }
 
-int cached_max_clusters(int dtype, int threads, bool gather, int cluster, size_t smem)
+// Layout of a stream_kernel CTA (histogram and gather list only).
+size_t layout_stream(bool gather, int64_t n_gather, sel::TopkArgs &a)
+{
+    a.slice = 0;
+    a.smem_buf_bytes = 0;
+    a.smem_hist_off = 0;
+    size_t off = static_cast<size_t>(a.hist_bins) * 4;
+    a.smem_mask_off = a.smem_list_off = static_cast<uint32_t>(off);
+    a.list_cap = 0;
+    a.smem_glist_off = static_cast<uint32_t>(off);
+    if (gather) off += static_cast<size_t>(round_up(n_gather * 4, 16));
+    return off;
+}
+
+// Workspace layout of split_kernel (see topk_impl.cuh); returns the total bytes.
+size_t layout_workspace(int dtype, int64_t rows, int parts, int64_t cap, sel::TopkArgs &a)
+{
+    a.parts = parts;
+    a.ws_counter_bytes = round_up(rows * 4, 256);
+    a.ws_head_bytes = round_up(2 * static_cast<int64_t>(parts) * 4, 16);
+    a.ws_bits_bytes = round_up(cap * elem_bytes(dtype), 16);
+    a.ws_part_bytes = a.ws_bits_bytes + round_up(cap * 4, 16);
+    a.ws_row_bytes = a.ws_head_bytes + static_cast<int64_t>(parts) * a.ws_part_bytes;
+    return static_cast<size_t>(a.ws_counter_bytes + rows * a.ws_row_bytes);
+}
+
+int cached_blocks_per_sm(int dtype, int mode, int threads, bool gather, size_t smem)
 {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int, int, size_t>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, dtype, threads, gather ? 1 : 0, cluster, smem);
+    const auto key = std::make_tuple(dev, dtype, mode, threads, gather ? 1 : 0, smem);
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    const int n = sel::topk_max_active_clusters(dtype, threads, gather, cluster, smem);
+    const int n = sel::topk_blocks_per_sm(dtype, mode, threads, gather, smem);
     std::lock_guard<std::mutex> g(mu);
     cache[key] = n;
     return n;
@@ -116,62 +137,86 @@ int hist_agg()
     return v;
 }
 
-// Tries a cluster size: slice, threads, layout, and whether it can be scheduled.
-bool try_cluster(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, int64_t cs,
-                 size_t limit, Plan &p, bool &too_big)
-{
-    const int64_t e = elem_bytes(dtype);
-    const int64_t slice = round_up(ceil_div(cols > 0 ? cols : 1, cs), 64);
-    too_big = slice > sel::kMaxSlice || slice * e > static_cast<int64_t>(sel::kMaxChunks) * sel::kChunkBytes;
-    if (too_big) return false;
-    sel::TopkArgs a = p.layout;
-    const size_t smem = layout_for(dtype, static_cast<int>(cs), slice, k, gather, n_gather, a);
-    if (smem > limit) {
-        too_big = true;
-        return false;
-    }
-    if (rows * cs > 0x7fffffffLL) return false;
-    const int threads = threads_for(slice);
-    if (cached_max_clusters(dtype, threads, gather, static_cast<int>(cs), smem) <= 0) return false;
-    p.cluster = static_cast<int>(cs);
-    p.threads = threads;
-    p.smem = smem;
-    p.layout = a;
-    return true;
-}
-
-// Chooses CTAs per row (cluster), the slice each CTA stages and the digit plan.
+// Chooses the kernel (row / split / stream), its CTA shape, shared memory and workspace.
 int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, Plan &p)
 {
-    digit_plan(dtype, cols, p.layout);
-    p.layout.agg = hist_agg();
-    p.layout.sample_step = 8;
-    p.layout.sample_min_cols = 8192;
+    sel::TopkArgs &a = p.layout;
+    digit_plan(dtype, cols, a);
+    a.agg = hist_agg();
+    a.sample_step = 8;
+    a.sample_min_cols = 8192;
     const size_t limit = sel::topk_smem_limit();
     const int sms = sel::device_sm_count();
     if (limit == 0 || sms == 0) return SEL_ECUDA;
     const int64_t e = elem_bytes(dtype);
-    const int64_t row_bytes = (cols > 0 ? cols : 1) * e;
-    int64_t want = ceil_div(row_bytes, kSliceTargetBytes);
+    const int64_t c1 = cols > 0 ? cols : 1;
+    const int64_t row_bytes = c1 * e;
+    const int64_t max_staged = std::min<int64_t>(sel::kMaxSlice, sel::kMaxChunks * sel::kChunkBytes / e);
+
+    // one CTA per row, the row staged whole
+    bool row_ok = false;
+    Plan row_plan = p;
+    {
+        const int64_t slice = round_up(c1, 64);
+        if (slice <= max_staged) {
+            const int64_t cap = std::min<int64_t>(slice, static_cast<int64_t>(k) + 2048);
+            const size_t smem = layout_staged(dtype, slice, cap, gather, n_gather, row_plan.layout);
+            const int threads = threads_for(slice);
+            if (smem <= limit && cached_blocks_per_sm(dtype, sel::kModeRow, threads, gather, smem) > 0) {
+                row_plan.mode = sel::kModeRow;
+                row_plan.threads = threads;
+                row_plan.smem = smem;
+                row_plan.grid = rows;
+                row_plan.ws_bytes = 0;
+                row_ok = true;
+            }
+        }
+    }
+    // few wide rows (or rows that do not fit one CTA): split them over several CTAs
+    const bool want_split = !row_ok || (rows < 2 * sms && row_bytes >= kSplitMinRowBytes);
+    if (!want_split) {
+        p = row_plan;
+        return SEL_OK;
+    }
+    int64_t parts = ceil_div(row_bytes, kSliceTargetBytes);
     if (rows < 2 * sms) {
-        // few rows: split them further so that every SM gets work
         const int64_t par = ceil_div(2 * sms, rows > 0 ? rows : 1);
-        const int64_t cap = ceil_div(row_bytes, kSliceMinBytes);
-        const int64_t extra = par < cap ? par : cap;
-        if (extra > want) want = extra;
+        parts = std::max(parts, std::min(par, ceil_div(row_bytes, kSliceMinBytes)));
     }
-    if (want > sel::kMaxCluster) want = sel::kMaxCluster;
-    if (want < 1) want = 1;
-    bool too_big = false;
-    // smallest cluster >= want whose slice fits in shared memory and can be scheduled
-    for (int64_t cs = want; cs <= sel::kMaxCluster; ++cs)
-        if (try_cluster(dtype, rows, cols, k, gather, n_gather, cs, limit, p, too_big)) return SEL_OK;
-    // a cluster that large could not be scheduled: try smaller ones that still fit
-    for (int64_t cs = want - 1; cs >= 1; --cs) {
-        if (try_cluster(dtype, rows, cols, k, gather, n_gather, cs, limit, p, too_big)) return SEL_OK;
-        if (too_big) break;
+    parts = std::max<int64_t>(2, std::min<int64_t>(parts, sel::kMaxParts));
+    const int64_t slice = round_up(ceil_div(c1, parts), 64);
+    parts = ceil_div(c1, slice);
+    if (slice <= max_staged && parts >= 2) {
+        Plan sp = p;
+        const int64_t cap = std::min<int64_t>(slice, 2 * ceil_div(k, parts) + 512);
+        const size_t smem = layout_staged(dtype, slice, cap, gather, n_gather, sp.layout);
+        if (smem <= limit && cached_blocks_per_sm(dtype, sel::kModeSplit, 256, gather, smem) > 0 &&
+            rows * parts <= 0x7fffffffLL) {
+            sp.mode = sel::kModeSplit;
+            sp.threads = 256;
+            sp.smem = smem;
+            sp.grid = rows * parts;
+            sp.ws_bytes = layout_workspace(dtype, rows, static_cast<int>(parts), cap, sp.layout);
+            p = sp;
+            return SEL_OK;
+        }
     }
-    return SEL_EUNSUPPORTED;
+    if (row_ok) {
+        p = row_plan;
+        return SEL_OK;
+    }
+    // rows too wide for the split plan: one CTA per row, passes over global memory
+    if (cols > 0x7fffffffLL) return SEL_EUNSUPPORTED;
+    Plan st = p;
+    const size_t smem = layout_stream(gather, n_gather, st.layout);
+    if (smem > limit || cached_blocks_per_sm(dtype, sel::kModeStream, 512, gather, smem) <= 0) return SEL_EUNSUPPORTED;
+    st.mode = sel::kModeStream;
+    st.threads = 512;
+    st.smem = smem;
+    st.grid = rows;
+    st.ws_bytes = 0;
+    p = st;
+    return SEL_OK;
 }
 
 // make_plan behind a cache: the plan depends only on the device and the call's shape.
@@ -232,6 +277,47 @@ int check_gather_key(const void *key, int64_t b, int64_t comp_len, int64_t d, in
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? SEL_OK : SEL_ECUDA; }
 
+int run_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride, const int32_t *row_end, int k,
+             int idx_dtype, int want_values, void *out_idx, int64_t out_idx_stride, void *out_val,
+             int64_t out_val_stride, const void *key, int64_t b, int64_t comp_len, int64_t d,
+             int64_t key_batch_stride, int64_t key_row_stride, int64_t n_gather, void *gather_out, void *workspace,
+             size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag, void *stream)
+{
+    Plan p;
+    int st = cached_plan(dtype, rows, cols, k, n_gather > 0, n_gather, p);
+    if (st != SEL_OK) return st;
+    if (p.ws_bytes > 0) {
+        if (!workspace || workspace_bytes < p.ws_bytes) return SEL_EINVAL;
+        if (!aligned(workspace, 256)) return SEL_EALIGN;
+    }
+    sel::TopkArgs a = p.layout;
+    a.x = x;
+    a.rows = rows;
+    a.cols = cols;
+    a.stride = stride;
+    a.row_end = row_end;
+    a.k = k;
+    a.idx_i64 = idx_dtype == SEL_I64;
+    a.want_values = want_values ? 1 : 0;
+    a.out_idx = out_idx;
+    a.out_idx_stride = out_idx_stride;
+    a.out_val = want_values ? out_val : nullptr;
+    a.out_val_stride = out_val_stride;
+    a.nan_flag = nan_flag;
+    a.err_flag = err_flag;
+    a.ws = static_cast<unsigned char *>(workspace);
+    a.key = static_cast<const uint16_t *>(key);
+    a.comp_len = comp_len;
+    a.d = d;
+    a.key_batch_stride = key_batch_stride;
+    a.key_row_stride = key_row_stride;
+    a.rows_per_batch = n_gather > 0 ? rows / b : 1;
+    a.n_gather = n_gather;
+    a.gather_out = static_cast<uint16_t *>(gather_out);
+    return status_of(sel::launch_topk(dtype == SEL_F32 ? 0 : 1, p.mode, p.threads, n_gather > 0, p.smem, a, p.grid,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -259,60 +345,29 @@ const char *sel_strerror(int status)
 int64_t sel_max_cols(int dtype)
 {
     if (dtype != SEL_F32 && dtype != SEL_BF16) return 0;
-    const size_t limit = sel::topk_smem_limit();
-    if (limit == 0) return 0;
-    // widest row: the largest schedulable cluster with the largest slice that fits in shared memory
-    for (int64_t cs = sel::kMaxCluster; cs >= 1; --cs) {
-        int64_t lo = 64, hi = sel::kMaxSlice;
-        Plan best;
-        bool found = false;
-        while (lo <= hi) {  // largest slice (multiple of 64) that fits and schedules, at k = SEL_MAX_K
-            const int64_t mid = (lo + hi) / 2 / 64 * 64;
-            Plan p;
-            digit_plan(dtype, mid * cs, p.layout);
-            bool too_big = false;
-            if (try_cluster(dtype, 1, mid * cs, SEL_MAX_K, false, 0, cs, limit, p, too_big) && p.cluster == cs) {
-                best = p;
-                found = true;
-                lo = mid + 64;
-            } else {
-                hi = mid - 64;
-            }
-        }
-        if (found) return best.layout.slice * cs;
-    }
-    return 0;
+    return 0x7fffffffLL;  // wider rows than one CTA can stage run split or streamed; indices are int32-safe
+}
+
+size_t sel_topk_workspace_size(int dtype, int64_t rows, int64_t cols, int k)
+{
+    if ((dtype != SEL_F32 && dtype != SEL_BF16) || rows <= 0 || cols < 0 || k < 1 || k > SEL_MAX_K) return 0;
+    Plan p;
+    if (cached_plan(dtype, rows, cols, k, false, 0, p) != SEL_OK) return 0;
+    return p.ws_bytes;
 }
 
 int sel_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride, const int32_t *row_end, int k,
              int sorted_index, int idx_dtype, int want_values, void *out_idx, int64_t out_idx_stride, void *out_val,
-             int64_t out_val_stride, int32_t *nan_flag, int32_t *err_flag, void *stream)
+             int64_t out_val_stride, void *workspace, size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag,
+             void *stream)
 {
     (void)sorted_index;  // the ordered compaction always yields ascending column order
-    int st = check_topk_args(x, dtype, rows, cols, stride, k, idx_dtype, want_values, out_idx, out_idx_stride, out_val,
-                             out_val_stride, true);
+    const int st = check_topk_args(x, dtype, rows, cols, stride, k, idx_dtype, want_values, out_idx, out_idx_stride,
+                                   out_val, out_val_stride, true);
     if (st != SEL_OK || rows == 0) return st;
-    Plan p;
-    st = cached_plan(dtype, rows, cols, k, false, 0, p);
-    if (st != SEL_OK) return st;
-    sel::TopkArgs a = p.layout;
-    a.x = x;
-    a.rows = rows;
-    a.cols = cols;
-    a.stride = stride;
-    a.row_end = row_end;
-    a.k = k;
-    a.idx_i64 = idx_dtype == SEL_I64;
-    a.want_values = want_values ? 1 : 0;
-    a.out_idx = out_idx;
-    a.out_idx_stride = out_idx_stride;
-    a.out_val = want_values ? out_val : nullptr;
-    a.out_val_stride = out_val_stride;
-    a.nan_flag = nan_flag;
-    a.err_flag = err_flag;
-    a.rows_per_batch = 1;
-    return status_of(sel::launch_topk(dtype == SEL_F32 ? 0 : 1, p.threads, false, p.cluster, p.smem, a,
-                                      static_cast<cudaStream_t>(stream)));
+    return run_topk(x, dtype, rows, cols, stride, row_end, k, idx_dtype, want_values, out_idx, out_idx_stride, out_val,
+                    out_val_stride, nullptr, 1, 0, 0, 0, 0, 0, nullptr, workspace, workspace_bytes, nan_flag, err_flag,
+                    stream);
 }
 
 int sel_gather_rows(const void *key, int64_t b, int64_t comp_len, int64_t d, int64_t key_batch_stride,
@@ -346,7 +401,7 @@ int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_
                     int k, int sorted_index, int idx_dtype, int want_values, void *out_idx, int64_t out_idx_stride,
                     void *out_val, int64_t out_val_stride, const void *key, int64_t b, int64_t comp_len, int64_t d,
                     int64_t key_batch_stride, int64_t key_row_stride, int64_t n_gather, void *gather_out,
-                    int32_t *nan_flag, int32_t *err_flag, void *stream)
+                    void *workspace, size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag, void *stream)
 {
     (void)sorted_index;
     int st = check_topk_args(x, dtype, rows, cols, stride, k, idx_dtype, want_values, out_idx, out_idx_stride, out_val,
@@ -358,34 +413,9 @@ int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_
         st = check_gather_key(key, b, comp_len, d, key_batch_stride, key_row_stride, rows, gather_out);
         if (st != SEL_OK) return st;
     }
-    Plan p;
-    st = cached_plan(dtype, rows, cols, k, n_gather > 0, n_gather, p);
-    if (st != SEL_OK) return st;
-    sel::TopkArgs a = p.layout;
-    a.x = x;
-    a.rows = rows;
-    a.cols = cols;
-    a.stride = stride;
-    a.row_end = row_end;
-    a.k = k;
-    a.idx_i64 = idx_dtype == SEL_I64;
-    a.want_values = want_values ? 1 : 0;
-    a.out_idx = out_idx;
-    a.out_idx_stride = out_idx_stride;
-    a.out_val = want_values ? out_val : nullptr;
-    a.out_val_stride = out_val_stride;
-    a.nan_flag = nan_flag;
-    a.err_flag = err_flag;
-    a.key = static_cast<const uint16_t *>(key);
-    a.comp_len = comp_len;
-    a.d = d;
-    a.key_batch_stride = key_batch_stride;
-    a.key_row_stride = key_row_stride;
-    a.rows_per_batch = n_gather > 0 ? rows / b : 1;
-    a.n_gather = n_gather;
-    a.gather_out = static_cast<uint16_t *>(gather_out);
-    return status_of(sel::launch_topk(dtype == SEL_F32 ? 0 : 1, p.threads, n_gather > 0, p.cluster, p.smem, a,
-                                      static_cast<cudaStream_t>(stream)));
+    return run_topk(x, dtype, rows, cols, stride, row_end, k, idx_dtype, want_values, out_idx, out_idx_stride, out_val,
+                    out_val_stride, key, n_gather > 0 ? b : 1, comp_len, d, key_batch_stride, key_row_stride, n_gather,
+                    gather_out, workspace, workspace_bytes, nan_flag, err_flag, stream);
 }
 
 }  // extern "C"

@@ -13,7 +13,10 @@ constexpr int kMaxLevels = 4;       // radix passes (digits) at most
 constexpr int kMaxSlice = 65536;    // elements of a row staged by one CTA (list offsets are 16-bit)
 constexpr int kMaxChunks = 16;      // bulk-copy chunks per CTA slice
 constexpr uint32_t kChunkBytes = 16384;
-constexpr int kMaxCluster = 16;     // CTAs splitting one row (non-portable above 8)
+constexpr int kMaxParts = 64;       // CTAs splitting one row (split_kernel)
+constexpr int kModeRow = 0;         // row_kernel: one CTA per row, row staged in shared memory
+constexpr int kModeSplit = 1;       // split_kernel: `parts` CTAs per row + last-arriver merge
+constexpr int kModeStream = 2;      // stream_kernel: one CTA per row, passes read global memory
 constexpr int kGatherThreads = 256;
 
 // Everything one selection launch needs; passed by value (kernel parameter space).
@@ -31,6 +34,7 @@ struct TopkArgs {
     int32_t *nan_flag;        // nullable
     int32_t *err_flag;        // nullable
     int64_t slice;            // elements of a row per CTA (multiple of 64)
+    int32_t parts;            // CTAs per row (split_kernel)
     int32_t nlevels;          // digits from the most significant end
     int32_t bits[kMaxLevels];
     int32_t hist_bins;        // 1 << max(bits)
@@ -44,6 +48,9 @@ struct TopkArgs {
     int32_t sample_step;      // > 1: the first digit's threshold is estimated from every
                               //      sample_step-th 16-byte vector of the row
     int32_t sample_min_cols;  // rows shorter than this use the exact first histogram
+    // split_kernel workspace (see topk_impl.cuh for the layout)
+    unsigned char *ws;
+    int64_t ws_counter_bytes, ws_row_bytes, ws_head_bytes, ws_part_bytes, ws_bits_bytes;
     // fused gather (ignored unless the gather variant is launched)
     const uint16_t *key;
     int64_t comp_len, d, key_batch_stride, key_row_stride, rows_per_batch;
@@ -63,22 +70,21 @@ struct GatherArgs {
     int32_t ctas_per_row;
 };
 
-// dtype: 0 fp32, 1 bf16.  threads: 128 | 256 | 512.  cluster: CTAs per row (1 = no cluster).
-// gather: fused variant.
-cudaError_t launch_topk(int dtype, int threads, bool gather, int cluster, size_t smem_bytes, const TopkArgs &a,
-                        cudaStream_t stream);
+// dtype: 0 fp32, 1 bf16.  mode: kModeRow | kModeSplit | kModeStream.  grid: CTAs to launch.
+cudaError_t launch_topk(int dtype, int mode, int threads, bool gather, size_t smem_bytes, const TopkArgs &a,
+                        int64_t grid, cudaStream_t stream);
+
+// CTAs of that kernel configuration that fit on one SM (0 = cannot launch).
+int topk_blocks_per_sm(int dtype, int mode, int threads, bool gather, size_t smem_bytes);
 
 // Per element type (topk_f32.cu / topk_bf16.cu).
-cudaError_t launch_topk_f32(int threads, bool gather, int cluster, size_t smem, const TopkArgs &a, cudaStream_t s);
-cudaError_t launch_topk_bf16(int threads, bool gather, int cluster, size_t smem, const TopkArgs &a, cudaStream_t s);
-int topk_occupancy_f32(int threads, bool gather, int cluster, size_t smem);
-int topk_occupancy_bf16(int threads, bool gather, int cluster, size_t smem);
+cudaError_t launch_topk_f32(int mode, int threads, bool gather, size_t smem, const TopkArgs &a, cudaStream_t s,
+                            int64_t grid, bool query, int *blocks_per_sm);
+cudaError_t launch_topk_bf16(int mode, int threads, bool gather, size_t smem, const TopkArgs &a, cudaStream_t s,
+                             int64_t grid, bool query, int *blocks_per_sm);
 
 // Max dynamic shared memory a selection CTA may use on the current device.
 size_t topk_smem_limit();
-
-// Number of clusters of `cluster` CTAs with `smem_bytes` each that can be co-resident (0 = cannot launch).
-int topk_max_active_clusters(int dtype, int threads, bool gather, int cluster, size_t smem_bytes);
 
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t stream);
 

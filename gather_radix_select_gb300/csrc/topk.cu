@@ -6,17 +6,23 @@
 
 namespace sel {
 
-cudaError_t launch_topk(int dtype, int threads, bool gather, int cluster, size_t smem, const TopkArgs &a,
+cudaError_t launch_topk(int dtype, int mode, int threads, bool gather, size_t smem, const TopkArgs &a, int64_t grid,
                         cudaStream_t stream)
 {
-    return dtype == 0 ? launch_topk_f32(threads, gather, cluster, smem, a, stream)
-                      : launch_topk_bf16(threads, gather, cluster, smem, a, stream);
+    return dtype == 0 ? launch_topk_f32(mode, threads, gather, smem, a, stream, grid, false, nullptr)
+                      : launch_topk_bf16(mode, threads, gather, smem, a, stream, grid, false, nullptr);
 }
 
-int topk_max_active_clusters(int dtype, int threads, bool gather, int cluster, size_t smem)
+int topk_blocks_per_sm(int dtype, int mode, int threads, bool gather, size_t smem)
 {
-    return dtype == 0 ? topk_occupancy_f32(threads, gather, cluster, smem)
-                      : topk_occupancy_bf16(threads, gather, cluster, smem);
+    int blocks = 0;
+    const cudaError_t e = dtype == 0 ? launch_topk_f32(mode, threads, gather, smem, TopkArgs{}, nullptr, 0, true, &blocks)
+                                     : launch_topk_bf16(mode, threads, gather, smem, TopkArgs{}, nullptr, 0, true, &blocks);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return blocks;
 }
 
 size_t topk_smem_limit()

@@ -4,14 +4,10 @@
 
 namespace sel {
 
-cudaError_t launch_topk_bf16(int threads, bool gather, int cluster, size_t smem, const TopkArgs &a, cudaStream_t s)
+cudaError_t launch_topk_bf16(int mode, int threads, bool gather, size_t smem, const TopkArgs &a, cudaStream_t s,
+                            int64_t grid, bool query, int *blocks_per_sm)
 {
-    return launch_e<uint16_t>(threads, gather, cluster, smem, a, s);
-}
-
-int topk_occupancy_bf16(int threads, bool gather, int cluster, size_t smem)
-{
-    return occupancy_e<uint16_t>(threads, gather, cluster, smem);
+    return launch_e<uint16_t>(mode, threads, gather, smem, a, s, grid, query, blocks_per_sm);
 }
 
 }  // namespace sel

@@ -1,5 +1,5 @@
-// topk_impl.cuh -- batched row-wise top-k by radix select, one row per CTA or per
-// thread-block cluster, with an optional fused gather of the selected key rows.
+// topk_impl.cuh -- batched row-wise top-k by radix select, with an optional
+// fused gather of the selected key rows.
 //
 // What is computed ("Speed up PyTorch TopK with DeepSelect": "Basic TopK
 // usage", "Working with variable-length rows", "NaN handling"): for each row
@@ -7,29 +7,36 @@
 // (ties: smaller column first), or, when n <= k, every valid column followed
 // by fills (index -1, value -inf).  Rows with n > k are checked for NaN.
 //
-// How (GB300 design):
-//   * A row is split into `slice`-element pieces, one per CTA of a cluster of
-//     `cluster` CTAs (1 <= cluster <= 16).  Each CTA stages its piece into
-//     shared memory with bulk async copies (cp.async.bulk, 16 KB chunks, one
-//     mbarrier each) and builds the first digit histogram while later chunks
-//     are still in flight: the row is read from HBM exactly once.
+// Three kernels, chosen per launch by the host plan:
+//   row_kernel    one CTA per row; the row is staged whole in shared memory.
+//   split_kernel  a wide row is cut into `parts` slices, one CTA each.  Every
+//                 CTA filters its slice down to an index-ordered candidate
+//                 list in a caller-provided workspace; the CTA that finishes
+//                 last (an atomic arrival counter -- nobody waits) selects
+//                 the k from the merged candidates.
+//   stream_kernel one CTA per row, the row read from global memory on every
+//                 radix pass (rows too wide for the split plan, and the exact
+//                 fallback of split_kernel).
+//
+// Building blocks (GB300 design):
+//   * Slices are staged into shared memory with bulk async copies
+//     (cp.async.bulk, 16 KB chunks, one mbarrier each); waiting threads sleep
+//     in hardware (try_wait with a suspend hint), bounded by a ~2 s budget.
 //   * Order-preserving key: fp32/bf16 bits -> unsigned key, larger float =>
 //     larger key, -0 folded onto +0.
-//   * Radix select over digits taken from the most significant end (e.g.
-//     11/11/10 bits for fp32).  Histograms live in shared memory; each warp
-//     aggregates equal digits with __match_any_sync so one atomicAdd per
-//     distinct digit per warp reaches shared memory.  In a cluster the CTAs'
-//     histograms are summed into CTA 0's shared memory through distributed
-//     shared memory (red.shared::cluster) behind a hardware cluster barrier
-//     -- no global scratch, no spin waits.
-//   * A level stops early when the threshold bin holds exactly the number of
-//     keys still needed.
-//   * Compaction is ordered: every warp owns a contiguous segment of the
-//     slice, segment bases come from exclusive scans (over warps, then over
-//     the CTAs of the cluster, in column order), and inside a warp positions
-//     come from warp scans.  Keys equal to the threshold are therefore taken
-//     in column order (smaller index wins), deterministically, and every
-//     row's output is in ascending column order -- sorted_index costs nothing.
+//   * Radix select over digits from the most significant end (11/11/10 bits
+//     fp32, 11/5 bf16, 8/8 for short bf16 rows); histograms in shared memory.
+//   * First digit: exact histogram while chunks land, or, for long rows, the
+//     histogram of every 8th 16-byte vector, from which a threshold digit is
+//     estimated with a margin; one pass then filters the keys at or above it
+//     into an index-ordered candidate list (mask byte per vector + block
+//     scan).  Too few candidates is detected and repaired exactly.
+//   * A level stops early when the threshold bin holds exactly the keys
+//     still needed.
+//   * Compaction is ordered: keys above the threshold class are all taken,
+//     keys in it are taken in column order until k are chosen (block scans
+//     give tie ranks and output positions).  Output rows therefore come in
+//     ascending column order and sorted_index costs nothing.
 #pragma once
 
 #include <cstdint>
@@ -58,6 +65,8 @@ struct Elem<uint32_t> {  // fp32 bit patterns
         u = (u == 0x80000000u) ? 0u : u;
         return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     }
+    static constexpr uint32_t kInfMagnitude = 0x7f800000u;
+    static __device__ __forceinline__ uint32_t magnitude(uint32_t u) { return u & 0x7fffffffu; }
     static __device__ __forceinline__ bool is_nan(uint32_t u) { return (u & 0x7fffffffu) > 0x7f800000u; }
     static __device__ __forceinline__ void unpack(const uint4 &q, uint32_t (&e)[4])
     {
@@ -79,6 +88,8 @@ struct Elem<uint16_t> {  // bf16 bit patterns
         u = (u == 0x8000u) ? 0u : u;
         return (u & 0x8000u) ? (~u & 0xffffu) : (u | 0x8000u);
     }
+    static constexpr uint32_t kInfMagnitude = 0x7f80u;
+    static __device__ __forceinline__ uint32_t magnitude(uint16_t h) { return h & 0x7fffu; }
     static __device__ __forceinline__ bool is_nan(uint16_t h) { return (h & 0x7fffu) > 0x7f80u; }
     static __device__ __forceinline__ void unpack(const uint4 &q, uint16_t (&e)[8])
     {
@@ -99,7 +110,7 @@ __device__ __forceinline__ void set_err(int32_t *flag, int32_t code)
 }
 
 // Bounded wait on an mbarrier phase: after ~2 s the wait gives up, records
-// a timeout in err_flag and lets the CTA run on (so cluster barriers stay matched).
+// a timeout in err_flag and lets the CTA run on (its results are then unspecified).
 __device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, int32_t *err)
 {
     constexpr uint32_t kSuspendNs = 100000;  // each try sleeps in hardware for up to 0.1 ms
@@ -271,87 +282,62 @@ struct MinBlocks {
     static constexpr int value = NT >= 512 ? 2 : (NT >= 256 ? 4 : 8);
 };
 
-template <typename E, int NT, bool CLUSTER, bool GATHER>
-__global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const TopkArgs a)
+// Short row (n <= k): columns 0..n-1 then fills; positions [j0, j1) of the output row.
+template <typename E, int NT, bool GATHER>
+__device__ void short_row(const TopkArgs &a, int64_t row, int64_t n, int j0, int j1)
 {
     using T = Elem<E>;
-    constexpr int V = T::V;
-    constexpr int W = NT / 32;
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint64_t s_bar[kMaxChunks];
-    __shared__ uint32_t s_warp[W];
-    __shared__ uint32_t s_wgt[W], s_weq[W];
-    __shared__ uint32_t s_wsel_base[W], s_weq_base[W];
-    __shared__ uint32_t s_res[4];       // broadcast result of a histogram reduction
-    __shared__ uint32_t s_all_g[kMaxCluster], s_all_e[kMaxCluster];  // per-CTA counts, written by the cluster
-    __shared__ uint32_t s_cta_sel[2];   // (selected before this CTA, selected by this CTA)
-    __shared__ uint32_t s_eq_before;    // keys of the threshold class before this CTA
+    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
+    for (int j = j0 + static_cast<int>(threadIdx.x); j < j1; j += NT) {
+        store_idx(a, row, j, j < n ? j : -1);
+        if (a.want_values) store_val<E>(a, row, j, j < n ? xrow[j] : static_cast<E>(T::kFill));
+    }
+    if (GATHER) {
+        const int64_t g1 = min(static_cast<int64_t>(j1), a.n_gather);
+        if (j0 < g1) gather_rows_of<NT>(a, row, j0, g1, nullptr, n);
+    }
+}
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t rank = CLUSTER ? cluster_rank() : 0u;
-    const uint32_t csize = CLUSTER ? cluster_size() : 1u;
-    const int64_t row = CLUSTER ? static_cast<int64_t>(cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
-    const bool agg = a.agg != 0;
-
+__device__ __forceinline__ int64_t valid_cols(const TopkArgs &a, int64_t row)
+{
     int64_t n = a.cols;
     if (a.row_end) {
         const int64_t re = a.row_end[row];
         n = re < 0 ? 0 : (re > a.cols ? a.cols : re);
     }
-    const int k = a.k;
-    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
+    return n;
+}
 
-    // ---------------------------------------------------------- short row
-    if (n <= k) {  // the same decision in every CTA of the cluster
-        const int per = (k + static_cast<int>(csize) - 1) / static_cast<int>(csize);
-        const int j0 = static_cast<int>(rank) * per;
-        const int j1 = min(k, j0 + per);
-        for (int j = j0 + tid; j < j1; j += NT) {
-            store_idx(a, row, j, j < n ? j : -1);
-            if (a.want_values) store_val<E>(a, row, j, j < n ? xrow[j] : static_cast<E>(T::kFill));
-        }
-        if (GATHER) {
-            const int64_t g1 = min(static_cast<int64_t>(j1), a.n_gather);
-            if (j0 < g1) gather_rows_of<NT>(a, row, j0, g1, nullptr, n);
-        }
-        return;
-    }
-
-    // ------------------------------------------------- stage the slice
+// Stages xrow[lo, lo+len) into smem (bulk copies for the 16-byte part, plain loads for the rest)
+// and adds every `step`-th 16-byte vector's top digits into hist while the chunks land.
+// Returns after a __syncthreads; hist must be zero on entry.
+template <typename E, int NT>
+__device__ void stage_and_histogram(const TopkArgs &a, const E *xrow, int64_t lo, int len, int step,
+                                    unsigned char *smem, uint32_t *hist, uint64_t *bars)
+{
+    using T = Elem<E>;
+    constexpr int V = T::V;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     E *buf = reinterpret_cast<E *>(smem);
-    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
-    const int64_t lo = static_cast<int64_t>(rank) * a.slice;
-    const int64_t hi = min(n, lo + a.slice);
-    const int len = hi > lo ? static_cast<int>(hi - lo) : 0;
     const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(E);
     const uint32_t bulk = bytes & ~15u;
     const int nchunks = static_cast<int>((bulk + kChunkBytes - 1) / kChunkBytes);
-    // sampled first digit: only every sample_step-th 16-byte vector feeds the first histogram
-    const bool sampled = a.sample_step > 1 && n >= 4LL * k && n >= static_cast<int64_t>(a.sample_min_cols);
-    const int step = sampled ? a.sample_step : 1;
-
+    const bool agg = a.agg != 0;
     if (tid == 0) {
-        for (int c = 0; c < nchunks; ++c) mbar_init(&s_bar[c], 1);
+        for (int c = 0; c < nchunks; ++c) mbar_init(&bars[c], 1);
         fence_mbar_init();
-    }
-    for (int i = tid; i < a.hist_bins; i += NT) hist[i] = 0u;
-    __syncthreads();
-    if (tid == 0) {
         const char *src = reinterpret_cast<const char *>(xrow + lo);
         for (int c = 0; c < nchunks; ++c) {
             const uint32_t nb = min(kChunkBytes, bulk - static_cast<uint32_t>(c) * kChunkBytes);
-            mbar_arrive_expect_tx(&s_bar[c], nb);
+            mbar_arrive_expect_tx(&bars[c], nb);
             bulk_load(smem + static_cast<size_t>(c) * kChunkBytes, src + static_cast<size_t>(c) * kChunkBytes, nb,
-                      &s_bar[c]);
+                      &bars[c]);
         }
     }
-    if (CLUSTER) cluster_sync();  // every CTA of the cluster has started before any remote access
-
-    // -------------- first-digit histogram (every step-th vector) while chunks land
+    __syncthreads();  // barriers initialised before anyone waits on them
     const int sh0 = T::KB - a.bits[0];
-    const int nb0 = 1 << a.bits[0];
     for (int c = 0; c < nchunks; ++c) {
-        wait_phase(&s_bar[c], 0u, a.err_flag);
+        wait_phase(&bars[c], 0u, a.err_flag);
         const uint32_t cb = min(kChunkBytes, bulk - static_cast<uint32_t>(c) * kChunkBytes);
         const int nv = static_cast<int>(cb >> 4);
         const uint4 *vb = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(c) * kChunkBytes);
@@ -364,109 +350,264 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
             for (int t = 0; t < V; ++t) hist_add(hist, T::key(el[t]) >> sh0, ok, lane, agg);
         }
     }
-    {
-        const int tail0 = static_cast<int>(bulk / sizeof(E));
-        if (tid < len - tail0) {  // < 16 bytes left over: plain loads
-            const E e = xrow[lo + tail0 + tid];
-            buf[tail0 + tid] = e;
-            if (!sampled) atomicAdd(&hist[T::key(e) >> sh0], 1u);
+    const int tail0 = static_cast<int>(bulk / sizeof(E));
+    if (tid < len - tail0) {  // < 16 bytes left over: plain loads
+        const E e = xrow[lo + tail0 + tid];
+        buf[tail0 + tid] = e;
+        if (step == 1) atomicAdd(&hist[T::key(e) >> sh0], 1u);
+    }
+    __syncthreads();
+}
+
+// One pass over the staged slice: mask byte per 16-byte vector (bit t: key >= tkey), NaN check
+// into nan_flag, then the index-ordered list of 16-bit offsets of the set bits.  Returns the
+// number of such keys; the list is written only if that number is <= cap.  Ends with __syncthreads.
+template <typename E, int NT>
+__device__ int filter_to_list(const TopkArgs &a, const E *buf, int len, uint32_t tkey, uint8_t *masks, uint16_t *list,
+                              int cap, uint32_t *s_warp)
+{
+    using T = Elem<E>;
+    constexpr int V = T::V;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nvt = (len + V - 1) / V;
+    const uint4 *vbuf = reinterpret_cast<const uint4 *>(buf);
+    uint32_t mag = 0;  // largest |x| bit pattern: a NaN iff above the infinity pattern
+    for (int base = warp * 32; base < nvt; base += NT) {
+        const int v = base + lane;
+        if (v < nvt) {
+            E el[V];
+            T::unpack(vbuf[v], el);
+            const int lim = min(V, len - v * V);
+            uint32_t m = 0;
+#pragma unroll
+            for (int t = 0; t < V; ++t) {
+                const bool in = t < lim;
+                mag = max(mag, in ? T::magnitude(el[t]) : 0u);
+                m |= static_cast<uint32_t>(in && T::key(el[t]) >= tkey) << t;
+            }
+            masks[v] = static_cast<uint8_t>(m);
+        }
+    }
+    if (__syncthreads_or(mag > T::kInfMagnitude) && tid == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
+    const int q = (nvt + NT - 1) / NT;
+    const int v0 = min(nvt, tid * q), v1 = min(nvt, v0 + q);
+    uint32_t c = 0;
+    for (int v = v0; v < v1; ++v) c += __popc(static_cast<uint32_t>(masks[v]));
+    uint32_t tot;
+    uint32_t pos = block_exclusive_scan<NT>(c, s_warp, tot);
+    if (tot <= static_cast<uint32_t>(cap)) {
+        for (int v = v0; v < v1; ++v) {
+            uint32_t m = masks[v];
+            while (m) {
+                const int b = __ffs(m) - 1;
+                list[pos++] = static_cast<uint16_t>(v * V + b);
+                m &= m - 1u;
+            }
         }
     }
     __syncthreads();
+    return static_cast<int>(tot);
+}
 
-    // Histogram reduction over the cluster: CTA 0's histogram is the merge target; CTA 0 evaluates
-    // `decide` on the total and stores s_res[0..3] into every CTA.  Leaves every local histogram zero.
-    auto reduce_decide = [&](int nb, auto &&decide) {
-        if constexpr (CLUSTER) {
-            if (rank != 0) {
-                for (int i = tid; i < nb; i += NT) {
-                    const uint32_t c = hist[i];
-                    if (c) {
-                        dsmem_add(map_to_rank(smem_addr(&hist[i]), 0u), c);
-                        hist[i] = 0u;
-                    }
-                }
-            }
-            cluster_sync();
-            if (rank == 0) {
-                decide(hist, nb);  // block-wide; ends with __syncthreads
-                for (int i = tid; i < nb; i += NT) hist[i] = 0u;
-                if (tid < static_cast<int>(csize)) {
-                    const uint32_t r = static_cast<uint32_t>(tid);
+// Sum of a histogram over the CTA (all threads get it).  Two __syncthreads.
+template <int NT>
+__device__ __forceinline__ uint32_t hist_total(const uint32_t *h, int nb, uint32_t *s_warp)
+{
+    const int tid = threadIdx.x;
+    uint32_t s = 0;
+    for (int i = tid; i < nb; i += NT) s += h[i];
+    s = __reduce_add_sync(kFull, s);
+    if ((tid & 31) == 0) s_warp[tid >> 5] = s;
+    __syncthreads();
+    uint32_t total = 0;
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) dsmem_store(map_to_rank(smem_addr(&s_res[w]), r), s_res[w]);
-                }
-            }
-            cluster_sync();
-        } else {
-            decide(hist, nb);
-            for (int i = tid; i < nb; i += NT) hist[i] = 0u;
-            __syncthreads();
-        }
-    };
-    // exact threshold digit for `need` keys: s_res = {digit, count above it, count in it, 0}
-    auto exact_threshold = [&](uint32_t need) {
-        return [&, need](const uint32_t *h, int nb) {
-            find_threshold<NT>(h, nb, need, s_res, s_warp);
-            if (tid == 0) s_res[3] = 0u;
-        };
-    };
+    for (int w = 0; w < NT / 32; ++w) total += s_warp[w];
+    __syncthreads();
+    return total;
+}
 
-    // ---- candidate filter: mask byte per vector (bit t: key >= tkey), NaN check, ordered list
-    uint16_t *list = reinterpret_cast<uint16_t *>(smem + a.smem_list_off);
+// Threshold digit estimated from a sample histogram: the highest digit at or above which the
+// sample holds mu*(1+1/8) + 3*sqrt(mu) + 4 keys, mu = the sample's expected share of the
+// `share` keys wanted out of `population`.  0 (keep everything) if that is the whole sample.
+template <int NT>
+__device__ uint32_t sample_threshold_digit(const uint32_t *h, int nb, float share, float population, uint32_t *s_res,
+                                           uint32_t *s_warp)
+{
+    const uint32_t total = hist_total<NT>(h, nb, s_warp);
+    const float mu = share * static_cast<float>(total) / population;
+    const float want = mu * 1.125f + 3.0f * sqrtf(mu) + 4.0f;
+    if (want >= static_cast<float>(total)) return 0u;
+    find_threshold<NT>(h, nb, static_cast<uint32_t>(want), s_res, s_warp);
+    return s_res[0];
+}
+
+// ---------------------------------------------------------------------------
+// Exact selection over keys held in global memory, split into up to kMaxParts
+// segments that are in column order (a whole row = one segment; the merged
+// candidates of a split row = one segment per part).  Single CTA.  Reads
+// through L2 (ld.global.cg) because other CTAs may have written the segments.
+// min_d0: fail (return false, nothing written) if the first threshold digit is
+// below it.  Writes the k outputs (and, with GATHER, the gathered rows).
+// ---------------------------------------------------------------------------
+template <typename E>
+struct Segments {
+    int n;                                  // number of segments
+    const E *bits[kMaxParts];               // raw element bits
+    const int32_t *cols[kMaxParts];         // column of each element, or null: col = base + i
+    int64_t base[kMaxParts];
+    uint32_t pre[kMaxParts + 1];            // prefix of the segment sizes
+};
+
+template <typename E>
+__device__ __forceinline__ E seg_bits(const Segments<E> &sg, int s, uint32_t i)
+{
+    return __ldcg(sg.bits[s] + i);
+}
+
+template <typename E>
+__device__ __forceinline__ int64_t seg_col(const Segments<E> &sg, int s, uint32_t i)
+{
+    return sg.cols[s] ? static_cast<int64_t>(__ldcg(sg.cols[s] + i)) : sg.base[s] + i;
+}
+
+template <typename E, int NT, bool GATHER>
+__device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E> &sg, uint32_t min_d0,
+                                 uint32_t *hist, uint32_t *s_res, uint32_t *s_warp, int32_t *glist)
+{
+    using T = Elem<E>;
+    const int tid = threadIdx.x;
+    const uint32_t total = sg.pre[sg.n];
+    uint32_t prefix = 0, need = static_cast<uint32_t>(a.k), cnt = 0;
+    int shift = T::KB;
+    for (int l = 0; l < a.nlevels && (l == 0 || cnt != need); ++l) {
+        const int bl = a.bits[l];
+        const int nsh = shift - bl;
+        const int nb = 1 << bl;
+        const uint32_t mask = static_cast<uint32_t>(nb - 1);
+        for (int s = 0; s < sg.n; ++s) {
+            const uint32_t cs = sg.pre[s + 1] - sg.pre[s];
+            for (uint32_t i = tid; i < cs; i += NT) {
+                const uint32_t kk = T::key(seg_bits(sg, s, i));
+                if (l == 0 || (kk >> shift) == prefix) atomicAdd(&hist[(kk >> nsh) & mask], 1u);
+            }
+        }
+        __syncthreads();
+        find_threshold<NT>(hist, nb, need, s_res, s_warp);
+        const uint32_t d = s_res[0];
+        for (int i = tid; i < nb; i += NT) hist[i] = 0u;
+        __syncthreads();
+        if (l == 0 && d < min_d0) return false;
+        prefix = (l == 0) ? d : ((prefix << bl) | d);
+        need -= s_res[1];
+        cnt = s_res[2];
+        shift = nsh;
+    }
+    const uint32_t P = prefix;
+    const int S = shift;
+    const uint32_t E_need = need;
+    // ordered compaction: thread t owns the flat run [t*m, t*m + m)
+    const uint32_t m = (total + NT - 1) / NT;
+    const uint32_t f0 = min(total, static_cast<uint32_t>(tid) * m), f1 = min(total, f0 + m);
+    int s0 = 0;
+    while (s0 + 1 < sg.n && sg.pre[s0 + 1] <= f0) ++s0;
+    uint32_t g = 0, q = 0;
+    {
+        int s = s0;
+        for (uint32_t f = f0; f < f1; ++f) {
+            while (f >= sg.pre[s + 1]) ++s;
+            const uint32_t c = T::key(seg_bits(sg, s, f - sg.pre[s])) >> S;
+            g += c > P;
+            q += c == P;
+        }
+    }
+    uint32_t tq;
+    uint32_t r = block_exclusive_scan<NT>(q, s_warp, tq);
+    const uint32_t sel = g + take_from_ties(E_need, r, q);
+    uint32_t ts;
+    uint32_t pos = block_exclusive_scan<NT>(sel, s_warp, ts);
+    {
+        int s = s0;
+        for (uint32_t f = f0; f < f1; ++f) {
+            while (f >= sg.pre[s + 1]) ++s;
+            const uint32_t i = f - sg.pre[s];
+            const E e = seg_bits(sg, s, i);
+            const uint32_t c = T::key(e) >> S;
+            bool take = c > P;
+            if (c == P) take = (r++ < E_need);
+            if (take) {
+                const int64_t col = seg_col(sg, s, i);
+                store_idx(a, row, pos, col);
+                if (a.want_values) store_val<E>(a, row, pos, e);
+                if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = static_cast<int32_t>(col);
+                ++pos;
+            }
+        }
+    }
+    if (GATHER) {
+        __syncthreads();
+        gather_rows_of<NT>(a, row, 0, a.n_gather, glist, 0);
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// row_kernel: one CTA per row, the row staged whole in shared memory.
+// ---------------------------------------------------------------------------
+template <typename E, int NT, bool GATHER>
+__global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const TopkArgs a)
+{
+    using T = Elem<E>;
+    constexpr int V = T::V;
+    constexpr int W = NT / 32;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ uint64_t s_bar[kMaxChunks];
+    __shared__ uint32_t s_warp[W];
+    __shared__ uint32_t s_wgt[W], s_weq[W];
+    __shared__ uint32_t s_wsel_base[W], s_weq_base[W];
+    __shared__ uint32_t s_res[4];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row = blockIdx.x;
+    const int64_t n = valid_cols(a, row);
+    const int k = a.k;
+    if (n <= k) {
+        short_row<E, NT, GATHER>(a, row, n, 0, k);
+        return;
+    }
+    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
+    E *buf = reinterpret_cast<E *>(smem);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
     uint8_t *masks = smem + a.smem_mask_off;
-    const int nvt = (len + V - 1) / V;  // 16-byte vectors in the slice (last one may be partial)
-    const uint4 *vbuf = reinterpret_cast<const uint4 *>(buf);
+    uint16_t *list = reinterpret_cast<uint16_t *>(smem + a.smem_list_off);
+    int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
+    const int len = static_cast<int>(n);
+    const int sh0 = T::KB - a.bits[0];
+    const int nb0 = 1 << a.bits[0];
+    const bool sampled = a.sample_step > 1 && n >= 4LL * k && n >= static_cast<int64_t>(a.sample_min_cols);
+
+    for (int i = tid; i < a.hist_bins; i += NT) hist[i] = 0u;
+    stage_and_histogram<E, NT>(a, xrow, 0, len, sampled ? a.sample_step : 1, smem, hist, s_bar);
+
+    // first digit: exact, or estimated from the sample and then made exact over the candidates
     int L = 0;
     bool list_ok = false;
-    auto build_list = [&](uint32_t tkey) {
-        bool has_nan = false;
-        for (int base = warp * 32; base < nvt; base += NT) {
-            const int v = base + lane;
-            if (v < nvt) {
-                E el[V];
-                T::unpack(vbuf[v], el);
-                uint32_t m = 0;
-#pragma unroll
-                for (int t = 0; t < V; ++t) {
-                    const bool in = v * V + t < len;
-                    has_nan |= in && T::is_nan(el[t]);
-                    m |= static_cast<uint32_t>(in && T::key(el[t]) >= tkey) << t;
-                }
-                masks[v] = static_cast<uint8_t>(m);
-            }
-        }
-        if (__syncthreads_or(has_nan) && tid == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
-        const int q = (nvt + NT - 1) / NT;
-        const int v0 = min(nvt, tid * q), v1 = min(nvt, v0 + q);
-        uint32_t c = 0;
-        for (int v = v0; v < v1; ++v) c += __popc(static_cast<uint32_t>(masks[v]));
-        uint32_t tot;
-        uint32_t pos = block_exclusive_scan<NT>(c, s_warp, tot);
-        list_ok = tot <= static_cast<uint32_t>(a.list_cap);
-        if (list_ok) {
-            for (int v = v0; v < v1; ++v) {
-                uint32_t m = masks[v];
-                while (m) {
-                    const int b = __ffs(m) - 1;
-                    list[pos++] = static_cast<uint16_t>(v * V + b);
-                    m &= m - 1u;
-                }
-            }
-        }
-        L = list_ok ? static_cast<int>(tot) : 0;
-        __syncthreads();
-    };
-    // histogram of the first digit over keys >= tkey (the list, or the whole slice when the list overflowed)
-    auto candidate_hist = [&](uint32_t tkey) {
+    bool exact = false;
+    if (sampled) {
+        const uint32_t dt = sample_threshold_digit<NT>(hist, nb0, static_cast<float>(k), static_cast<float>(n), s_res,
+                                                       s_warp);
+        for (int i = tid; i < nb0; i += NT) hist[i] = 0u;
+        const uint32_t tkey = dt << sh0;
+        L = filter_to_list<E, NT>(a, buf, len, tkey, masks, list, a.list_cap, s_warp);
+        list_ok = L <= a.list_cap;
         if (list_ok) {
             for (int i = tid; i < L; i += NT) atomicAdd(&hist[T::key(buf[list[i]]) >> sh0], 1u);
         } else {
+            const int nvt = (len + V - 1) / V;
             for (int base = warp * 32; base < nvt; base += NT) {
                 const int v = base + lane;
                 if (v < nvt) {
                     E el[V];
-                    T::unpack(vbuf[v], el);
+                    T::unpack(reinterpret_cast<const uint4 *>(buf)[v], el);
 #pragma unroll
                     for (int t = 0; t < V; ++t) {
                         const uint32_t kk = T::key(el[t]);
@@ -476,72 +617,37 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
             }
         }
         __syncthreads();
-    };
-
-    bool exact_done = false;
-    if (sampled) {
-        // threshold estimate from the sample: the highest digit that keeps, with a 4-sigma margin,
-        // at least k keys of the whole row at or above it
-        reduce_decide(nb0, [&](const uint32_t *h, int nb) {
-            uint32_t s = 0;
-            for (int i = tid; i < nb; i += NT) s += h[i];
-            s = __reduce_add_sync(kFull, s);
-            if (lane == 0) s_warp[warp] = s;
+        exact = hist_total<NT>(hist, nb0, s_warp) >= static_cast<uint32_t>(k);
+        if (!exact) {  // the estimate was too high: exact histogram of the whole slice
+            for (int i = tid; i < nb0; i += NT) hist[i] = 0u;
             __syncthreads();
-            uint32_t total = 0;
+            const int nvt = (len + V - 1) / V;
+            for (int base = warp * 32; base < nvt; base += NT) {
+                const int v = base + lane;
+                if (v < nvt) {
+                    E el[V];
+                    T::unpack(reinterpret_cast<const uint4 *>(buf)[v], el);
 #pragma unroll
-            for (int w = 0; w < W; ++w) total += s_warp[w];
-            __syncthreads();
-            const float mu = static_cast<float>(k) * static_cast<float>(total) / static_cast<float>(n);
-            const float want = mu + 4.0f * sqrtf(mu) + 2.0f;
-            if (want >= static_cast<float>(total)) {
-                if (tid == 0) {
-                    s_res[0] = 0u;
-                    s_res[3] = 0u;
+                    for (int t = 0; t < V; ++t)
+                        if (v * V + t < len) atomicAdd(&hist[T::key(el[t]) >> sh0], 1u);
                 }
-                __syncthreads();
-            } else {
-                find_threshold<NT>(h, nb, static_cast<uint32_t>(want), s_res, s_warp);
             }
-        });
-        const uint32_t tkey = s_res[0] << sh0;
-        build_list(tkey);
-        candidate_hist(tkey);
-        // exact first digit among the candidates; flag 1 when fewer than k keys reached the estimate
-        reduce_decide(nb0, [&](const uint32_t *h, int nb) {
-            uint32_t s = 0;
-            for (int i = tid; i < nb; i += NT) s += h[i];
-            s = __reduce_add_sync(kFull, s);
-            if (lane == 0) s_warp[warp] = s;
             __syncthreads();
-            uint32_t total = 0;
-#pragma unroll
-            for (int w = 0; w < W; ++w) total += s_warp[w];
-            __syncthreads();
-            if (total < static_cast<uint32_t>(k)) {
-                if (tid == 0) s_res[3] = 1u;
-                __syncthreads();
-            } else {
-                find_threshold<NT>(h, nb, static_cast<uint32_t>(k), s_res, s_warp);
-                if (tid == 0) s_res[3] = 0u;
-                __syncthreads();
-            }
-        });
-        exact_done = s_res[3] == 0u;
-        if (!exact_done) {
-            // the estimate was too high: exact histogram of the whole slice, then the list again
-            list_ok = false;
-            candidate_hist(0u);
         }
     }
-    if (!exact_done) {
-        reduce_decide(nb0, exact_threshold(static_cast<uint32_t>(k)));
-        build_list(s_res[0] << sh0);
+    find_threshold<NT>(hist, nb0, static_cast<uint32_t>(k), s_res, s_warp);
+    for (int i = tid; i < nb0; i += NT) hist[i] = 0u;
+    __syncthreads();
+    if (!exact) {
+        L = filter_to_list<E, NT>(a, buf, len, s_res[0] << sh0, masks, list, a.list_cap, s_warp);
+        list_ok = L <= a.list_cap;
     }
     uint32_t prefix = s_res[0];  // selection class: (key >> shift) == prefix
     int shift = sh0;
     uint32_t need = static_cast<uint32_t>(k) - s_res[1];
     uint32_t cnt = s_res[2];
+    const int nvt = (len + V - 1) / V;
+    const uint4 *vbuf = reinterpret_cast<const uint4 *>(buf);
 
     // ---------------------------------------------------- further levels
     for (int l = 1; l < a.nlevels && cnt != need; ++l) {
@@ -569,7 +675,9 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
             }
         }
         __syncthreads();
-        reduce_decide(nb, exact_threshold(need));
+        find_threshold<NT>(hist, nb, need, s_res, s_warp);
+        for (int i = tid; i < nb; i += NT) hist[i] = 0u;
+        __syncthreads();
         prefix = (prefix << bl) | s_res[0];
         need -= s_res[1];
         cnt = s_res[2];
@@ -580,36 +688,6 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
     const uint32_t E_need = need;  // keys of class P still to take, in column order
 
     // --------------------------------------------- ordered write of the k
-    int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
-    auto exchange_cta_totals = [&](uint32_t tg, uint32_t te) {
-        // (selected before this CTA, threshold-class keys before this CTA) over the cluster, in rank order
-        if constexpr (CLUSTER) {
-            // every CTA stores its two counts into slot `rank` of every CTA of the cluster
-            if (tid < static_cast<int>(csize)) {
-                const uint32_t r = static_cast<uint32_t>(tid);
-                dsmem_store(map_to_rank(smem_addr(&s_all_g[rank]), r), tg);
-                dsmem_store(map_to_rank(smem_addr(&s_all_e[rank]), r), te);
-            }
-            cluster_sync();
-        } else {
-            __syncthreads();
-        }
-        if (tid == 0) {
-            uint32_t eqb = 0, selb = 0;
-            if constexpr (CLUSTER) {
-                for (uint32_t r = 0; r < rank; ++r) {
-                    const uint32_t g = s_all_g[r], e = s_all_e[r];
-                    selb += g + take_from_ties(E_need, eqb, e);
-                    eqb += e;
-                }
-            }
-            s_cta_sel[0] = selb;
-            s_cta_sel[1] = tg + take_from_ties(E_need, eqb, te);
-            s_eq_before = eqb;
-        }
-        __syncthreads();
-    };
-
     if (list_ok) {
         const int m = (L + NT - 1) / NT;
         const int i0 = min(L, tid * m), i1 = min(L, i0 + m);
@@ -619,15 +697,11 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
             g += c > P;
             q += c == P;
         }
-        uint32_t tg, tq;
-        (void)block_exclusive_scan<NT>(g, s_warp, tg);
-        const uint32_t qx = block_exclusive_scan<NT>(q, s_warp, tq);
-        exchange_cta_totals(tg, tq);
-        uint32_t r = s_eq_before + qx;
+        uint32_t tq;
+        uint32_t r = block_exclusive_scan<NT>(q, s_warp, tq);
         const uint32_t sel = g + take_from_ties(E_need, r, q);
         uint32_t ts;
-        uint32_t pos = s_cta_sel[0] + block_exclusive_scan<NT>(sel, s_warp, ts);
-        const uint32_t cta_base = s_cta_sel[0];
+        uint32_t pos = block_exclusive_scan<NT>(sel, s_warp, ts);
         for (int i = i0; i < i1; ++i) {
             const int o = list[i];
             const E e = buf[o];
@@ -635,16 +709,15 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
             bool take = c > P;
             if (c == P) take = (r++ < E_need);
             if (take) {
-                const int64_t col = lo + o;
-                store_idx(a, row, pos, col);
+                store_idx(a, row, pos, o);
                 if (a.want_values) store_val<E>(a, row, pos, e);
-                if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos - cta_base] = static_cast<int32_t>(col);
+                if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = o;
                 ++pos;
             }
         }
     } else {
-        // full-slice fallback (threshold bin too large for the list): warp-segment counts, then an
-        // ordered write in which every warp walks its own contiguous segment
+        // full-slice path (candidates overflowed the list): warp-segment counts, then an ordered
+        // write in which every warp walks its own contiguous segment
         const int seg = ((len + W - 1) / W + 32 * V - 1) / (32 * V) * (32 * V);
         const int w_lo = min(len, warp * seg);
         const int w_hi = min(len, w_lo + seg);
@@ -668,14 +741,8 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
             s_weq[warp] = eq;
         }
         __syncthreads();
-        uint32_t tg = 0, te = 0;
-        for (int w = 0; w < W; ++w) {
-            tg += s_wgt[w];
-            te += s_weq[w];
-        }
-        exchange_cta_totals(tg, te);
         if (tid == 0) {
-            uint32_t ws = s_cta_sel[0], we = s_eq_before;
+            uint32_t ws = 0, we = 0;
             for (int w = 0; w < W; ++w) {
                 s_wsel_base[w] = ws;
                 s_weq_base[w] = we;
@@ -684,7 +751,6 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
             }
         }
         __syncthreads();
-        const uint32_t cta_base = s_cta_sel[0];
         uint32_t eq_run = s_weq_base[warp];
         uint32_t sel_run = s_wsel_base[warp];
         for (int base = w_lo; base < w_hi; base += 32 * V) {
@@ -717,11 +783,9 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
 #pragma unroll
             for (int t = 0; t < V; ++t) {
                 if ((sm >> t) & 1u) {
-                    const int64_t col = lo + o + t;
-                    store_idx(a, row, pos, col);
+                    store_idx(a, row, pos, o + t);
                     if (a.want_values) store_val<E>(a, row, pos, el[t]);
-                    if (GATHER && static_cast<int64_t>(pos) < a.n_gather)
-                        glist[pos - cta_base] = static_cast<int32_t>(col);
+                    if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = o + t;
                     ++pos;
                 }
             }
@@ -729,26 +793,189 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) topk_kernel(const To
             sel_run += ts;
         }
     }
-
-    // ---------------------------------------------------- fused gather
     if (GATHER) {
         __syncthreads();
-        const int64_t g0 = s_cta_sel[0];
-        const int64_t g1 = min(g0 + static_cast<int64_t>(s_cta_sel[1]), a.n_gather);
-        if (g0 < g1) gather_rows_of<NT>(a, row, g0, g1, glist, 0);
+        gather_rows_of<NT>(a, row, 0, a.n_gather, glist, 0);
     }
-    // no cluster barrier here: after the totals exchange no CTA touches another CTA's shared memory
 }
 
-// Raises the kernel's dynamic shared-memory limit (and allows clusters above 8) once per device;
-// later calls that need no more than what was set skip the driver call.
-template <typename E, int NT, bool C, bool G>
-cudaError_t prepare_variant(int cluster, size_t smem)
+// ---------------------------------------------------------------------------
+// split_kernel: `parts` CTAs per row; grid = rows * parts.
+// Workspace (caller-owned, 256-byte aligned, zero before first use; every
+// completed launch leaves it that way):
+//   [0, ws_counter_bytes)         uint32 arrival counter per row
+//   per row r, at ws_counter_bytes + r * ws_row_bytes:
+//     uint32 count[parts], uint32 tkey[parts]       (padded to 16 bytes)
+//     per part p, at ws_head_bytes + p * ws_part_bytes:
+//       E bits[part_cap] (padded to 16 bytes), int32 cols[part_cap]
+// ---------------------------------------------------------------------------
+template <typename E, int NT, bool GATHER>
+__global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const TopkArgs a)
+{
+    using T = Elem<E>;
+    constexpr int W = NT / 32;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ uint64_t s_bar[kMaxChunks];
+    __shared__ uint32_t s_warp[W];
+    __shared__ uint32_t s_res[4];
+    __shared__ uint32_t s_last;
+    __shared__ Segments<E> s_seg;
+
+    const int tid = threadIdx.x;
+    const int P = a.parts;
+    const int64_t row = blockIdx.x / P;
+    const int part = static_cast<int>(blockIdx.x - row * P);
+    const int64_t n = valid_cols(a, row);
+    const int k = a.k;
+    if (n <= k) {
+        if (part == 0) short_row<E, NT, GATHER>(a, row, n, 0, k);
+        return;
+    }
+    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
+    E *buf = reinterpret_cast<E *>(smem);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
+    uint8_t *masks = smem + a.smem_mask_off;
+    uint16_t *list = reinterpret_cast<uint16_t *>(smem + a.smem_list_off);
+    int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
+    const int sh0 = T::KB - a.bits[0];
+    const int nb0 = 1 << a.bits[0];
+    const int64_t lo = static_cast<int64_t>(part) * a.slice;
+    const int64_t hi = min(n, lo + a.slice);
+    const int len = hi > lo ? static_cast<int>(hi - lo) : 0;
+
+    unsigned char *wrow = a.ws + a.ws_counter_bytes + row * a.ws_row_bytes;
+    uint32_t *w_count = reinterpret_cast<uint32_t *>(wrow);
+    uint32_t *w_tkey = w_count + P;
+    unsigned char *wpart = wrow + a.ws_head_bytes + static_cast<int64_t>(part) * a.ws_part_bytes;
+    E *w_bits = reinterpret_cast<E *>(wpart);
+    int32_t *w_cols = reinterpret_cast<int32_t *>(wpart + a.ws_bits_bytes);
+
+    // ---- local candidates: keys at or above a threshold estimated from this slice's sample
+    for (int i = tid; i < a.hist_bins; i += NT) hist[i] = 0u;
+    uint32_t tkey = 0;
+    int L = 0;
+    if (len > 0) {
+        const bool sampled = len > a.list_cap && a.sample_step > 1;
+        stage_and_histogram<E, NT>(a, xrow, lo, len, sampled ? a.sample_step : 1, smem, hist, s_bar);
+        if (sampled) {
+            // this slice's expected share of the k, plus margins
+            const float share = static_cast<float>(k) * static_cast<float>(len) / static_cast<float>(n);
+            tkey = sample_threshold_digit<NT>(hist, nb0, share, static_cast<float>(len), s_res, s_warp) << sh0;
+        }
+        L = filter_to_list<E, NT>(a, buf, len, tkey, masks, list, a.list_cap, s_warp);
+        const bool fits = L <= a.list_cap;
+        if (fits) {
+            for (int i = tid; i < L; i += NT) {
+                const int o = list[i];
+                w_bits[i] = buf[o];
+                w_cols[i] = static_cast<int32_t>(lo + o);
+            }
+        }
+        if (tid == 0) {
+            w_count[part] = fits ? static_cast<uint32_t>(L) : 0xffffffffu;
+            w_tkey[part] = tkey;
+        }
+    } else if (tid == 0) {
+        w_count[part] = 0u;
+        w_tkey[part] = 0u;
+    }
+
+    // ---- arrival: the last CTA of the row to finish does the selection
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t *counter = reinterpret_cast<uint32_t *>(a.ws) + row;
+        s_last = (atomicAdd(counter, 1u) == static_cast<uint32_t>(P - 1)) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    if (tid == 0) {
+        bool ok = true;
+        uint32_t pre = 0, dmax = 0;
+        s_seg.n = P;
+        for (int p = 0; p < P; ++p) {
+            const uint32_t c = __ldcg(w_count + p);
+            const uint32_t tk = __ldcg(w_tkey + p);
+            if (c == 0xffffffffu) ok = false;
+            unsigned char *wp = wrow + a.ws_head_bytes + static_cast<int64_t>(p) * a.ws_part_bytes;
+            s_seg.bits[p] = reinterpret_cast<const E *>(wp);
+            s_seg.cols[p] = reinterpret_cast<const int32_t *>(wp + a.ws_bits_bytes);
+            s_seg.base[p] = 0;
+            s_seg.pre[p] = pre;
+            pre += ok ? c : 0u;
+            dmax = max(dmax, tk >> sh0);
+        }
+        s_seg.pre[P] = pre;
+        if (pre < static_cast<uint32_t>(k)) ok = false;
+        s_res[3] = ok ? (dmax + 1u) : 0u;  // 0: go straight to the exact row path
+    }
+    __syncthreads();
+    const uint32_t min_d0 = s_res[3];
+    bool done = false;
+    if (min_d0 != 0u) done = select_segments<E, NT, GATHER>(a, row, s_seg, min_d0 - 1u, hist, s_res, s_warp, glist);
+    if (!done) {
+        __syncthreads();
+        if (tid == 0) {
+            s_seg.n = 1;
+            s_seg.bits[0] = xrow;
+            s_seg.cols[0] = nullptr;
+            s_seg.base[0] = 0;
+            s_seg.pre[0] = 0;
+            s_seg.pre[1] = static_cast<uint32_t>(n);
+        }
+        __syncthreads();
+        select_segments<E, NT, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
+    }
+    if (tid == 0) reinterpret_cast<uint32_t *>(a.ws)[row] = 0u;  // ready for the next launch
+}
+
+// ---------------------------------------------------------------------------
+// stream_kernel: one CTA per row; every radix pass reads the row from global
+// memory.  For rows wider than the split plan covers.
+// ---------------------------------------------------------------------------
+template <typename E, int NT, bool GATHER>
+__global__ void __launch_bounds__(NT, MinBlocks<NT>::value) stream_kernel(const TopkArgs a)
+{
+    using T = Elem<E>;
+    constexpr int W = NT / 32;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ uint32_t s_warp[W];
+    __shared__ uint32_t s_res[4];
+    __shared__ Segments<E> s_seg;
+    const int tid = threadIdx.x;
+    const int64_t row = blockIdx.x;
+    const int64_t n = valid_cols(a, row);
+    if (n <= a.k) {
+        short_row<E, NT, GATHER>(a, row, n, 0, a.k);
+        return;
+    }
+    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
+    int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
+    for (int i = tid; i < a.hist_bins; i += NT) hist[i] = 0u;
+    uint32_t mag = 0;
+    for (int64_t j = tid; j < n; j += NT) mag = max(mag, T::magnitude(xrow[j]));
+    if (__syncthreads_or(mag > T::kInfMagnitude) && tid == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
+    if (tid == 0) {
+        s_seg.n = 1;
+        s_seg.bits[0] = xrow;
+        s_seg.cols[0] = nullptr;
+        s_seg.base[0] = 0;
+        s_seg.pre[0] = 0;
+        s_seg.pre[1] = static_cast<uint32_t>(n);
+    }
+    __syncthreads();
+    select_segments<E, NT, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device; later calls that need no more
+// than what was set skip the driver call.
+template <typename K>
+cudaError_t raise_smem_limit(K kern, int *set_smem, size_t smem)
 {
     constexpr int kMaxDevices = 64;
-    static int set_smem[kMaxDevices] = {};
-    static bool set_cluster[kMaxDevices] = {};
-    auto kern = topk_kernel<E, NT, C, G>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -758,104 +985,68 @@ cudaError_t prepare_variant(int cluster, size_t smem)
         if (e != cudaSuccess) return e;
         if (cacheable) set_smem[dev] = static_cast<int>(smem);
     }
-    if (C && cluster > 8 && (!cacheable || !set_cluster[dev])) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        if (cacheable) set_cluster[dev] = true;
-    }
     return cudaSuccess;
 }
 
-template <typename E, int NT, bool C, bool G>
-cudaError_t launch_variant(int cluster, size_t smem, const TopkArgs &a, cudaStream_t stream)
+template <typename E, int NT, bool G>
+cudaError_t launch_one(int mode, size_t smem, const TopkArgs &a, cudaStream_t stream, int64_t grid, bool query,
+                       int *blocks_per_sm)
 {
-    auto kern = topk_kernel<E, NT, C, G>;
-    cudaError_t e = prepare_variant<E, NT, C, G>(cluster, smem);
+    static int set_row[64] = {}, set_split[64] = {}, set_stream[64] = {};
+    cudaError_t e;
+    if (mode == kModeRow)
+        e = raise_smem_limit(row_kernel<E, NT, G>, set_row, smem);
+    else if (mode == kModeSplit)
+        e = raise_smem_limit(split_kernel<E, NT, G>, set_split, smem);
+    else
+        e = raise_smem_limit(stream_kernel<E, NT, G>, set_stream, smem);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.rows * (C ? cluster : 1)), 1, 1);
-    cfg.blockDim = dim3(NT, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    if (C) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+    if (query) {
+        if (mode == kModeRow)
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, row_kernel<E, NT, G>, NT, smem);
+        if (mode == kModeSplit)
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, split_kernel<E, NT, G>, NT, smem);
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, stream_kernel<E, NT, G>, NT, smem);
     }
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const dim3 g(static_cast<unsigned>(grid)), b(NT);
+    if (mode == kModeRow)
+        row_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
+    else if (mode == kModeSplit)
+        split_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
+    else
+        stream_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
+    return cudaGetLastError();
 }
 
-template <typename E, int NT, bool C, bool G>
-int max_clusters_variant(int cluster, size_t smem)
-{
-    auto kern = topk_kernel<E, NT, C, G>;
-    if (prepare_variant<E, NT, C, G>(cluster, smem) != cudaSuccess) return 0;
-    if (!C) {
-        int blocks = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, NT, smem) != cudaSuccess) return 0;
-        return blocks * device_sm_count();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
-    cfg.blockDim = dim3(NT, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
-
-// Dispatch over (dtype, threads, cluster?, gather?) to one of the 24 instantiations.
-template <typename E, int NT>
-cudaError_t launch_nt(bool gather, int cluster, size_t smem, const TopkArgs &a, cudaStream_t s)
-{
-    if (cluster > 1)
-        return gather ? launch_variant<E, NT, true, true>(cluster, smem, a, s)
-                      : launch_variant<E, NT, true, false>(cluster, smem, a, s);
-    return gather ? launch_variant<E, NT, false, true>(1, smem, a, s) : launch_variant<E, NT, false, false>(1, smem, a, s);
-}
-
-template <typename E, int NT>
-int occupancy_nt(bool gather, int cluster, size_t smem)
-{
-    if (cluster > 1)
-        return gather ? max_clusters_variant<E, NT, true, true>(cluster, smem)
-                      : max_clusters_variant<E, NT, true, false>(cluster, smem);
-    return gather ? max_clusters_variant<E, NT, false, true>(1, smem) : max_clusters_variant<E, NT, false, false>(1, smem);
-}
-
+// Dispatch over (threads, gather) for one element type.  Thread counts: row_kernel 128/256/512,
+// split_kernel 256, stream_kernel 512.
 template <typename E>
-cudaError_t launch_e(int threads, bool gather, int cluster, size_t smem, const TopkArgs &a, cudaStream_t s)
+cudaError_t launch_e(int mode, int threads, bool gather, size_t smem, const TopkArgs &a, cudaStream_t s,
+                     int64_t grid, bool query, int *blocks_per_sm)
 {
+    if (mode == kModeSplit) {
+        if (threads != 256) return cudaErrorInvalidValue;
+        return gather ? launch_one<E, 256, true>(mode, smem, a, s, grid, query, blocks_per_sm)
+                      : launch_one<E, 256, false>(mode, smem, a, s, grid, query, blocks_per_sm);
+    }
+    if (mode == kModeStream) {
+        if (threads != 512) return cudaErrorInvalidValue;
+        return gather ? launch_one<E, 512, true>(mode, smem, a, s, grid, query, blocks_per_sm)
+                      : launch_one<E, 512, false>(mode, smem, a, s, grid, query, blocks_per_sm);
+    }
     switch (threads) {
-    case 128: return launch_nt<E, 128>(gather, cluster, smem, a, s);
-    case 256: return launch_nt<E, 256>(gather, cluster, smem, a, s);
-    case 512: return launch_nt<E, 512>(gather, cluster, smem, a, s);
+    case 128:
+        return gather ? launch_one<E, 128, true>(mode, smem, a, s, grid, query, blocks_per_sm)
+                      : launch_one<E, 128, false>(mode, smem, a, s, grid, query, blocks_per_sm);
+    case 256:
+        return gather ? launch_one<E, 256, true>(mode, smem, a, s, grid, query, blocks_per_sm)
+                      : launch_one<E, 256, false>(mode, smem, a, s, grid, query, blocks_per_sm);
+    case 512:
+        return gather ? launch_one<E, 512, true>(mode, smem, a, s, grid, query, blocks_per_sm)
+                      : launch_one<E, 512, false>(mode, smem, a, s, grid, query, blocks_per_sm);
     default: return cudaErrorInvalidValue;
-    }
-}
-
-template <typename E>
-int occupancy_e(int threads, bool gather, int cluster, size_t smem)
-{
-    switch (threads) {
-    case 128: return occupancy_nt<E, 128>(gather, cluster, smem);
-    case 256: return occupancy_nt<E, 256>(gather, cluster, smem);
-    case 512: return occupancy_nt<E, 512>(gather, cluster, smem);
-    default: return 0;
     }
 }
 

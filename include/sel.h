@@ -25,7 +25,8 @@
  *
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller; the library
- *     allocates no device or host memory on any call.
+ *     allocates no device or host memory on any call.  Scratch, where a shape
+ *     needs it, is a caller-owned workspace (sel_topk_workspace_size).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *     void*; NULL = the legacy default stream).  No call synchronises.
  *   - The return value is a sel_status.  Argument errors are found on the
@@ -97,18 +98,28 @@ SEL_API int sel_stride_requirement(int *in_align_bytes, int *out_align_bytes);
  *   idx_dtype   SEL_I32 | SEL_I64.
  *   out_idx     [rows, out_idx_stride] of idx_dtype; columns [0, k) written.
  *   out_val     [rows, out_val_stride] of `dtype`, or NULL when want_values == 0.
+ *   workspace   device scratch of at least sel_topk_workspace_size(dtype, rows,
+ *               cols, k) bytes, 256-byte aligned, filled with zeros before its
+ *               first use (every completed call leaves it that way); may be
+ *               NULL when that size is 0.  Calls that run at the same time
+ *               need separate workspaces.
  *   nan_flag, err_flag   optional device int32 flags (see above).
  * Errors: SEL_EINVAL (k out of range, negative sizes, stride < cols, output
- * strides < k, null required pointer, bad enum), SEL_EALIGN, SEL_EUNSUPPORTED
- * (a row wider than the widest supported split: see sel_max_cols),
- * SEL_ECUDA (launch failure).  rows == 0 returns SEL_OK without a launch. */
+ * strides < k, null required pointer, bad enum, missing or short workspace),
+ * SEL_EALIGN, SEL_EUNSUPPORTED (cols > 2^31 - 1), SEL_ECUDA (launch failure).
+ * rows == 0 returns SEL_OK without a launch. */
 SEL_API int sel_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride,
              const int32_t *row_end, int k, int sorted_index, int idx_dtype, int want_values,
              void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride,
+             void *workspace, size_t workspace_bytes,
              int32_t *nan_flag, int32_t *err_flag, void *stream);
 
-/* Largest `cols` sel_topk accepts for `dtype` on the current device (a row is
- * split over at most one thread-block cluster whose shared memory holds it). */
+/* Scratch bytes sel_topk / sel_topk_gather need for this shape on the current
+ * device: non-zero only when few rows are wide enough to be split over several
+ * CTAs, whose candidate lists meet in the workspace.  0 on invalid arguments. */
+SEL_API size_t sel_topk_workspace_size(int dtype, int64_t rows, int64_t cols, int k);
+
+/* Largest `cols` sel_topk accepts for `dtype` (indices must fit int32). */
 SEL_API int64_t sel_max_cols(int dtype);
 
 /* Flat row gather:  out[r, j, :] = key[b_r, max(idx[r, j], 0), :],
@@ -132,13 +143,14 @@ SEL_API int sel_gather_rows(const void *key, int64_t b, int64_t comp_len, int64_
  * sel_topk (out_idx may be NULL when the indices themselves are not needed);
  * the gather arguments are those of sel_gather_rows with idx taken from the
  * selection.  Fill positions (-1) of short rows gather position 0, as in
- * sel_gather_rows. */
+ * sel_gather_rows.  The workspace rule is that of sel_topk. */
 SEL_API int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride,
                     const int32_t *row_end, int k, int sorted_index, int idx_dtype, int want_values,
                     void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride,
                     const void *key, int64_t b, int64_t comp_len, int64_t d,
                     int64_t key_batch_stride, int64_t key_row_stride, int64_t n_gather,
-                    void *gather_out, int32_t *nan_flag, int32_t *err_flag, void *stream);
+                    void *gather_out, void *workspace, size_t workspace_bytes,
+                    int32_t *nan_flag, int32_t *err_flag, void *stream);
 
 /* Static message for a sel_status value. */
 SEL_API const char *sel_strerror(int status);

@@ -24,7 +24,7 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == sorted(["sel_gather_rows", "sel_max_cols", "sel_stride_requirement",
-                                         "sel_strerror", "sel_topk", "sel_topk_gather"])
+                                         "sel_strerror", "sel_topk", "sel_topk_gather", "sel_topk_workspace_size"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -50,7 +50,7 @@ FAKE = 0x10000  # never dereferenced: every call below is rejected on the host
 def topk(lib, x=FAKE, dtype=0, rows=4, cols=64, stride=64, k=8, idx_dtype=0, want_values=0, out_idx=FAKE,
          out_idx_stride=8, out_val=None, out_val_stride=0):
     return lib.sel_topk(x, dtype, rows, cols, stride, None, k, 0, idx_dtype, want_values, out_idx, out_idx_stride,
-                        out_val, out_val_stride, None, None, None)
+                        out_val, out_val_stride, None, 0, None, None, None)
 
 
 def test_topk_rejections(lib):
@@ -71,6 +71,14 @@ def test_topk_rejections(lib):
     assert topk(lib, rows=0) == 0                       # nothing to do, no launch
 
 
+def test_workspace_size_rejects_bad_arguments(lib):
+    # invalid shapes answer 0 without touching the device
+    assert lib.sel_topk_workspace_size(7, 4, 64, 8) == 0
+    assert lib.sel_topk_workspace_size(0, 4, 64, 0) == 0
+    assert lib.sel_topk_workspace_size(0, 4, 64, 5000) == 0
+    assert lib.sel_topk_workspace_size(0, 0, 64, 8) == 0
+
+
 def test_gather_rejections(lib):
     EINVAL, EALIGN = 1, 2
     def g(key=FAKE, b=1, comp_len=10, d=64, kbs=640, krs=64, idx=FAKE, idx_dtype=0, rows=4, n=3, irs=3, out=FAKE):
@@ -86,10 +94,10 @@ def test_gather_rejections(lib):
 
 def test_fused_rejections(lib):
     r = lib.sel_topk_gather(FAKE, 0, 4, 64, 64, None, 8, 0, 0, 0, None, 0, None, 0,
-                            FAKE, 1, 64, 64, 64 * 64, 64, 9, FAKE, None, None, None)
+                            FAKE, 1, 64, 64, 64 * 64, 64, 9, FAKE, None, 0, None, None, None)
     assert r == 1  # n_gather > k
     r = lib.sel_topk_gather(FAKE, 0, 4, 64, 64, None, 8, 0, 0, 0, None, 0, None, 0,
-                            FAKE, 3, 64, 64, 64 * 64, 64, 8, FAKE, None, None, None)
+                            FAKE, 3, 64, 64, 64 * 64, 64, 8, FAKE, None, 0, None, None, None)
     assert r == 1  # rows not a multiple of b
 
 

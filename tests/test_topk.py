@@ -184,6 +184,12 @@ EDGE = [
     ("f32", 320, 16384, 4096, "strided_large"),
     ("bf16", 320, 32768, 4096, "strided_large"),
     ("bf16", 2, 262144, 4096, "strided_large"),
+    # split rows whose per-slice estimates miss the true threshold (sorted rows)
+    ("f32", 4, 70000, 1000, "ascending"),
+    ("bf16", 4, 204800, 1024, "descending"),
+    ("bf16", 3, 204800, 1024, "ascending"),
+    # rows wider than the split plan covers: streamed passes over global memory
+    ("f32", 1, 3000000, 500, "normal"),
 ]
 
 
