@@ -69,17 +69,13 @@ def workspace_size(dtype: torch.dtype, rows: int, cols: int, k: int, device=None
 
 
 def _workspace(nbytes: int, device, stream):
-    """A zero-filled scratch buffer of >= nbytes, cached per (device, stream).
-
-    Every completed call leaves the buffer's counters zero again, so it is
-    reused as is; calls on the same stream never overlap.
-    """
+    """A scratch buffer of >= nbytes, cached per (device, stream) (calls on one stream never overlap)."""
     if nbytes == 0:
         return None, 0
     key = (device.index, stream.cuda_stream)
     buf = _WORKSPACES.get(key)
     if buf is None or buf.numel() < nbytes:
-        buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
         _WORKSPACES[key] = buf
     return buf, buf.numel()
 
@@ -132,8 +128,8 @@ def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_ind
     int32 CUDA tensors the kernel ORs / writes into.  ``output_idx`` /
     ``output_val`` are optional caller-owned [rows, >=k] buffers (row strides
     a multiple of the output alignment); results go to their first k columns.
-    ``workspace`` (uint8 CUDA tensor, zero-filled before first use) is only
-    needed by a few wide rows; by default a cached buffer is used.
+    ``workspace`` (uint8 CUDA tensor) is only needed when few wide rows are
+    split over several CTAs; by default a cached buffer is used.
     """
     _check_x(x)
     rows, cols = x.shape

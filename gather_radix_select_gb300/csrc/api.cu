@@ -314,6 +314,12 @@ int run_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
     a.rows_per_batch = n_gather > 0 ? rows / b : 1;
     a.n_gather = n_gather;
     a.gather_out = static_cast<uint16_t *>(gather_out);
+    if (p.ws_bytes > 0) {
+        // arrival counters start at zero on every launch, whatever the workspace held before
+        const cudaError_t e = cudaMemsetAsync(workspace, 0, static_cast<size_t>(a.ws_counter_bytes),
+                                              static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return SEL_ECUDA;
+    }
     return status_of(sel::launch_topk(dtype == SEL_F32 ? 0 : 1, p.mode, p.threads, n_gather > 0, p.smem, a, p.grid,
                                       static_cast<cudaStream_t>(stream)));
 }

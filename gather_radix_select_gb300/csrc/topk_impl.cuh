@@ -801,9 +801,9 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
 
 // ---------------------------------------------------------------------------
 // split_kernel: `parts` CTAs per row; grid = rows * parts.
-// Workspace (caller-owned, 256-byte aligned, zero before first use; every
-// completed launch leaves it that way):
-//   [0, ws_counter_bytes)         uint32 arrival counter per row
+// Workspace (caller-owned, 256-byte aligned):
+//   [0, ws_counter_bytes)         uint32 arrival counter per row (zeroed on the
+//                                 stream before every launch)
 //   per row r, at ws_counter_bytes + r * ws_row_bytes:
 //     uint32 count[parts], uint32 tkey[parts]       (padded to 16 bytes)
 //     per part p, at ws_head_bytes + p * ws_part_bytes:
@@ -928,7 +928,6 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
         __syncthreads();
         select_segments<E, NT, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
     }
-    if (tid == 0) reinterpret_cast<uint32_t *>(a.ws)[row] = 0u;  // ready for the next launch
 }
 
 // ---------------------------------------------------------------------------

@@ -99,10 +99,10 @@ SEL_API int sel_stride_requirement(int *in_align_bytes, int *out_align_bytes);
  *   out_idx     [rows, out_idx_stride] of idx_dtype; columns [0, k) written.
  *   out_val     [rows, out_val_stride] of `dtype`, or NULL when want_values == 0.
  *   workspace   device scratch of at least sel_topk_workspace_size(dtype, rows,
- *               cols, k) bytes, 256-byte aligned, filled with zeros before its
- *               first use (every completed call leaves it that way); may be
- *               NULL when that size is 0.  Calls that run at the same time
- *               need separate workspaces.
+ *               cols, k) bytes, 256-byte aligned, any contents (its counters
+ *               are cleared on `stream` by the call); may be NULL when that
+ *               size is 0.  Calls that run at the same time need separate
+ *               workspaces.
  *   nan_flag, err_flag   optional device int32 flags (see above).
  * Errors: SEL_EINVAL (k out of range, negative sizes, stride < cols, output
  * strides < k, null required pointer, bad enum, missing or short workspace),

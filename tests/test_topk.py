@@ -189,7 +189,7 @@ EDGE = [
     ("bf16", 4, 204800, 1024, "descending"),
     ("bf16", 3, 204800, 1024, "ascending"),
     # rows wider than the split plan covers: streamed passes over global memory
-    ("f32", 1, 3000000, 500, "normal"),
+    ("f32", 1, 5000000, 500, "normal"),
 ]
 
 
