@@ -880,7 +880,8 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
         w_tkey[part] = 0u;
     }
 
-    // ---- arrival: the last CTA of the row to finish does the selection
+    // ---- arrival: the last CTA of the row to finish does the selection (its histogram must be clear)
+    for (int i = tid; i < a.hist_bins; i += NT) hist[i] = 0u;
     __threadfence();
     __syncthreads();
     if (tid == 0) {
