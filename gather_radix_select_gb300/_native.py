@@ -11,7 +11,8 @@ import threading
 
 from . import build as _build
 
-SEL_OK, SEL_EINVAL, SEL_EALIGN, SEL_EUNSUPPORTED, SEL_ECUDA, SEL_ETIMEOUT = range(6)
+SEL_OK, SEL_EINVAL, SEL_EALIGN, SEL_EUNSUPPORTED, SEL_ECUDA, SEL_ETIMEOUT, SEL_ESCRATCH = range(7)
+SEL_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 SEL_F32, SEL_BF16 = 0, 1
 SEL_I32, SEL_I64 = 0, 1
 SEL_MAX_K = 4096
@@ -30,6 +31,8 @@ SIGNATURES = {
                                _vp, _i64, _vp, _i64,
                                _vp, _i64, _i64, _i64, _i64, _i64, _i64, _vp,
                                _vp, ctypes.c_size_t, _vp, _vp, _vp]),
+    "sel_topk_noalloc": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _int, _int, _int, _int,
+                                _vp, _i64, _vp, _i64, _vp, _vp, _vp]),
     "sel_strerror": (ctypes.c_char_p, [_int]),
 }
 

@@ -344,6 +344,7 @@ const char *sel_strerror(int status)
     case SEL_EUNSUPPORTED: return "unsupported shape or type";
     case SEL_ECUDA: return "CUDA runtime error";
     case SEL_ETIMEOUT: return "a bounded device wait timed out";
+    case SEL_ESCRATCH: return "shape needs more scratch than sel_topk_noalloc's built-in array (use sel_topk with a workspace)";
     default: return "unknown status";
     }
 }

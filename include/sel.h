@@ -25,8 +25,10 @@
  *
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller; the library
- *     allocates no device or host memory on any call.  Scratch, where a shape
- *     needs it, is a caller-owned workspace (sel_topk_workspace_size).
+ *     allocates no device memory on any call (it keeps small host-side caches
+ *     of launch plans).  Scratch, where a shape needs it, is a caller-owned
+ *     workspace (sel_topk_workspace_size), or the built-in array of
+ *     sel_topk_noalloc.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *     void*; NULL = the legacy default stream).  No call synchronises.
  *   - The return value is a sel_status.  Argument errors are found on the
@@ -72,7 +74,8 @@ typedef enum {
     SEL_EALIGN = 2,       /* a pointer or row stride breaks the alignment rule */
     SEL_EUNSUPPORTED = 3, /* dtype / width outside what the kernels handle */
     SEL_ECUDA = 4,        /* a CUDA runtime call failed (launch, attribute query) */
-    SEL_ETIMEOUT = 5      /* (device flag only) a bounded device wait ran out */
+    SEL_ETIMEOUT = 5,     /* (device flag only) a bounded device wait ran out */
+    SEL_ESCRATCH = 6      /* sel_topk_noalloc: the shape needs more scratch than the built-in array */
 } sel_status;
 
 enum { SEL_F32 = 0, SEL_BF16 = 1 };  /* input element type */
@@ -151,6 +154,32 @@ SEL_API int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols
                     int64_t key_batch_stride, int64_t key_row_stride, int64_t n_gather,
                     void *gather_out, void *workspace, size_t workspace_bytes,
                     int32_t *nan_flag, int32_t *err_flag, void *stream);
+
+/* Size of the device array sel_topk_noalloc takes its scratch from (32 MiB). */
+#define SEL_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* sel_topk without a workspace argument, for callers that cannot allocate
+ * device memory (for example code running while a framework has reserved the
+ * whole device pool for itself, or a C caller with no device allocator).
+ * There is no counterpart on the pages this library follows: it is an
+ * addition of this library.
+ *   Arguments, results and errors are those of sel_topk.  Shapes for which
+ *   sel_topk_workspace_size exceeds SEL_NOALLOC_SCRATCH_BYTES are rejected
+ *   with SEL_ESCRATCH before anything is launched; use sel_topk with a
+ *   workspace for those.
+ *   The scratch is one file-scope device array per GPU, loaded with the
+ *   library and held until the process exits; nothing is allocated by the
+ *   call.  The first call on each device that needs scratch looks up the
+ *   array's device address (with that device current); make that first call
+ *   before any stream capture.
+ *   Every call shares the array and it keeps the previous call's contents:
+ *   the counters that must start at zero are cleared on `stream` by each call.
+ *   Calls that overlap on the GPU (other streams, other host threads) race on
+ *   the array and give undefined results: serialise them. */
+SEL_API int sel_topk_noalloc(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride,
+                     const int32_t *row_end, int k, int sorted_index, int idx_dtype, int want_values,
+                     void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride,
+                     int32_t *nan_flag, int32_t *err_flag, void *stream);
 
 /* Static message for a sel_status value. */
 SEL_API const char *sel_strerror(int status);

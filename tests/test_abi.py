@@ -24,7 +24,8 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == sorted(["sel_gather_rows", "sel_max_cols", "sel_stride_requirement",
-                                         "sel_strerror", "sel_topk", "sel_topk_gather", "sel_topk_workspace_size"])
+                                         "sel_strerror", "sel_topk", "sel_topk_gather", "sel_topk_noalloc",
+                                         "sel_topk_workspace_size"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -39,7 +40,7 @@ def test_stride_requirement_and_messages(lib):
     assert lib.sel_stride_requirement(ctypes.byref(a), ctypes.byref(b)) == 0
     assert (a.value, b.value) == (16, 16)
     assert lib.sel_stride_requirement(None, None) == 0
-    for st in range(6):
+    for st in range(7):
         assert lib.sel_strerror(st)
     assert lib.sel_strerror(99) == b"unknown status"
 
