@@ -63,20 +63,21 @@ int threads_for(int64_t slice)
 }
 
 // Shared-memory layout of one CTA staging `slice` elements with a candidate list of `cap`
-// entries; returns the total bytes.
+// entries: slice | masks | list | histogram | gather list.  Everything in front of the histogram
+// doubles as the staging area of split_kernel's merge.  Returns the total bytes.
 size_t layout_staged(int dtype, int64_t slice, int64_t cap, bool gather, int64_t n_gather, sel::TopkArgs &a)
 {
     const int64_t e = elem_bytes(dtype);
     a.slice = slice;
     size_t off = static_cast<size_t>(round_up(slice * e, 128));
     a.smem_buf_bytes = static_cast<uint32_t>(off);
-    a.smem_hist_off = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(a.hist_bins) * 4;
     a.smem_mask_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(round_up(ceil_div(slice, 16 / e), 16));
     a.list_cap = static_cast<int32_t>(cap);
     a.smem_list_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(round_up(cap * 2, 16));
+    a.smem_hist_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(a.hist_bins) * 4;
     a.smem_glist_off = static_cast<uint32_t>(off);
     if (gather) off += static_cast<size_t>(round_up(n_gather * 4, 16));
     return off;
@@ -192,6 +193,7 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
         const size_t smem = layout_staged(dtype, slice, cap, gather, n_gather, sp.layout);
         if (smem <= limit && cached_blocks_per_sm(dtype, sel::kModeSplit, 256, gather, smem) > 0 &&
             rows * parts <= 0x7fffffffLL) {
+            sp.layout.sample_step = 4;  // each slice estimates its own threshold: a denser sample
             sp.mode = sel::kModeSplit;
             sp.threads = 256;
             sp.smem = smem;

@@ -46,6 +46,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, ui
     return ok != 0;
 }
 
+// Orders this thread's earlier generic-proxy global accesses (and those it has synchronised
+// with) before its later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // --------------------------------------------------------- bulk async copy
 // global -> this CTA's shared memory; completion counted on `bar` in bytes.
 // dst, src and bytes must all be multiples of 16.

@@ -426,28 +426,66 @@ __device__ __forceinline__ uint32_t hist_total(const uint32_t *h, int nb, uint32
     return total;
 }
 
-// Threshold digit estimated from a sample histogram: the highest digit at or above which the
-// sample holds mu*(1+1/8) + 3*sqrt(mu) + 4 keys, mu = the sample's expected share of the
-// `share` keys wanted out of `population`.  0 (keep everything) if that is the whole sample.
-template <int NT>
-__device__ uint32_t sample_threshold_digit(const uint32_t *h, int nb, float share, float population, uint32_t *s_res,
-                                           uint32_t *s_warp)
+// Threshold key estimated from a sample: every `step`-th of the first `nvb` full 16-byte vectors
+// of buf, whose top-digit histogram is in h.  mu = the sample's expected share of the `share`
+// keys wanted out of `population`; the estimate keeps mu*(1+1/8) + 3*sqrt(mu) + 4 sampled keys at
+// or above it.  The top digit comes from h, a second digit from the sampled keys in that bin, so
+// the key is resolved to 22 bits (fp32) or fully (bf16).  0 (keep everything) if that is the
+// whole sample.  Leaves h zero.
+template <typename E, int NT>
+__device__ uint32_t sample_threshold_key(const TopkArgs &a, const E *buf, int nvb, int step, uint32_t *h,
+                                         float share, float population, uint32_t *s_res, uint32_t *s_warp)
 {
-    const uint32_t total = hist_total<NT>(h, nb, s_warp);
+    using T = Elem<E>;
+    constexpr int V = T::V;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sh0 = T::KB - a.bits[0];
+    const int nb0 = 1 << a.bits[0];
+    const uint32_t total = hist_total<NT>(h, nb0, s_warp);
     const float mu = share * static_cast<float>(total) / population;
     const float want = mu * 1.125f + 3.0f * sqrtf(mu) + 4.0f;
-    if (want >= static_cast<float>(total)) return 0u;
-    find_threshold<NT>(h, nb, static_cast<uint32_t>(want), s_res, s_warp);
-    return s_res[0];
+    if (want >= static_cast<float>(total)) {
+        for (int i = tid; i < nb0; i += NT) h[i] = 0u;
+        __syncthreads();
+        return 0u;
+    }
+    find_threshold<NT>(h, nb0, static_cast<uint32_t>(want), s_res, s_warp);
+    const uint32_t d = s_res[0];
+    const uint32_t need2 = static_cast<uint32_t>(want) - s_res[1];
+    for (int i = tid; i < nb0; i += NT) h[i] = 0u;
+    __syncthreads();
+    const int b2 = sh0 < 11 ? sh0 : 11;  // refinement digit: the next bits below the top digit
+    const int sh1 = sh0 - b2;
+    const uint32_t m2 = (1u << b2) - 1u;
+    const uint4 *vb = reinterpret_cast<const uint4 *>(buf);
+    for (int base = warp * 32; base * step < nvb; base += NT) {
+        const int v = (base + lane) * step;
+        if (v < nvb) {
+            E el[V];
+            T::unpack(vb[v], el);
+#pragma unroll
+            for (int t = 0; t < V; ++t) {
+                const uint32_t kk = T::key(el[t]);
+                if ((kk >> sh0) == d) atomicAdd(&h[(kk >> sh1) & m2], 1u);
+            }
+        }
+    }
+    __syncthreads();
+    find_threshold<NT>(h, 1 << b2, need2, s_res, s_warp);
+    const uint32_t key = (d << sh0) | (s_res[0] << sh1);
+    for (int i = tid; i < (1 << b2); i += NT) h[i] = 0u;
+    __syncthreads();
+    return key;
 }
 
 // ---------------------------------------------------------------------------
-// Exact selection over keys held in global memory, split into up to kMaxParts
-// segments that are in column order (a whole row = one segment; the merged
-// candidates of a split row = one segment per part).  Single CTA.  Reads
-// through L2 (ld.global.cg) because other CTAs may have written the segments.
-// min_d0: fail (return false, nothing written) if the first threshold digit is
-// below it.  Writes the k outputs (and, with GATHER, the gathered rows).
+// Exact selection over keys split into up to kMaxParts segments in column
+// order (a whole row in global memory = one segment; the merged candidates of
+// a split row = one segment per part, staged in shared memory or left in the
+// workspace).  Single CTA.  max_tkey: the selection is valid only if every key
+// of the final threshold class is >= max_tkey (each part kept only keys >= its
+// own estimate); otherwise return false before anything is written.  Writes
+// the k outputs (and, with GATHER, the gathered rows).
 // ---------------------------------------------------------------------------
 template <typename E>
 struct Segments {
@@ -461,7 +499,7 @@ struct Segments {
 template <typename E>
 __device__ __forceinline__ E seg_bits(const Segments<E> &sg, int s, uint32_t i)
 {
-    return __ldcg(sg.bits[s] + i);
+    return sg.bits[s][i];  // generic load: the segments are in shared or in global memory
 }
 
 template <typename E>
@@ -471,7 +509,7 @@ __device__ __forceinline__ int64_t seg_col(const Segments<E> &sg, int s, uint32_
 }
 
 template <typename E, int NT, bool GATHER>
-__device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E> &sg, uint32_t min_d0,
+__device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E> &sg, uint32_t max_tkey,
                                  uint32_t *hist, uint32_t *s_res, uint32_t *s_warp, int32_t *glist)
 {
     using T = Elem<E>;
@@ -496,7 +534,7 @@ __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E
         const uint32_t d = s_res[0];
         for (int i = tid; i < nb; i += NT) hist[i] = 0u;
         __syncthreads();
-        if (l == 0 && d < min_d0) return false;
+        if (l == 0 && d < (max_tkey >> nsh)) return false;
         prefix = (l == 0) ? d : ((prefix << bl) | d);
         need -= s_res[1];
         cnt = s_res[2];
@@ -505,6 +543,7 @@ __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E
     const uint32_t P = prefix;
     const int S = shift;
     const uint32_t E_need = need;
+    if ((P << S) < max_tkey) return false;
     // ordered compaction: thread t owns the flat run [t*m, t*m + m)
     const uint32_t m = (total + NT - 1) / NT;
     const uint32_t f0 = min(total, static_cast<uint32_t>(tid) * m), f1 = min(total, f0 + m);
@@ -593,10 +632,9 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
     bool list_ok = false;
     bool exact = false;
     if (sampled) {
-        const uint32_t dt = sample_threshold_digit<NT>(hist, nb0, static_cast<float>(k), static_cast<float>(n), s_res,
-                                                       s_warp);
-        for (int i = tid; i < nb0; i += NT) hist[i] = 0u;
-        const uint32_t tkey = dt << sh0;
+        const uint32_t tkey = sample_threshold_key<E, NT>(a, buf, static_cast<int>((len * sizeof(E)) >> 4),
+                                                          a.sample_step, hist, static_cast<float>(k),
+                                                          static_cast<float>(n), s_res, s_warp);
         L = filter_to_list<E, NT>(a, buf, len, tkey, masks, list, a.list_cap, s_warp);
         list_ok = L <= a.list_cap;
         if (list_ok) {
@@ -820,6 +858,9 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
     __shared__ uint32_t s_res[4];
     __shared__ uint32_t s_last;
     __shared__ Segments<E> s_seg;
+    __shared__ uint32_t s_stage_off[kMaxParts];
+    __shared__ uint32_t s_staged;
+    __shared__ uint64_t s_merge_bar;
 
     const int tid = threadIdx.x;
     const int P = a.parts;
@@ -860,7 +901,8 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
         if (sampled) {
             // this slice's expected share of the k, plus margins
             const float share = static_cast<float>(k) * static_cast<float>(len) / static_cast<float>(n);
-            tkey = sample_threshold_digit<NT>(hist, nb0, share, static_cast<float>(len), s_res, s_warp) << sh0;
+            tkey = sample_threshold_key<E, NT>(a, buf, static_cast<int>((len * sizeof(E)) >> 4), a.sample_step, hist,
+                                               share, static_cast<float>(len), s_res, s_warp);
         }
         L = filter_to_list<E, NT>(a, buf, len, tkey, masks, list, a.list_cap, s_warp);
         const bool fits = L <= a.list_cap;
@@ -894,28 +936,48 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
 
     if (tid == 0) {
         bool ok = true;
-        uint32_t pre = 0, dmax = 0;
+        uint32_t pre = 0, tmax = 0, staged = 0;
         s_seg.n = P;
         for (int p = 0; p < P; ++p) {
             const uint32_t c = __ldcg(w_count + p);
             const uint32_t tk = __ldcg(w_tkey + p);
             if (c == 0xffffffffu) ok = false;
+            const uint32_t cc = ok ? c : 0u;
             unsigned char *wp = wrow + a.ws_head_bytes + static_cast<int64_t>(p) * a.ws_part_bytes;
             s_seg.bits[p] = reinterpret_cast<const E *>(wp);
             s_seg.cols[p] = reinterpret_cast<const int32_t *>(wp + a.ws_bits_bytes);
             s_seg.base[p] = 0;
             s_seg.pre[p] = pre;
-            pre += ok ? c : 0u;
-            dmax = max(dmax, tk >> sh0);
+            s_stage_off[p] = staged;
+            pre += cc;
+            staged += (cc * static_cast<uint32_t>(sizeof(E)) + 15u) & ~15u;
+            tmax = max(tmax, tk);
         }
         s_seg.pre[P] = pre;
         if (pre < static_cast<uint32_t>(k)) ok = false;
-        s_res[3] = ok ? (dmax + 1u) : 0u;  // 0: go straight to the exact row path
+        s_res[3] = ok ? 1u : 0u;
+        s_res[2] = tmax;
+        // candidate keys -> shared memory (one bulk copy per part) when they fit in front of the histogram
+        s_staged = (ok && staged <= a.smem_hist_off) ? staged : 0u;
+        if (s_staged) {
+            fence_proxy_async_global();  // the parts' candidate stores -> this bulk copy's reads
+            mbar_init(&s_merge_bar, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&s_merge_bar, staged);
+            for (int p = 0; p < P; ++p) {
+                const uint32_t bytes = (s_seg.pre[p + 1] - s_seg.pre[p]) * static_cast<uint32_t>(sizeof(E));
+                const uint32_t padded = (bytes + 15u) & ~15u;
+                if (padded) bulk_load(smem + s_stage_off[p], s_seg.bits[p], padded, &s_merge_bar);
+                s_seg.bits[p] = reinterpret_cast<const E *>(smem + s_stage_off[p]);
+            }
+        }
     }
     __syncthreads();
-    const uint32_t min_d0 = s_res[3];
+    if (s_staged) wait_phase(&s_merge_bar, 0u, a.err_flag);
+    const bool cand_ok = s_res[3] != 0u;
+    const uint32_t max_tkey = s_res[2];
     bool done = false;
-    if (min_d0 != 0u) done = select_segments<E, NT, GATHER>(a, row, s_seg, min_d0 - 1u, hist, s_res, s_warp, glist);
+    if (cand_ok) done = select_segments<E, NT, GATHER>(a, row, s_seg, max_tkey, hist, s_res, s_warp, glist);
     if (!done) {
         __syncthreads();
         if (tid == 0) {
