@@ -7,7 +7,9 @@
 // (ties: smaller column first), or, when n <= k, every valid column followed
 // by fills (index -1, value -inf).  Rows with n > k are checked for NaN.
 //
-// Three kernels, chosen per launch by the host plan:
+// Four kernels, chosen per launch by the host plan:
+//   warp_kernel   one warp per short row (<= 2048 bf16 / 1024 fp32), staged in
+//                 the warp's own shared memory; no CTA-wide barrier.
 //   row_kernel    one CTA per row; the row is staged whole in shared memory.
 //   split_kernel  a wide row is cut into `parts` slices, one CTA each.  Every
 //                 CTA filters its slice down to an index-ordered candidate
@@ -68,6 +70,17 @@ struct Elem<uint32_t> {  // fp32 bit patterns
     static constexpr uint32_t kInfMagnitude = 0x7f800000u;
     static __device__ __forceinline__ uint32_t magnitude(uint32_t u) { return u & 0x7fffffffu; }
     static __device__ __forceinline__ bool is_nan(uint32_t u) { return (u & 0x7fffffffu) > 0x7f800000u; }
+    static constexpr uint32_t kSignKey = 0x80000000u;  // key of +0 and -0
+    // Bit t set when key(element t) >= tkey, for a threshold above +/-0 (tkey > kSignKey), where
+    // that is a signed compare of the raw bits with ts = tkey ^ kSignKey; folds |x| into mag.
+    static __device__ __forceinline__ uint32_t ge_mask_positive(const uint4 &q, uint32_t ts, uint32_t &mag)
+    {
+        const int t = static_cast<int>(ts);
+        mag = max(mag, max(max(q.x & 0x7fffffffu, q.y & 0x7fffffffu), max(q.z & 0x7fffffffu, q.w & 0x7fffffffu)));
+        return static_cast<uint32_t>(static_cast<int>(q.x) >= t) | (static_cast<uint32_t>(static_cast<int>(q.y) >= t) << 1) |
+               (static_cast<uint32_t>(static_cast<int>(q.z) >= t) << 2) |
+               (static_cast<uint32_t>(static_cast<int>(q.w) >= t) << 3);
+    }
     static __device__ __forceinline__ void unpack(const uint4 &q, uint32_t (&e)[4])
     {
         e[0] = q.x;
@@ -75,6 +88,7 @@ struct Elem<uint32_t> {  // fp32 bit patterns
         e[2] = q.z;
         e[3] = q.w;
     }
+    static __device__ __forceinline__ uint4 pack(const uint32_t (&e)[4]) { return make_uint4(e[0], e[1], e[2], e[3]); }
 };
 
 template <>
@@ -91,6 +105,22 @@ struct Elem<uint16_t> {  // bf16 bit patterns
     static constexpr uint32_t kInfMagnitude = 0x7f80u;
     static __device__ __forceinline__ uint32_t magnitude(uint16_t h) { return h & 0x7fffu; }
     static __device__ __forceinline__ bool is_nan(uint16_t h) { return (h & 0x7fffu) > 0x7f80u; }
+    static constexpr uint32_t kSignKey = 0x8000u;  // key of +0 and -0
+    // As for fp32, on the two 16-bit halves of each word (element 2i low, 2i+1 high).
+    static __device__ __forceinline__ uint32_t ge_mask_positive(const uint4 &q, uint32_t ts, uint32_t &mag)
+    {
+        const int t = static_cast<int>(ts << 16);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        uint32_t m = 0, mm = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            m |= static_cast<uint32_t>(static_cast<int>(w[i] << 16) >= t) << (2 * i);
+            m |= static_cast<uint32_t>(static_cast<int>(w[i] & 0xffff0000u) >= t) << (2 * i + 1);
+            mm = __vmaxu2(mm, w[i] & 0x7fff7fffu);
+        }
+        mag = max(mag, max(mm & 0xffffu, mm >> 16));
+        return m;
+    }
     static __device__ __forceinline__ void unpack(const uint4 &q, uint16_t (&e)[8])
     {
         e[0] = (uint16_t)(q.x & 0xffffu);
@@ -101,6 +131,11 @@ struct Elem<uint16_t> {  // bf16 bit patterns
         e[5] = (uint16_t)(q.z >> 16);
         e[6] = (uint16_t)(q.w & 0xffffu);
         e[7] = (uint16_t)(q.w >> 16);
+    }
+    static __device__ __forceinline__ uint4 pack(const uint16_t (&e)[8])
+    {
+        return make_uint4(e[0] | (static_cast<uint32_t>(e[1]) << 16), e[2] | (static_cast<uint32_t>(e[3]) << 16),
+                          e[4] | (static_cast<uint32_t>(e[5]) << 16), e[6] | (static_cast<uint32_t>(e[7]) << 16));
     }
 };
 
@@ -372,18 +407,26 @@ __device__ int filter_to_list(const TopkArgs &a, const E *buf, int len, uint32_t
     const int nvt = (len + V - 1) / V;
     const uint4 *vbuf = reinterpret_cast<const uint4 *>(buf);
     uint32_t mag = 0;  // largest |x| bit pattern: a NaN iff above the infinity pattern
+    const bool positive = tkey > T::kSignKey;  // raw-bit compare suffices above +/-0
+    const uint32_t ts = tkey ^ T::kSignKey;
+    const int nfull = len / V;                 // vectors with every element in range
     for (int base = warp * 32; base < nvt; base += NT) {
         const int v = base + lane;
         if (v < nvt) {
-            E el[V];
-            T::unpack(vbuf[v], el);
-            const int lim = min(V, len - v * V);
+            const uint4 q = vbuf[v];
             uint32_t m = 0;
+            if (positive && v < nfull) {
+                m = T::ge_mask_positive(q, ts, mag);
+            } else {
+                E el[V];
+                T::unpack(q, el);
+                const int lim = min(V, len - v * V);
 #pragma unroll
-            for (int t = 0; t < V; ++t) {
-                const bool in = t < lim;
-                mag = max(mag, in ? T::magnitude(el[t]) : 0u);
-                m |= static_cast<uint32_t>(in && T::key(el[t]) >= tkey) << t;
+                for (int t = 0; t < V; ++t) {
+                    const bool in = t < lim;
+                    mag = max(mag, in ? T::magnitude(el[t]) : 0u);
+                    m |= static_cast<uint32_t>(in && T::key(el[t]) >= tkey) << t;
+                }
             }
             masks[v] = static_cast<uint8_t>(m);
         }
@@ -1032,6 +1075,227 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) stream_kernel(const 
     select_segments<E, NT, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
 }
 
+// ---------------------------------------------------------------------------
+// warp_kernel: one warp per short row (at most kWarpRowVecs 16-byte vectors:
+// 2048 bf16 / 1024 fp32).  Each warp stages its row in its own slice of
+// shared memory and synchronises only with itself: 8-bit radix levels on a
+// per-warp histogram, ordered compaction by warp scans, then the fused gather
+// of the selected key rows.  grid = ceil(rows / warps per CTA).
+// Shared memory: W rows of kWarpRowVecs vectors | W x 256 bins | W x n_gather gather list.
+// ---------------------------------------------------------------------------
+constexpr int kWarpRowVecs = 256;
+
+template <typename E, int NT, bool GATHER>
+__global__ void __launch_bounds__(NT) warp_kernel(const TopkArgs a)
+{
+    using T = Elem<E>;
+    constexpr int V = T::V;
+    constexpr int W = NT / 32;
+    constexpr int kBins = 256;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * W + warp;
+    if (row >= a.rows) return;
+    uint4 *rbuf = reinterpret_cast<uint4 *>(smem) + warp * kWarpRowVecs;
+    uint32_t *h = reinterpret_cast<uint32_t *>(smem + W * kWarpRowVecs * 16) + warp * kBins;
+    int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + W * kWarpRowVecs * 16 + W * kBins * 4) +
+                                  static_cast<int64_t>(warp) * a.n_gather
+                            : nullptr;
+    const int64_t n64 = valid_cols(a, row);
+    const int k = a.k;
+    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
+    if (n64 <= k) {  // short row, by this warp
+        for (int j = lane; j < k; j += 32) {
+            store_idx(a, row, j, j < n64 ? j : -1);
+            if (a.want_values) store_val<E>(a, row, j, j < n64 ? xrow[j] : static_cast<E>(T::kFill));
+            if (GATHER && j < a.n_gather) glist[j] = j < n64 ? j : 0;
+        }
+    } else {
+        const int n = static_cast<int>(n64);
+        const int nfull = n / V;
+        const int nvt = (n + V - 1) / V;
+        // stage: full vectors with 16-byte loads (8 in flight per lane), the tail element by element
+        for (int v0 = 0; v0 < nfull; v0 += 8 * 32) {
+            uint4 q[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < nfull) q[u] = __ldg(reinterpret_cast<const uint4 *>(xrow) + v);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < nfull) rbuf[v] = q[u];
+            }
+        }
+        if (nfull < nvt && lane == 0) {
+            E el[V];
+#pragma unroll
+            for (int t = 0; t < V; ++t) el[t] = (nfull * V + t < n) ? xrow[nfull * V + t] : static_cast<E>(0);
+            rbuf[nfull] = T::pack(el);
+        }
+        for (int b = lane; b < kBins; b += 32) h[b] = 0u;
+        __syncwarp();
+        // level 0 histogram + NaN check
+        uint32_t mag = 0;
+        const int sh0 = T::KB - 8;
+        for (int v = lane; v < nvt; v += 32) {
+            E el[V];
+            T::unpack(rbuf[v], el);
+            const int lim = min(V, n - v * V);
+#pragma unroll
+            for (int t = 0; t < V; ++t) {
+                if (t < lim) {
+                    mag = max(mag, T::magnitude(el[t]));
+                    atomicAdd(&h[T::key(el[t]) >> sh0], 1u);
+                }
+            }
+        }
+        if (__any_sync(kFull, mag > T::kInfMagnitude) && lane == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
+        uint32_t prefix = 0, need = static_cast<uint32_t>(k), cnt = 0;
+        int shift = T::KB;
+        for (int l = 0; l < T::KB / 8; ++l) {
+            const int nsh = shift - 8;
+            if (l > 0) {
+                for (int v = lane; v < nvt; v += 32) {
+                    E el[V];
+                    T::unpack(rbuf[v], el);
+                    const int lim = min(V, n - v * V);
+#pragma unroll
+                    for (int t = 0; t < V; ++t) {
+                        const uint32_t kk = T::key(el[t]);
+                        if (t < lim && (kk >> shift) == prefix) atomicAdd(&h[(kk >> nsh) & 0xffu], 1u);
+                    }
+                }
+            }
+            __syncwarp();
+            // threshold digit: lane l owns bins [8l, 8l + 8); counts above come from a reversed scan
+            uint32_t c[8], s = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                c[j] = h[lane * 8 + j];
+                s += c[j];
+            }
+            uint32_t inc = s;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_down_sync(kFull, inc, o);
+                if (lane + o < 32) inc += y;
+            }
+            const uint32_t above_lane = inc - s;
+            const bool mine = above_lane < need && inc >= need;
+            uint32_t d = 0, above = 0, dc = 0;
+            if (mine) {
+                uint32_t acc = above_lane;
+                bool found = false;
+#pragma unroll
+                for (int j = 7; j >= 0; --j) {
+                    if (!found) {
+                        if (acc + c[j] >= need) {
+                            d = static_cast<uint32_t>(lane * 8 + j);
+                            above = acc;
+                            dc = c[j];
+                            found = true;
+                        } else {
+                            acc += c[j];
+                        }
+                    }
+                }
+            }
+            const int src = __ffs(__ballot_sync(kFull, mine)) - 1;
+            d = __shfl_sync(kFull, d, src);
+            above = __shfl_sync(kFull, above, src);
+            dc = __shfl_sync(kFull, dc, src);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) h[lane * 8 + j] = 0u;
+            __syncwarp();
+            prefix = (l == 0) ? d : ((prefix << 8) | d);
+            need -= above;
+            cnt = dc;
+            shift = nsh;
+            if (cnt == need) break;
+        }
+        const uint32_t P = prefix;
+        const int S = shift;
+        const uint32_t E_need = need;
+        // ordered compaction: in iteration i lane l holds vector 32i + l, so (i, l, t) is column order
+        uint32_t eq_run = 0, sel_run = 0;
+        for (int v0 = 0; v0 < nvt; v0 += 32) {
+            const int v = v0 + lane;
+            uint32_t gm = 0, qm = 0;
+            E el[V];
+            if (v < nvt) {
+                T::unpack(rbuf[v], el);
+                const int lim = min(V, n - v * V);
+#pragma unroll
+                for (int t = 0; t < V; ++t) {
+                    if (t < lim) {
+                        const uint32_t cc = T::key(el[t]) >> S;
+                        gm |= static_cast<uint32_t>(cc > P) << t;
+                        qm |= static_cast<uint32_t>(cc == P) << t;
+                    }
+                }
+            }
+            if (!__any_sync(kFull, (gm | qm) != 0u)) continue;
+            uint32_t tq;
+            uint32_t r = eq_run + warp_exclusive_scan(static_cast<uint32_t>(__popc(qm)), lane, tq);
+            uint32_t sm = gm;
+#pragma unroll
+            for (int t = 0; t < V; ++t) {
+                if ((qm >> t) & 1u) {
+                    if (r < E_need) sm |= 1u << t;
+                    ++r;
+                }
+            }
+            uint32_t ts;
+            uint32_t pos = sel_run + warp_exclusive_scan(static_cast<uint32_t>(__popc(sm)), lane, ts);
+#pragma unroll
+            for (int t = 0; t < V; ++t) {
+                if ((sm >> t) & 1u) {
+                    const int col = v * V + t;
+                    store_idx(a, row, pos, col);
+                    if (a.want_values) store_val<E>(a, row, pos, el[t]);
+                    if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = col;
+                    ++pos;
+                }
+            }
+            eq_run += tq;
+            sel_run += ts;
+        }
+    }
+    if (GATHER) {
+        __syncwarp();
+        const int vpr = static_cast<int>(a.d >> 3);
+        const int vsh = (vpr & (vpr - 1)) == 0 ? __ffs(vpr) - 1 : -1;
+        const uint16_t *kb = a.key + (row / a.rows_per_batch) * a.key_batch_stride;
+        uint4 *ob = reinterpret_cast<uint4 *>(a.gather_out + row * a.n_gather * a.d);
+        const int total = static_cast<int>(a.n_gather) * vpr;
+        constexpr int U = 4;
+        for (int t0 = lane; t0 < total; t0 += U * 32) {
+            uint4 val[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = t0 + u * 32;
+                val[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (t < total) {
+                    const int jj = vsh >= 0 ? (t >> vsh) : t / vpr;
+                    int64_t p = glist[jj];
+                    if (p < 0) p = 0;
+                    if (p < a.comp_len)
+                        val[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + (t - jj * vpr));
+                    else if (t - jj * vpr == 0)
+                        set_err(a.err_flag, kStatusInval);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = t0 + u * 32;
+                if (t < total) __stcs(ob + t, val[u]);
+            }
+        }
+    }
+}
+
 // Raises a kernel's dynamic shared-memory limit once per device; later calls that need no more
 // than what was set skip the driver call.
 template <typename K>
@@ -1054,9 +1318,11 @@ template <typename E, int NT, bool G>
 cudaError_t launch_one(int mode, size_t smem, const TopkArgs &a, cudaStream_t stream, int64_t grid, bool query,
                        int *blocks_per_sm)
 {
-    static int set_row[64] = {}, set_split[64] = {}, set_stream[64] = {};
+    static int set_row[64] = {}, set_split[64] = {}, set_stream[64] = {}, set_warp[64] = {};
     cudaError_t e;
-    if (mode == kModeRow)
+    if (mode == kModeWarp)
+        e = raise_smem_limit(warp_kernel<E, NT, G>, set_warp, smem);
+    else if (mode == kModeRow)
         e = raise_smem_limit(row_kernel<E, NT, G>, set_row, smem);
     else if (mode == kModeSplit)
         e = raise_smem_limit(split_kernel<E, NT, G>, set_split, smem);
@@ -1064,6 +1330,8 @@ cudaError_t launch_one(int mode, size_t smem, const TopkArgs &a, cudaStream_t st
         e = raise_smem_limit(stream_kernel<E, NT, G>, set_stream, smem);
     if (e != cudaSuccess) return e;
     if (query) {
+        if (mode == kModeWarp)
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, warp_kernel<E, NT, G>, NT, smem);
         if (mode == kModeRow)
             return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, row_kernel<E, NT, G>, NT, smem);
         if (mode == kModeSplit)
@@ -1073,7 +1341,9 @@ cudaError_t launch_one(int mode, size_t smem, const TopkArgs &a, cudaStream_t st
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
     const dim3 g(static_cast<unsigned>(grid)), b(NT);
-    if (mode == kModeRow)
+    if (mode == kModeWarp)
+        warp_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
+    else if (mode == kModeRow)
         row_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
     else if (mode == kModeSplit)
         split_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
@@ -1089,6 +1359,11 @@ cudaError_t launch_e(int mode, int threads, bool gather, size_t smem, const Topk
                      int64_t grid, bool query, int *blocks_per_sm)
 {
     if (mode == kModeSplit) {
+        if (threads != 256) return cudaErrorInvalidValue;
+        return gather ? launch_one<E, 256, true>(mode, smem, a, s, grid, query, blocks_per_sm)
+                      : launch_one<E, 256, false>(mode, smem, a, s, grid, query, blocks_per_sm);
+    }
+    if (mode == kModeWarp) {
         if (threads != 256) return cudaErrorInvalidValue;
         return gather ? launch_one<E, 256, true>(mode, smem, a, s, grid, query, blocks_per_sm)
                       : launch_one<E, 256, false>(mode, smem, a, s, grid, query, blocks_per_sm);
