@@ -172,6 +172,15 @@ __device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t digit, bool va
     }
 }
 
+// Warp-aggregated shared histogram increment: lanes with equal digits are grouped with
+// __match_any_sync and only the group leader adds the group's size.  For digits that pile
+// up on few bins (candidates near the threshold, tie-heavy classes).  All 32 lanes must call.
+__device__ __forceinline__ void hist_add_grouped(uint32_t *hist, uint32_t digit, bool valid, int lane)
+{
+    const unsigned peers = __match_any_sync(kFull, valid ? digit : 0xffffffffu);
+    if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
+}
+
 __device__ __forceinline__ uint32_t warp_exclusive_scan(uint32_t v, int lane, uint32_t &total)
 {
     uint32_t inc = v;
@@ -565,11 +574,14 @@ __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E
         const int nsh = shift - bl;
         const int nb = 1 << bl;
         const uint32_t mask = static_cast<uint32_t>(nb - 1);
+        const int lane = tid & 31;
         for (int s = 0; s < sg.n; ++s) {
             const uint32_t cs = sg.pre[s + 1] - sg.pre[s];
-            for (uint32_t i = tid; i < cs; i += NT) {
-                const uint32_t kk = T::key(seg_bits(sg, s, i));
-                if (l == 0 || (kk >> shift) == prefix) atomicAdd(&hist[(kk >> nsh) & mask], 1u);
+            for (uint32_t b = tid & ~31u; b < cs; b += NT) {  // warp-uniform trip count
+                const uint32_t i = b + lane;
+                const bool in = i < cs;
+                const uint32_t kk = in ? T::key(seg_bits(sg, s, i)) : 0u;
+                hist_add_grouped(hist, (kk >> nsh) & mask, in && (l == 0 || (kk >> shift) == prefix), lane);
             }
         }
         __syncthreads();
@@ -607,6 +619,11 @@ __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E
     const uint32_t sel = g + take_from_ties(E_need, r, q);
     uint32_t ts;
     uint32_t pos = block_exclusive_scan<NT>(sel, s_warp, ts);
+    // The histogram is free now.  When it can hold a 16-bit source index per output position,
+    // record which entry lands where, then write the outputs position by position: the column
+    // loads are independent (many in flight) and the stores coalesce.
+    const bool by_position = total <= 65535u && static_cast<uint32_t>(a.k) <= 2u * static_cast<uint32_t>(a.hist_bins);
+    uint16_t *src = reinterpret_cast<uint16_t *>(hist);
     {
         int s = s0;
         for (uint32_t f = f0; f < f1; ++f) {
@@ -617,11 +634,48 @@ __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E
             bool take = c > P;
             if (c == P) take = (r++ < E_need);
             if (take) {
-                const int64_t col = seg_col(sg, s, i);
-                store_idx(a, row, pos, col);
-                if (a.want_values) store_val<E>(a, row, pos, e);
-                if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = static_cast<int32_t>(col);
+                if (by_position) {
+                    src[pos] = static_cast<uint16_t>(f);
+                } else {
+                    const int64_t col = seg_col(sg, s, i);
+                    store_idx(a, row, pos, col);
+                    if (a.want_values) store_val<E>(a, row, pos, e);
+                    if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = static_cast<int32_t>(col);
+                }
                 ++pos;
+            }
+        }
+    }
+    if (by_position) {
+        __syncthreads();
+        constexpr int U = 4;
+        for (int j0 = tid; j0 < a.k; j0 += U * NT) {
+            int64_t col[U];
+            E val[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + u * NT;
+                if (j < a.k) {
+                    const uint32_t f = src[j];
+                    int lo = 0, hi = sg.n - 1;  // the segment holding flat index f
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (sg.pre[mid] <= f) lo = mid;
+                        else hi = mid - 1;
+                    }
+                    const uint32_t i = f - sg.pre[lo];
+                    val[u] = seg_bits(sg, lo, i);
+                    col[u] = seg_col(sg, lo, i);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + u * NT;
+                if (j < a.k) {
+                    store_idx(a, row, j, col[u]);
+                    if (a.want_values) store_val<E>(a, row, j, val[u]);
+                    if (GATHER && j < a.n_gather) glist[j] = static_cast<int32_t>(col[u]);
+                }
             }
         }
     }
@@ -681,7 +735,11 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
         L = filter_to_list<E, NT>(a, buf, len, tkey, masks, list, a.list_cap, s_warp);
         list_ok = L <= a.list_cap;
         if (list_ok) {
-            for (int i = tid; i < L; i += NT) atomicAdd(&hist[T::key(buf[list[i]]) >> sh0], 1u);
+            for (int b = warp * 32; b < L; b += NT) {
+                const int i = b + lane;
+                const bool in = i < L;
+                hist_add_grouped(hist, in ? T::key(buf[list[i]]) >> sh0 : 0u, in, lane);
+            }
         } else {
             const int nvt = (len + V - 1) / V;
             for (int base = warp * 32; base < nvt; base += NT) {
@@ -737,9 +795,11 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
         const int nb = 1 << bl;
         const uint32_t mask = static_cast<uint32_t>(nb - 1);
         if (list_ok) {
-            for (int i = tid; i < L; i += NT) {
-                const uint32_t kk = T::key(buf[list[i]]);
-                if ((kk >> shift) == prefix) atomicAdd(&hist[(kk >> nsh) & mask], 1u);
+            for (int b = warp * 32; b < L; b += NT) {
+                const int i = b + lane;
+                const bool in = i < L;
+                const uint32_t kk = in ? T::key(buf[list[i]]) : 0u;
+                hist_add_grouped(hist, (kk >> nsh) & mask, in && (kk >> shift) == prefix, lane);
             }
         } else {
             for (int base = warp * 32; base < nvt; base += NT) {
@@ -977,41 +1037,73 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
     if (!s_last) return;
     __threadfence();
 
-    if (tid == 0) {
-        bool ok = true;
-        uint32_t pre = 0, tmax = 0, staged = 0;
-        s_seg.n = P;
-        for (int p = 0; p < P; ++p) {
-            const uint32_t c = __ldcg(w_count + p);
-            const uint32_t tk = __ldcg(w_tkey + p);
-            if (c == 0xffffffffu) ok = false;
-            const uint32_t cc = ok ? c : 0u;
-            unsigned char *wp = wrow + a.ws_head_bytes + static_cast<int64_t>(p) * a.ws_part_bytes;
-            s_seg.bits[p] = reinterpret_cast<const E *>(wp);
-            s_seg.cols[p] = reinterpret_cast<const int32_t *>(wp + a.ws_bits_bytes);
-            s_seg.base[p] = 0;
-            s_seg.pre[p] = pre;
-            s_stage_off[p] = staged;
-            pre += cc;
-            staged += (cc * static_cast<uint32_t>(sizeof(E)) + 15u) & ~15u;
-            tmax = max(tmax, tk);
+    if (tid < 32) {
+        // warp 0 reads the parts' counts (lane p and p + 32) and lays out the merged segments
+        const int lane = tid;
+        uint32_t c[2], tk[2], bytes[2];
+        bool bad = false;
+        uint32_t tmax = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int p = lane + 32 * h;
+            c[h] = 0u;
+            tk[h] = 0u;
+            if (p < P) {
+                c[h] = __ldcg(w_count + p);
+                tk[h] = __ldcg(w_tkey + p);
+                if (c[h] == 0xffffffffu) bad = true;
+            }
+            tmax = max(tmax, tk[h]);
         }
-        s_seg.pre[P] = pre;
-        if (pre < static_cast<uint32_t>(k)) ok = false;
-        s_res[3] = ok ? 1u : 0u;
-        s_res[2] = tmax;
-        // candidate keys -> shared memory (one bulk copy per part) when they fit in front of the histogram
-        s_staged = (ok && staged <= a.smem_hist_off) ? staged : 0u;
+        bad = __any_sync(kFull, bad);
+        tmax = __reduce_max_sync(kFull, tmax);
+        uint32_t pre_base = 0, off_base = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int p = lane + 32 * h;
+            const uint32_t cc = bad ? 0u : c[h];
+            bytes[h] = (cc * static_cast<uint32_t>(sizeof(E)) + 15u) & ~15u;
+            uint32_t tot_c, tot_b;
+            const uint32_t xc = warp_exclusive_scan(cc, lane, tot_c);
+            const uint32_t xb = warp_exclusive_scan(bytes[h], lane, tot_b);
+            if (p < P) {
+                unsigned char *wp = wrow + a.ws_head_bytes + static_cast<int64_t>(p) * a.ws_part_bytes;
+                s_seg.bits[p] = reinterpret_cast<const E *>(wp);
+                s_seg.cols[p] = reinterpret_cast<const int32_t *>(wp + a.ws_bits_bytes);
+                s_seg.base[p] = 0;
+                s_seg.pre[p] = pre_base + xc;
+                s_stage_off[p] = off_base + xb;
+            }
+            pre_base += tot_c;
+            off_base += tot_b;
+        }
+        if (lane == 0) {
+            s_seg.n = P;
+            s_seg.pre[P] = pre_base;
+            const bool ok = !bad && pre_base >= static_cast<uint32_t>(k);
+            s_res[3] = ok ? 1u : 0u;
+            s_res[2] = tmax;
+            // candidate keys -> shared memory when they fit in front of the histogram
+            s_staged = (ok && off_base <= a.smem_hist_off) ? off_base : 0u;
+            if (s_staged) {
+                fence_proxy_async_global();  // the parts' candidate stores -> the bulk copies' reads
+                mbar_init(&s_merge_bar, 1);
+                fence_mbar_init();
+                mbar_arrive_expect_tx(&s_merge_bar, off_base);
+            }
+        }
+        __syncwarp();
         if (s_staged) {
-            fence_proxy_async_global();  // the parts' candidate stores -> this bulk copy's reads
-            mbar_init(&s_merge_bar, 1);
-            fence_mbar_init();
-            mbar_arrive_expect_tx(&s_merge_bar, staged);
-            for (int p = 0; p < P; ++p) {
-                const uint32_t bytes = (s_seg.pre[p + 1] - s_seg.pre[p]) * static_cast<uint32_t>(sizeof(E));
-                const uint32_t padded = (bytes + 15u) & ~15u;
-                if (padded) bulk_load(smem + s_stage_off[p], s_seg.bits[p], padded, &s_merge_bar);
-                s_seg.bits[p] = reinterpret_cast<const E *>(smem + s_stage_off[p]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int p = lane + 32 * h;
+                if (p < P) {
+                    if (bytes[h]) {
+                        fence_proxy_async_global();
+                        bulk_load(smem + s_stage_off[p], s_seg.bits[p], bytes[h], &s_merge_bar);
+                    }
+                    s_seg.bits[p] = reinterpret_cast<const E *>(smem + s_stage_off[p]);
+                }
             }
         }
     }
@@ -1139,16 +1231,15 @@ __global__ void __launch_bounds__(NT) warp_kernel(const TopkArgs a)
         // level 0 histogram + NaN check
         uint32_t mag = 0;
         const int sh0 = T::KB - 8;
-        for (int v = lane; v < nvt; v += 32) {
+        for (int v0 = 0; v0 < nvt; v0 += 32) {  // warp-uniform: the grouped adds need every lane
+            const int v = v0 + lane;
             E el[V];
-            T::unpack(rbuf[v], el);
-            const int lim = min(V, n - v * V);
+            T::unpack(v < nvt ? rbuf[v] : make_uint4(0u, 0u, 0u, 0u), el);
+            const int lim = v < nvt ? min(V, n - v * V) : 0;
 #pragma unroll
             for (int t = 0; t < V; ++t) {
-                if (t < lim) {
-                    mag = max(mag, T::magnitude(el[t]));
-                    atomicAdd(&h[T::key(el[t]) >> sh0], 1u);
-                }
+                if (t < lim) mag = max(mag, T::magnitude(el[t]));
+                hist_add_grouped(h, T::key(el[t]) >> sh0, t < lim, lane);
             }
         }
         if (__any_sync(kFull, mag > T::kInfMagnitude) && lane == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
@@ -1157,14 +1248,15 @@ __global__ void __launch_bounds__(NT) warp_kernel(const TopkArgs a)
         for (int l = 0; l < T::KB / 8; ++l) {
             const int nsh = shift - 8;
             if (l > 0) {
-                for (int v = lane; v < nvt; v += 32) {
+                for (int v0 = 0; v0 < nvt; v0 += 32) {
+                    const int v = v0 + lane;
                     E el[V];
-                    T::unpack(rbuf[v], el);
-                    const int lim = min(V, n - v * V);
+                    T::unpack(v < nvt ? rbuf[v] : make_uint4(0u, 0u, 0u, 0u), el);
+                    const int lim = v < nvt ? min(V, n - v * V) : 0;
 #pragma unroll
                     for (int t = 0; t < V; ++t) {
                         const uint32_t kk = T::key(el[t]);
-                        if (t < lim && (kk >> shift) == prefix) atomicAdd(&h[(kk >> nsh) & 0xffu], 1u);
+                        hist_add_grouped(h, (kk >> nsh) & 0xffu, t < lim && (kk >> shift) == prefix, lane);
                     }
                 }
             }
