@@ -154,20 +154,6 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
     const int64_t row_bytes = c1 * e;
     const int64_t max_staged = std::min<int64_t>(sel::kMaxSlice, sel::kMaxChunks * sel::kChunkBytes / e);
 
-    // short rows: one warp per row (8 warps per CTA), each staged in the warp's own shared memory
-    if (c1 * e <= 256 * 16) {
-        Plan wp = p;
-        const size_t smem = static_cast<size_t>(8 * (256 * 16 + 256 * 4)) + (gather ? static_cast<size_t>(8 * n_gather * 4) : 0);
-        if (smem <= limit && cached_blocks_per_sm(dtype, sel::kModeWarp, 256, gather, smem) > 0) {
-            wp.mode = sel::kModeWarp;
-            wp.threads = 256;
-            wp.smem = smem;
-            wp.grid = ceil_div(rows, 8);
-            wp.ws_bytes = 0;
-            p = wp;
-            return SEL_OK;
-        }
-    }
     // one CTA per row, the row staged whole
     bool row_ok = false;
     Plan row_plan = p;

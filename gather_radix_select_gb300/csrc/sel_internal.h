@@ -17,7 +17,6 @@ constexpr int kMaxParts = 64;       // CTAs splitting one row (split_kernel)
 constexpr int kModeRow = 0;         // row_kernel: one CTA per row, row staged in shared memory
 constexpr int kModeSplit = 1;       // split_kernel: `parts` CTAs per row + last-arriver merge
 constexpr int kModeStream = 2;      // stream_kernel: one CTA per row, passes read global memory
-constexpr int kModeWarp = 3;        // warp_kernel: one warp per short row
 constexpr int kGatherThreads = 256;
 
 // Everything one selection launch needs; passed by value (kernel parameter space).

@@ -7,9 +7,7 @@
 // (ties: smaller column first), or, when n <= k, every valid column followed
 // by fills (index -1, value -inf).  Rows with n > k are checked for NaN.
 //
-// Four kernels, chosen per launch by the host plan:
-//   warp_kernel   one warp per short row (<= 2048 bf16 / 1024 fp32), staged in
-//                 the warp's own shared memory; no CTA-wide barrier.
+// Three kernels, chosen per launch by the host plan:
 //   row_kernel    one CTA per row; the row is staged whole in shared memory.
 //   split_kernel  a wide row is cut into `parts` slices, one CTA each.  Every
 //                 CTA filters its slice down to an index-ordered candidate
@@ -686,6 +684,161 @@ __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E
     return true;
 }
 
+// The merged candidates of a split row after staging: segment s's keys sit in shared memory at
+// byte offset stage_off[s] (16-byte aligned), the segments back to back.  Same result as
+// select_segments, but every pass walks 16-byte vectors of the staged bytes (V keys at once)
+// instead of single elements; the segment of a vector comes from a short binary search.
+template <typename E, int NT, bool GATHER>
+__device__ bool select_staged(const TopkArgs &a, int64_t row, const Segments<E> &sg, const uint32_t *stage_off,
+                              uint32_t staged_bytes, const unsigned char *stage, uint32_t max_tkey, uint32_t *hist,
+                              uint32_t *s_res, uint32_t *s_warp, int32_t *glist)
+{
+    using T = Elem<E>;
+    constexpr int V = T::V;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int nvec = static_cast<int>(staged_bytes >> 4);
+    const uint4 *sv = reinterpret_cast<const uint4 *>(stage);
+    // segment of staged vector v and the number of its keys that are real (< V in a segment's last vector)
+    auto locate = [&](int v, int &seg, int &first) {
+        int lo = 0, hi = sg.n - 1;
+        const uint32_t byte = static_cast<uint32_t>(v) << 4;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (stage_off[mid] <= byte) lo = mid;
+            else hi = mid - 1;
+        }
+        seg = lo;
+        first = static_cast<int>((byte - stage_off[lo]) / sizeof(E));  // index of the vector's first key
+        const int count = static_cast<int>(sg.pre[lo + 1] - sg.pre[lo]);
+        return min(V, count - first);
+    };
+    uint32_t prefix = 0, need = static_cast<uint32_t>(a.k), cnt = 0;
+    int shift = T::KB;
+    for (int l = 0; l < a.nlevels && (l == 0 || cnt != need); ++l) {
+        const int bl = a.bits[l];
+        const int nsh = shift - bl;
+        const int nb = 1 << bl;
+        const uint32_t mask = static_cast<uint32_t>(nb - 1);
+        for (int b = tid & ~31; b < nvec; b += NT) {  // warp-uniform trip count
+            const int v = b + lane;
+            int seg = 0, first = 0, lim = 0;
+            E el[V];
+            if (v < nvec) lim = locate(v, seg, first);
+            T::unpack(v < nvec ? sv[v] : make_uint4(0u, 0u, 0u, 0u), el);
+#pragma unroll
+            for (int t = 0; t < V; ++t) {
+                const uint32_t kk = T::key(el[t]);
+                hist_add_grouped(hist, (kk >> nsh) & mask, t < lim && (l == 0 || (kk >> shift) == prefix), lane);
+            }
+        }
+        __syncthreads();
+        find_threshold<NT>(hist, nb, need, s_res, s_warp);
+        const uint32_t d = s_res[0];
+        for (int i = tid; i < nb; i += NT) hist[i] = 0u;
+        __syncthreads();
+        if (l == 0 && d < (max_tkey >> nsh)) return false;
+        prefix = (l == 0) ? d : ((prefix << bl) | d);
+        need -= s_res[1];
+        cnt = s_res[2];
+        shift = nsh;
+    }
+    const uint32_t P = prefix;
+    const int S = shift;
+    const uint32_t E_need = need;
+    if ((P << S) < max_tkey) return false;
+    // ordered compaction over vectors: thread t owns vectors [t*m, t*m + m) (staged order = column order)
+    const int m = (nvec + NT - 1) / NT;
+    const int v0 = min(nvec, tid * m), v1 = min(nvec, v0 + m);
+    uint32_t g = 0, q = 0;
+    for (int v = v0; v < v1; ++v) {
+        int seg, first;
+        const int lim = locate(v, seg, first);
+        E el[V];
+        T::unpack(sv[v], el);
+#pragma unroll
+        for (int t = 0; t < V; ++t) {
+            if (t < lim) {
+                const uint32_t c = T::key(el[t]) >> S;
+                g += c > P;
+                q += c == P;
+            }
+        }
+    }
+    uint32_t tq;
+    uint32_t r = block_exclusive_scan<NT>(q, s_warp, tq);
+    const uint32_t sel = g + take_from_ties(E_need, r, q);
+    uint32_t ts;
+    uint32_t pos = block_exclusive_scan<NT>(sel, s_warp, ts);
+    const uint32_t total = sg.pre[sg.n];
+    const bool by_position = total <= 65535u && static_cast<uint32_t>(a.k) <= 2u * static_cast<uint32_t>(a.hist_bins);
+    uint16_t *src = reinterpret_cast<uint16_t *>(hist);  // the histogram is free now
+    for (int v = v0; v < v1; ++v) {
+        int seg, first;
+        const int lim = locate(v, seg, first);
+        E el[V];
+        T::unpack(sv[v], el);
+#pragma unroll
+        for (int t = 0; t < V; ++t) {
+            if (t < lim) {
+                const uint32_t c = T::key(el[t]) >> S;
+                bool take = c > P;
+                if (c == P) take = (r++ < E_need);
+                if (take) {
+                    const uint32_t i = static_cast<uint32_t>(first + t);
+                    if (by_position) {
+                        src[pos] = static_cast<uint16_t>(sg.pre[seg] + i);
+                    } else {
+                        const int64_t col = seg_col(sg, seg, i);
+                        store_idx(a, row, pos, col);
+                        if (a.want_values) store_val<E>(a, row, pos, el[t]);
+                        if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = static_cast<int32_t>(col);
+                    }
+                    ++pos;
+                }
+            }
+        }
+    }
+    if (by_position) {
+        // output position j: its source entry, column from the workspace (independent loads), key from smem
+        __syncthreads();
+        constexpr int U = 4;
+        for (int j0 = tid; j0 < a.k; j0 += U * NT) {
+            int64_t col[U];
+            E val[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + u * NT;
+                if (j < a.k) {
+                    const uint32_t f = src[j];
+                    int lo = 0, hi = sg.n - 1;
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (sg.pre[mid] <= f) lo = mid;
+                        else hi = mid - 1;
+                    }
+                    const uint32_t i = f - sg.pre[lo];
+                    val[u] = seg_bits(sg, lo, i);
+                    col[u] = seg_col(sg, lo, i);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + u * NT;
+                if (j < a.k) {
+                    store_idx(a, row, j, col[u]);
+                    if (a.want_values) store_val<E>(a, row, j, val[u]);
+                    if (GATHER && j < a.n_gather) glist[j] = static_cast<int32_t>(col[u]);
+                }
+            }
+        }
+    }
+    if (GATHER) {
+        __syncthreads();
+        gather_rows_of<NT>(a, row, 0, a.n_gather, glist, 0);
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 // row_kernel: one CTA per row, the row staged whole in shared memory.
 // ---------------------------------------------------------------------------
@@ -1112,7 +1265,11 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
     const bool cand_ok = s_res[3] != 0u;
     const uint32_t max_tkey = s_res[2];
     bool done = false;
-    if (cand_ok) done = select_segments<E, NT, GATHER>(a, row, s_seg, max_tkey, hist, s_res, s_warp, glist);
+    if (cand_ok) {
+        done = s_staged ? select_staged<E, NT, GATHER>(a, row, s_seg, s_stage_off, s_staged, smem, max_tkey, hist,
+                                                       s_res, s_warp, glist)
+                        : select_segments<E, NT, GATHER>(a, row, s_seg, max_tkey, hist, s_res, s_warp, glist);
+    }
     if (!done) {
         __syncthreads();
         if (tid == 0) {
@@ -1167,227 +1324,6 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) stream_kernel(const 
     select_segments<E, NT, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
 }
 
-// ---------------------------------------------------------------------------
-// warp_kernel: one warp per short row (at most kWarpRowVecs 16-byte vectors:
-// 2048 bf16 / 1024 fp32).  Each warp stages its row in its own slice of
-// shared memory and synchronises only with itself: 8-bit radix levels on a
-// per-warp histogram, ordered compaction by warp scans, then the fused gather
-// of the selected key rows.  grid = ceil(rows / warps per CTA).
-// Shared memory: W rows of kWarpRowVecs vectors | W x 256 bins | W x n_gather gather list.
-// ---------------------------------------------------------------------------
-constexpr int kWarpRowVecs = 256;
-
-template <typename E, int NT, bool GATHER>
-__global__ void __launch_bounds__(NT) warp_kernel(const TopkArgs a)
-{
-    using T = Elem<E>;
-    constexpr int V = T::V;
-    constexpr int W = NT / 32;
-    constexpr int kBins = 256;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * W + warp;
-    if (row >= a.rows) return;
-    uint4 *rbuf = reinterpret_cast<uint4 *>(smem) + warp * kWarpRowVecs;
-    uint32_t *h = reinterpret_cast<uint32_t *>(smem + W * kWarpRowVecs * 16) + warp * kBins;
-    int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + W * kWarpRowVecs * 16 + W * kBins * 4) +
-                                  static_cast<int64_t>(warp) * a.n_gather
-                            : nullptr;
-    const int64_t n64 = valid_cols(a, row);
-    const int k = a.k;
-    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
-    if (n64 <= k) {  // short row, by this warp
-        for (int j = lane; j < k; j += 32) {
-            store_idx(a, row, j, j < n64 ? j : -1);
-            if (a.want_values) store_val<E>(a, row, j, j < n64 ? xrow[j] : static_cast<E>(T::kFill));
-            if (GATHER && j < a.n_gather) glist[j] = j < n64 ? j : 0;
-        }
-    } else {
-        const int n = static_cast<int>(n64);
-        const int nfull = n / V;
-        const int nvt = (n + V - 1) / V;
-        // stage: full vectors with 16-byte loads (8 in flight per lane), the tail element by element
-        for (int v0 = 0; v0 < nfull; v0 += 8 * 32) {
-            uint4 q[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int v = v0 + u * 32 + lane;
-                if (v < nfull) q[u] = __ldg(reinterpret_cast<const uint4 *>(xrow) + v);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int v = v0 + u * 32 + lane;
-                if (v < nfull) rbuf[v] = q[u];
-            }
-        }
-        if (nfull < nvt && lane == 0) {
-            E el[V];
-#pragma unroll
-            for (int t = 0; t < V; ++t) el[t] = (nfull * V + t < n) ? xrow[nfull * V + t] : static_cast<E>(0);
-            rbuf[nfull] = T::pack(el);
-        }
-        for (int b = lane; b < kBins; b += 32) h[b] = 0u;
-        __syncwarp();
-        // level 0 histogram + NaN check
-        uint32_t mag = 0;
-        const int sh0 = T::KB - 8;
-        for (int v0 = 0; v0 < nvt; v0 += 32) {  // warp-uniform: the grouped adds need every lane
-            const int v = v0 + lane;
-            E el[V];
-            T::unpack(v < nvt ? rbuf[v] : make_uint4(0u, 0u, 0u, 0u), el);
-            const int lim = v < nvt ? min(V, n - v * V) : 0;
-#pragma unroll
-            for (int t = 0; t < V; ++t) {
-                if (t < lim) mag = max(mag, T::magnitude(el[t]));
-                hist_add_grouped(h, T::key(el[t]) >> sh0, t < lim, lane);
-            }
-        }
-        if (__any_sync(kFull, mag > T::kInfMagnitude) && lane == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
-        uint32_t prefix = 0, need = static_cast<uint32_t>(k), cnt = 0;
-        int shift = T::KB;
-        for (int l = 0; l < T::KB / 8; ++l) {
-            const int nsh = shift - 8;
-            if (l > 0) {
-                for (int v0 = 0; v0 < nvt; v0 += 32) {
-                    const int v = v0 + lane;
-                    E el[V];
-                    T::unpack(v < nvt ? rbuf[v] : make_uint4(0u, 0u, 0u, 0u), el);
-                    const int lim = v < nvt ? min(V, n - v * V) : 0;
-#pragma unroll
-                    for (int t = 0; t < V; ++t) {
-                        const uint32_t kk = T::key(el[t]);
-                        hist_add_grouped(h, (kk >> nsh) & 0xffu, t < lim && (kk >> shift) == prefix, lane);
-                    }
-                }
-            }
-            __syncwarp();
-            // threshold digit: lane l owns bins [8l, 8l + 8); counts above come from a reversed scan
-            uint32_t c[8], s = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                c[j] = h[lane * 8 + j];
-                s += c[j];
-            }
-            uint32_t inc = s;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_down_sync(kFull, inc, o);
-                if (lane + o < 32) inc += y;
-            }
-            const uint32_t above_lane = inc - s;
-            const bool mine = above_lane < need && inc >= need;
-            uint32_t d = 0, above = 0, dc = 0;
-            if (mine) {
-                uint32_t acc = above_lane;
-                bool found = false;
-#pragma unroll
-                for (int j = 7; j >= 0; --j) {
-                    if (!found) {
-                        if (acc + c[j] >= need) {
-                            d = static_cast<uint32_t>(lane * 8 + j);
-                            above = acc;
-                            dc = c[j];
-                            found = true;
-                        } else {
-                            acc += c[j];
-                        }
-                    }
-                }
-            }
-            const int src = __ffs(__ballot_sync(kFull, mine)) - 1;
-            d = __shfl_sync(kFull, d, src);
-            above = __shfl_sync(kFull, above, src);
-            dc = __shfl_sync(kFull, dc, src);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) h[lane * 8 + j] = 0u;
-            __syncwarp();
-            prefix = (l == 0) ? d : ((prefix << 8) | d);
-            need -= above;
-            cnt = dc;
-            shift = nsh;
-            if (cnt == need) break;
-        }
-        const uint32_t P = prefix;
-        const int S = shift;
-        const uint32_t E_need = need;
-        // ordered compaction: in iteration i lane l holds vector 32i + l, so (i, l, t) is column order
-        uint32_t eq_run = 0, sel_run = 0;
-        for (int v0 = 0; v0 < nvt; v0 += 32) {
-            const int v = v0 + lane;
-            uint32_t gm = 0, qm = 0;
-            E el[V];
-            if (v < nvt) {
-                T::unpack(rbuf[v], el);
-                const int lim = min(V, n - v * V);
-#pragma unroll
-                for (int t = 0; t < V; ++t) {
-                    if (t < lim) {
-                        const uint32_t cc = T::key(el[t]) >> S;
-                        gm |= static_cast<uint32_t>(cc > P) << t;
-                        qm |= static_cast<uint32_t>(cc == P) << t;
-                    }
-                }
-            }
-            if (!__any_sync(kFull, (gm | qm) != 0u)) continue;
-            uint32_t tq;
-            uint32_t r = eq_run + warp_exclusive_scan(static_cast<uint32_t>(__popc(qm)), lane, tq);
-            uint32_t sm = gm;
-#pragma unroll
-            for (int t = 0; t < V; ++t) {
-                if ((qm >> t) & 1u) {
-                    if (r < E_need) sm |= 1u << t;
-                    ++r;
-                }
-            }
-            uint32_t ts;
-            uint32_t pos = sel_run + warp_exclusive_scan(static_cast<uint32_t>(__popc(sm)), lane, ts);
-#pragma unroll
-            for (int t = 0; t < V; ++t) {
-                if ((sm >> t) & 1u) {
-                    const int col = v * V + t;
-                    store_idx(a, row, pos, col);
-                    if (a.want_values) store_val<E>(a, row, pos, el[t]);
-                    if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = col;
-                    ++pos;
-                }
-            }
-            eq_run += tq;
-            sel_run += ts;
-        }
-    }
-    if (GATHER) {
-        __syncwarp();
-        const int vpr = static_cast<int>(a.d >> 3);
-        const int vsh = (vpr & (vpr - 1)) == 0 ? __ffs(vpr) - 1 : -1;
-        const uint16_t *kb = a.key + (row / a.rows_per_batch) * a.key_batch_stride;
-        uint4 *ob = reinterpret_cast<uint4 *>(a.gather_out + row * a.n_gather * a.d);
-        const int total = static_cast<int>(a.n_gather) * vpr;
-        constexpr int U = 4;
-        for (int t0 = lane; t0 < total; t0 += U * 32) {
-            uint4 val[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int t = t0 + u * 32;
-                val[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (t < total) {
-                    const int jj = vsh >= 0 ? (t >> vsh) : t / vpr;
-                    int64_t p = glist[jj];
-                    if (p < 0) p = 0;
-                    if (p < a.comp_len)
-                        val[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + (t - jj * vpr));
-                    else if (t - jj * vpr == 0)
-                        set_err(a.err_flag, kStatusInval);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int t = t0 + u * 32;
-                if (t < total) __stcs(ob + t, val[u]);
-            }
-        }
-    }
-}
-
 // Raises a kernel's dynamic shared-memory limit once per device; later calls that need no more
 // than what was set skip the driver call.
 template <typename K>
@@ -1410,11 +1346,9 @@ template <typename E, int NT, bool G>
 cudaError_t launch_one(int mode, size_t smem, const TopkArgs &a, cudaStream_t stream, int64_t grid, bool query,
                        int *blocks_per_sm)
 {
-    static int set_row[64] = {}, set_split[64] = {}, set_stream[64] = {}, set_warp[64] = {};
+    static int set_row[64] = {}, set_split[64] = {}, set_stream[64] = {};
     cudaError_t e;
-    if (mode == kModeWarp)
-        e = raise_smem_limit(warp_kernel<E, NT, G>, set_warp, smem);
-    else if (mode == kModeRow)
+    if (mode == kModeRow)
         e = raise_smem_limit(row_kernel<E, NT, G>, set_row, smem);
     else if (mode == kModeSplit)
         e = raise_smem_limit(split_kernel<E, NT, G>, set_split, smem);
@@ -1422,8 +1356,6 @@ cudaError_t launch_one(int mode, size_t smem, const TopkArgs &a, cudaStream_t st
         e = raise_smem_limit(stream_kernel<E, NT, G>, set_stream, smem);
     if (e != cudaSuccess) return e;
     if (query) {
-        if (mode == kModeWarp)
-            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, warp_kernel<E, NT, G>, NT, smem);
         if (mode == kModeRow)
             return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, row_kernel<E, NT, G>, NT, smem);
         if (mode == kModeSplit)
@@ -1433,9 +1365,7 @@ cudaError_t launch_one(int mode, size_t smem, const TopkArgs &a, cudaStream_t st
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
     const dim3 g(static_cast<unsigned>(grid)), b(NT);
-    if (mode == kModeWarp)
-        warp_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
-    else if (mode == kModeRow)
+    if (mode == kModeRow)
         row_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
     else if (mode == kModeSplit)
         split_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
@@ -1451,11 +1381,6 @@ cudaError_t launch_e(int mode, int threads, bool gather, size_t smem, const Topk
                      int64_t grid, bool query, int *blocks_per_sm)
 {
     if (mode == kModeSplit) {
-        if (threads != 256) return cudaErrorInvalidValue;
-        return gather ? launch_one<E, 256, true>(mode, smem, a, s, grid, query, blocks_per_sm)
-                      : launch_one<E, 256, false>(mode, smem, a, s, grid, query, blocks_per_sm);
-    }
-    if (mode == kModeWarp) {
         if (threads != 256) return cudaErrorInvalidValue;
         return gather ? launch_one<E, 256, true>(mode, smem, a, s, grid, query, blocks_per_sm)
                       : launch_one<E, 256, false>(mode, smem, a, s, grid, query, blocks_per_sm);
