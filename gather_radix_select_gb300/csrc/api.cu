@@ -3,7 +3,9 @@
 // kernels of topk.cu and gather.cu.
 #include <cstdint>
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
+#include <string>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -18,6 +20,8 @@ constexpr int kOutAlign = 16;  // output rows start on 16 bytes
 constexpr int64_t kSliceTargetBytes = 32 * 1024;  // split_kernel: bytes of a row per CTA
 constexpr int64_t kSliceMinBytes = 16 * 1024;     // ... at least, when splitting further for parallelism
 constexpr int64_t kSplitMinRowBytes = 64 * 1024;  // rows narrower than this never split
+constexpr int64_t kWideMaxRowBytes = 4 << 20;     // wider rows, when few, split over CTAs instead
+constexpr int kWideHistBins = 2048;               // wide_kernel's range histogram (select_regions)
 
 int elem_bytes(int dtype) { return dtype == SEL_F32 ? 4 : 2; }
 int idx_bytes(int idx_dtype) { return idx_dtype == SEL_I64 ? 8 : 4; }
@@ -138,8 +142,62 @@ int hist_agg()
     return v;
 }
 
-// Chooses the kernel (row / split / stream), its CTA shape, shared memory and workspace.
-int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, Plan &p)
+// Candidate capacity of wide_kernel for rows of `cols` elements.  The threshold is estimated
+// from a sample of up to kWideSampleKeys keys (whole 16-byte vectors) (mu = k * sample / cols of the k
+// expected there, keeping mu * 9/8 + 3 sqrt(mu) + 4 sampled keys); the list holds that many
+// scaled to the row, plus four standard deviations of the count.
+int64_t wide_cap(int dtype, int64_t cols, int k)
+{
+    const int64_t e = elem_bytes(dtype);
+    const int64_t nvec = cols * e / 16;
+    const int64_t sample = std::min<int64_t>(nvec, sel::kWideSampleKeys / (16 / e)) * (16 / e);
+    if (sample <= 0) return round_up(cols, 8);
+    const double f = static_cast<double>(sample) / static_cast<double>(cols);
+    const double mu = static_cast<double>(k) * f;
+    const double kept = mu * 1.125 + 3.0 * std::sqrt(mu) + 4.0;
+    const int64_t cap = static_cast<int64_t>((kept + 4.0 * std::sqrt(kept)) / f) + 64;
+    return std::min(cap, round_up(cols, 8));
+}
+
+// Layout of a wide_kernel CTA: histogram | W candidate regions of (key bits, column) pairs |
+// gather list.  Each warp's region holds its share of `cap` plus slack for the uneven spread
+// of candidates over the warps, and one more pair that absorbs writes past the capacity.
+size_t layout_wide(int64_t cap, bool gather, int64_t n_gather, sel::TopkArgs &a)
+{
+    constexpr int W = sel::kWideThreads / 32;
+    const int64_t per = ceil_div(cap, W);
+    const int64_t capw = per + static_cast<int64_t>(4.0 * std::sqrt(static_cast<double>(per))) + 16;
+    a.slice = 0;
+    a.smem_buf_bytes = 0;
+    a.smem_hist_off = 0;
+    a.hist_bins = std::max(a.hist_bins, kWideHistBins);  // also holds the range histogram
+    size_t off = static_cast<size_t>(a.hist_bins) * 4;
+    a.list_cap = static_cast<int32_t>(capw);
+    a.region_stride = static_cast<int32_t>(round_up(capw + 1, 2));
+    a.smem_list_off = static_cast<uint32_t>(off);
+    a.smem_mask_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(W) * static_cast<size_t>(a.region_stride) * 8;
+    a.smem_glist_off = static_cast<uint32_t>(off);
+    if (gather) off += static_cast<size_t>(round_up(n_gather * 4, 16));
+    return off;
+}
+
+// Forced kernel choice for tuning and tests: SEL_PLAN=row|split|wide|stream (when that kernel can
+// run the shape).  Unset: the automatic plan.
+int plan_override()
+{
+    const char *e = std::getenv("SEL_PLAN");
+    if (!e) return -1;
+    const std::string v(e);
+    if (v == "row") return sel::kModeRow;
+    if (v == "split") return sel::kModeSplit;
+    if (v == "stream") return sel::kModeStream;
+    if (v == "wide") return sel::kModeWide;
+    return -1;
+}
+
+// Chooses the kernel (row / split / wide / stream), its CTA shape, shared memory and workspace.
+int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, int force, Plan &p)
 {
     sel::TopkArgs &a = p.layout;
     digit_plan(dtype, cols, a);
@@ -173,41 +231,75 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
             }
         }
     }
-    // few wide rows (or rows that do not fit one CTA): split them over several CTAs
-    const bool want_split = !row_ok || (rows < 2 * sms && row_bytes >= kSplitMinRowBytes);
-    if (!want_split) {
-        p = row_plan;
-        return SEL_OK;
-    }
-    int64_t parts = ceil_div(row_bytes, kSliceTargetBytes);
-    if (rows < 2 * sms) {
-        const int64_t par = ceil_div(2 * sms, rows > 0 ? rows : 1);
-        parts = std::max(parts, std::min(par, ceil_div(row_bytes, kSliceMinBytes)));
-    }
-    parts = std::max<int64_t>(2, std::min<int64_t>(parts, sel::kMaxParts));
-    const int64_t slice = round_up(ceil_div(c1, parts), 64);
-    parts = ceil_div(c1, slice);
-    if (slice <= max_staged && parts >= 2) {
-        Plan sp = p;
-        const int64_t cap = std::min<int64_t>(slice, 2 * ceil_div(k, parts) + 512);
-        const size_t smem = layout_staged(dtype, slice, cap, gather, n_gather, sp.layout);
-        if (smem <= limit && cached_blocks_per_sm(dtype, sel::kModeSplit, 256, gather, smem) > 0 &&
-            rows * parts <= 0x7fffffffLL) {
-            sp.layout.sample_step = 4;  // each slice estimates its own threshold: a denser sample
-            sp.mode = sel::kModeSplit;
-            sp.threads = 256;
-            sp.smem = smem;
-            sp.grid = rows * parts;
-            sp.ws_bytes = layout_workspace(dtype, rows, static_cast<int>(parts), cap, sp.layout);
-            p = sp;
-            return SEL_OK;
+    // one CTA per row, one streaming pass into per-warp candidate lists
+    bool wide_ok = false;
+    Plan wide_plan = p;
+    if (cols <= 0x7fffffffLL) {
+        Plan wp = p;
+        const size_t smem = layout_wide(wide_cap(dtype, c1, k), gather, n_gather, wp.layout);
+        if (smem <= limit && cached_blocks_per_sm(dtype, sel::kModeWide, sel::kWideThreads, gather, smem) > 0) {
+            wp.mode = sel::kModeWide;
+            wp.threads = sel::kWideThreads;
+            wp.smem = smem;
+            wp.grid = rows;
+            wp.ws_bytes = 0;
+            wide_plan = wp;
+            wide_ok = true;
         }
     }
-    if (row_ok) {
+    if (force == sel::kModeRow && row_ok) {
         p = row_plan;
         return SEL_OK;
     }
-    // rows too wide for the split plan: one CTA per row, passes over global memory
+    if (force == sel::kModeWide && wide_ok) {
+        p = wide_plan;
+        return SEL_OK;
+    }
+    // few wide rows (or rows that do not fit one CTA) leave the row plan
+    const bool leave_row = !row_ok || (rows < 2 * sms && row_bytes >= kSplitMinRowBytes);
+    if (!leave_row && force < 0) {
+        p = row_plan;
+        return SEL_OK;
+    }
+    if (force < 0 && wide_ok && !row_ok && (row_bytes <= kWideMaxRowBytes || rows >= sms)) {
+        p = wide_plan;
+        return SEL_OK;
+    }
+    if (force < 0 || force == sel::kModeSplit) {
+        int64_t parts = ceil_div(row_bytes, kSliceTargetBytes);
+        if (rows < 2 * sms) {
+            const int64_t par = ceil_div(2 * sms, rows > 0 ? rows : 1);
+            parts = std::max(parts, std::min(par, ceil_div(row_bytes, kSliceMinBytes)));
+        }
+        parts = std::max<int64_t>(2, std::min<int64_t>(parts, sel::kMaxParts));
+        const int64_t slice = round_up(ceil_div(c1, parts), 64);
+        parts = ceil_div(c1, slice);
+        if (slice <= max_staged && parts >= 2) {
+            Plan sp = p;
+            const int64_t cap = std::min<int64_t>(slice, 2 * ceil_div(k, parts) + 512);
+            const size_t smem = layout_staged(dtype, slice, cap, gather, n_gather, sp.layout);
+            if (smem <= limit && cached_blocks_per_sm(dtype, sel::kModeSplit, 256, gather, smem) > 0 &&
+                rows * parts <= 0x7fffffffLL) {
+                sp.layout.sample_step = 4;  // each slice estimates its own threshold: a denser sample
+                sp.mode = sel::kModeSplit;
+                sp.threads = 256;
+                sp.smem = smem;
+                sp.grid = rows * parts;
+                sp.ws_bytes = layout_workspace(dtype, rows, static_cast<int>(parts), cap, sp.layout);
+                p = sp;
+                return SEL_OK;
+            }
+        }
+    }
+    if (row_ok && force != sel::kModeStream) {
+        p = row_plan;
+        return SEL_OK;
+    }
+    if (wide_ok && force != sel::kModeStream) {
+        p = wide_plan;
+        return SEL_OK;
+    }
+    // otherwise one CTA per row, passes over global memory
     if (cols > 0x7fffffffLL) return SEL_EUNSUPPORTED;
     Plan st = p;
     const size_t smem = layout_stream(gather, n_gather, st.layout);
@@ -225,10 +317,11 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
 int cached_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, Plan &p)
 {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int64_t, int64_t, int, int64_t>, Plan> cache;
+    static std::map<std::tuple<int, int, int64_t, int64_t, int, int64_t, int>, Plan> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SEL_ECUDA;
-    const auto key = std::make_tuple(dev, dtype, rows, cols, k, gather ? n_gather : -1);
+    const int force = plan_override();
+    const auto key = std::make_tuple(dev, dtype, rows, cols, k, gather ? n_gather : -1, force);
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
@@ -237,7 +330,7 @@ int cached_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64
             return SEL_OK;
         }
     }
-    const int st = make_plan(dtype, rows, cols, k, gather, n_gather, p);
+    const int st = make_plan(dtype, rows, cols, k, gather, n_gather, force, p);
     if (st != SEL_OK) return st;
     std::lock_guard<std::mutex> g(mu);
     if (cache.size() > 4096) cache.clear();

@@ -1,6 +1,6 @@
 // ptx.cuh -- thin inline-PTX wrappers used by the selection and gather kernels
-// (sm_90+ features: mbarrier, bulk async copies, thread-block clusters and
-// distributed shared memory).  Everything here is a single PTX instruction.
+// (sm_90+ features: mbarrier and bulk async copies).  Everything here is a
+// single PTX instruction.
 #pragma once
 
 #include <cstdint>
@@ -29,6 +29,26 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                  "r"(bytes)
                  : "memory");
+}
+
+// Plain arrival (count 1, no transaction bytes).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Non-blocking: whether the phase with `parity` has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 // Suspends the thread (no issue slots used) until the phase with `parity` completes or
@@ -63,61 +83,6 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
             smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
-}
-
-// ----------------------------------------------------------------- cluster
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_id_x()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-
-// All threads of all CTAs of the cluster; release/acquire orders shared::cluster accesses.
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-
-// Address of the same shared variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void dsmem_add(uint32_t caddr, uint32_t v)
-{
-    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void dsmem_store(uint32_t caddr, uint32_t v)
-{
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t dsmem_load(uint32_t caddr)
-{
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
-    return v;
 }
 
 }  // namespace sel

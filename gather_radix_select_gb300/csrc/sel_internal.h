@@ -13,10 +13,13 @@ constexpr int kMaxLevels = 4;       // radix passes (digits) at most
 constexpr int kMaxSlice = 65536;    // elements of a row staged by one CTA (list offsets are 16-bit)
 constexpr int kMaxChunks = 16;      // bulk-copy chunks per CTA slice
 constexpr uint32_t kChunkBytes = 16384;
+constexpr int kWideSampleKeys = 2048;  // wide_kernel: keys in a row's threshold sample (16-byte vectors)
+constexpr int kWideThreads = 512;
 constexpr int kMaxParts = 64;       // CTAs splitting one row (split_kernel)
 constexpr int kModeRow = 0;         // row_kernel: one CTA per row, row staged in shared memory
 constexpr int kModeSplit = 1;       // split_kernel: `parts` CTAs per row + last-arriver merge
 constexpr int kModeStream = 2;      // stream_kernel: one CTA per row, passes read global memory
+constexpr int kModeWide = 3;        // wide_kernel: one CTA per row, one streaming pass into per-warp lists
 constexpr int kGatherThreads = 256;
 
 // Everything one selection launch needs; passed by value (kernel parameter space).
@@ -44,6 +47,7 @@ struct TopkArgs {
     uint32_t smem_list_off;   // offset of the candidate list (16-bit offsets within the slice)
     uint32_t smem_glist_off;  // offset of the gather position list (fused only)
     int32_t list_cap;         // capacity of the candidate list
+    int32_t region_stride;    // wide_kernel: candidate pairs per warp region (capacity list_cap + 1)
     int32_t agg;              // 1: first-pass histogram with warp-aggregated atomics
     int32_t sample_step;      // > 1: the first digit's threshold is estimated from every
                               //      sample_step-th 16-byte vector of the row
@@ -70,7 +74,7 @@ struct GatherArgs {
     int32_t ctas_per_row;
 };
 
-// dtype: 0 fp32, 1 bf16.  mode: kModeRow | kModeSplit | kModeStream.  grid: CTAs to launch.
+// dtype: 0 fp32, 1 bf16.  mode: kModeRow | kModeSplit | kModeStream | kModeWide.  grid: CTAs to launch.
 cudaError_t launch_topk(int dtype, int mode, int threads, bool gather, size_t smem_bytes, const TopkArgs &a,
                         int64_t grid, cudaStream_t stream);
 

@@ -7,16 +7,19 @@
 // (ties: smaller column first), or, when n <= k, every valid column followed
 // by fills (index -1, value -inf).  Rows with n > k are checked for NaN.
 //
-// Three kernels, chosen per launch by the host plan:
+// Four kernels, chosen per launch by the host plan:
 //   row_kernel    one CTA per row; the row is staged whole in shared memory.
+//   wide_kernel   one CTA per row for rows too wide to stage: the row streams
+//                 through a ring of shared-memory chunks, is filtered on
+//                 arrival into a candidate list in shared memory, and the
+//                 selection runs on that list (the row is read once).
 //   split_kernel  a wide row is cut into `parts` slices, one CTA each.  Every
 //                 CTA filters its slice down to an index-ordered candidate
 //                 list in a caller-provided workspace; the CTA that finishes
 //                 last (an atomic arrival counter -- nobody waits) selects
 //                 the k from the merged candidates.
 //   stream_kernel one CTA per row, the row read from global memory on every
-//                 radix pass (rows too wide for the split plan, and the exact
-//                 fallback of split_kernel).
+//                 radix pass (the exact fallback of the others).
 //
 // Building blocks (GB300 design):
 //   * Slices are staged into shared memory with bulk async copies
@@ -79,6 +82,44 @@ struct Elem<uint32_t> {  // fp32 bit patterns
                (static_cast<uint32_t>(static_cast<int>(q.z) >= t) << 2) |
                (static_cast<uint32_t>(static_cast<int>(q.w) >= t) << 3);
     }
+    // NaN detection on raw words without per-element work: a positive NaN is the largest signed
+    // pattern (> 0x7f800000), a negative NaN the largest unsigned one (> 0xff800000).
+    static constexpr uint32_t kSmaxInit = 0x80000000u, kUmaxInit = 0u;
+    static __device__ __forceinline__ void nan_acc(const uint4 &q, uint32_t &smax, uint32_t &umax)
+    {
+        const int m = max(max(static_cast<int>(q.x), static_cast<int>(q.y)), max(static_cast<int>(q.z), static_cast<int>(q.w)));
+        smax = static_cast<uint32_t>(max(static_cast<int>(smax), m));
+        umax = max(umax, max(max(q.x, q.y), max(q.z, q.w)));
+    }
+    static __device__ __forceinline__ void nan_acc1(uint32_t u, uint32_t &smax, uint32_t &umax)
+    {
+        smax = static_cast<uint32_t>(max(static_cast<int>(smax), static_cast<int>(u)));
+        umax = max(umax, u);
+    }
+    static __device__ __forceinline__ bool has_nan(uint32_t smax, uint32_t umax)
+    {
+        return static_cast<int>(smax) > 0x7f800000 || umax > 0xff800000u;
+    }
+    // As ge_mask_positive, without the magnitude.
+    static __device__ __forceinline__ uint32_t ge_mask_raw(const uint4 &q, uint32_t ts)
+    {
+        const int t = static_cast<int>(ts);
+        return static_cast<uint32_t>(static_cast<int>(q.x) >= t) | (static_cast<uint32_t>(static_cast<int>(q.y) >= t) << 1) |
+               (static_cast<uint32_t>(static_cast<int>(q.z) >= t) << 2) |
+               (static_cast<uint32_t>(static_cast<int>(q.w) >= t) << 3);
+    }
+    // Bit t set when key(element t) >= tkey (any threshold).
+    static __device__ __forceinline__ uint32_t ge_mask_key(const uint4 &q, uint32_t tkey)
+    {
+        return static_cast<uint32_t>(key(q.x) >= tkey) | (static_cast<uint32_t>(key(q.y) >= tkey) << 1) |
+               (static_cast<uint32_t>(key(q.z) >= tkey) << 2) | (static_cast<uint32_t>(key(q.w) >= tkey) << 3);
+    }
+    // element t (0..3) of a vector
+    static __device__ __forceinline__ uint32_t lane_of(const uint4 &q, int t)
+    {
+        const uint32_t lo = (t & 1) ? q.y : q.x, hi = (t & 1) ? q.w : q.z;
+        return (t & 2) ? hi : lo;
+    }
     static __device__ __forceinline__ void unpack(const uint4 &q, uint32_t (&e)[4])
     {
         e[0] = q.x;
@@ -118,6 +159,54 @@ struct Elem<uint16_t> {  // bf16 bit patterns
         }
         mag = max(mag, max(mm & 0xffffu, mm >> 16));
         return m;
+    }
+    // As for fp32, per 16-bit half: a positive NaN half is the largest signed half (> 0x7f80), a
+    // negative NaN half the largest unsigned one (> 0xff80).
+    static constexpr uint32_t kSmaxInit = 0x80008000u, kUmaxInit = 0u;
+    static __device__ __forceinline__ void nan_acc(const uint4 &q, uint32_t &smax, uint32_t &umax)
+    {
+        smax = __vmaxs2(smax, __vmaxs2(__vmaxs2(q.x, q.y), __vmaxs2(q.z, q.w)));
+        umax = __vmaxu2(umax, __vmaxu2(__vmaxu2(q.x, q.y), __vmaxu2(q.z, q.w)));
+    }
+    static __device__ __forceinline__ void nan_acc1(uint16_t h, uint32_t &smax, uint32_t &umax)
+    {
+        smax = __vmaxs2(smax, static_cast<uint32_t>(h) | 0x80000000u);  // other half: the signed minimum
+        umax = __vmaxu2(umax, static_cast<uint32_t>(h));
+    }
+    static __device__ __forceinline__ bool has_nan(uint32_t smax, uint32_t umax)
+    {
+        return static_cast<int16_t>(smax & 0xffffu) > 0x7f80 || static_cast<int16_t>(smax >> 16) > 0x7f80 ||
+               (umax & 0xffffu) > 0xff80u || (umax >> 16) > 0xff80u;
+    }
+    static __device__ __forceinline__ uint32_t ge_mask_raw(const uint4 &q, uint32_t ts)
+    {
+        const int t = static_cast<int>(ts << 16);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            m |= static_cast<uint32_t>(static_cast<int>(w[i] << 16) >= t) << (2 * i);
+            m |= static_cast<uint32_t>(static_cast<int>(w[i] & 0xffff0000u) >= t) << (2 * i + 1);
+        }
+        return m;
+    }
+    static __device__ __forceinline__ uint32_t ge_mask_key(const uint4 &q, uint32_t tkey)
+    {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            m |= static_cast<uint32_t>(key(static_cast<uint16_t>(w[i] & 0xffffu)) >= tkey) << (2 * i);
+            m |= static_cast<uint32_t>(key(static_cast<uint16_t>(w[i] >> 16)) >= tkey) << (2 * i + 1);
+        }
+        return m;
+    }
+    // element t (0..7) of a vector
+    static __device__ __forceinline__ uint16_t lane_of(const uint4 &q, int t)
+    {
+        const uint32_t lo = (t & 2) ? q.y : q.x, hi = (t & 2) ? q.w : q.z;
+        const uint32_t w = (t & 4) ? hi : lo;
+        return static_cast<uint16_t>((t & 1) ? (w >> 16) : (w & 0xffffu));
     }
     static __device__ __forceinline__ void unpack(const uint4 &q, uint16_t (&e)[8])
     {
@@ -1324,6 +1413,444 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) stream_kernel(const 
     select_segments<E, NT, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
 }
 
+// ---------------------------------------------------------------------------
+// wide_kernel: one CTA per row for rows too wide to stage whole; two CTAs
+// share an SM, so one CTA's selection overlaps the other's streaming.
+//  1. Threshold estimate from a strided sample of the row's 16-byte vectors
+//     (kWideSampleKeys keys), held in registers: its top-digit histogram and a
+//     second digit give a key that about mu*9/8 + 3 sqrt(mu) + 4 sampled keys
+//     reach (mu: the sample's share of the k).
+//  2. One pass over the row, read from HBM once: warp w streams a contiguous
+//     range of the row's vectors with kWideUnroll coalesced 128-bit loads in
+//     flight per lane and appends the (key bits, column) pairs at or above
+//     the estimate to its own region of the candidate list, in column order.
+//     No block-wide synchronisation while streaming.
+//  3. Exact selection on the regions (select_regions), using the largest
+//     candidate key, tracked while streaming, to scale its digits.
+//  Too few candidates, or a region overflowing, falls back to exact passes
+//  over the row in global memory.
+// Shared memory: histogram | candidate regions (W x region_stride pairs; the
+// last pair of a region absorbs writes past its capacity) | gather list.
+// ---------------------------------------------------------------------------
+constexpr int kWideUnroll = 4;
+
+// Threshold key estimated from `ns` sample vectors held in registers: thread t holds samples
+// t, t + NT, ... in q[].  share / population: the k wanted out of the row's n.  Leaves h zero.
+template <typename E, int NT, int kS>
+__device__ uint32_t estimate_threshold(const TopkArgs &a, const uint4 (&q)[kS], int ns, float share,
+                                       float population, uint32_t *h, uint32_t *s_res, uint32_t *s_warp)
+{
+    using T = Elem<E>;
+    constexpr int V = T::V;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int sh0 = T::KB - a.bits[0];
+    const int nb0 = 1 << a.bits[0];
+#pragma unroll
+    for (int j = 0; j < kS; ++j) {
+        const bool ok = tid + j * NT < ns;
+        E el[V];
+        T::unpack(q[j], el);
+#pragma unroll
+        for (int t = 0; t < V; ++t) hist_add(h, T::key(el[t]) >> sh0, ok, lane, a.agg != 0);
+    }
+    __syncthreads();
+    const float total = static_cast<float>(ns) * V;
+    const float mu = share * total / population;
+    const float want = mu * 1.125f + 3.0f * sqrtf(mu) + 4.0f;
+    if (want >= total) {
+        for (int i = tid; i < nb0; i += NT) h[i] = 0u;
+        __syncthreads();
+        return 0u;
+    }
+    find_threshold<NT>(h, nb0, static_cast<uint32_t>(want), s_res, s_warp);
+    const uint32_t d = s_res[0];
+    const uint32_t need2 = static_cast<uint32_t>(want) - s_res[1];
+    for (int i = tid; i < nb0; i += NT) h[i] = 0u;
+    __syncthreads();
+    const int b2 = sh0 < 11 ? sh0 : 11;  // refinement digit: the next bits below the top digit
+    const int sh1 = sh0 - b2;
+    const uint32_t m2 = (1u << b2) - 1u;
+#pragma unroll
+    for (int j = 0; j < kS; ++j) {
+        if (tid + j * NT < ns) {
+            E el[V];
+            T::unpack(q[j], el);
+#pragma unroll
+            for (int t = 0; t < V; ++t) {
+                const uint32_t kk = T::key(el[t]);
+                if ((kk >> sh0) == d) atomicAdd(&h[(kk >> sh1) & m2], 1u);
+            }
+        }
+    }
+    __syncthreads();
+    find_threshold<NT>(h, 1 << b2, need2, s_res, s_warp);
+    const uint32_t key = (d << sh0) | (s_res[0] << sh1);
+    for (int i = tid; i < (1 << b2); i += NT) h[i] = 0u;
+    __syncthreads();
+    return key;
+}
+
+// Exact selection over candidates kept in per-warp regions: warp w's region holds cnt[w]
+// (key bits, column) pairs in column order, and the regions follow each other in column order;
+// every candidate key lies in [tlo, thi].
+// Fast path: one histogram level over kRangeBins digits of (key - tlo), scaled to the range
+// [tlo, thi] so that the candidates spread over the bins (plain atomics); the threshold bin, if
+// it holds at most kRankMax pairs, is resolved exactly by ranking its members (larger key first,
+// then smaller column), and the winners are marked in place (column bit 31).  Otherwise radix
+// levels over the full key find the threshold class and ballots give tie ranks.  The compaction
+// then runs warp by warp over its own region (a prefix over the per-warp counts orders the
+// regions), so outputs come in ascending column order.  Writes the k outputs (and, with GATHER,
+// the gathered rows).  s_gq: 3 * W words of scratch; hist: hist_bins words, zero on entry
+// (left dirty).
+constexpr int kRangeBins = 2048;
+constexpr int kRankMax = 512;
+
+// Calls f(i, pair) for every pair i < c of a region, four pairs per lane in flight (any order).
+template <typename F>
+__device__ __forceinline__ void for_region(const uint2 *reg, uint32_t c, int lane, F f)
+{
+    uint32_t i0 = 0;
+    for (; i0 + 128 <= c; i0 += 128) {
+        uint2 e[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) e[u] = reg[i0 + u * 32 + lane];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) f(i0 + u * 32 + lane, e[u]);
+    }
+    for (uint32_t i = i0 + lane; i < c; i += 32) f(i, reg[i]);
+}
+
+template <typename E, int NT, bool GATHER>
+__device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int rs, const uint32_t *cnt, uint32_t tlo,
+                               uint32_t thi, uint32_t *hist, uint32_t *s_res, uint32_t *s_warp, uint32_t *s_gq,
+                               int32_t *glist)
+{
+    using T = Elem<E>;
+    constexpr int W = NT / 32;
+    constexpr uint32_t kMark = 0x80000000u;
+    __shared__ uint32_t s_nbin;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint2 *reg = list + warp * rs;
+    const uint32_t c = cnt[warp];
+    const uint32_t lt = (1u << lane) - 1u;
+    // digit of a key in the fast path: (key - tlo) >> rsh, in [0, kRangeBins)
+    const uint32_t span = thi - tlo;
+    const int rsh = span < kRangeBins ? 0 : (32 - __clz(span)) - 11;
+    for_region(reg, c, lane, [&](uint32_t, uint2 e) { atomicAdd(&hist[(T::key(static_cast<E>(e.x)) - tlo) >> rsh], 1u); });
+    if (tid == 0) s_nbin = 0u;
+    if (tid < W) s_gq[2 * W + tid] = 0u;
+    __syncthreads();
+    find_threshold<NT>(hist, kRangeBins, static_cast<uint32_t>(a.k), s_res, s_warp);
+    const uint32_t dstar = s_res[0], above = s_res[1], inbin = s_res[2];
+    const uint32_t bneed = static_cast<uint32_t>(a.k) - above;  // taken from the threshold bin
+    const bool whole = inbin == bneed;
+    // kind of the compaction: 0 = range digits (the whole bin, or its marked members);
+    // 1 = full-key classes (a crowded threshold bin)
+    const int kind = (whole || inbin <= static_cast<uint32_t>(kRankMax)) ? 0 : 1;
+    uint32_t P = 0, E_need = 0;
+    int S = 0;
+    if (kind == 0) {
+        // per-warp counts above the bin and in it; the bin's members (key, column, list position)
+        // gathered into the histogram, which is free now
+        uint32_t *bk = hist, *bc = hist + kRankMax, *bi = hist + 2 * kRankMax;
+        uint32_t na = 0, nin = 0;
+        for_region(reg, c, lane, [&](uint32_t i, uint2 e) {
+            const uint32_t kk = T::key(static_cast<E>(e.x));
+            const uint32_t d = (kk - tlo) >> rsh;
+            na += d > dstar;
+            if (d == dstar) {
+                ++nin;
+                if (!whole) {
+                    const uint32_t slot = atomicAdd(&s_nbin, 1u);
+                    bk[slot] = kk;
+                    bc[slot] = e.y;
+                    bi[slot] = static_cast<uint32_t>(warp * rs) + i;
+                }
+            }
+        });
+        na = __reduce_add_sync(kFull, na);
+        nin = __reduce_add_sync(kFull, nin);
+        if (lane == 0) {
+            s_gq[warp] = na;
+            s_gq[W + warp] = nin;
+        }
+        __syncthreads();  // bin members and counts complete
+        if (!whole) {
+            // rank of a member among the bin's (larger key first, then smaller column): one warp
+            // per member, its lanes comparing against the other members
+            for (uint32_t m = warp; m < inbin; m += W) {
+                const uint32_t km = bk[m], cm = bc[m];
+                uint32_t beats = 0;
+                for (uint32_t j = lane; j < inbin; j += 32) beats += (bk[j] > km) | ((bk[j] == km) & (bc[j] < cm));
+                if (__reduce_add_sync(kFull, beats) < bneed && lane == 0) {
+                    list[bi[m]].y = cm | kMark;
+                    atomicAdd(&s_gq[2 * W + bi[m] / static_cast<uint32_t>(rs)], 1u);
+                }
+            }
+            __syncthreads();
+        }
+    } else {
+        for (int i = tid; i < kRangeBins; i += NT) hist[i] = 0u;
+        __syncthreads();
+        uint32_t prefix = 0, need = static_cast<uint32_t>(a.k), cls = 0;
+        int shift = T::KB;
+        for (int l = 0; l < a.nlevels && (l == 0 || cls != need); ++l) {
+            const int bl = a.bits[l];
+            const int nsh = shift - bl;
+            const int nb = 1 << bl;
+            const uint32_t mask = static_cast<uint32_t>(nb - 1);
+            for (uint32_t i0 = 0; i0 < c; i0 += 32) {  // warp-uniform trip count
+                const uint32_t i = i0 + lane;
+                const bool in = i < c;
+                const uint32_t kk = in ? T::key(static_cast<E>(reg[i].x)) : 0u;
+                hist_add_grouped(hist, (kk >> nsh) & mask, in && (l == 0 || (kk >> shift) == prefix), lane);
+            }
+            __syncthreads();
+            find_threshold<NT>(hist, nb, need, s_res, s_warp);
+            for (int i = tid; i < nb; i += NT) hist[i] = 0u;
+            __syncthreads();
+            prefix = (l == 0) ? s_res[0] : ((prefix << bl) | s_res[0]);
+            need -= s_res[1];
+            cls = s_res[2];
+            shift = nsh;
+        }
+        P = prefix;
+        S = shift;
+        E_need = need;
+        uint32_t g = 0, q = 0;
+        for_region(reg, c, lane, [&](uint32_t, uint2 e) {
+            const uint32_t cc = T::key(static_cast<E>(e.x)) >> S;
+            g += cc > P;
+            q += cc == P;
+        });
+        g = __reduce_add_sync(kFull, g);
+        q = __reduce_add_sync(kFull, q);
+        if (lane == 0) {
+            s_gq[warp] = g;
+            s_gq[W + warp] = q;
+        }
+        __syncthreads();
+    }
+    // outputs of the regions before this warp's (and, for full-key classes, their ties)
+    auto taken_of = [&](int w, uint32_t ties_before) {
+        if (kind == 1) return s_gq[w] + take_from_ties(E_need, ties_before, s_gq[W + w]);
+        return s_gq[w] + (whole ? s_gq[W + w] : s_gq[2 * W + w]);
+    };
+    uint32_t ties = 0, pos = 0;
+    for (int w = 0; w < warp; ++w) {
+        pos += taken_of(w, ties);
+        ties += s_gq[W + w];
+    }
+    // the region in order, four chunks of 32 pairs loaded ahead
+    constexpr int kAhead = 4;
+    for (uint32_t i0 = 0; i0 < c; i0 += 32 * kAhead) {
+        uint2 ev[kAhead];
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            const uint32_t i = i0 + u * 32 + lane;
+            ev[u] = i < c ? reg[i] : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            const bool in = i0 + u * 32 + lane < c;
+            const uint2 e = ev[u];
+            const uint32_t kk = T::key(static_cast<E>(e.x));
+            bool gt, eq = false;
+            if (kind == 0) {
+                const uint32_t d = (kk - tlo) >> rsh;
+                gt = in && (d > dstar || (d == dstar && (whole || (e.y & kMark))));
+            } else {
+                const uint32_t cc = kk >> S;
+                gt = in && cc > P;
+                eq = in && cc == P;
+            }
+            const uint32_t be = __ballot_sync(kFull, eq);
+            const bool take = gt || (eq && ties + __popc(be & lt) < E_need);
+            const uint32_t bt = __ballot_sync(kFull, take);
+            if (take) {
+                const uint32_t p = pos + __popc(bt & lt);
+                const int32_t col = static_cast<int32_t>(e.y & ~kMark);
+                store_idx(a, row, p, col);
+                if (a.want_values) store_val<E>(a, row, p, static_cast<E>(e.x));
+                if (GATHER && static_cast<int64_t>(p) < a.n_gather) glist[p] = col;
+            }
+            ties += __popc(be);
+            pos += __popc(bt);
+        }
+    }
+    if (GATHER) {
+        __syncthreads();
+        gather_rows_of<NT>(a, row, 0, a.n_gather, glist, 0);
+    }
+}
+
+template <typename E, int NT, bool GATHER>
+__global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
+{
+    using T = Elem<E>;
+    constexpr int V = T::V;
+    constexpr int W = NT / 32;
+    constexpr int U = kWideUnroll;
+    constexpr int kSV = kWideSampleKeys / V;     // sample vectors
+    constexpr int kS = (kSV + NT - 1) / NT;      // sample vectors per thread
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ uint32_t s_warp[W];
+    __shared__ uint32_t s_res[4];
+    __shared__ uint32_t s_cnt[W];
+    __shared__ uint32_t s_kmax[W];
+    __shared__ uint32_t s_gq[3 * W];
+    __shared__ Segments<E> s_seg;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row = blockIdx.x;
+    const int64_t n = valid_cols(a, row);
+    const int k = a.k;
+    if (n <= k) {
+        short_row<E, NT, GATHER>(a, row, n, 0, k);
+        return;
+    }
+    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
+    const uint4 *xv = reinterpret_cast<const uint4 *>(xrow);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
+    uint2 *list = reinterpret_cast<uint2 *>(smem + a.smem_list_off);
+    int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
+    const int rs = a.region_stride;
+    const uint32_t capw = static_cast<uint32_t>(a.list_cap);
+    const int64_t nvec = (n * static_cast<int64_t>(sizeof(E))) >> 4;  // full 16-byte vectors
+    const int64_t tail0 = nvec * V;
+    for (int i = tid; i < a.hist_bins; i += NT) hist[i] = 0u;
+
+    // ---- 1. threshold estimate from a strided sample of the row's vectors
+    const int ns = static_cast<int>(nvec < kSV ? nvec : kSV);
+    const int64_t step = ns > 0 ? nvec / ns : 1;
+    uint4 sq[kS];
+#pragma unroll
+    for (int j = 0; j < kS; ++j) {
+        const int i = tid + j * NT;
+        sq[j] = i < ns ? __ldg(xv + i * step) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // warp w streams vectors [vb, ve); its first loads are issued before the estimate
+    const int64_t per = nvec / W, rem = nvec % W;
+    const int64_t vb = warp * per + (warp < rem ? warp : rem);
+    const int64_t ve = vb + per + (warp < rem ? 1 : 0);
+    uint4 q[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t v = vb + u * 32 + lane;
+        q[u] = v < ve ? __ldcs(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();  // histogram cleared
+    const uint32_t tkey = ns > 0 ? estimate_threshold<E, NT, kS>(a, sq, ns, static_cast<float>(k),
+                                                                 static_cast<float>(n), hist, s_res, s_warp)
+                                 : 0u;
+
+    // ---- 2. one pass: warp w streams its vectors into its region
+    uint2 *reg = list + warp * rs;
+    const bool positive = tkey > T::kSignKey;  // raw-bit compare suffices above +/-0
+    const uint32_t tsg = tkey ^ T::kSignKey;
+    uint32_t smax = T::kSmaxInit, umax = T::kUmaxInit;
+    uint32_t off = 0;   // pairs appended to this warp's region (warp-uniform)
+    uint32_t kmax = 0;  // largest candidate key seen by this lane
+    for (int64_t base = vb; base < ve; base += 32 * U) {
+        if (base != vb) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = base + u * 32 + lane;
+                q[u] = v < ve ? __ldcs(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        uint32_t pm[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            T::nan_acc(q[u], smax, umax);  // zero vectors past the range are NaN-free
+            if (positive) {
+                pm[u] = T::ge_mask_raw(q[u], tsg);  // and select nothing
+            } else {
+                pm[u] = base + u * 32 + lane < ve ? T::ge_mask_key(q[u], tkey) : 0u;
+            }
+        }
+        // offsets in (u, lane) order: warp scans of the counts, two u's per word (16-bit fields)
+        uint32_t ex[U], tot = 0;
+#pragma unroll
+        for (int u = 0; u < U; u += 2) {
+            const uint32_t cw = static_cast<uint32_t>(__popc(pm[u])) | (static_cast<uint32_t>(__popc(pm[u + 1])) << 16);
+            uint32_t inc = cw;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const uint32_t all = __shfl_sync(kFull, inc, 31);
+            const uint32_t e = inc - cw;
+            ex[u] = tot + (e & 0xffffu);
+            tot += all & 0xffffu;
+            ex[u + 1] = tot + (e >> 16);
+            tot += all >> 16;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint32_t m = pm[u];
+            if (!m) continue;
+            const uint4 qu = q[u];
+            const int col0 = static_cast<int>((base + u * 32 + lane) * V);
+            uint32_t p = off + ex[u];
+            do {
+                const int t = __ffs(m) - 1;
+                m &= m - 1u;
+                const E e = T::lane_of(qu, t);
+                kmax = max(kmax, T::key(e));
+                reg[p < capw ? p : capw] = make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(col0 + t));
+                ++p;
+            } while (m);
+        }
+        off += tot;
+    }
+    if (warp == W - 1) {  // the < 16-byte tail, after the last vector
+        const int64_t j = tail0 + lane;
+        const bool in = j < n;
+        const E e = in ? xrow[j] : static_cast<E>(0);
+        if (in) T::nan_acc1(e, smax, umax);
+        const bool pass = in && T::key(e) >= tkey;
+        const uint32_t bp = __ballot_sync(kFull, pass);
+        if (pass) {
+            kmax = max(kmax, T::key(e));
+            const uint32_t p = off + __popc(bp & ((1u << lane) - 1u));
+            reg[p < capw ? p : capw] = make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(j));
+        }
+        off += __popc(bp);
+    }
+    kmax = __reduce_max_sync(kFull, kmax);
+    if (lane == 0) {
+        s_cnt[warp] = off;
+        s_kmax[warp] = kmax;
+    }
+    if (__syncthreads_or(T::has_nan(smax, umax)) && tid == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
+
+    // ---- 3. exact selection on the regions, or the fallback
+    uint32_t L = 0, thi = 0;
+    bool over = false;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+        L += s_cnt[w];
+        over |= s_cnt[w] > capw;
+        thi = max(thi, s_kmax[w]);
+    }
+    if (!over && L >= static_cast<uint32_t>(k)) {
+        select_regions<E, NT, GATHER>(a, row, list, rs, s_cnt, tkey, thi, hist, s_res, s_warp, s_gq, glist);
+        return;
+    }
+    if (tid == 0) {
+        s_seg.n = 1;
+        s_seg.bits[0] = xrow;
+        s_seg.cols[0] = nullptr;
+        s_seg.base[0] = 0;
+        s_seg.pre[0] = 0;
+        s_seg.pre[1] = static_cast<uint32_t>(n);
+    }
+    __syncthreads();
+    select_segments<E, NT, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
+}
+
 // Raises a kernel's dynamic shared-memory limit once per device; later calls that need no more
 // than what was set skip the driver call.
 template <typename K>
@@ -1342,40 +1869,40 @@ cudaError_t raise_smem_limit(K kern, int *set_smem, size_t smem)
     return cudaSuccess;
 }
 
+// Kernel of a mode for one element type, CTA size and gather flag; null where that combination
+// is never launched (row_kernel: 128/256/512 threads; split_kernel: 256; stream and wide: 512).
+template <typename E, int NT, bool G>
+void (*kernel_of(int mode))(TopkArgs)
+{
+    if (mode == kModeRow) return row_kernel<E, NT, G>;
+    if constexpr (NT == 256) {
+        if (mode == kModeSplit) return split_kernel<E, NT, G>;
+    }
+    if constexpr (NT == 512) {
+        if (mode == kModeStream) return stream_kernel<E, NT, G>;
+        if (mode == kModeWide) return wide_kernel<E, NT, G>;
+    }
+    return nullptr;
+}
+
 template <typename E, int NT, bool G>
 cudaError_t launch_one(int mode, size_t smem, const TopkArgs &a, cudaStream_t stream, int64_t grid, bool query,
                        int *blocks_per_sm)
 {
-    static int set_row[64] = {}, set_split[64] = {}, set_stream[64] = {};
-    cudaError_t e;
-    if (mode == kModeRow)
-        e = raise_smem_limit(row_kernel<E, NT, G>, set_row, smem);
-    else if (mode == kModeSplit)
-        e = raise_smem_limit(split_kernel<E, NT, G>, set_split, smem);
-    else
-        e = raise_smem_limit(stream_kernel<E, NT, G>, set_stream, smem);
+    static int set_smem[4][64] = {};
+    void (*kern)(TopkArgs) = kernel_of<E, NT, G>(mode);
+    if (!kern || mode < 0 || mode > 3) return cudaErrorInvalidValue;
+    cudaError_t e = raise_smem_limit(kern, set_smem[mode], smem);
     if (e != cudaSuccess) return e;
-    if (query) {
-        if (mode == kModeRow)
-            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, row_kernel<E, NT, G>, NT, smem);
-        if (mode == kModeSplit)
-            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, split_kernel<E, NT, G>, NT, smem);
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, stream_kernel<E, NT, G>, NT, smem);
-    }
+    if (query) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kern, NT, smem);
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const dim3 g(static_cast<unsigned>(grid)), b(NT);
-    if (mode == kModeRow)
-        row_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
-    else if (mode == kModeSplit)
-        split_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
-    else
-        stream_kernel<E, NT, G><<<g, b, smem, stream>>>(a);
+    kern<<<dim3(static_cast<unsigned>(grid)), dim3(NT), smem, stream>>>(a);
     return cudaGetLastError();
 }
 
 // Dispatch over (threads, gather) for one element type.  Thread counts: row_kernel 128/256/512,
-// split_kernel 256, stream_kernel 512.
+// split_kernel 256, stream_kernel and wide_kernel 512.
 template <typename E>
 cudaError_t launch_e(int mode, int threads, bool gather, size_t smem, const TopkArgs &a, cudaStream_t s,
                      int64_t grid, bool query, int *blocks_per_sm)
@@ -1385,7 +1912,7 @@ cudaError_t launch_e(int mode, int threads, bool gather, size_t smem, const Topk
         return gather ? launch_one<E, 256, true>(mode, smem, a, s, grid, query, blocks_per_sm)
                       : launch_one<E, 256, false>(mode, smem, a, s, grid, query, blocks_per_sm);
     }
-    if (mode == kModeStream) {
+    if (mode == kModeStream || mode == kModeWide) {
         if (threads != 512) return cudaErrorInvalidValue;
         return gather ? launch_one<E, 512, true>(mode, smem, a, s, grid, query, blocks_per_sm)
                       : launch_one<E, 512, false>(mode, smem, a, s, grid, query, blocks_per_sm);

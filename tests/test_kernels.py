@@ -1,0 +1,127 @@
+"""Each selection kernel, forced with SEL_PLAN, against the oracle on every row.
+
+The automatic plan sends a shape to one kernel; these cases force the
+others onto the same shapes so that every kernel's paths run: several ring
+chunks with a ragged tail, a ring that holds the whole row, threshold
+estimates that keep too few or too many keys (sorted rows, constant rows),
+ties, infinities, variable row ends, NaN rows and the fused gather.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+from tests._util import compare_with_oracle, to_bits, to_torch
+from tests.test_topk import make_case, run
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # (dtype, rows, cols, k, kind)
+    ("f32", 3, 70001, 1000, "normal"),
+    ("bf16", 2, 204803, 1024, "normal"),
+    ("f32", 2, 20000, 300, "normal"),
+    ("bf16", 3, 100000, 4096, "ascending"),
+    ("bf16", 3, 100000, 4096, "descending"),
+    ("f32", 2, 100000, 64, "equal"),
+    ("f32", 2, 100003, 4096, "zeros_inf"),
+    ("bf16", 5, 70000, 700, "levels"),
+    ("f32", 4, 131072, 4096, "normal"),
+]
+
+MODES = ["wide", "split", "stream"]
+
+
+def padded(dtype, rows, cols, k, kind, row_end=None):
+    seed = zlib.crc32(repr((dtype, rows, cols, k, kind)).encode())
+    e = syn.elem_bytes(dtype)
+    stride = (cols * e + 15) // 16 * 16 // e
+    return make_case(dtype, rows, cols, k, kind, seed, stride=stride, row_end=row_end)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+def test_forced_kernel(mode, case, monkeypatch):
+    monkeypatch.setenv("SEL_PLAN", mode)
+    dtype, rows, cols, k, kind = case
+    w = padded(*case)
+    x, end, vals, idx, nan, err = run(w)
+    assert err == 0 and nan == 0
+    compare_with_oracle(w, np.arange(rows), idx.cpu().numpy(), to_bits(vals), True)
+    x, end, vals, idx, nan, err = run(w, sorted_index=False, idx_dtype="i64", want_values=False)
+    assert err == 0
+    compare_with_oracle(w, np.arange(rows), idx.cpu().numpy(), None, False)
+
+
+# shapes for the per-warp candidate regions of the streaming kernel: thresholds at or below zero
+# (raw-bit compare not usable), rows shorter than one 16-byte vector, ragged tails, candidates
+# piling into one warp's range, and a row whose every element ties
+WIDE_CASES = [
+    ("f32", 3, 5000, 4096, "normal"),
+    ("bf16", 2, 3000, 2999, "normal"),
+    ("f32", 4, 3, 1, "normal"),
+    ("bf16", 4, 7, 2, "normal"),
+    ("bf16", 3, 100007, 333, "zeros_inf"),
+    ("f32", 2, 66001, 4096, "ascending"),
+    ("bf16", 2, 70000, 1000, "equal"),
+    ("f32", 2, 131072, 4096, "two_level"),
+]
+
+
+@pytest.mark.parametrize("case", WIDE_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_wide_kernel_paths(case, monkeypatch):
+    monkeypatch.setenv("SEL_PLAN", "wide")
+    w = padded(*case)
+    x, end, vals, idx, nan, err = run(w)
+    assert err == 0 and nan == 0
+    compare_with_oracle(w, np.arange(case[1]), idx.cpu().numpy(), to_bits(vals), True)
+    x, end, vals, idx, nan, err = run(w, sorted_index=False, idx_dtype="i64", want_values=False)
+    assert err == 0
+    compare_with_oracle(w, np.arange(case[1]), idx.cpu().numpy(), None, False)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_forced_row_end_and_nan(mode, monkeypatch):
+    monkeypatch.setenv("SEL_PLAN", mode)
+    rows, cols, k = 6, 90000, 2000
+    row_end = np.array([0, 1999, 2000, 2001, 45000, 200000], dtype=np.int32)
+    w = padded("f32", rows, cols, k, "normal", row_end=row_end)
+    x, end, vals, idx, nan, err = run(w)
+    assert err == 0 and nan == 0
+    compare_with_oracle(w, np.arange(rows), idx.cpu().numpy(), to_bits(vals), True)
+    # a NaN inside the valid part of a long row raises the flag; one past row_end does not
+    bits = w["x"].copy()
+    bits[4, 50000] = 0x7FC00000  # beyond row_end[4] = 45000: ignored
+    w2 = dict(w, x=bits)
+    _, _, _, _, nan, err = run(w2)
+    assert err == 0 and nan == 0
+    bits[5, 70000] = 0x7FC00000
+    w3 = dict(w, x=bits)
+    _, _, vals, idx, nan, err = run(w3)
+    assert err == 0 and nan == 1
+    compare_with_oracle(w3, np.arange(5), idx.cpu().numpy()[:5], to_bits(vals)[:5], True)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_forced_fused_gather(mode, monkeypatch):
+    monkeypatch.setenv("SEL_PLAN", mode)
+    import gather_radix_select_gb300 as g
+    rng = np.random.default_rng(5)
+    b, rows, cols, k, ng, d = 2, 4, 150000, 1024, 700, 64
+    v = rng.standard_normal((rows, cols)).astype(np.float32)
+    x = to_torch(syn.f32_to_bf16_bits(v), "bf16")
+    key_bits = syn.f32_to_bf16_bits(rng.standard_normal((b, cols, d)).astype(np.float32)).reshape(b, cols, d)
+    key = to_torch(key_bits, "bf16")
+    end = torch.from_numpy(np.array([150000, 1000, 90001, 149999], dtype=np.int32)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, fidx, fout = g.topk_gather(x, k, key, ng, end=end, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o_idx, _, _ = oracle.topk(syn.f32_to_bf16_bits(v), "bf16", k, row_end=end.cpu().numpy(), sorted_index=True,
+                              cols=cols)
+    assert (fidx.cpu().numpy().astype(np.int64) == o_idx).all()
+    want, bad = oracle.gather_rows(key_bits, o_idx[:, :ng], b)
+    assert bad == 0 and (to_bits(fout) == want).all()

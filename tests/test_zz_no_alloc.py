@@ -69,8 +69,9 @@ def same(a, b):
     assert na == nb and ea == eb == 0
 
 
-def test_noalloc_matches_workspace_entry_point_on_split_rows():
-    # four 204800-wide bf16 rows: split over many CTAs, so the scratch is really used
+def test_noalloc_matches_workspace_entry_point_on_split_rows(monkeypatch):
+    # four 204800-wide bf16 rows split over many CTAs (forced), so the scratch is really used
+    monkeypatch.setenv("SEL_PLAN", "split")
     w = syn.workload("indexer_bf16_4x204800_k1024")
     x = torch.from_numpy(w["x"].view(np.int16)).view(torch.bfloat16).cuda()
     need, res = run_both(x, 1, w["rows"], w["cols"], w["k"], 0, True)
@@ -79,7 +80,8 @@ def test_noalloc_matches_workspace_entry_point_on_split_rows():
     same(res[0], res[2])
 
 
-def test_noalloc_matches_on_fp32_split_rows_with_row_end_and_nan():
+def test_noalloc_matches_on_fp32_split_rows_with_row_end_and_nan(monkeypatch):
+    monkeypatch.setenv("SEL_PLAN", "split")
     rng = np.random.default_rng(31)
     rows, cols, k = 6, 131072, 4096
     v = (rng.standard_normal((rows, cols)) * 2).astype(np.float32)
@@ -93,7 +95,7 @@ def test_noalloc_matches_on_fp32_split_rows_with_row_end_and_nan():
     assert res[0][2] == 1
 
 
-def test_noalloc_without_scratch_and_oversize_rejection():
+def test_noalloc_without_scratch_and_oversize_rejection(monkeypatch):
     # a shape that needs no scratch runs too
     rng = np.random.default_rng(5)
     x = torch.from_numpy(rng.standard_normal((300, 2048)).astype(np.float32)).cuda()
@@ -102,6 +104,7 @@ def test_noalloc_without_scratch_and_oversize_rejection():
     same(res[0], res[1])
     same(res[0], res[2])
     # a shape whose scratch exceeds the built-in array is refused before any launch
+    monkeypatch.setenv("SEL_PLAN", "split")
     L = lib()
     from gather_radix_select_gb300 import _native
     rows, cols = 300, 2_000_000
