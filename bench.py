@@ -139,6 +139,37 @@ class ClockSampler:
 # GPU arm
 # ----------------------------------------------------------------------------
 
+def kernel_source_hash() -> str:
+    """Short hash of the selection kernels' source: a stored DRAM traffic figure is used only while it
+    still describes the kernels that run."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("topk_impl.cuh", "sel_internal.h", "ptx.cuh"):
+        with open(os.path.join(ROOT, "gather_radix_select_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def stored_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of `kernel` on `workload`
+    from profiles/traffic.md, or None when absent or taken on other kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    src = kernel_source_hash()
+    for ln in lines:
+        cells = [c.strip() for c in ln.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == workload and cells[1] == kernel and cells[3] == src:
+            try:
+                return int(cells[2])
+            except ValueError:
+                return None
+    return None
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -322,7 +353,11 @@ def gpu_arm(args):
         e2e_ms, h2d, d2h = e2e_measure(w, dev, max(2, min(args.steps, 10)), 2)
         per = per_workload(args, dev, flush, peak) if not args.no_per_workload else None
         cpu = cpu_baseline(args.workload)
-        kname = "topk_kernel<bf16,gather>" if w.get("key") is not None else "topk_kernel"
+        import gather_radix_select_gb300 as g
+
+        fused = w.get("key") is not None
+        kname = g.kernel_name(runner.x.dtype, w["rows"], w["cols"], w["k"], w["n_gather"] if fused else 0)
+        traffic = stored_traffic(args.workload, kname)
         result = {
             "metric": METRIC,
             "value": round(value, 2),
@@ -342,8 +377,9 @@ def gpu_arm(args):
                        "l2": "flushed before every timed step (256 MiB write, untimed)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": kname,
-                         "peak_kind": peak_kind},
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": kname + ("<%s,gather>" % w["dtype"] if fused else "<%s>" % w["dtype"]),
+                         "algorithmic_bytes": nbytes, "peak_kind": peak_kind},
             "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "ms_per_step": round(e2e_ms, 4)},
@@ -372,7 +408,9 @@ def per_workload(args, dev, flush, peak):
         ms = statistics.median(times)
         nb = step_bytes(w)
         tb = topk_bytes(w)
-        out[name] = {"ms": round(ms, 5), "rows_per_s": round(w["rows"] / (ms * 1e-3), 1),
+        fused = w.get("key") is not None
+        out[name] = {"kernel": r.g.kernel_name(r.x.dtype, w["rows"], w["cols"], w["k"], w["n_gather"] if fused else 0),
+                     "ms": round(ms, 5), "rows_per_s": round(w["rows"] / (ms * 1e-3), 1),
                      "gbs": round(nb / (ms * 1e-3) / 1e9, 2), "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
                      "bytes": nb, "topk_bytes": tb, "fused_gather": w.get("key") is not None}
         if w.get("key") is not None:

@@ -20,7 +20,8 @@ import torch
 from . import _native
 from ._native import SelError, SEL_MAX_K
 
-__all__ = ["topk", "gather_rows", "topk_gather", "stride_requirement", "max_cols", "workspace_size", "SelError",
+__all__ = ["topk", "gather_rows", "topk_gather", "stride_requirement", "max_cols", "workspace_size", "kernel_name",
+           "SelError",
            "SEL_MAX_K", "library_path"]
 
 _DTYPES = {torch.float32: _native.SEL_F32, torch.bfloat16: _native.SEL_BF16}
@@ -66,6 +67,15 @@ def workspace_size(dtype: torch.dtype, rows: int, cols: int, k: int, device=None
     """Scratch bytes a top-k call of this shape needs on ``device`` (0 for most shapes)."""
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         return int(_native.load().sel_topk_workspace_size(_DTYPES[dtype], rows, cols, int(k)))
+
+
+def kernel_name(dtype: torch.dtype, rows: int, cols: int, k: int, n_gather: int = 0, device=None) -> str:
+    """Kernel a top-k (n_gather == 0) or fused top-k + gather call of this shape launches on ``device``."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        name = _native.load().sel_topk_kernel_name(_DTYPES[dtype], rows, cols, int(k), int(n_gather))
+    if name is None:
+        raise ValueError("invalid shape for kernel_name")
+    return name.decode()
 
 
 def _workspace(nbytes: int, device, stream):

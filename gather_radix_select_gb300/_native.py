@@ -34,6 +34,7 @@ SIGNATURES = {
     "sel_topk_noalloc": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _int, _int, _int, _int,
                                 _vp, _i64, _vp, _i64, _vp, _vp, _vp]),
     "sel_strerror": (ctypes.c_char_p, [_int]),
+    "sel_topk_kernel_name": (ctypes.c_char_p, [_int, _i64, _i64, _int, _i64]),
 }
 
 _lock = threading.Lock()

@@ -458,6 +458,21 @@ size_t sel_topk_workspace_size(int dtype, int64_t rows, int64_t cols, int k)
     return p.ws_bytes;
 }
 
+const char *sel_topk_kernel_name(int dtype, int64_t rows, int64_t cols, int k, int64_t n_gather)
+{
+    if ((dtype != SEL_F32 && dtype != SEL_BF16) || rows <= 0 || cols < 0 || k < 1 || k > SEL_MAX_K) return nullptr;
+    if (n_gather < 0 || n_gather > k) return nullptr;
+    Plan p;
+    if (cached_plan(dtype, rows, cols, k, n_gather > 0, n_gather, p) != SEL_OK) return nullptr;
+    switch (p.mode) {
+    case sel::kModeRow: return "row_kernel";
+    case sel::kModeSplit: return "split_kernel";
+    case sel::kModeWide: return "wide_kernel";
+    case sel::kModeStream: return "stream_kernel";
+    default: return nullptr;
+    }
+}
+
 int sel_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride, const int32_t *row_end, int k,
              int sorted_index, int idx_dtype, int want_values, void *out_idx, int64_t out_idx_stride, void *out_val,
              int64_t out_val_stride, void *workspace, size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag,

@@ -24,8 +24,8 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == sorted(["sel_gather_rows", "sel_max_cols", "sel_stride_requirement",
-                                         "sel_strerror", "sel_topk", "sel_topk_gather", "sel_topk_noalloc",
-                                         "sel_topk_workspace_size"])
+                                         "sel_strerror", "sel_topk", "sel_topk_gather", "sel_topk_kernel_name",
+                                         "sel_topk_noalloc", "sel_topk_workspace_size"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -78,6 +78,14 @@ def test_workspace_size_rejects_bad_arguments(lib):
     assert lib.sel_topk_workspace_size(0, 4, 64, 0) == 0
     assert lib.sel_topk_workspace_size(0, 4, 64, 5000) == 0
     assert lib.sel_topk_workspace_size(0, 0, 64, 8) == 0
+
+
+def test_kernel_name_rejects_bad_arguments(lib):
+    # invalid shapes answer NULL without touching the device
+    assert lib.sel_topk_kernel_name(7, 4, 64, 8, 0) is None
+    assert lib.sel_topk_kernel_name(0, 4, 64, 0, 0) is None
+    assert lib.sel_topk_kernel_name(1, 4, 64, 8, 9) is None
+    assert lib.sel_topk_kernel_name(1, 4, 64, 8, -1) is None
 
 
 def test_gather_rejections(lib):
