@@ -143,14 +143,15 @@ int hist_agg()
 }
 
 // Candidate capacity of wide_kernel for rows of `cols` elements.  The threshold is estimated
-// from a sample of up to kWideSampleKeys keys (whole 16-byte vectors) (mu = k * sample / cols of the k
+// from a sample of up to kWideThreads * kWideSampleVecsPerLane 16-byte vectors (mu = k * sample / cols of the k
 // expected there, keeping mu * 9/8 + 3 sqrt(mu) + 4 sampled keys); the list holds that many
 // scaled to the row, plus four standard deviations of the count.
 int64_t wide_cap(int dtype, int64_t cols, int k)
 {
     const int64_t e = elem_bytes(dtype);
     const int64_t nvec = cols * e / 16;
-    const int64_t sample = std::min<int64_t>(nvec, sel::kWideSampleKeys / (16 / e)) * (16 / e);
+    const int64_t sample =
+        std::min<int64_t>(nvec, static_cast<int64_t>(sel::kWideThreads) * sel::kWideSampleVecsPerLane) * (16 / e);
     if (sample <= 0) return round_up(cols, 8);
     const double f = static_cast<double>(sample) / static_cast<double>(cols);
     const double mu = static_cast<double>(k) * f;

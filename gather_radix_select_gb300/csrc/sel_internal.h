@@ -13,7 +13,7 @@ constexpr int kMaxLevels = 4;       // radix passes (digits) at most
 constexpr int kMaxSlice = 65536;    // elements of a row staged by one CTA (list offsets are 16-bit)
 constexpr int kMaxChunks = 16;      // bulk-copy chunks per CTA slice
 constexpr uint32_t kChunkBytes = 16384;
-constexpr int kWideSampleKeys = 2048;  // wide_kernel: keys in a row's threshold sample (16-byte vectors)
+constexpr int kWideSampleVecsPerLane = 1;  // wide_kernel: 16-byte vectors per lane in the threshold sample
 constexpr int kWideThreads = 512;
 constexpr int kMaxParts = 64;       // CTAs splitting one row (split_kernel)
 constexpr int kModeRow = 0;         // row_kernel: one CTA per row, row staged in shared memory

@@ -91,6 +91,12 @@ struct Elem<uint32_t> {  // fp32 bit patterns
         smax = static_cast<uint32_t>(max(static_cast<int>(smax), m));
         umax = max(umax, max(max(q.x, q.y), max(q.z, q.w)));
     }
+    // Only the negative-NaN half of nan_acc: enough where every positive NaN passes the filter
+    // (a positive threshold) and is checked among the candidates.
+    static __device__ __forceinline__ void nan_acc_neg(const uint4 &q, uint32_t &umax)
+    {
+        umax = max(umax, max(max(q.x, q.y), max(q.z, q.w)));
+    }
     static __device__ __forceinline__ void nan_acc1(uint32_t u, uint32_t &smax, uint32_t &umax)
     {
         smax = static_cast<uint32_t>(max(static_cast<int>(smax), static_cast<int>(u)));
@@ -166,6 +172,10 @@ struct Elem<uint16_t> {  // bf16 bit patterns
     static __device__ __forceinline__ void nan_acc(const uint4 &q, uint32_t &smax, uint32_t &umax)
     {
         smax = __vmaxs2(smax, __vmaxs2(__vmaxs2(q.x, q.y), __vmaxs2(q.z, q.w)));
+        umax = __vmaxu2(umax, __vmaxu2(__vmaxu2(q.x, q.y), __vmaxu2(q.z, q.w)));
+    }
+    static __device__ __forceinline__ void nan_acc_neg(const uint4 &q, uint32_t &umax)
+    {
         umax = __vmaxu2(umax, __vmaxu2(__vmaxu2(q.x, q.y), __vmaxu2(q.z, q.w)));
     }
     static __device__ __forceinline__ void nan_acc1(uint16_t h, uint32_t &smax, uint32_t &umax)
@@ -1416,8 +1426,9 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) stream_kernel(const 
 // ---------------------------------------------------------------------------
 // wide_kernel: one CTA per row for rows too wide to stage whole; two CTAs
 // share an SM, so one CTA's selection overlaps the other's streaming.
-//  1. Threshold estimate from a strided sample of the row's 16-byte vectors
-//     (kWideSampleKeys keys), held in registers: its top-digit histogram and a
+//  1. Threshold estimate from a sample held in registers -- the first
+//     16-byte vector of every lane's stream (16 runs of 32 consecutive
+//     vectors spread over the row), loaded anyway: its top-digit histogram and a
 //     second digit give a key that about mu*9/8 + 3 sqrt(mu) + 4 sampled keys
 //     reach (mu: the sample's share of the k).
 //  2. One pass over the row, read from HBM once: warp w streams a contiguous
@@ -1434,10 +1445,14 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) stream_kernel(const 
 // ---------------------------------------------------------------------------
 constexpr int kWideUnroll = 4;
 
-// Threshold key estimated from `ns` sample vectors held in registers: thread t holds samples
-// t, t + NT, ... in q[].  share / population: the k wanted out of the row's n.  Leaves h zero.
-template <typename E, int NT, int kS>
-__device__ uint32_t estimate_threshold(const TopkArgs &a, const uint4 (&q)[kS], int ns, float share,
+// Threshold key estimated from sample vectors held in registers: q[0, kSU) of each thread, those
+// with bit j of `ok` set valid, `ns` valid vectors over the CTA.  share / population: the k wanted
+// out of the row's n.  mu = the sample's expected share of the k; the estimate keeps
+// mu*(1+1/8) + 3*sqrt(mu) + 4 sampled keys at or above it: the top digit from a histogram, a
+// second digit from the sampled keys in that bin, so the key is resolved to 22 bits (fp32) or
+// fully (bf16).  0 (keep everything) if that is the whole sample.  Leaves h zero.
+template <typename E, int NT, int kSU, int kQ>
+__device__ uint32_t estimate_threshold(const TopkArgs &a, const uint4 (&q)[kQ], uint32_t ok, int ns, float share,
                                        float population, uint32_t *h, uint32_t *s_res, uint32_t *s_warp)
 {
     using T = Elem<E>;
@@ -1446,12 +1461,12 @@ __device__ uint32_t estimate_threshold(const TopkArgs &a, const uint4 (&q)[kS], 
     const int sh0 = T::KB - a.bits[0];
     const int nb0 = 1 << a.bits[0];
 #pragma unroll
-    for (int j = 0; j < kS; ++j) {
-        const bool ok = tid + j * NT < ns;
+    for (int j = 0; j < kSU; ++j) {
+        const bool okj = (ok >> j) & 1u;
         E el[V];
         T::unpack(q[j], el);
 #pragma unroll
-        for (int t = 0; t < V; ++t) hist_add(h, T::key(el[t]) >> sh0, ok, lane, a.agg != 0);
+        for (int t = 0; t < V; ++t) hist_add(h, T::key(el[t]) >> sh0, okj, lane, a.agg != 0);
     }
     __syncthreads();
     const float total = static_cast<float>(ns) * V;
@@ -1471,8 +1486,8 @@ __device__ uint32_t estimate_threshold(const TopkArgs &a, const uint4 (&q)[kS], 
     const int sh1 = sh0 - b2;
     const uint32_t m2 = (1u << b2) - 1u;
 #pragma unroll
-    for (int j = 0; j < kS; ++j) {
-        if (tid + j * NT < ns) {
+    for (int j = 0; j < kSU; ++j) {
+        if ((ok >> j) & 1u) {
             E el[V];
             T::unpack(q[j], el);
 #pragma unroll
@@ -1691,8 +1706,8 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
     constexpr int V = T::V;
     constexpr int W = NT / 32;
     constexpr int U = kWideUnroll;
-    constexpr int kSV = kWideSampleKeys / V;     // sample vectors
-    constexpr int kS = (kSV + NT - 1) / NT;      // sample vectors per thread
+    constexpr int kSU = kWideSampleVecsPerLane;
+    static_assert(kSU <= U, "the sample comes from the first loads");
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ uint32_t s_warp[W];
     __shared__ uint32_t s_res[4];
@@ -1720,16 +1735,9 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
     const int64_t tail0 = nvec * V;
     for (int i = tid; i < a.hist_bins; i += NT) hist[i] = 0u;
 
-    // ---- 1. threshold estimate from a strided sample of the row's vectors
-    const int ns = static_cast<int>(nvec < kSV ? nvec : kSV);
-    const int64_t step = ns > 0 ? nvec / ns : 1;
-    uint4 sq[kS];
-#pragma unroll
-    for (int j = 0; j < kS; ++j) {
-        const int i = tid + j * NT;
-        sq[j] = i < ns ? __ldg(xv + i * step) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    // warp w streams vectors [vb, ve); its first loads are issued before the estimate
+    // ---- 1. warp w streams vectors [vb, ve) of the row; its first loads double as the sample
+    //         for the threshold estimate (kWideSampleVecsPerLane vectors per lane: 16 runs of
+    //         consecutive vectors spread over the row)
     const int64_t per = nvec / W, rem = nvec % W;
     const int64_t vb = warp * per + (warp < rem ? warp : rem);
     const int64_t ve = vb + per + (warp < rem ? 1 : 0);
@@ -1739,9 +1747,17 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
         const int64_t v = vb + u * 32 + lane;
         q[u] = v < ve ? __ldcs(xv + v) : make_uint4(0u, 0u, 0u, 0u);
     }
+    uint32_t ok = 0;
+#pragma unroll
+    for (int j = 0; j < kSU; ++j) ok |= static_cast<uint32_t>(vb + j * 32 + lane < ve) << j;
+    int ns = 0;  // valid sample vectors over the CTA
+    for (int w = 0; w < W; ++w) {
+        const int64_t size = per + (w < rem ? 1 : 0);
+        ns += static_cast<int>(size < 32 * kSU ? size : 32 * kSU);
+    }
     __syncthreads();  // histogram cleared
-    const uint32_t tkey = ns > 0 ? estimate_threshold<E, NT, kS>(a, sq, ns, static_cast<float>(k),
-                                                                 static_cast<float>(n), hist, s_res, s_warp)
+    const uint32_t tkey = ns > 0 ? estimate_threshold<E, NT, kSU, U>(a, q, ok, ns, static_cast<float>(k),
+                                                                     static_cast<float>(n), hist, s_res, s_warp)
                                  : 0u;
 
     // ---- 2. one pass: warp w streams its vectors into its region
@@ -1751,21 +1767,34 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
     uint32_t smax = T::kSmaxInit, umax = T::kUmaxInit;
     uint32_t off = 0;   // pairs appended to this warp's region (warp-uniform)
     uint32_t kmax = 0;  // largest candidate key seen by this lane
+    // a positive NaN among the candidates; an estimate above the +inf key came from a sampled NaN
+    bool pnan = tkey > T::key(static_cast<E>(T::kInfMagnitude));
     for (int64_t base = vb; base < ve; base += 32 * U) {
         if (base != vb) {
+            if (base + 32 * U <= ve) {  // a full iteration (warp-uniform): no bounds checks
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = base + u * 32 + lane;
-                q[u] = v < ve ? __ldcs(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+                for (int u = 0; u < U; ++u) q[u] = __ldcs(xv + base + u * 32 + lane);
+            } else {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = base + u * 32 + lane;
+                    q[u] = v < ve ? __ldcs(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+                }
             }
         }
         uint32_t pm[U];
+        if (positive) {
+            // zero vectors past the range select nothing and are NaN-free; a positive NaN always
+            // passes, so only negative NaNs need the running maximum
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            T::nan_acc(q[u], smax, umax);  // zero vectors past the range are NaN-free
-            if (positive) {
-                pm[u] = T::ge_mask_raw(q[u], tsg);  // and select nothing
-            } else {
+            for (int u = 0; u < U; ++u) {
+                T::nan_acc_neg(q[u], umax);
+                pm[u] = T::ge_mask_raw(q[u], tsg);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                T::nan_acc(q[u], smax, umax);
                 pm[u] = base + u * 32 + lane < ve ? T::ge_mask_key(q[u], tkey) : 0u;
             }
         }
@@ -1799,6 +1828,7 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
                 m &= m - 1u;
                 const E e = T::lane_of(qu, t);
                 kmax = max(kmax, T::key(e));
+                pnan |= T::is_nan(e);
                 reg[p < capw ? p : capw] = make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(col0 + t));
                 ++p;
             } while (m);
@@ -1824,7 +1854,7 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
         s_cnt[warp] = off;
         s_kmax[warp] = kmax;
     }
-    if (__syncthreads_or(T::has_nan(smax, umax)) && tid == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
+    if (__syncthreads_or(pnan || T::has_nan(smax, umax)) && tid == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
 
     // ---- 3. exact selection on the regions, or the fallback
     uint32_t L = 0, thi = 0;
