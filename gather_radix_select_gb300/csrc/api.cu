@@ -22,6 +22,7 @@ constexpr int64_t kSliceMinBytes = 16 * 1024;     // ... at least, when splittin
 constexpr int64_t kSplitMinRowBytes = 64 * 1024;  // rows narrower than this never split
 constexpr int64_t kWideMaxRowBytes = 4 << 20;     // wider rows, when few, split over CTAs instead
 constexpr int kWideHistBins = 2048;               // wide_kernel's range histogram (select_regions)
+constexpr int64_t kRegMaxRowBytes = 16 * 1024;    // longer rows take the staged row kernel by default
 
 int elem_bytes(int dtype) { return dtype == SEL_F32 ? 4 : 2; }
 int idx_bytes(int idx_dtype) { return idx_dtype == SEL_I64 ? 8 : 4; }
@@ -87,6 +88,22 @@ size_t layout_staged(int dtype, int64_t slice, int64_t cap, bool gather, int64_t
     return off;
 }
 
+// Layout of a reg_kernel CTA: histogram | source column per output position (16-bit) | gather
+// list.  Returns the total bytes.
+size_t layout_reg(int k, bool gather, int64_t n_gather, sel::TopkArgs &a)
+{
+    a.slice = 0;
+    a.smem_buf_bytes = 0;
+    a.smem_hist_off = 0;
+    size_t off = static_cast<size_t>(a.hist_bins) * 4;
+    a.smem_list_off = a.smem_mask_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(round_up(static_cast<int64_t>(k) * 2, 16));
+    a.list_cap = 0;
+    a.smem_glist_off = static_cast<uint32_t>(off);
+    if (gather) off += static_cast<size_t>(round_up(n_gather * 4, 16));
+    return off;
+}
+
 // Layout of a stream_kernel CTA (histogram and gather list only).
 size_t layout_stream(bool gather, int64_t n_gather, sel::TopkArgs &a)
 {
@@ -132,14 +149,11 @@ int cached_blocks_per_sm(int dtype, int mode, int threads, bool gather, size_t s
 }
 
 // First-pass histogram flavour: SEL_HIST_AGG=1 selects warp-aggregated atomics
-// (__match_any_sync), anything else plain shared atomics (the default).
+// (__match_any_sync), anything else plain shared atomics (the default).  Read per call.
 int hist_agg()
 {
-    static const int v = [] {
-        const char *e = std::getenv("SEL_HIST_AGG");
-        return (e && e[0] == '1') ? 1 : 0;
-    }();
-    return v;
+    const char *e = std::getenv("SEL_HIST_AGG");
+    return (e && e[0] == '1') ? 1 : 0;
 }
 
 // Candidate capacity of wide_kernel for rows of `cols` elements.  The threshold is estimated
@@ -180,11 +194,14 @@ size_t layout_wide(int64_t cap, bool gather, int64_t n_gather, sel::TopkArgs &a)
     off += static_cast<size_t>(W) * static_cast<size_t>(a.region_stride) * 8;
     a.smem_glist_off = static_cast<uint32_t>(off);
     if (gather) off += static_cast<size_t>(round_up(n_gather * 4, 16));
+    off = static_cast<size_t>(round_up(static_cast<int64_t>(off), 16));
+    a.smem_stage_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(W) * sel::kWideStage * (16 + 4);
     return off;
 }
 
-// Forced kernel choice for tuning and tests: SEL_PLAN=row|split|wide|stream (when that kernel can
-// run the shape).  Unset: the automatic plan.
+// Forced kernel choice for tuning and tests: SEL_PLAN=reg|row|split|wide|stream (when that kernel
+// can run the shape).  Unset: the automatic plan.
 int plan_override()
 {
     const char *e = std::getenv("SEL_PLAN");
@@ -194,6 +211,7 @@ int plan_override()
     if (v == "split") return sel::kModeSplit;
     if (v == "stream") return sel::kModeStream;
     if (v == "wide") return sel::kModeWide;
+    if (v == "reg") return sel::kModeReg8;
     return -1;
 }
 
@@ -213,6 +231,38 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
     const int64_t row_bytes = c1 * e;
     const int64_t max_staged = std::min<int64_t>(sel::kMaxSlice, sel::kMaxChunks * sel::kChunkBytes / e);
 
+    // one CTA per row held in registers: the smallest tile (threads x 16-byte vectors a thread)
+    // that holds the row
+    bool reg_ok = false;
+    Plan reg_plan = p;
+    {
+        struct Tile {
+            int mode, threads, vecs;
+        };
+        const Tile tiles[] = {{sel::kModeReg2, 128, 2}, {sel::kModeReg8, 128, 8}, {sel::kModeReg8, 256, 8},
+                              {sel::kModeReg8, 512, 8}};
+        for (const Tile &t : tiles) {
+            if (c1 > static_cast<int64_t>(t.threads) * t.vecs * (16 / e)) continue;
+            Plan rp = p;
+            const size_t smem = layout_reg(k, gather, n_gather, rp.layout);
+            if (smem > limit || cached_blocks_per_sm(dtype, t.mode, t.threads, gather, smem) <= 0) continue;
+            rp.mode = t.mode;
+            rp.threads = t.threads;
+            rp.smem = smem;
+            rp.grid = rows;
+            rp.ws_bytes = 0;
+            reg_plan = rp;
+            reg_ok = true;
+            break;
+        }
+    }
+    // measured: the register tiles beat the staged row kernel on rows of up to 1024 16-byte
+    // vectors; on longer rows every radix pass over all registers costs more than the staged
+    // kernel's sampled estimate and candidate list
+    if (reg_ok && ((force < 0 && row_bytes <= kRegMaxRowBytes) || force == sel::kModeReg8)) {
+        p = reg_plan;
+        return SEL_OK;
+    }
     // one CTA per row, the row staged whole
     bool row_ok = false;
     Plan row_plan = p;
@@ -318,11 +368,11 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
 int cached_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, Plan &p)
 {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int64_t, int64_t, int, int64_t, int>, Plan> cache;
+    static std::map<std::tuple<int, int, int64_t, int64_t, int, int64_t, int, int>, Plan> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SEL_ECUDA;
     const int force = plan_override();
-    const auto key = std::make_tuple(dev, dtype, rows, cols, k, gather ? n_gather : -1, force);
+    const auto key = std::make_tuple(dev, dtype, rows, cols, k, gather ? n_gather : -1, force, hist_agg());
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
@@ -470,6 +520,8 @@ const char *sel_topk_kernel_name(int dtype, int64_t rows, int64_t cols, int k, i
     case sel::kModeSplit: return "split_kernel";
     case sel::kModeWide: return "wide_kernel";
     case sel::kModeStream: return "stream_kernel";
+    case sel::kModeReg2:
+    case sel::kModeReg8: return "reg_kernel";
     default: return nullptr;
     }
 }

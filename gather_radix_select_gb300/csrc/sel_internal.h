@@ -13,13 +13,17 @@ constexpr int kMaxLevels = 4;       // radix passes (digits) at most
 constexpr int kMaxSlice = 65536;    // elements of a row staged by one CTA (list offsets are 16-bit)
 constexpr int kMaxChunks = 16;      // bulk-copy chunks per CTA slice
 constexpr uint32_t kChunkBytes = 16384;
-constexpr int kWideSampleVecsPerLane = 1;  // wide_kernel: 16-byte vectors per lane in the threshold sample
+constexpr int kWideStage = 64;              // wide_kernel: staged candidate vectors per warp
+constexpr int kWideSampleVecsPerLane = 2;  // wide_kernel: 16-byte vectors per lane in the threshold sample
 constexpr int kWideThreads = 512;
 constexpr int kMaxParts = 64;       // CTAs splitting one row (split_kernel)
 constexpr int kModeRow = 0;         // row_kernel: one CTA per row, row staged in shared memory
 constexpr int kModeSplit = 1;       // split_kernel: `parts` CTAs per row + last-arriver merge
 constexpr int kModeStream = 2;      // stream_kernel: one CTA per row, passes read global memory
 constexpr int kModeWide = 3;        // wide_kernel: one CTA per row, one streaming pass into per-warp lists
+constexpr int kModeReg2 = 4;        // reg_kernel: one CTA per row held in registers, 2 vectors a thread
+constexpr int kModeReg8 = 5;        // reg_kernel: 8 vectors a thread
+constexpr int kNumModes = 6;
 constexpr int kGatherThreads = 256;
 
 // Everything one selection launch needs; passed by value (kernel parameter space).
@@ -46,6 +50,7 @@ struct TopkArgs {
     uint32_t smem_mask_off;   // offset of the per-vector candidate masks (one byte per 16-byte vector)
     uint32_t smem_list_off;   // offset of the candidate list (16-bit offsets within the slice)
     uint32_t smem_glist_off;  // offset of the gather position list (fused only)
+    uint32_t smem_stage_off;  // wide_kernel: staged candidate vectors
     int32_t list_cap;         // capacity of the candidate list
     int32_t region_stride;    // wide_kernel: candidate pairs per warp region (capacity list_cap + 1)
     int32_t agg;              // 1: first-pass histogram with warp-aggregated atomics
@@ -74,7 +79,7 @@ struct GatherArgs {
     int32_t ctas_per_row;
 };
 
-// dtype: 0 fp32, 1 bf16.  mode: kModeRow | kModeSplit | kModeStream | kModeWide.  grid: CTAs to launch.
+// dtype: 0 fp32, 1 bf16.  mode: one of the kMode* values.  grid: CTAs to launch.
 cudaError_t launch_topk(int dtype, int mode, int threads, bool gather, size_t smem_bytes, const TopkArgs &a,
                         int64_t grid, cudaStream_t stream);
 

@@ -106,6 +106,12 @@ struct Elem<uint32_t> {  // fp32 bit patterns
     {
         return static_cast<int>(smax) > 0x7f800000 || umax > 0xff800000u;
     }
+    // Whether some element's key is >= tkey, for a threshold above +/-0 (ts = tkey ^ kSignKey).
+    static __device__ __forceinline__ bool any_ge_raw(const uint4 &q, uint32_t ts)
+    {
+        return max(max(static_cast<int>(q.x), static_cast<int>(q.y)), max(static_cast<int>(q.z), static_cast<int>(q.w))) >=
+               static_cast<int>(ts);
+    }
     // As ge_mask_positive, without the magnitude.
     static __device__ __forceinline__ uint32_t ge_mask_raw(const uint4 &q, uint32_t ts)
     {
@@ -187,6 +193,12 @@ struct Elem<uint16_t> {  // bf16 bit patterns
     {
         return static_cast<int16_t>(smax & 0xffffu) > 0x7f80 || static_cast<int16_t>(smax >> 16) > 0x7f80 ||
                (umax & 0xffffu) > 0xff80u || (umax >> 16) > 0xff80u;
+    }
+    static __device__ __forceinline__ bool any_ge_raw(const uint4 &q, uint32_t ts)
+    {
+        const uint32_t m = __vmaxs2(__vmaxs2(q.x, q.y), __vmaxs2(q.z, q.w));
+        const int t = static_cast<int>(ts << 16);
+        return static_cast<int>(m << 16) >= t || static_cast<int>(m & 0xffff0000u) >= t;
     }
     static __device__ __forceinline__ uint32_t ge_mask_raw(const uint4 &q, uint32_t ts)
     {
@@ -939,6 +951,154 @@ __device__ bool select_staged(const TopkArgs &a, int64_t row, const Segments<E> 
 }
 
 // ---------------------------------------------------------------------------
+// reg_kernel: one CTA per row, the row held in registers.  Thread t owns a
+// contiguous run of re <= R 16-byte vectors (re sized to the row's valid
+// length, so short rows keep every thread busy; the part past the row's end
+// is read with scalar loads, nothing beyond it), so the
+// radix levels run straight from registers, and the thread order is the
+// column order: one pair of block scans orders the compaction.  The
+// compaction records each output position's source column in shared memory,
+// and the outputs are then written in position order (coalesced).
+// Shared memory: histogram | source columns (k x 16 bits) | gather list.
+// ---------------------------------------------------------------------------
+template <int NT, int R>
+struct RegMinBlocks {  // a register budget that holds the run (R vectors) without spilling
+    static constexpr int value = R <= 2 ? MinBlocks<NT>::value : (NT >= 512 ? 1 : (NT >= 256 ? 2 : 4));
+};
+
+template <typename E, int NT, int R, bool GATHER>
+__global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(const TopkArgs a)
+{
+    using T = Elem<E>;
+    constexpr int V = T::V;
+    static_assert(NT * R * V <= 65536, "source columns are 16-bit");
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ uint32_t s_warp[NT / 32];
+    __shared__ uint32_t s_res[4];
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int64_t row = blockIdx.x;
+    const int64_t n = valid_cols(a, row);
+    const int k = a.k;
+    if (n <= k) {
+        short_row<E, NT, GATHER>(a, row, n, 0, k);
+        return;
+    }
+    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
+    uint16_t *src = reinterpret_cast<uint16_t *>(smem + a.smem_list_off);
+    int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
+    for (int i = tid; i < a.hist_bins; i += NT) hist[i] = 0u;
+
+    // ---- the thread's run: re vectors (the row's vectors spread evenly over the threads; slots
+    //      j >= re are skipped, warp-uniformly), cnt valid elements from column e0
+    const int nv = static_cast<int>((n + V - 1) / V);  // vectors holding the row, the last maybe partial
+    const int re = (nv + NT - 1) / NT;                 // <= R by the plan
+    const int e0 = tid * re * V;
+    const int cnt = static_cast<int>(n - e0 < 0 ? 0 : (n - e0 > re * V ? re * V : n - e0));
+    const int nfull = cnt / V;
+    const uint4 *xv = reinterpret_cast<const uint4 *>(xrow) + tid * re;
+    uint4 q[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) q[j] = j < nfull ? __ldg(xv + j) : make_uint4(0u, 0u, 0u, 0u);
+    if (nfull < re && cnt > nfull * V) {  // the row ends inside this vector: scalar loads
+        E el[V];
+#pragma unroll
+        for (int t = 0; t < V; ++t) el[t] = nfull * V + t < cnt ? xrow[e0 + nfull * V + t] : static_cast<E>(0);
+        const uint4 part = T::pack(el);
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+            if (j == nfull) q[j] = part;
+    }
+    uint32_t smax = T::kSmaxInit, umax = T::kUmaxInit;
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+        if (j < re) T::nan_acc(q[j], smax, umax);  // zero padding is NaN-free
+    if (__syncthreads_or(T::has_nan(smax, umax)) && tid == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
+
+    // ---- radix levels from the most significant digit, over the registers
+    uint32_t prefix = 0, need = static_cast<uint32_t>(k), cls = 0;
+    int shift = T::KB;
+    for (int l = 0; l < a.nlevels && (l == 0 || cls != need); ++l) {
+        const int bl = a.bits[l];
+        const int nsh = shift - bl;
+        const int nb = 1 << bl;
+        const uint32_t mask = static_cast<uint32_t>(nb - 1);
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            if (j < re) {
+                E el[V];
+                T::unpack(q[j], el);
+#pragma unroll
+                for (int t = 0; t < V; ++t) {
+                    const uint32_t kk = T::key(el[t]);
+                    hist_add(hist, (kk >> nsh) & mask, j * V + t < cnt && (l == 0 || (kk >> shift) == prefix),
+                             lane, a.agg != 0);
+                }
+            }
+        }
+        __syncthreads();
+        find_threshold<NT>(hist, nb, need, s_res, s_warp);
+        for (int i = tid; i < nb; i += NT) hist[i] = 0u;
+        __syncthreads();
+        prefix = (l == 0) ? s_res[0] : ((prefix << bl) | s_res[0]);
+        need -= s_res[1];
+        cls = s_res[2];
+        shift = nsh;
+    }
+    const uint32_t P = prefix;
+    const int S = shift;
+    const uint32_t E_need = need;
+
+    // ---- ordered compaction: the run's keys above the class, then its ties in column order
+    uint32_t g = 0, qq = 0;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        if (j < re) {
+            E el[V];
+            T::unpack(q[j], el);
+#pragma unroll
+            for (int t = 0; t < V; ++t) {
+                const uint32_t c = T::key(el[t]) >> S;
+                const bool in = j * V + t < cnt;
+                g += in && c > P;
+                qq += in && c == P;
+            }
+        }
+    }
+    uint32_t tq;
+    uint32_t r = block_exclusive_scan<NT>(qq, s_warp, tq);
+    const uint32_t sel = g + take_from_ties(E_need, r, qq);
+    uint32_t ts;
+    uint32_t pos = block_exclusive_scan<NT>(sel, s_warp, ts);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        if (j < re) {
+            E el[V];
+            T::unpack(q[j], el);
+#pragma unroll
+            for (int t = 0; t < V; ++t) {
+                const uint32_t c = T::key(el[t]) >> S;
+                const bool in = j * V + t < cnt;
+                bool take = in && c > P;
+                if (in && c == P) take = r++ < E_need;
+                if (take) src[pos++] = static_cast<uint16_t>(e0 + j * V + t);
+            }
+        }
+    }
+    __syncthreads();
+    for (int p = tid; p < k; p += NT) {  // outputs in position order
+        const int col = src[p];
+        store_idx(a, row, p, col);
+        if (a.want_values) store_val<E>(a, row, p, xrow[col]);
+        if (GATHER && p < a.n_gather) glist[p] = col;
+    }
+    if (GATHER) {
+        __syncthreads();
+        gather_rows_of<NT>(a, row, 0, a.n_gather, glist, 0);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // row_kernel: one CTA per row, the row staged whole in shared memory.
 // ---------------------------------------------------------------------------
 template <typename E, int NT, bool GATHER>
@@ -1441,9 +1601,11 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) stream_kernel(const 
 //  Too few candidates, or a region overflowing, falls back to exact passes
 //  over the row in global memory.
 // Shared memory: histogram | candidate regions (W x region_stride pairs; the
-// last pair of a region absorbs writes past its capacity) | gather list.
+// last pair of a region absorbs writes past its capacity) | gather list |
+// staging (W x kStage 16-byte vectors, then W x kStage first columns).
 // ---------------------------------------------------------------------------
 constexpr int kWideUnroll = 4;
+constexpr int kStage = kWideStage;
 
 // Threshold key estimated from sample vectors held in registers: q[0, kSU) of each thread, those
 // with bit j of `ok` set valid, `ns` valid vectors over the CTA.  share / population: the k wanted
@@ -1769,6 +1931,40 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
     uint32_t kmax = 0;  // largest candidate key seen by this lane
     // a positive NaN among the candidates; an estimate above the +inf key came from a sampled NaN
     bool pnan = tkey > T::key(static_cast<E>(T::kInfMagnitude));
+    // Vectors holding a candidate are staged (16-byte vector + its first column, in column order)
+    // in the warp's buffer of kStage entries, and expanded into (key, column) pairs a full
+    // buffer at a time, one staged vector per lane.
+    uint4 *stv = reinterpret_cast<uint4 *>(smem + a.smem_stage_off) + warp * kStage;
+    int32_t *stc = reinterpret_cast<int32_t *>(smem + a.smem_stage_off + W * kStage * 16) + warp * kStage;
+    int sc = 0;  // staged vectors (warp-uniform)
+    auto expand = [&]() {
+        __syncwarp();
+        for (int r0 = 0; r0 < sc; r0 += 32) {
+            const int i = r0 + lane;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            int cb = 0;
+            uint32_t m = 0;
+            if (i < sc) {
+                v = stv[i];
+                cb = stc[i];
+                m = positive ? T::ge_mask_raw(v, tsg) : T::ge_mask_key(v, tkey);
+            }
+            uint32_t tot;
+            uint32_t p = off + warp_exclusive_scan(static_cast<uint32_t>(__popc(m)), lane, tot);
+            while (m) {
+                const int t = __ffs(m) - 1;
+                m &= m - 1u;
+                const E e = T::lane_of(v, t);
+                kmax = max(kmax, T::key(e));
+                pnan |= T::is_nan(e);
+                reg[p < capw ? p : capw] = make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(cb + t));
+                ++p;
+            }
+            off += tot;
+        }
+        sc = 0;
+        __syncwarp();
+    };
     for (int64_t base = vb; base < ve; base += 32 * U) {
         if (base != vb) {
             if (base + 32 * U <= ve) {  // a full iteration (warp-uniform): no bounds checks
@@ -1782,59 +1978,32 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
                 }
             }
         }
-        uint32_t pm[U];
-        if (positive) {
-            // zero vectors past the range select nothing and are NaN-free; a positive NaN always
-            // passes, so only negative NaNs need the running maximum
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                T::nan_acc_neg(q[u], umax);
-                pm[u] = T::ge_mask_raw(q[u], tsg);
-            }
-        } else {
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                T::nan_acc(q[u], smax, umax);
-                pm[u] = base + u * 32 + lane < ve ? T::ge_mask_key(q[u], tkey) : 0u;
-            }
-        }
-        // offsets in (u, lane) order: warp scans of the counts, two u's per word (16-bit fields)
-        uint32_t ex[U], tot = 0;
-#pragma unroll
-        for (int u = 0; u < U; u += 2) {
-            const uint32_t cw = static_cast<uint32_t>(__popc(pm[u])) | (static_cast<uint32_t>(__popc(pm[u + 1])) << 16);
-            uint32_t inc = cw;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(kFull, inc, o);
-                if (lane >= o) inc += y;
-            }
-            const uint32_t all = __shfl_sync(kFull, inc, 31);
-            const uint32_t e = inc - cw;
-            ex[u] = tot + (e & 0xffffu);
-            tot += all & 0xffffu;
-            ex[u + 1] = tot + (e >> 16);
-            tot += all >> 16;
-        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            uint32_t m = pm[u];
-            if (!m) continue;
-            const uint4 qu = q[u];
-            const int col0 = static_cast<int>((base + u * 32 + lane) * V);
-            uint32_t p = off + ex[u];
-            do {
-                const int t = __ffs(m) - 1;
-                m &= m - 1u;
-                const E e = T::lane_of(qu, t);
-                kmax = max(kmax, T::key(e));
-                pnan |= T::is_nan(e);
-                reg[p < capw ? p : capw] = make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(col0 + t));
-                ++p;
-            } while (m);
+            bool any;
+            if (positive) {
+                // zero vectors past the range select nothing and are NaN-free; a positive NaN
+                // always passes, so only negative NaNs need the running maximum
+                T::nan_acc_neg(q[u], umax);
+                any = T::any_ge_raw(q[u], tsg);
+            } else {
+                T::nan_acc(q[u], smax, umax);
+                any = base + u * 32 + lane < ve && T::ge_mask_key(q[u], tkey) != 0u;
+            }
+            const uint32_t b = __ballot_sync(kFull, any);
+            if (b) {
+                const int nb = __popc(b);
+                if (sc + nb > kStage) expand();
+                if (any) {
+                    const int slot = sc + __popc(b & ((1u << lane) - 1u));
+                    stv[slot] = q[u];
+                    stc[slot] = static_cast<int32_t>((base + u * 32 + lane) * V);
+                }
+                sc += nb;
+            }
         }
-        off += tot;
     }
+    if (sc) expand();
     if (warp == W - 1) {  // the < 16-byte tail, after the last vector
         const int64_t j = tail0 + lane;
         const bool in = j < n;
@@ -1900,11 +2069,16 @@ cudaError_t raise_smem_limit(K kern, int *set_smem, size_t smem)
 }
 
 // Kernel of a mode for one element type, CTA size and gather flag; null where that combination
-// is never launched (row_kernel: 128/256/512 threads; split_kernel: 256; stream and wide: 512).
+// is never launched (row_kernel and reg_kernel with 8 vectors a thread: 128/256/512 threads;
+// reg_kernel with 2 vectors a thread: 128; split_kernel: 256; stream and wide: 512).
 template <typename E, int NT, bool G>
 void (*kernel_of(int mode))(TopkArgs)
 {
     if (mode == kModeRow) return row_kernel<E, NT, G>;
+    if (mode == kModeReg8) return reg_kernel<E, NT, 8, G>;
+    if constexpr (NT == 128) {
+        if (mode == kModeReg2) return reg_kernel<E, NT, 2, G>;
+    }
     if constexpr (NT == 256) {
         if (mode == kModeSplit) return split_kernel<E, NT, G>;
     }
@@ -1919,9 +2093,9 @@ template <typename E, int NT, bool G>
 cudaError_t launch_one(int mode, size_t smem, const TopkArgs &a, cudaStream_t stream, int64_t grid, bool query,
                        int *blocks_per_sm)
 {
-    static int set_smem[4][64] = {};
+    static int set_smem[kNumModes][64] = {};
     void (*kern)(TopkArgs) = kernel_of<E, NT, G>(mode);
-    if (!kern || mode < 0 || mode > 3) return cudaErrorInvalidValue;
+    if (!kern || mode < 0 || mode >= kNumModes) return cudaErrorInvalidValue;
     cudaError_t e = raise_smem_limit(kern, set_smem[mode], smem);
     if (e != cudaSuccess) return e;
     if (query) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kern, NT, smem);

@@ -126,8 +126,8 @@ SEL_API size_t sel_topk_workspace_size(int dtype, int64_t rows, int64_t cols, in
 SEL_API int64_t sel_max_cols(int dtype);
 
 /* Name of the kernel a sel_topk (n_gather == 0) or sel_topk_gather call of this
- * shape launches on the current device: "row_kernel", "wide_kernel",
- * "split_kernel" or "stream_kernel" (static strings, never freed), or NULL on
+ * shape launches on the current device: "reg_kernel", "row_kernel",
+ * "wide_kernel", "split_kernel" or "stream_kernel" (static strings, never freed), or NULL on
  * invalid arguments.  A diagnostic for profiling and reports; it launches
  * nothing.  The tutorial has no counterpart: it is this library's own plan. */
 SEL_API const char *sel_topk_kernel_name(int dtype, int64_t rows, int64_t cols, int k, int64_t n_gather);

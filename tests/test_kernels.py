@@ -34,6 +34,35 @@ CASES = [
 
 MODES = ["wide", "split", "stream"]
 
+# shapes the register-resident kernel holds (bf16 up to 32768 columns, fp32 up to 16384): every
+# tile size, ragged tails ending inside a vector, ties, infinities and near-full selections
+REG_CASES = [
+    ("bf16", 5, 2000, 512, "normal"),
+    ("bf16", 3, 2047, 700, "levels"),
+    ("f32", 4, 1021, 300, "zeros_inf"),
+    ("f32", 3, 4093, 4000, "normal"),
+    ("bf16", 4, 8191, 2048, "levels"),
+    ("f32", 2, 16384, 4096, "two_level"),
+    ("bf16", 3, 16383, 64, "equal"),
+    ("bf16", 2, 32768, 4096, "ascending"),
+    ("f32", 3, 9999, 1, "descending"),
+]
+
+
+@pytest.mark.parametrize("case", REG_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_reg_kernel(case, monkeypatch):
+    monkeypatch.setenv("SEL_PLAN", "reg")
+    import gather_radix_select_gb300 as g
+    dtype, rows, cols, k, kind = case
+    assert g.kernel_name(torch.float32 if dtype == "f32" else torch.bfloat16, rows, cols, k) == "reg_kernel"
+    w = padded(*case)
+    x, end, vals, idx, nan, err = run(w)
+    assert err == 0 and nan == 0
+    compare_with_oracle(w, np.arange(rows), idx.cpu().numpy(), to_bits(vals), True)
+    x, end, vals, idx, nan, err = run(w, sorted_index=False, idx_dtype="i64", want_values=False)
+    assert err == 0
+    compare_with_oracle(w, np.arange(rows), idx.cpu().numpy(), None, False)
+
 
 def padded(dtype, rows, cols, k, kind, row_end=None):
     seed = zlib.crc32(repr((dtype, rows, cols, k, kind)).encode())
@@ -83,39 +112,39 @@ def test_wide_kernel_paths(case, monkeypatch):
     compare_with_oracle(w, np.arange(case[1]), idx.cpu().numpy(), None, False)
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES + ["reg"])
 def test_forced_row_end_and_nan(mode, monkeypatch):
     monkeypatch.setenv("SEL_PLAN", mode)
-    rows, cols, k = 6, 90000, 2000
-    row_end = np.array([0, 1999, 2000, 2001, 45000, 200000], dtype=np.int32)
+    rows, cols, k = 6, (12000 if mode == "reg" else 90000), 2000
+    row_end = np.array([0, 1999, 2000, 2001, cols // 2, 200000], dtype=np.int32)
     w = padded("f32", rows, cols, k, "normal", row_end=row_end)
     x, end, vals, idx, nan, err = run(w)
     assert err == 0 and nan == 0
     compare_with_oracle(w, np.arange(rows), idx.cpu().numpy(), to_bits(vals), True)
     # a NaN inside the valid part of a long row raises the flag; one past row_end does not
     bits = w["x"].copy()
-    bits[4, 50000] = 0x7FC00000  # beyond row_end[4] = 45000: ignored
+    bits[4, cols // 2 + 5] = 0x7FC00000  # beyond row_end[4]: ignored
     w2 = dict(w, x=bits)
     _, _, _, _, nan, err = run(w2)
     assert err == 0 and nan == 0
-    bits[5, 70000] = 0x7FC00000
+    bits[5, cols - 100] = 0xFFC00000  # a negative NaN
     w3 = dict(w, x=bits)
     _, _, vals, idx, nan, err = run(w3)
     assert err == 0 and nan == 1
     compare_with_oracle(w3, np.arange(5), idx.cpu().numpy()[:5], to_bits(vals)[:5], True)
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES + ["reg"])
 def test_forced_fused_gather(mode, monkeypatch):
     monkeypatch.setenv("SEL_PLAN", mode)
     import gather_radix_select_gb300 as g
     rng = np.random.default_rng(5)
-    b, rows, cols, k, ng, d = 2, 4, 150000, 1024, 700, 64
+    b, rows, cols, k, ng, d = 2, 4, (30000 if mode == "reg" else 150000), 1024, 700, 64
     v = rng.standard_normal((rows, cols)).astype(np.float32)
     x = to_torch(syn.f32_to_bf16_bits(v), "bf16")
     key_bits = syn.f32_to_bf16_bits(rng.standard_normal((b, cols, d)).astype(np.float32)).reshape(b, cols, d)
     key = to_torch(key_bits, "bf16")
-    end = torch.from_numpy(np.array([150000, 1000, 90001, 149999], dtype=np.int32)).cuda()
+    end = torch.from_numpy(np.array([cols, 1000, cols * 3 // 5 + 1, cols - 1], dtype=np.int32)).cuda()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     _, fidx, fout = g.topk_gather(x, k, key, ng, end=end, err_flag=err)
     torch.cuda.synchronize()
