@@ -23,6 +23,8 @@ constexpr int64_t kSplitMinRowBytes = 64 * 1024;  // rows narrower than this nev
 constexpr int64_t kWideMaxRowBytes = 4 << 20;     // wider rows, when few, split over CTAs instead
 constexpr int kWideHistBins = 2048;               // wide_kernel's range histogram (select_regions)
 constexpr int64_t kRegMaxRowBytes = 16 * 1024;    // longer rows take the staged row kernel by default
+constexpr int kWideSplitCtasPerSm = 6;            // wide rows: split them until this many CTAs per SM
+constexpr int64_t kWidePartMinBytes = 32 * 1024;  // ... but no part smaller than this
 
 int elem_bytes(int dtype) { return dtype == SEL_F32 ? 4 : 2; }
 int idx_bytes(int idx_dtype) { return idx_dtype == SEL_I64 ? 8 : 4; }
@@ -174,6 +176,23 @@ int64_t wide_cap(int dtype, int64_t cols, int k)
     return std::min(cap, round_up(cols, 8));
 }
 
+// Candidate pairs one of P parts of a row may leave (its part of wide_cap: the part estimates the
+// row's threshold from its own sample, so it keeps its share of what the whole row would keep).
+int64_t wide_part_cap(int dtype, int64_t cols, int k, int parts)
+{
+    const int64_t e = elem_bytes(dtype);
+    const int64_t part_cols = ceil_div(cols, parts);
+    const int64_t nvec = part_cols * e / 16;
+    const int64_t sample =
+        std::min<int64_t>(nvec, static_cast<int64_t>(sel::kWideThreads) * sel::kWideSampleVecsPerLane) * (16 / e);
+    if (sample <= 0) return round_up(part_cols, 8);
+    const double f = static_cast<double>(sample) / static_cast<double>(part_cols);
+    const double mu = static_cast<double>(k) * static_cast<double>(sample) / static_cast<double>(cols);
+    const double kept = mu * 1.125 + 3.0 * std::sqrt(mu) + 4.0;
+    const int64_t cap = static_cast<int64_t>((kept + 4.0 * std::sqrt(kept)) / f) + 64;
+    return std::min(cap, round_up(part_cols, 8) + 8);
+}
+
 // Layout of a wide_kernel CTA: histogram | W candidate regions of (key bits, column) pairs |
 // gather list.  Each warp's region holds its share of `cap` plus slack for the uneven spread
 // of candidates over the warps, and one more pair that absorbs writes past the capacity.
@@ -202,6 +221,14 @@ size_t layout_wide(int64_t cap, bool gather, int64_t n_gather, sel::TopkArgs &a)
 
 // Forced kernel choice for tuning and tests: SEL_PLAN=reg|row|split|wide|stream (when that kernel
 // can run the shape).  Unset: the automatic plan.
+// SEL_PARTS=n: streaming kernel parts per row (tuning).
+int parts_override()
+{
+    const char *e = std::getenv("SEL_PARTS");
+    const int v = e ? std::atoi(e) : 0;
+    return v > 0 ? v : 0;
+}
+
 int plan_override()
 {
     const char *e = std::getenv("SEL_PLAN");
@@ -216,7 +243,8 @@ int plan_override()
 }
 
 // Chooses the kernel (row / split / wide / stream), its CTA shape, shared memory and workspace.
-int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, int force, Plan &p)
+int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, int force, int force_parts,
+              Plan &p)
 {
     sel::TopkArgs &a = p.layout;
     digit_plan(dtype, cols, a);
@@ -282,18 +310,41 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
             }
         }
     }
-    // one CTA per row, one streaming pass into per-warp candidate lists
+    // one CTA per row, one streaming pass into per-warp candidate lists; when the rows are fewer
+    // than half the SMs, each row is streamed by `parts` CTAs whose candidate lists meet in the
+    // workspace.  (Measured: a part carries ~10 us of fixed latency -- estimate, fences, merge --
+    // so splitting pays only when most SMs would otherwise idle.)
     bool wide_ok = false;
     Plan wide_plan = p;
     if (cols <= 0x7fffffffLL) {
+        int64_t parts = 1;
+        if (2 * rows < sms) {
+            parts = ceil_div(static_cast<int64_t>(kWideSplitCtasPerSm) * sms, rows > 0 ? rows : 1);
+            parts = std::min<int64_t>(parts, std::max<int64_t>(1, row_bytes / kWidePartMinBytes));
+            parts = std::min<int64_t>(parts, sel::kMaxParts);
+        }
+        if (force_parts > 0) parts = std::min<int64_t>(force_parts, sel::kMaxParts);
         Plan wp = p;
-        const size_t smem = layout_wide(wide_cap(dtype, c1, k), gather, n_gather, wp.layout);
-        if (smem <= limit && cached_blocks_per_sm(dtype, sel::kModeWide, sel::kWideThreads, gather, smem) > 0) {
-            wp.mode = sel::kModeWide;
+        const int64_t part_cap = parts > 1 ? wide_part_cap(dtype, c1, k, static_cast<int>(parts)) : 0;
+        const int64_t cap = parts > 1 ? parts * part_cap : wide_cap(dtype, c1, k);
+        const size_t smem = layout_wide(cap, gather, n_gather, wp.layout);
+        const int mode = parts > 1 ? sel::kModeWideSplit : sel::kModeWide;
+        if (smem <= limit && cached_blocks_per_sm(dtype, mode, sel::kWideThreads, gather, smem) > 0 &&
+            rows * parts <= 0x7fffffffLL) {
+            wp.mode = mode;
             wp.threads = sel::kWideThreads;
             wp.smem = smem;
-            wp.grid = rows;
+            wp.grid = rows * parts;
             wp.ws_bytes = 0;
+            if (parts > 1) {
+                sel::TopkArgs &l = wp.layout;
+                l.parts = static_cast<int32_t>(parts);
+                l.part_cap = static_cast<int32_t>(part_cap);
+                l.ws_counter_bytes = round_up(rows * 4, 256);
+                l.ws_part_bytes = round_up(16 + part_cap * 8, 16);
+                l.ws_row_bytes = parts * l.ws_part_bytes;
+                wp.ws_bytes = static_cast<size_t>(l.ws_counter_bytes + rows * l.ws_row_bytes);
+            }
             wide_plan = wp;
             wide_ok = true;
         }
@@ -368,11 +419,12 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
 int cached_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, Plan &p)
 {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int64_t, int64_t, int, int64_t, int, int>, Plan> cache;
+    static std::map<std::tuple<int, int, int64_t, int64_t, int, int64_t, int, int, int>, Plan> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SEL_ECUDA;
-    const int force = plan_override();
-    const auto key = std::make_tuple(dev, dtype, rows, cols, k, gather ? n_gather : -1, force, hist_agg());
+    const int force = plan_override(), force_parts = parts_override();
+    const auto key =
+        std::make_tuple(dev, dtype, rows, cols, k, gather ? n_gather : -1, force, hist_agg(), force_parts);
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
@@ -381,7 +433,7 @@ int cached_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64
             return SEL_OK;
         }
     }
-    const int st = make_plan(dtype, rows, cols, k, gather, n_gather, force, p);
+    const int st = make_plan(dtype, rows, cols, k, gather, n_gather, force, force_parts, p);
     if (st != SEL_OK) return st;
     std::lock_guard<std::mutex> g(mu);
     if (cache.size() > 4096) cache.clear();
@@ -518,7 +570,8 @@ const char *sel_topk_kernel_name(int dtype, int64_t rows, int64_t cols, int k, i
     switch (p.mode) {
     case sel::kModeRow: return "row_kernel";
     case sel::kModeSplit: return "split_kernel";
-    case sel::kModeWide: return "wide_kernel";
+    case sel::kModeWide:
+    case sel::kModeWideSplit: return "wide_kernel";
     case sel::kModeStream: return "stream_kernel";
     case sel::kModeReg2:
     case sel::kModeReg8: return "reg_kernel";

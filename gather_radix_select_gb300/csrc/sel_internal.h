@@ -23,7 +23,8 @@ constexpr int kModeStream = 2;      // stream_kernel: one CTA per row, passes re
 constexpr int kModeWide = 3;        // wide_kernel: one CTA per row, one streaming pass into per-warp lists
 constexpr int kModeReg2 = 4;        // reg_kernel: one CTA per row held in registers, 2 vectors a thread
 constexpr int kModeReg8 = 5;        // reg_kernel: 8 vectors a thread
-constexpr int kNumModes = 6;
+constexpr int kModeWideSplit = 6;   // wide_kernel over `parts` CTAs per row, last-arriver merge
+constexpr int kNumModes = 7;
 constexpr int kGatherThreads = 256;
 
 // Everything one selection launch needs; passed by value (kernel parameter space).
@@ -53,6 +54,7 @@ struct TopkArgs {
     uint32_t smem_stage_off;  // wide_kernel: staged candidate vectors
     int32_t list_cap;         // capacity of the candidate list
     int32_t region_stride;    // wide_kernel: candidate pairs per warp region (capacity list_cap + 1)
+    int32_t part_cap;         // wide_kernel over parts: candidate pairs a part may leave in the workspace
     int32_t agg;              // 1: first-pass histogram with warp-aggregated atomics
     int32_t sample_step;      // > 1: the first digit's threshold is estimated from every
                               //      sample_step-th 16-byte vector of the row

@@ -1861,7 +1861,7 @@ __device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int 
     }
 }
 
-template <typename E, int NT, bool GATHER>
+template <typename E, int NT, bool GATHER, bool SPLIT>
 __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
 {
     using T = Elem<E>;
@@ -1879,11 +1879,13 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
     __shared__ Segments<E> s_seg;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t row = blockIdx.x;
+    const int P = SPLIT ? a.parts : 1;
+    const int64_t row = SPLIT ? static_cast<int64_t>(blockIdx.x) / P : static_cast<int64_t>(blockIdx.x);
+    const int part = SPLIT ? static_cast<int>(blockIdx.x % static_cast<unsigned>(P)) : 0;
     const int64_t n = valid_cols(a, row);
     const int k = a.k;
     if (n <= k) {
-        short_row<E, NT, GATHER>(a, row, n, 0, k);
+        if (part == 0) short_row<E, NT, GATHER>(a, row, n, 0, k);
         return;
     }
     const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
@@ -1897,11 +1899,12 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
     const int64_t tail0 = nvec * V;
     for (int i = tid; i < a.hist_bins; i += NT) hist[i] = 0u;
 
-    // ---- 1. warp w streams vectors [vb, ve) of the row; its first loads double as the sample
-    //         for the threshold estimate (kWideSampleVecsPerLane vectors per lane: 16 runs of
-    //         consecutive vectors spread over the row)
-    const int64_t per = nvec / W, rem = nvec % W;
-    const int64_t vb = warp * per + (warp < rem ? warp : rem);
+    // ---- 1. this CTA's vectors [pv0, pv1) (the row, or one of its P parts); warp w streams
+    //         [vb, ve) of them, and its first loads double as the sample for the threshold
+    //         estimate (kWideSampleVecsPerLane vectors per lane: 16 runs of consecutive vectors)
+    const int64_t pv0 = nvec * part / P, pv1 = nvec * (part + 1) / P;
+    const int64_t per = (pv1 - pv0) / W, rem = (pv1 - pv0) % W;
+    const int64_t vb = pv0 + warp * per + (warp < rem ? warp : rem);
     const int64_t ve = vb + per + (warp < rem ? 1 : 0);
     uint4 q[U];
 #pragma unroll
@@ -2004,7 +2007,7 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
         }
     }
     if (sc) expand();
-    if (warp == W - 1) {  // the < 16-byte tail, after the last vector
+    if (warp == W - 1 && part == P - 1) {  // the < 16-byte tail, after the last vector
         const int64_t j = tail0 + lane;
         const bool in = j < n;
         const E e = in ? xrow[j] : static_cast<E>(0);
@@ -2025,9 +2028,84 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
     }
     if (__syncthreads_or(pnan || T::has_nan(smax, umax)) && tid == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
 
+    uint32_t tlo = tkey;  // every candidate key is at or above it
+    bool over = false;    // a region (or a part's workspace) overflowed
+    if constexpr (SPLIT) {
+        // ---- a part: its candidates go to the workspace in column order (regions in warp order),
+        //      then a header (count, estimate, largest key); the part that arrives last merges
+        __shared__ uint32_t s_last;
+        __shared__ uint4 s_head[kMaxParts];
+        uint32_t pre = 0, tp = 0, thp = 0;
+        bool povf = false;
+        for (int w = 0; w < W; ++w) {
+            const uint32_t c = s_cnt[w];
+            pre += w < warp ? c : 0u;
+            tp += c;
+            povf |= c > capw;
+            thp = max(thp, s_kmax[w]);
+        }
+        povf |= tp > static_cast<uint32_t>(a.part_cap);
+        unsigned char *prow = a.ws + a.ws_counter_bytes + row * a.ws_row_bytes;
+        if (!povf) {
+            uint2 *dst = reinterpret_cast<uint2 *>(prow + part * a.ws_part_bytes + 16) + pre;
+            const uint32_t c = s_cnt[warp];
+            for (uint32_t i = lane; i < c; i += 32) __stcg(dst + i, reg[i]);
+        }
+        if (tid == 0)
+            __stcg(reinterpret_cast<uint4 *>(prow + part * a.ws_part_bytes), make_uint4(povf ? 0xffffffffu : tp, tkey, thp, 0u));
+        __threadfence();  // this thread's workspace writes, before the arrival below
+        __syncthreads();
+        if (tid == 0) s_last = atomicAdd(reinterpret_cast<uint32_t *>(a.ws) + row, 1u) == static_cast<uint32_t>(P - 1);
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();  // the other parts' writes, before reading them
+        if (tid < P) s_head[tid] = __ldcg(reinterpret_cast<const uint4 *>(prow + tid * a.ws_part_bytes));
+        __syncthreads();
+        // keys at or above the highest estimate are all in the union of the parts' lists
+        uint32_t total = 0, tmax = 0, thi_all = 0;
+        for (int p = 0; p < P; ++p) {
+            const uint4 h = s_head[p];
+            over |= h.x == 0xffffffffu;
+            total += h.x == 0xffffffffu ? 0u : h.x;
+            tmax = max(tmax, h.y);
+            thi_all = max(thi_all, h.z);
+        }
+        if (!over) {
+            // warp w takes the flat range [f0, f1) of the parts' lists (parts in order), keeping
+            // the pairs at or above tmax in its region
+            const uint32_t f0 = static_cast<uint32_t>(static_cast<uint64_t>(total) * warp / W);
+            const uint32_t f1 = static_cast<uint32_t>(static_cast<uint64_t>(total) * (warp + 1) / W);
+            uint32_t cw = 0, base = 0;
+            int p = 0;
+            while (p < P && base + s_head[p].x <= f0) base += s_head[p++].x;
+            for (uint32_t f = f0; f < f1 && p < P; base += s_head[p++].x) {
+                const uint32_t end = min(f1, base + s_head[p].x);
+                const uint2 *pp = reinterpret_cast<const uint2 *>(prow + p * a.ws_part_bytes + 16);
+                for (uint32_t i0 = f; i0 < end; i0 += 32) {
+                    const uint32_t i = i0 + lane;
+                    const bool in = i < end;
+                    const uint2 e = in ? __ldcg(pp + (i - base)) : make_uint2(0u, 0u);
+                    const bool keep = in && T::key(static_cast<E>(e.x)) >= tmax;
+                    const uint32_t bk = __ballot_sync(kFull, keep);
+                    if (keep) {
+                        const uint32_t q2 = cw + __popc(bk & ((1u << lane) - 1u));
+                        reg[q2 < capw ? q2 : capw] = e;
+                    }
+                    cw += __popc(bk);
+                }
+                f = end;
+            }
+            if (lane == 0) {
+                s_cnt[warp] = cw;
+                s_kmax[warp] = thi_all;
+            }
+        }
+        tlo = tmax;
+        __syncthreads();
+    }
+
     // ---- 3. exact selection on the regions, or the fallback
     uint32_t L = 0, thi = 0;
-    bool over = false;
 #pragma unroll
     for (int w = 0; w < W; ++w) {
         L += s_cnt[w];
@@ -2035,7 +2113,7 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
         thi = max(thi, s_kmax[w]);
     }
     if (!over && L >= static_cast<uint32_t>(k)) {
-        select_regions<E, NT, GATHER>(a, row, list, rs, s_cnt, tkey, thi, hist, s_res, s_warp, s_gq, glist);
+        select_regions<E, NT, GATHER>(a, row, list, rs, s_cnt, tlo, thi, hist, s_res, s_warp, s_gq, glist);
         return;
     }
     if (tid == 0) {
@@ -2084,7 +2162,8 @@ void (*kernel_of(int mode))(TopkArgs)
     }
     if constexpr (NT == 512) {
         if (mode == kModeStream) return stream_kernel<E, NT, G>;
-        if (mode == kModeWide) return wide_kernel<E, NT, G>;
+        if (mode == kModeWide) return wide_kernel<E, NT, G, false>;
+        if (mode == kModeWideSplit) return wide_kernel<E, NT, G, true>;
     }
     return nullptr;
 }
@@ -2116,7 +2195,7 @@ cudaError_t launch_e(int mode, int threads, bool gather, size_t smem, const Topk
         return gather ? launch_one<E, 256, true>(mode, smem, a, s, grid, query, blocks_per_sm)
                       : launch_one<E, 256, false>(mode, smem, a, s, grid, query, blocks_per_sm);
     }
-    if (mode == kModeStream || mode == kModeWide) {
+    if (mode == kModeStream || mode == kModeWide || mode == kModeWideSplit) {
         if (threads != 512) return cudaErrorInvalidValue;
         return gather ? launch_one<E, 512, true>(mode, smem, a, s, grid, query, blocks_per_sm)
                       : launch_one<E, 512, false>(mode, smem, a, s, grid, query, blocks_per_sm);

@@ -85,6 +85,20 @@ def test_forced_kernel(mode, case, monkeypatch):
     compare_with_oracle(w, np.arange(rows), idx.cpu().numpy(), None, False)
 
 
+@pytest.mark.parametrize("parts", ["1", "2", "7", "64"])
+def test_wide_parts(parts, monkeypatch):
+    # the streaming kernel on one CTA per row, and with rows split over CTAs whose candidate lists
+    # meet in the workspace (the last part to arrive merges)
+    monkeypatch.setenv("SEL_PLAN", "wide")
+    monkeypatch.setenv("SEL_PARTS", parts)
+    for case in (("f32", 3, 131075, 4096, "normal"), ("bf16", 2, 204803, 1024, "levels"),
+                 ("f32", 2, 70001, 100, "descending"), ("bf16", 3, 100000, 3000, "zeros_inf")):
+        w = padded(*case)
+        x, end, vals, idx, nan, err = run(w)
+        assert err == 0 and nan == 0
+        compare_with_oracle(w, np.arange(case[1]), idx.cpu().numpy(), to_bits(vals), True)
+
+
 # shapes for the per-warp candidate regions of the streaming kernel: thresholds at or below zero
 # (raw-bit compare not usable), rows shorter than one 16-byte vector, ragged tails, candidates
 # piling into one warp's range, and a row whose every element ties
