@@ -221,6 +221,15 @@ size_t layout_wide(int64_t cap, bool gather, int64_t n_gather, sel::TopkArgs &a)
 
 // Forced kernel choice for tuning and tests: SEL_PLAN=reg|row|split|wide|stream (when that kernel
 // can run the shape).  Unset: the automatic plan.
+// SEL_ROW_SAMPLE=1: the staged row kernel estimates the threshold from every 8th vector on long
+// rows instead of taking the exact first histogram while the row lands (tuning; measured slower
+// on the bf16 [12288, 16384] and fp32 [4, 8192] workloads, hence off by default).
+int row_sample()
+{
+    const char *e = std::getenv("SEL_ROW_SAMPLE");
+    return (e && e[0] == '1') ? 1 : 0;
+}
+
 // SEL_PARTS=n: streaming kernel parts per row (tuning).
 int parts_override()
 {
@@ -249,7 +258,7 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
     sel::TopkArgs &a = p.layout;
     digit_plan(dtype, cols, a);
     a.agg = hist_agg();
-    a.sample_step = 8;
+    a.sample_step = row_sample() ? 8 : 1;
     a.sample_min_cols = 8192;
     const size_t limit = sel::topk_smem_limit();
     const int sms = sel::device_sm_count();
@@ -424,7 +433,8 @@ int cached_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64
     if (cudaGetDevice(&dev) != cudaSuccess) return SEL_ECUDA;
     const int force = plan_override(), force_parts = parts_override();
     const auto key =
-        std::make_tuple(dev, dtype, rows, cols, k, gather ? n_gather : -1, force, hist_agg(), force_parts);
+        std::make_tuple(dev, dtype, rows, cols, k, gather ? n_gather : -1, force, hist_agg() + 2 * row_sample(),
+                        force_parts);
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);

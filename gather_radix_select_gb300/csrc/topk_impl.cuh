@@ -1255,6 +1255,10 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
         const uint32_t sel = g + take_from_ties(E_need, r, q);
         uint32_t ts;
         uint32_t pos = block_exclusive_scan<NT>(sel, s_warp, ts);
+        // each output position's column goes to the (free) histogram first when it fits (16 bits
+        // each); the outputs are then written in position order, coalesced
+        const bool by_position = static_cast<uint32_t>(k) <= 2u * static_cast<uint32_t>(a.hist_bins);
+        uint16_t *src = reinterpret_cast<uint16_t *>(hist);
         for (int i = i0; i < i1; ++i) {
             const int o = list[i];
             const E e = buf[o];
@@ -1262,10 +1266,23 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
             bool take = c > P;
             if (c == P) take = (r++ < E_need);
             if (take) {
-                store_idx(a, row, pos, o);
-                if (a.want_values) store_val<E>(a, row, pos, e);
-                if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = o;
+                if (by_position) {
+                    src[pos] = static_cast<uint16_t>(o);
+                } else {
+                    store_idx(a, row, pos, o);
+                    if (a.want_values) store_val<E>(a, row, pos, e);
+                    if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = o;
+                }
                 ++pos;
+            }
+        }
+        if (by_position) {
+            __syncthreads();
+            for (int p = tid; p < k; p += NT) {
+                const int o = src[p];
+                store_idx(a, row, p, o);
+                if (a.want_values) store_val<E>(a, row, p, buf[o]);
+                if (GATHER && p < a.n_gather) glist[p] = o;
             }
         }
     } else {
@@ -1818,8 +1835,11 @@ __device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int 
         pos += taken_of(w, ties);
         ties += s_gq[W + w];
     }
-    // the region in order, four chunks of 32 pairs loaded ahead
+    // the region in order, four chunks of 32 pairs loaded ahead; output rows addressed once
     constexpr int kAhead = 4;
+    int32_t *oi32 = a.out_idx && !a.idx_i64 ? static_cast<int32_t *>(a.out_idx) + row * a.out_idx_stride : nullptr;
+    int64_t *oi64 = a.out_idx && a.idx_i64 ? static_cast<int64_t *>(a.out_idx) + row * a.out_idx_stride : nullptr;
+    E *ov = a.want_values ? static_cast<E *>(a.out_val) + row * a.out_val_stride : nullptr;
     for (uint32_t i0 = 0; i0 < c; i0 += 32 * kAhead) {
         uint2 ev[kAhead];
 #pragma unroll
@@ -1847,8 +1867,9 @@ __device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int 
             if (take) {
                 const uint32_t p = pos + __popc(bt & lt);
                 const int32_t col = static_cast<int32_t>(e.y & ~kMark);
-                store_idx(a, row, p, col);
-                if (a.want_values) store_val<E>(a, row, p, static_cast<E>(e.x));
+                if (oi64) oi64[p] = col;
+                else if (oi32) oi32[p] = col;
+                if (ov) ov[p] = static_cast<E>(e.x);
                 if (GATHER && static_cast<int64_t>(p) < a.n_gather) glist[p] = col;
             }
             ties += __popc(be);
