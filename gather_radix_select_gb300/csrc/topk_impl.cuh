@@ -2102,17 +2102,24 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
             for (uint32_t f = f0; f < f1 && p < P; base += s_head[p++].x) {
                 const uint32_t end = min(f1, base + s_head[p].x);
                 const uint2 *pp = reinterpret_cast<const uint2 *>(prow + p * a.ws_part_bytes + 16);
-                for (uint32_t i0 = f; i0 < end; i0 += 32) {
-                    const uint32_t i = i0 + lane;
-                    const bool in = i < end;
-                    const uint2 e = in ? __ldcg(pp + (i - base)) : make_uint2(0u, 0u);
-                    const bool keep = in && T::key(static_cast<E>(e.x)) >= tmax;
-                    const uint32_t bk = __ballot_sync(kFull, keep);
-                    if (keep) {
-                        const uint32_t q2 = cw + __popc(bk & ((1u << lane) - 1u));
-                        reg[q2 < capw ? q2 : capw] = e;
+                constexpr int kAhead = 4;  // chunks of 32 pairs loaded ahead
+                for (uint32_t i0 = f; i0 < end; i0 += 32 * kAhead) {
+                    uint2 ev[kAhead];
+#pragma unroll
+                    for (int u = 0; u < kAhead; ++u) {
+                        const uint32_t i = i0 + u * 32 + lane;
+                        ev[u] = i < end ? __ldcg(pp + (i - base)) : make_uint2(0u, 0u);
                     }
-                    cw += __popc(bk);
+#pragma unroll
+                    for (int u = 0; u < kAhead; ++u) {
+                        const bool keep = i0 + u * 32 + lane < end && T::key(static_cast<E>(ev[u].x)) >= tmax;
+                        const uint32_t bk = __ballot_sync(kFull, keep);
+                        if (keep) {
+                            const uint32_t q2 = cw + __popc(bk & ((1u << lane) - 1u));
+                            reg[q2 < capw ? q2 : capw] = ev[u];
+                        }
+                        cw += __popc(bk);
+                    }
                 }
                 f = end;
             }
