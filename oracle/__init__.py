@@ -74,14 +74,18 @@ def value_fill_bits(dtype: str) -> int:
 
 
 def topk(x_bits: np.ndarray, dtype: str, k: int, row_end=None, sorted_index: bool = False,
-         cols: int | None = None):
+         cols: int | None = None, sorted_value: bool = False):
     """Row-wise top-k by full sort (value descending, smaller index first on ties).
 
     x_bits : uint32 (fp32) or uint16 (bf16) bit array [rows, stride]; the
              first ``cols`` columns (default: all) are data.
     Returns (idx int64 [rows, k], bits uint32 [rows, k], row_nan int32 [rows]).
     Unsorted results come in value-descending order; sorted ones by index.
+    ``sorted_value``: every row (short ones too) by value descending, ties by
+    index, a NaN above every number, fills last.
     """
+    if sorted_index and sorted_value:
+        raise ValueError("sorted_index and sorted_value exclude each other")
     x_bits = np.ascontiguousarray(x_bits)
     want = np.uint32 if dtype == "f32" else np.uint16
     if x_bits.dtype != want or x_bits.ndim != 2:
@@ -97,7 +101,7 @@ def topk(x_bits: np.ndarray, dtype: str, k: int, row_end=None, sorted_index: boo
     out_bits = np.empty((rows, k), dtype=np.uint32)
     row_nan = np.empty((rows,), dtype=np.int32)
     rc = _load().oracle_topk(x_bits.ctypes.data, _dtype_code(dtype), rows, cols, stride,
-                             None if re is None else re.ctypes.data, k, int(bool(sorted_index)),
+                             None if re is None else re.ctypes.data, k, 2 if sorted_value else int(bool(sorted_index)),
                              out_idx.ctypes.data, out_bits.ctypes.data, row_nan.ctypes.data)
     if rc != 0:
         raise ValueError("oracle_topk rejected its arguments")

@@ -83,6 +83,23 @@ static int by_value_desc_then_index(const void *a, const void *b)
     return 0;
 }
 
+/* Value order of the output ("Performance and advanced tips", item 3: results
+ * ordered by value): larger value first, equal values by smaller index, and a
+ * NaN (only short rows, which are not checked, can keep one) above every
+ * number, NaNs among themselves by index. */
+static int by_value_nan_first_then_index(const void *a, const void *b)
+{
+    const oracle_item *p = (const oracle_item *)a;
+    const oracle_item *q = (const oracle_item *)b;
+    const int pn = p->v != p->v, qn = q->v != q->v;
+    if (pn != qn) return pn ? -1 : 1;
+    if (!pn) {
+        if (p->v > q->v) return -1;
+        if (p->v < q->v) return 1;
+    }
+    return p->i < q->i ? -1 : (p->i > q->i);
+}
+
 static int by_index(const void *a, const void *b)
 {
     const oracle_item *p = (const oracle_item *)a;
@@ -106,15 +123,20 @@ uint32_t oracle_value_fill_bits(int dtype)
  *                                  the 16 bf16 bits), fills = -inf bits
  *   row_nan  int32 [rows]          1 if the row was checked and holds a NaN
  *
- * Order of the k entries: by value descending (ties by index) unless
- * sorted_index, then by index ascending.  Returns 0, or -1 on bad arguments
- * or allocation failure.
+ * sorted_index picks the order of a row's k entries:
+ *   0  long rows by value descending (ties by index), short rows by index;
+ *   1  by index ascending ("Basic TopK usage");
+ *   2  by value descending for every row, equal values by index, a NaN above
+ *      every number, fills last.
+ * Returns 0, or -1 on bad arguments or allocation failure.
  */
 int oracle_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride,
                 const int32_t *row_end, int64_t k, int sorted_index,
                 int64_t *out_idx, uint32_t *out_bits, int32_t *row_nan)
 {
     if (!x || !out_idx || !out_bits || !row_nan || rows < 0 || cols < 0 || stride < cols || k < 1)
+        return -1;
+    if (sorted_index < 0 || sorted_index > 2)
         return -1;
     if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
         return -1;
@@ -133,12 +155,20 @@ int oracle_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t st
         uint32_t *ob = out_bits + r * k;
         row_nan[r] = 0;
         if (n <= k) {
-            /* short row: every valid column, in order, then fills; no NaN check */
+            /* short row: every valid column, in order (value order in mode 2), then fills;
+             * no NaN check */
+            for (int64_t j = 0; j < n; ++j) {
+                uint32_t bits;
+                items[j].v = element_value(x, dtype, r * stride + j, &bits);
+                items[j].i = j;
+            }
+            if (sorted_index == 2)
+                qsort(items, (size_t)n, sizeof(oracle_item), by_value_nan_first_then_index);
             for (int64_t j = 0; j < k; ++j) {
                 if (j < n) {
                     uint32_t bits;
-                    (void)element_value(x, dtype, r * stride + j, &bits);
-                    oi[j] = j;
+                    (void)element_value(x, dtype, r * stride + items[j].i, &bits);
+                    oi[j] = items[j].i;
                     ob[j] = bits;
                 } else {
                     oi[j] = -1;
@@ -165,7 +195,7 @@ int oracle_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t st
             continue;
         }
         qsort(items, (size_t)n, sizeof(oracle_item), by_value_desc_then_index);
-        if (sorted_index)
+        if (sorted_index == 1)
             qsort(items, (size_t)k, sizeof(oracle_item), by_index);
         for (int64_t j = 0; j < k; ++j) {
             uint32_t bits;

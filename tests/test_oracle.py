@@ -100,6 +100,45 @@ def test_oracle_unsorted_order_is_value_descending(dtype):
             assert idx[0][a] < idx[0][b]
 
 
+def stable_sort_order(v_f32, n, k):
+    """Value order by a library routine: a stable descending torch.sort on CPU
+    (ties keep index order, NaN ranks above every number, -0 == +0)."""
+    t = torch.sort(torch.from_numpy(np.ascontiguousarray(v_f32[:n])), descending=True, stable=True)
+    got = t.indices[:k].tolist()
+    return got + [-1] * (k - len(got))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("kind", ["small_ints", "two_level", "normal"])
+def test_value_order_matches_stable_torch_sort(dtype, kind):
+    rng = np.random.default_rng(23)
+    rows, cols = 6, 300
+    x = np.stack([tiny_row(kind, cols, rng, dtype) for _ in range(rows)])
+    end = np.array([300, 299, 64, 65, 1, 0], np.int32)
+    for k in (1, 7, 64, 65, 301):
+        idx, bits, nan = oracle.topk(x, dtype, k, row_end=end, sorted_value=True)
+        for r in range(rows):
+            v = oracle.bits_to_values(x[r], dtype).astype(np.float32)
+            assert idx[r].tolist() == stable_sort_order(v, int(end[r]), k), (k, r)
+            n_ok = min(int(end[r]), k)
+            assert (bits[r][:n_ok] == x[r][idx[r][:n_ok]]).all()
+            assert (bits[r][n_ok:] == oracle.value_fill_bits(dtype)).all()
+        assert not nan.any()
+
+
+def test_value_order_short_row_nan_and_signed_zero():
+    # short rows are not checked for NaN; in value order a NaN ranks above every number
+    v = np.array([1.0, np.nan, -0.0, 0.0, 2.0, -np.nan, 2.0, -np.inf], dtype=np.float32)
+    x = f32bits(v)[None, :].copy()
+    idx, bits, nan = oracle.topk(x, "f32", 10, sorted_value=True)
+    assert idx[0].tolist() == [1, 5, 4, 6, 0, 2, 3, 7, -1, -1]
+    assert idx[0].tolist() == stable_sort_order(v, 8, 10)
+    assert nan[0] == 0
+    assert bits[0][5] == 0x80000000 and bits[0][6] == 0  # -0 (column 2) before +0 (column 3): a tie
+    with pytest.raises(ValueError):
+        oracle.topk(x, "f32", 3, sorted_index=True, sorted_value=True)
+
+
 # --------------------------------------------------------------------------
 # hand-worked closed forms
 # --------------------------------------------------------------------------
@@ -369,6 +408,11 @@ MUTATIONS = {
                                     "if (p->v < q->v) return -1;\n    if (p->v > q->v) return 1;"),
     "row_end_off_by_one": ("n = row_end[r];", "n = row_end[r] + 1;"),
     "short_row_boundary": ("if (n <= k) {", "if (n < k) {"),
+    "value_order_nan_last": ("if (pn != qn) return pn ? -1 : 1;", "if (pn != qn) return pn ? 1 : -1;"),
+    "value_order_ascending": ("        if (p->v > q->v) return -1;\n        if (p->v < q->v) return 1;",
+                              "        if (p->v < q->v) return -1;\n        if (p->v > q->v) return 1;"),
+    "value_order_ties_flipped": ("return p->i < q->i ? -1 : (p->i > q->i);", "return p->i > q->i ? -1 : (p->i < q->i);"),
+    "value_order_short_rows_by_index": ("if (sorted_index == 2)", "if (sorted_index == 3)"),
 }
 
 
@@ -415,6 +459,23 @@ def _pins_pass(lib):
                     nan.ctypes.data)
     if nan[0] != 0 or idx[0].tolist() != [0, 1, 2, 3]:
         return False
+    # value order against a stable descending torch.sort: long and short rows with ties, -0/+0,
+    # and a short row holding NaNs
+    rows = [tiny_row(kind, 12, rng, "f32") for kind in ("small_ints", "two_level", "normal")]
+    rows.append(np.array([0.0, -0.0, 1.0, -0.0, 0.0, 1.0], np.float32))
+    rows.append(np.array([np.nan, 1.0, np.nan, 2.0, -np.inf, 2.0], np.float32))
+    for v in rows:
+        n = len(v)
+        x = f32bits(v)[None, :].copy()
+        has_nan = bool(np.isnan(v).any())
+        for k in range(n if has_nan else 1, n + 2):
+            idx = np.empty((1, k), np.int64)
+            bits = np.empty((1, k), np.uint32)
+            nan = np.empty((1,), np.int32)
+            lib.oracle_topk(x.ctypes.data, 0, 1, n, n, None, k, 2, idx.ctypes.data, bits.ctypes.data,
+                            nan.ctypes.data)
+            if idx[0].tolist() != stable_sort_order(v, n, k):
+                return False
     return True
 
 
