@@ -182,12 +182,15 @@ def measured_peaks():
 class Runner:
     """Device-resident inputs/outputs of one workload and the call that is timed."""
 
-    def __init__(self, w, dev):
+    def __init__(self, w, dev, sorted_value=False):
         import torch
 
         import gather_radix_select_gb300 as g
 
         self.g, self.torch, self.w, self.dev = g, torch, w, dev
+        # value-ordered output instead of the workload's own order (a second launch per step)
+        self.sorted_value = sorted_value
+        self.sorted_index = w["sorted_index"] and not sorted_value
         if w["dtype"] == "f32":
             self.x = torch.from_numpy(w["x"].view(np.int32)).view(torch.float32).to(dev)
         else:
@@ -209,17 +212,20 @@ class Runner:
         if w["want_values"]:
             vpad = (k + 3) // 4 * 4 if w["dtype"] == "f32" else (k + 7) // 8 * 8
             self.out_val = torch.empty((w["rows"], vpad), dtype=self.x.dtype, device=dev)
-        self.launches_per_step = 1
+        # one fused launch; value order adds the ordering launch (and then a separate gather)
+        self.launches_per_step = 1 if not sorted_value else (3 if self.key is not None else 2)
 
     def step(self):
         w = self.w
         if self.key is not None:
             return self.g.topk_gather(self.x, w["k"], self.key, w["n_gather"], end=self.end,
-                                      sorted_index=w["sorted_index"], indices_type=self.idx_t,
+                                      sorted_index=self.sorted_index, sorted_value=self.sorted_value,
+                                      indices_type=self.idx_t,
                                       return_value=w["want_values"], gather_out=self.gout,
                                       output_idx=self.out_idx, output_val=self.out_val,
                                       nan_flag=self.nan, err_flag=self.err)
-        return self.g.topk(self.x, w["k"], end=self.end, sorted_index=w["sorted_index"], indices_type=self.idx_t,
+        return self.g.topk(self.x, w["k"], end=self.end, sorted_index=self.sorted_index,
+                           sorted_value=self.sorted_value, indices_type=self.idx_t,
                            return_value=w["want_values"], output_idx=self.out_idx, output_val=self.out_val,
                            nan_flag=self.nan, err_flag=self.err)
 
@@ -352,6 +358,7 @@ def gpu_arm(args):
         achieved = nbytes / (kernel_ms * 1e-3) / 1e9
         e2e_ms, h2d, d2h = e2e_measure(w, dev, max(2, min(args.steps, 10)), 2)
         per = per_workload(args, dev, flush, peak) if not args.no_per_workload else None
+        pair = pair_gather_measure(dev, flush, peak) if not args.no_per_workload else None
         cpu = cpu_baseline(args.workload)
         import gather_radix_select_gb300 as g
 
@@ -389,6 +396,7 @@ def gpu_arm(args):
             "wall_s_timed_region": round(wall, 4),
             "device_err_flag": err_flag,
             "per_workload": per,
+            "pair_gather": pair,
         }
     if dist:
         dist.barrier()
@@ -421,9 +429,58 @@ def per_workload(args, dev, flush, peak):
             t2 = statistics.median(time_steps(r2, 10, 3, flush))
             out[name]["topk_only_ms"] = round(t2, 5)
             out[name]["topk_only_gbs"] = round(tb / (t2 * 1e-3) / 1e9, 2)
+            del r2
+        # the same step with value-ordered output (selection + ordering launch; same algorithmic bytes)
+        r3 = Runner(w, dev, sorted_value=True)
+        t3 = statistics.median(time_steps(r3, 10, 3, flush))
+        out[name]["value_order_ms"] = round(t3, 5)
+        out[name]["value_order_gbs"] = round(nb / (t3 * 1e-3) / 1e9, 2)
+        del r3
         del r
         torch.cuda.empty_cache()
     return out
+
+
+class _Call:
+    """A timed call for time_steps."""
+
+    def __init__(self, fn):
+        import torch
+
+        self.torch, self.step = torch, fn
+
+
+def pair_gather_measure(dev, flush, peak):
+    """The Indexer KL loss's double gather (1024 rows x 512 positions; index key d=128 and
+    attention key d=512, compressed length 2048) in one launch, beside the same two gathers
+    as separate launches."""
+    import torch
+
+    import gather_radix_select_gb300 as g
+
+    w = syn.kl_pair_gather()
+    key = torch.from_numpy(w["key"].view(np.int16)).view(torch.bfloat16).to(dev)
+    key2 = torch.from_numpy(w["key2"].view(np.int16)).view(torch.bfloat16).to(dev)
+    pos = torch.from_numpy(w["pos"]).to(dev)
+    R, n, d, d2 = w["rows"], w["n"], w["d"], w["d2"]
+    out = torch.empty((R, n, d), dtype=torch.bfloat16, device=dev)
+    out2 = torch.empty((R, n, d2), dtype=torch.bfloat16, device=dev)
+    uniq = len(np.unique(np.maximum(w["pos"], 0)))
+    nbytes = R * n * 4 + uniq * (d + d2) * 2 + R * n * (d + d2) * 2
+    t1 = statistics.median(time_steps(_Call(lambda: g.gather_rows_pair(key, key2, pos, out=out, out2=out2)),
+                                      10, 3, flush))
+
+    def two():
+        g.gather_rows(key, pos, out=out)
+        g.gather_rows(key2, pos, out=out2)
+
+    t2 = statistics.median(time_steps(_Call(two), 10, 3, flush))
+    res = {"workload": "kl_pair_gather_bf16_1024x512_d128_d512", "ms": round(t1, 5),
+           "gbs": round(nbytes / (t1 * 1e-3) / 1e9, 2), "frac_of_peak": round(nbytes / (t1 * 1e-3) / 1e9 / peak, 4),
+           "bytes": nbytes, "two_launches_ms": round(t2, 5)}
+    del out, out2
+    torch.cuda.empty_cache()
+    return res
 
 
 # ----------------------------------------------------------------------------

@@ -20,7 +20,7 @@ import torch
 from . import _native
 from ._native import SelError, SEL_MAX_K
 
-__all__ = ["topk", "gather_rows", "topk_gather", "stride_requirement", "max_cols", "workspace_size", "kernel_name",
+__all__ = ["topk", "gather_rows", "gather_rows_pair", "topk_gather", "stride_requirement", "max_cols", "workspace_size", "kernel_name",
            "SelError",
            "SEL_MAX_K", "library_path"]
 
@@ -124,8 +124,15 @@ def _row_stride(x):
     return x.stride(0) if x.size(0) > 1 else max(x.stride(0), x.size(1))
 
 
+def _order(sorted_index: bool, sorted_value: bool) -> int:
+    # SEL_UNSORTED / SEL_SORT_INDEX / SEL_SORT_VALUE
+    if sorted_index and sorted_value:
+        raise ValueError("sorted_index and sorted_value exclude each other")
+    return 2 if sorted_value else int(bool(sorted_index))
+
+
 def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_index: bool = False,
-         indices_type: torch.dtype = torch.int32, return_value: bool = True,
+         sorted_value: bool = False, indices_type: torch.dtype = torch.int32, return_value: bool = True,
          output_idx: torch.Tensor | None = None, output_val: torch.Tensor | None = None,
          nan_flag: torch.Tensor | None = None, err_flag: torch.Tensor | None = None, stream=None,
          workspace: torch.Tensor | None = None):
@@ -133,7 +140,9 @@ def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_ind
 
     Returns ``(values, indices)``; ``values`` is None when ``return_value``
     is False.  Rows shorter than k (per ``end``) are filled with index -1 and
-    value -inf.  Outputs may be non-contiguous (row strides padded to the
+    value -inf.  ``sorted_index``: each row by index ascending;
+    ``sorted_value``: by value descending, equal values by index (a second
+    launch).  Outputs may be non-contiguous (row strides padded to the
     output alignment).  ``nan_flag`` / ``err_flag`` are optional caller-zeroed
     int32 CUDA tensors the kernel ORs / writes into.  ``output_idx`` /
     ``output_val`` are optional caller-owned [rows, >=k] buffers (row strides
@@ -142,6 +151,7 @@ def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_ind
     split over several CTAs; by default a cached buffer is used.
     """
     _check_x(x)
+    order = _order(sorted_index, sorted_value)
     rows, cols = x.shape
     dev = x.device
     end = _check_end(end, rows, dev)
@@ -168,7 +178,7 @@ def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_ind
         s = stream if stream is not None else torch.cuda.current_stream(dev)
         ws, ws_bytes = _ws_for(lib, workspace, x.dtype, rows, cols, k, dev, s)
         st = lib.sel_topk(
-            _ptr(x), _DTYPES[x.dtype], rows, cols, _row_stride(x), _ptr(end), int(k), int(bool(sorted_index)),
+            _ptr(x), _DTYPES[x.dtype], rows, cols, _row_stride(x), _ptr(end), int(k), order,
             _IDX[indices_type], int(bool(return_value)), _ptr(idx), idx.stride(0) if rows > 1 else max(idx.stride(0), k),
             _ptr(val), 0 if val is None else (val.stride(0) if rows > 1 else max(val.stride(0), k)),
             _ptr(ws), ws_bytes, _ptr(nan_flag), _ptr(err_flag), ctypes.c_void_p(s.cuda_stream))
@@ -223,8 +233,44 @@ def gather_rows(key: torch.Tensor, idx: torch.Tensor, *, out: torch.Tensor | Non
     return out
 
 
+def gather_rows_pair(key: torch.Tensor, key2: torch.Tensor, idx: torch.Tensor, *, out: torch.Tensor | None = None,
+                     out2: torch.Tensor | None = None, err_flag: torch.Tensor | None = None, stream=None):
+    """``gather_rows`` of two keys at the same positions, in one launch.
+
+    key: bf16 [b, comp_len, d]; key2: bf16 [b, comp_len, d2] (same b and
+    comp_len, each may be strided); idx: int32/int64 [rows, n].  Returns
+    ``(out, out2)``, bf16 [rows, n, d] and [rows, n, d2].
+    """
+    kbs, krs = _key_strides(key)
+    kbs2, krs2 = _key_strides(key2)
+    b, comp_len, d = key.shape
+    if key2.shape[0] != b or key2.shape[1] != comp_len or key2.device != key.device:
+        raise ValueError("key2 must be [b, comp_len, d2] with key's b and comp_len, on key's device")
+    d2 = key2.shape[2]
+    if idx.dim() != 2 or idx.dtype not in _IDX or idx.device != key.device:
+        raise ValueError("idx must be a 2-D int32/int64 tensor on key's device")
+    if idx.size(1) > 1 and idx.stride(1) != 1:
+        raise ValueError("idx rows must be contiguous")
+    rows, n = idx.shape
+    outs = []
+    for o, dd in ((out, d), (out2, d2)):
+        if o is None:
+            o = torch.empty((rows, n, dd), dtype=torch.bfloat16, device=key.device)
+        elif o.shape != (rows, n, dd) or not o.is_contiguous() or o.dtype != torch.bfloat16:
+            raise ValueError("outputs must be contiguous bf16 [rows, n, d] tensors")
+        outs.append(o)
+    with torch.cuda.device(key.device):
+        st = _native.load().sel_gather_rows_pair(
+            _ptr(key), d, kbs, krs, _ptr(key2), d2, kbs2, krs2, b, comp_len, _ptr(idx), _IDX[idx.dtype], rows, n,
+            idx.stride(0) if rows > 1 else max(idx.stride(0), n), _ptr(outs[0]), _ptr(outs[1]), _ptr(err_flag),
+            _stream(key.device, stream))
+    _native.check(st, "sel_gather_rows_pair")
+    return outs[0], outs[1]
+
+
 def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, end: torch.Tensor | None = None,
-                sorted_index: bool = False, indices_type: torch.dtype = torch.int32, return_value: bool = False,
+                sorted_index: bool = False, sorted_value: bool = False, indices_type: torch.dtype = torch.int32,
+                return_value: bool = False,
                 return_indices: bool = True, gather_out: torch.Tensor | None = None,
                 output_idx: torch.Tensor | None = None, output_val: torch.Tensor | None = None,
                 nan_flag: torch.Tensor | None = None, err_flag: torch.Tensor | None = None, stream=None,
@@ -232,9 +278,12 @@ def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, en
     """``topk`` then ``gather_rows`` of the first ``n_gather`` selected columns, in one launch.
 
     Returns ``(values, indices, gathered)`` with ``gathered`` bf16
-    [rows, n_gather, d]; values / indices are None when not requested.
+    [rows, n_gather, d]; values / indices are None when not requested.  With
+    ``sorted_value`` the gathered columns are the n_gather largest values, in
+    value order (selection, ordering and gather run as three launches).
     """
     _check_x(x)
+    order = _order(sorted_index, sorted_value)
     rows, cols = x.shape
     dev = x.device
     end = _check_end(end, rows, dev)
@@ -242,9 +291,9 @@ def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, en
     b, comp_len, d = key.shape
     if key.device != dev:
         raise ValueError("key must be on x's device")
-    if not return_indices:
+    if not return_indices and order != 2:
         idx = None
-    else:
+    else:  # value order gathers from the ordered index rows, so they are always written
         idx = output_idx if output_idx is not None else _padded_rows(rows, k, indices_type, dev)
     if not return_value:
         val = None
@@ -259,13 +308,15 @@ def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, en
         s = stream if stream is not None else torch.cuda.current_stream(dev)
         ws, ws_bytes = _ws_for(lib, workspace, x.dtype, rows, cols, k, dev, s)
         st = lib.sel_topk_gather(
-            _ptr(x), _DTYPES[x.dtype], rows, cols, _row_stride(x), _ptr(end), int(k), int(bool(sorted_index)),
+            _ptr(x), _DTYPES[x.dtype], rows, cols, _row_stride(x), _ptr(end), int(k), order,
             _IDX[indices_type], int(bool(return_value)),
             _ptr(idx), 0 if idx is None else (idx.stride(0) if rows > 1 else max(idx.stride(0), k)),
             _ptr(val), 0 if val is None else (val.stride(0) if rows > 1 else max(val.stride(0), k)),
             _ptr(key), b, comp_len, d, kbs, krs, int(n_gather), _ptr(gather_out),
             _ptr(ws), ws_bytes, _ptr(nan_flag), _ptr(err_flag), ctypes.c_void_p(s.cuda_stream))
     _native.check(st, "sel_topk_gather")
+    if not return_indices:
+        idx = None
     if idx is not None and output_idx is not None:
         idx = idx[:, :k]
     if val is not None and output_val is not None:

@@ -27,6 +27,8 @@ SIGNATURES = {
     "sel_max_cols": (_i64, [_int]),
     "sel_gather_rows": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _int, _i64, _i64, _i64,
                                _vp, _vp, _vp]),
+    "sel_gather_rows_pair": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _int,
+                                    _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "sel_topk_gather": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _int, _int, _int, _int,
                                _vp, _i64, _vp, _i64,
                                _vp, _i64, _i64, _i64, _i64, _i64, _i64, _vp,

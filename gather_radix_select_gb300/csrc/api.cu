@@ -485,6 +485,22 @@ int check_gather_key(const void *key, int64_t b, int64_t comp_len, int64_t d, in
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? SEL_OK : SEL_ECUDA; }
 
+// Re-orders finished output rows by value (SEL_SORT_VALUE).
+int value_order(const void *x, int dtype, int64_t rows, int64_t stride, int k, int idx_dtype, int want_values,
+                void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride, void *stream)
+{
+    sel::OrderArgs a{};
+    a.x = x;
+    a.x_stride = stride;
+    a.rows = rows;
+    a.k = k;
+    a.out_idx = out_idx;
+    a.out_idx_stride = out_idx_stride;
+    a.out_val = want_values ? out_val : nullptr;
+    a.out_val_stride = out_val_stride;
+    return status_of(sel::launch_value_order(dtype, idx_dtype == SEL_I64, a, static_cast<cudaStream_t>(stream)));
+}
+
 int run_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride, const int32_t *row_end, int k,
              int idx_dtype, int want_values, void *out_idx, int64_t out_idx_stride, void *out_val,
              int64_t out_val_stride, const void *key, int64_t b, int64_t comp_len, int64_t d,
@@ -594,13 +610,17 @@ int sel_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
              int64_t out_val_stride, void *workspace, size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag,
              void *stream)
 {
-    (void)sorted_index;  // the ordered compaction always yields ascending column order
+    // The ordered compaction always yields ascending column order: SEL_SORT_INDEX costs nothing.
+    if (sorted_index < SEL_UNSORTED || sorted_index > SEL_SORT_VALUE) return SEL_EINVAL;
     const int st = check_topk_args(x, dtype, rows, cols, stride, k, idx_dtype, want_values, out_idx, out_idx_stride,
                                    out_val, out_val_stride, true);
     if (st != SEL_OK || rows == 0) return st;
-    return run_topk(x, dtype, rows, cols, stride, row_end, k, idx_dtype, want_values, out_idx, out_idx_stride, out_val,
-                    out_val_stride, nullptr, 1, 0, 0, 0, 0, 0, nullptr, workspace, workspace_bytes, nan_flag, err_flag,
-                    stream);
+    const int rc = run_topk(x, dtype, rows, cols, stride, row_end, k, idx_dtype, want_values, out_idx, out_idx_stride,
+                            out_val, out_val_stride, nullptr, 1, 0, 0, 0, 0, 0, nullptr, workspace, workspace_bytes,
+                            nan_flag, err_flag, stream);
+    if (rc != SEL_OK || sorted_index != SEL_SORT_VALUE) return rc;
+    return value_order(x, dtype, rows, stride, k, idx_dtype, want_values, out_idx, out_idx_stride, out_val,
+                       out_val_stride, stream);
 }
 
 int sel_gather_rows(const void *key, int64_t b, int64_t comp_len, int64_t d, int64_t key_batch_stride,
@@ -630,21 +650,65 @@ int sel_gather_rows(const void *key, int64_t b, int64_t comp_len, int64_t d, int
     return status_of(sel::launch_gather(a, static_cast<cudaStream_t>(stream)));
 }
 
+int sel_gather_rows_pair(const void *key, int64_t d, int64_t key_batch_stride, int64_t key_row_stride,
+                         const void *key2, int64_t d2, int64_t key2_batch_stride, int64_t key2_row_stride, int64_t b,
+                         int64_t comp_len, const void *idx, int idx_dtype, int64_t rows, int64_t n,
+                         int64_t idx_row_stride, void *out, void *out2, int32_t *err_flag, void *stream)
+{
+    if (idx_dtype != SEL_I32 && idx_dtype != SEL_I64) return SEL_EINVAL;
+    if (n < 0 || rows < 0) return SEL_EINVAL;
+    if (rows == 0 || n == 0) return (b >= 1 && rows % (b > 0 ? b : 1) == 0) ? SEL_OK : SEL_EINVAL;
+    int st = check_gather_key(key, b, comp_len, d, key_batch_stride, key_row_stride, rows, out);
+    if (st != SEL_OK) return st;
+    st = check_gather_key(key2, b, comp_len, d2, key2_batch_stride, key2_row_stride, rows, out2);
+    if (st != SEL_OK) return st;
+    if (!idx || idx_row_stride < n) return SEL_EINVAL;
+    sel::GatherArgs a{};
+    a.key = static_cast<const uint16_t *>(key);
+    a.comp_len = comp_len;
+    a.d = d;
+    a.key_batch_stride = key_batch_stride;
+    a.key_row_stride = key_row_stride;
+    a.key2 = static_cast<const uint16_t *>(key2);
+    a.d2 = d2;
+    a.key2_batch_stride = key2_batch_stride;
+    a.key2_row_stride = key2_row_stride;
+    a.out2 = static_cast<uint16_t *>(out2);
+    a.idx = idx;
+    a.idx_i64 = idx_dtype == SEL_I64;
+    a.rows = rows;
+    a.n = n;
+    a.idx_row_stride = idx_row_stride;
+    a.rows_per_batch = rows / b;
+    a.out = static_cast<uint16_t *>(out);
+    a.err_flag = err_flag;
+    return status_of(sel::launch_gather(a, static_cast<cudaStream_t>(stream)));
+}
+
 int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride, const int32_t *row_end,
                     int k, int sorted_index, int idx_dtype, int want_values, void *out_idx, int64_t out_idx_stride,
                     void *out_val, int64_t out_val_stride, const void *key, int64_t b, int64_t comp_len, int64_t d,
                     int64_t key_batch_stride, int64_t key_row_stride, int64_t n_gather, void *gather_out,
                     void *workspace, size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag, void *stream)
 {
-    (void)sorted_index;
+    if (sorted_index < SEL_UNSORTED || sorted_index > SEL_SORT_VALUE) return SEL_EINVAL;
+    const bool by_value = sorted_index == SEL_SORT_VALUE;
     int st = check_topk_args(x, dtype, rows, cols, stride, k, idx_dtype, want_values, out_idx, out_idx_stride, out_val,
-                             out_val_stride, false);
+                             out_val_stride, by_value);
     if (st != SEL_OK) return st;
     if (n_gather < 0 || n_gather > k) return SEL_EINVAL;
     if (rows == 0) return (b >= 1) ? SEL_OK : SEL_EINVAL;
     if (n_gather > 0) {
         st = check_gather_key(key, b, comp_len, d, key_batch_stride, key_row_stride, rows, gather_out);
         if (st != SEL_OK) return st;
+    }
+    if (by_value) {
+        // selection, then ordering, then the gather of the first n_gather ordered columns
+        st = sel_topk(x, dtype, rows, cols, stride, row_end, k, sorted_index, idx_dtype, want_values, out_idx,
+                      out_idx_stride, out_val, out_val_stride, workspace, workspace_bytes, nan_flag, err_flag, stream);
+        if (st != SEL_OK || n_gather == 0) return st;
+        return sel_gather_rows(key, b, comp_len, d, key_batch_stride, key_row_stride, out_idx, idx_dtype, rows,
+                               n_gather, out_idx_stride, gather_out, err_flag, stream);
     }
     return run_topk(x, dtype, rows, cols, stride, row_end, k, idx_dtype, want_values, out_idx, out_idx_stride, out_val,
                     out_val_stride, key, n_gather > 0 ? b : 1, comp_len, d, key_batch_stride, key_row_stride, n_gather,

@@ -10,6 +10,11 @@
 // positions in shared memory and streams whole key rows with 16-byte loads
 // (key rows are re-read many times and stay in L2) and 16-byte streaming
 // stores (the output is written once and never re-read here).
+//
+// The pair form serves the same pull request's Indexer KL loss, which gathers
+// two keys of different widths (the index key and the attention key) at the
+// same positions: one launch stages the positions once and fills both
+// outputs.
 #include <cstdint>
 
 #include "sel_internal.h"
@@ -20,6 +25,35 @@ namespace {
 constexpr int kPairsPerCta = 256;
 constexpr int kUnroll = 4;
 constexpr int32_t kStatusInval = 1;
+
+// Copies the key rows at positions s_pos[0, np) (batch base kb, rows of d elements) to the
+// contiguous output rows at ob; a position of -1 yields a zero row.
+__device__ __forceinline__ void copy_rows(const uint16_t *kb, int64_t row_stride, int64_t d, uint16_t *out, int np,
+                                          const int64_t *s_pos)
+{
+    const int vpr = static_cast<int>(d >> 3);  // 16-byte vectors per key row
+    const int vsh = (vpr & (vpr - 1)) == 0 ? __ffs(vpr) - 1 : -1;  // log2(vpr), or -1
+    uint4 *ob = reinterpret_cast<uint4 *>(out);
+    const int total = np * vpr;
+    for (int t0 = threadIdx.x; t0 < total; t0 += kUnroll * kGatherThreads) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int t = t0 + u * kGatherThreads;
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (t < total) {
+                const int jj = vsh >= 0 ? (t >> vsh) : t / vpr;
+                const int64_t p = s_pos[jj];
+                if (p >= 0) v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * row_stride) + (t - jj * vpr));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int t = t0 + u * kGatherThreads;
+            if (t < total) __stcs(ob + t, v[u]);
+        }
+    }
+}
 
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs a)
 {
@@ -42,29 +76,11 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs
         s_pos[i] = p;
     }
     __syncthreads();
-    const int vpr = static_cast<int>(a.d >> 3);  // 16-byte vectors per key row
-    const int vsh = (vpr & (vpr - 1)) == 0 ? __ffs(vpr) - 1 : -1;  // log2(vpr), or -1
-    const uint16_t *kb = a.key + (row / a.rows_per_batch) * a.key_batch_stride;
-    uint4 *ob = reinterpret_cast<uint4 *>(a.out + (row * a.n + j0) * a.d);
-    const int total = np * vpr;
-    for (int t0 = threadIdx.x; t0 < total; t0 += kUnroll * kGatherThreads) {
-        uint4 v[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int t = t0 + u * kGatherThreads;
-            v[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (t < total) {
-                const int jj = vsh >= 0 ? (t >> vsh) : t / vpr;
-                const int64_t p = s_pos[jj];
-                if (p >= 0) v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + (t - jj * vpr));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int t = t0 + u * kGatherThreads;
-            if (t < total) __stcs(ob + t, v[u]);
-        }
-    }
+    const int64_t batch = row / a.rows_per_batch;
+    copy_rows(a.key + batch * a.key_batch_stride, a.key_row_stride, a.d, a.out + (row * a.n + j0) * a.d, np, s_pos);
+    if (a.out2)
+        copy_rows(a.key2 + batch * a.key2_batch_stride, a.key2_row_stride, a.d2, a.out2 + (row * a.n + j0) * a.d2, np,
+                  s_pos);
 }
 
 }  // namespace

@@ -76,10 +76,30 @@ struct GatherArgs {
     int32_t idx_i64;
     int64_t rows, n, idx_row_stride, rows_per_batch;
     uint16_t *out;
+    // optional second key gathered at the same positions (same b and comp_len); out2 null = none
+    const uint16_t *key2;
+    int64_t d2, key2_batch_stride, key2_row_stride;
+    uint16_t *out2;
     int32_t *err_flag;
     int64_t pairs_per_cta;    // (row, position) pairs handled by one CTA
     int32_t ctas_per_row;
 };
+
+// Re-ordering of finished output rows by value (order.cu).
+struct OrderArgs {
+    const void *x;            // the selection's input rows (values are read here when out_val is null)
+    int64_t x_stride;         // elements
+    int64_t rows;
+    int32_t k;
+    int32_t p2;               // items sorted per row: k rounded up to 8 x a multiple of 32 threads (set by the launcher)
+    void *out_idx;            // [rows, out_idx_stride] int32 or int64
+    int64_t out_idx_stride;
+    void *out_val;            // nullable: [rows, out_val_stride] value bits
+    int64_t out_val_stride;
+};
+
+// dtype: 0 fp32, 1 bf16.  Sorts each output row by value descending (ties: column ascending).
+cudaError_t launch_value_order(int dtype, bool idx_i64, const OrderArgs &a, cudaStream_t stream);
 
 // dtype: 0 fp32, 1 bf16.  mode: one of the kMode* values.  grid: CTAs to launch.
 cudaError_t launch_topk(int dtype, int mode, int threads, bool gather, size_t smem_bytes, const TopkArgs &a,

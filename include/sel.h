@@ -80,6 +80,9 @@ typedef enum {
 
 enum { SEL_F32 = 0, SEL_BF16 = 1 };  /* input element type */
 enum { SEL_I32 = 0, SEL_I64 = 1 };   /* index element type */
+/* Order of a row's k entries (the sorted_index argument; "Performance and
+ * advanced tips", item 3: results ordered by index or by value). */
+enum { SEL_UNSORTED = 0, SEL_SORT_INDEX = 1, SEL_SORT_VALUE = 2 };
 
 #define SEL_MAX_K 4096
 
@@ -97,7 +100,11 @@ SEL_API int sel_stride_requirement(int *in_align_bytes, int *out_align_bytes);
  *   row_end     int32 [rows] exclusive end per row, clamped on the device to
  *               [0, cols]; NULL means cols for every row.
  *   k           1..SEL_MAX_K.  k > cols is allowed (every row is then short).
- *   sorted_index  nonzero: each row's indices ascending (values follow).
+ *   sorted_index  SEL_UNSORTED: any order.  SEL_SORT_INDEX: each row's indices
+ *               ascending (values follow).  SEL_SORT_VALUE: values descending,
+ *               equal values by index ascending, fills last; a NaN (possible
+ *               only in a short row, which is not checked) counts above every
+ *               number.  Value order is a second launch after the selection.
  *   idx_dtype   SEL_I32 | SEL_I64.
  *   out_idx     [rows, out_idx_stride] of idx_dtype; columns [0, k) written.
  *   out_val     [rows, out_val_stride] of `dtype`, or NULL when want_values == 0.
@@ -148,12 +155,29 @@ SEL_API int sel_gather_rows(const void *key, int64_t b, int64_t comp_len, int64_
                     const void *idx, int idx_dtype, int64_t rows, int64_t n, int64_t idx_row_stride,
                     void *out, int32_t *err_flag, void *stream);
 
+/* Two flat row gathers at the same positions, in one launch (MindSpore
+ * hyper-parallel pull request "perf/gather-index-select": the Indexer KL loss
+ * gathers the index key and the attention key with one index list):
+ *     out [r, j, :] = key [b_r, max(idx[r, j], 0), :]   (d  elements a row)
+ *     out2[r, j, :] = key2[b_r, max(idx[r, j], 0), :]   (d2 elements a row)
+ * Both keys are bf16 [b, comp_len, *] with their own strides; every argument
+ * means what it means in sel_gather_rows, and the same checks apply to each
+ * key.  A position >= comp_len gives zero rows in both outputs and sets
+ * err_flag = SEL_EINVAL. */
+SEL_API int sel_gather_rows_pair(const void *key, int64_t d, int64_t key_batch_stride, int64_t key_row_stride,
+                                 const void *key2, int64_t d2, int64_t key2_batch_stride, int64_t key2_row_stride,
+                                 int64_t b, int64_t comp_len, const void *idx, int idx_dtype, int64_t rows, int64_t n,
+                                 int64_t idx_row_stride, void *out, void *out2, int32_t *err_flag, void *stream);
+
 /* sel_topk followed by sel_gather_rows of the first n_gather output columns
  * (n_gather <= k), in one launch.  The top-k arguments are those of
  * sel_topk (out_idx may be NULL when the indices themselves are not needed);
  * the gather arguments are those of sel_gather_rows with idx taken from the
  * selection.  Fill positions (-1) of short rows gather position 0, as in
- * sel_gather_rows.  The workspace rule is that of sel_topk. */
+ * sel_gather_rows.  The workspace rule is that of sel_topk.  With
+ * SEL_SORT_VALUE the gathered columns are those of the value-ordered output
+ * (the n_gather largest values); that takes three launches (selection,
+ * ordering, gather) and out_idx must not be NULL. */
 SEL_API int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride,
                     const int32_t *row_end, int k, int sorted_index, int idx_dtype, int want_values,
                     void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride,

@@ -218,3 +218,22 @@ def gather_positions(seed: int, rows: int, n: int, comp_len: int, neg_frac: floa
     if neg_frac > 0:
         pos[g.random((rows, n)) < neg_frac] = -1
     return pos.astype(np.int32)
+
+
+def kl_pair_gather(rows: int = 1024, n: int = 512, comp_len: int = 2048, d: int = 128, d2: int = 512, b: int = 1,
+                   seed: int = SEED_BASE + 6) -> dict:
+    """Inputs of the Indexer KL loss's double gather.
+
+    MindSpore hyper-parallel pull request "perf/gather-index-select": per
+    query chunk the loss gathers 1024 rows x 512 selected positions twice,
+    from the index key (head_dim 128) and from the attention key (512), at
+    compressed length 2048.  Keys are bf16 N(0,1) [b, comp_len, d|d2];
+    positions are uniform in [0, comp_len) with 2% set to -1 (the fills of
+    short rows, read as position 0).
+    """
+    g = rng_for(seed)
+    key = f32_to_bf16_bits(g.standard_normal((b, comp_len, d), dtype=np.float32))
+    key2 = f32_to_bf16_bits(g.standard_normal((b, comp_len, d2), dtype=np.float32))
+    pos = gather_positions(seed + 1, rows, n, comp_len, neg_frac=0.02)
+    return {"key": key, "key2": key2, "pos": pos, "rows": rows, "n": n, "comp_len": comp_len, "d": d, "d2": d2,
+            "b": b}

@@ -23,7 +23,7 @@ def declared_symbols():
 
 
 def test_header_declares_the_boundary():
-    assert declared_symbols() == sorted(["sel_gather_rows", "sel_max_cols", "sel_stride_requirement",
+    assert declared_symbols() == sorted(["sel_gather_rows", "sel_gather_rows_pair", "sel_max_cols", "sel_stride_requirement",
                                          "sel_strerror", "sel_topk", "sel_topk_gather", "sel_topk_kernel_name",
                                          "sel_topk_noalloc", "sel_topk_workspace_size"])
 
@@ -49,9 +49,9 @@ FAKE = 0x10000  # never dereferenced: every call below is rejected on the host
 
 
 def topk(lib, x=FAKE, dtype=0, rows=4, cols=64, stride=64, k=8, idx_dtype=0, want_values=0, out_idx=FAKE,
-         out_idx_stride=8, out_val=None, out_val_stride=0):
-    return lib.sel_topk(x, dtype, rows, cols, stride, None, k, 0, idx_dtype, want_values, out_idx, out_idx_stride,
-                        out_val, out_val_stride, None, 0, None, None, None)
+         out_idx_stride=8, out_val=None, out_val_stride=0, sorted_index=0):
+    return lib.sel_topk(x, dtype, rows, cols, stride, None, k, sorted_index, idx_dtype, want_values, out_idx,
+                        out_idx_stride, out_val, out_val_stride, None, 0, None, None, None)
 
 
 def test_topk_rejections(lib):
@@ -69,7 +69,10 @@ def test_topk_rejections(lib):
     assert topk(lib, cols=65, stride=65) == EALIGN      # 260-byte rows
     assert topk(lib, dtype=1, cols=60, stride=60) == EALIGN
     assert topk(lib, out_idx_stride=9) == EALIGN        # 36-byte output rows
+    assert topk(lib, sorted_index=3) == EINVAL          # SEL_UNSORTED / SEL_SORT_INDEX / SEL_SORT_VALUE only
+    assert topk(lib, sorted_index=-1) == EINVAL
     assert topk(lib, rows=0) == 0                       # nothing to do, no launch
+    assert topk(lib, rows=0, sorted_index=2) == 0
 
 
 def test_workspace_size_rejects_bad_arguments(lib):
@@ -101,6 +104,22 @@ def test_gather_rejections(lib):
     assert g(rows=0) == 0 and g(n=0) == 0
 
 
+def test_gather_pair_rejections(lib):
+    EINVAL, EALIGN = 1, 2
+    def g(key=FAKE, d=64, kbs=640, krs=64, key2=FAKE, d2=256, kbs2=2560, krs2=256, b=1, comp_len=10, idx=FAKE,
+          idx_dtype=0, rows=4, n=3, irs=3, out=FAKE, out2=FAKE):
+        return lib.sel_gather_rows_pair(key, d, kbs, krs, key2, d2, kbs2, krs2, b, comp_len, idx, idx_dtype, rows,
+                                        n, irs, out, out2, None, None)
+    assert g(d2=12, krs2=12, kbs2=120) == EALIGN   # second key rows not whole 16-byte vectors
+    assert g(krs2=128) == EINVAL                   # second key row stride < d2
+    assert g(key2=None) == EINVAL
+    assert g(out2=None) == EINVAL
+    assert g(key2=FAKE + 2) == EALIGN
+    assert g(rows=5, b=2) == EINVAL
+    assert g(idx_dtype=2) == EINVAL
+    assert g(rows=0) == 0 and g(n=0) == 0
+
+
 def test_fused_rejections(lib):
     r = lib.sel_topk_gather(FAKE, 0, 4, 64, 64, None, 8, 0, 0, 0, None, 0, None, 0,
                             FAKE, 1, 64, 64, 64 * 64, 64, 9, FAKE, None, 0, None, None, None)
@@ -108,6 +127,12 @@ def test_fused_rejections(lib):
     r = lib.sel_topk_gather(FAKE, 0, 4, 64, 64, None, 8, 0, 0, 0, None, 0, None, 0,
                             FAKE, 3, 64, 64, 64 * 64, 64, 8, FAKE, None, 0, None, None, None)
     assert r == 1  # rows not a multiple of b
+    r = lib.sel_topk_gather(FAKE, 0, 4, 64, 64, None, 8, 2, 0, 0, None, 0, None, 0,
+                            FAKE, 1, 64, 64, 64 * 64, 64, 8, FAKE, None, 0, None, None, None)
+    assert r == 1  # value order gathers from the index rows, so out_idx is required
+    r = lib.sel_topk_gather(FAKE, 0, 4, 64, 64, None, 8, 5, 0, 0, FAKE, 8, None, 0,
+                            FAKE, 1, 64, 64, 64 * 64, 64, 8, FAKE, None, 0, None, None, None)
+    assert r == 1  # bad order
 
 
 def test_product_has_no_cpu_path():

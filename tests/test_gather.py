@@ -151,3 +151,65 @@ def test_fused_small_cases_match_separate():
                                                       vals.view(torch.int16) if dtype == "bf16" else
                                                       vals.view(torch.int32))
         assert torch.equal(fout.view(torch.int16), out.view(torch.int16))
+
+
+# --------------------------------------------------------------------------
+# two keys at the same positions (the Indexer KL loss's index key + attention key)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("b", [1, 3])
+@pytest.mark.parametrize("idx_dtype", ["i32", "i64"])
+def test_gather_pair_matches_oracle(b, idx_dtype):
+    comp_len, d, d2, rows_per_b, n = 300, 64, 256, 5, 70
+    g = np.random.default_rng(30 + b)
+    key = syn.f32_to_bf16_bits(g.standard_normal((b, comp_len, d)).astype(np.float32))
+    base2 = syn.f32_to_bf16_bits(g.standard_normal((b, comp_len, d2 + 64)).astype(np.float32))
+    k2 = key_tensor(base2)[:, :, 32:32 + d2]  # row stride d2 + 64: a non-contiguous second key
+    assert not k2.is_contiguous()
+    pos = syn.gather_positions(50 + b, b * rows_per_b, n, comp_len, neg_frac=0.1)
+    pos[0, :3] = pos[0, 3]  # repeated positions
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, out2 = gsel().gather_rows_pair(key_tensor(key), k2, torch.from_numpy(pos).to(IDX_DTYPE[idx_dtype]).cuda(),
+                                        err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert out.shape == (b * rows_per_b, n, d) and out2.shape == (b * rows_per_b, n, d2)
+    want, bad = oracle.gather_rows(key, pos, b)
+    want2, bad2 = oracle.gather_rows(base2[:, :, 32:32 + d2], pos, b)
+    assert bad == 0 and bad2 == 0
+    assert (to_bits(out) == want).all()
+    assert (to_bits(out2) == want2).all()
+
+
+def test_gather_pair_out_of_range_zero_rows_and_flag():
+    key = syn.f32_to_bf16_bits(np.ones((1, 10, 16), np.float32))
+    key2 = syn.f32_to_bf16_bits(np.full((1, 10, 32), 2.0, np.float32))
+    pos = np.array([[1, 10, -1]], dtype=np.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, out2 = gsel().gather_rows_pair(key_tensor(key), key_tensor(key2), torch.from_numpy(pos).cuda(), err_flag=err)
+    out, out2 = to_bits(out), to_bits(out2)
+    assert int(err.item()) == 1
+    assert (out[0, 1] == 0).all() and (out2[0, 1] == 0).all()
+    assert (out[0, 2] == key[0, 0]).all() and (out2[0, 2] == key2[0, 0]).all()
+
+
+def test_gather_pair_full_size():
+    # 1024 rows x 512 positions, index key d=128 and attention key d=512 at compressed length 2048
+    w = syn.kl_pair_gather()
+    key, key2 = key_tensor(w["key"]), key_tensor(w["key2"])
+    pos = torch.from_numpy(w["pos"]).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, out2 = gsel().gather_rows_pair(key, key2, pos, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    # every row: the flat index_select form on the device
+    flat = pos.to(torch.int64).clamp(min=0).reshape(-1)
+    assert torch.equal(out.view(torch.int16), torch.index_select(key[0], 0, flat).view(torch.int16).view(out.shape))
+    assert torch.equal(out2.view(torch.int16),
+                       torch.index_select(key2[0], 0, flat).view(torch.int16).view(out2.shape))
+    # sampled rows: the oracle
+    rows = np.linspace(0, w["rows"] - 1, 16).astype(np.int64)
+    want, _ = oracle.gather_rows(w["key"], w["pos"][rows], 1)
+    want2, _ = oracle.gather_rows(w["key2"], w["pos"][rows], 1)
+    assert (to_bits(out[torch.from_numpy(rows).cuda()]) == want).all()
+    assert (to_bits(out2[torch.from_numpy(rows).cuda()]) == want2).all()
