@@ -9,7 +9,8 @@ brute force below, written from the definitions on the pages:
 * "Speed up PyTorch TopK with DeepSelect" (tutorial) -- "Basic TopK usage",
   "Working with variable-length rows", "NaN handling", "Supported workloads";
 * MindSpore hyper-parallel pull request "perf/gather-index-select" -- the
-  identity key[b, pos] == index_select(key_flat, b * comp_len + pos).
+  identity key[b, pos] == index_select(key_flat, b * comp_len + pos), and the
+  block-level candidate positions of its ``compressed_candidate_topk`` chain.
 
 Every oracle function here is pinned by ``tests/test_oracle.py`` against
 things other than itself (brute force, closed forms, numpy / torch CPU
@@ -133,6 +134,40 @@ def gather_rows(key_bits: np.ndarray, idx: np.ndarray, b: int | None = None):
     if bad < 0:
         raise ValueError("oracle_gather_rows rejected its arguments")
     return out, int(bad)
+
+
+def block_candidates(score_bits: np.ndarray, dtype: str, topk_blocks: int, block_size: int, pos_end=None):
+    """Block-level candidate positions of the ``compressed_candidate_topk`` chain
+    (MindSpore hyper-parallel pull request "perf/gather-index-select": a top-k over
+    blocks expanded to ``topk_blocks * block_size`` positions, then its Sort and
+    MaskedFill steps), written as its definition.
+
+    Row r has the valid positions [0, pe) with pe = clamp(pos_end[r], 0, n_blocks *
+    block_size); block c covers positions [c * block_size, (c + 1) * block_size) and
+    is a candidate when it holds a valid position (c * block_size < pe).  The
+    ``topk_blocks`` candidates with the largest scores are chosen by ``topk``'s rule
+    (smaller block first on ties; all candidates when there are fewer).  Each chosen
+    block contributes its valid positions; they are listed in ascending order and
+    the rest of the row is -1.
+
+    score_bits : uint32 (fp32) / uint16 (bf16) bits [rows, n_blocks].
+    Returns (positions int64 [rows, topk_blocks * block_size], row_nan int32 [rows]).
+    """
+    rows, n_blocks = score_bits.shape
+    limit = n_blocks * block_size
+    if pos_end is None:
+        pe = np.full(rows, limit, dtype=np.int64)
+    else:
+        pe = np.clip(np.asarray(pos_end, dtype=np.int64), 0, limit)
+    n_cand = (pe + block_size - 1) // block_size
+    blocks, _, row_nan = topk(score_bits, dtype, topk_blocks, row_end=n_cand.astype(np.int32), sorted_index=True)
+    out = np.full((rows, topk_blocks * block_size), -1, dtype=np.int64)
+    for r in range(rows):
+        pos = [int(c) * block_size + i for c in blocks[r] if c >= 0 for i in range(block_size)
+               if int(c) * block_size + i < pe[r]]
+        pos.sort()
+        out[r, :len(pos)] = pos
+    return out, row_nan
 
 
 # --------------------------------------------------------------------------

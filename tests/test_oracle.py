@@ -140,6 +140,58 @@ def test_value_order_short_row_nan_and_signed_zero():
 
 
 # --------------------------------------------------------------------------
+# block-level candidate positions
+# --------------------------------------------------------------------------
+
+def test_block_candidates_handworked():
+    # blocks of 3 positions; scores 0.5, 2.0, 1.0, 2.0; valid positions [0, 11)
+    v = f32bits([0.5, 2.0, 1.0, 2.0])[None, :]
+    pos, nan = oracle.block_candidates(v, "f32", 2, 3, pos_end=np.array([11], np.int32))
+    # blocks 1 and 3 tie at 2.0 and beat the rest; block 3 holds 9, 10 (11 is past the end)
+    assert pos[0].tolist() == [3, 4, 5, 9, 10, -1] and nan[0] == 0
+    # end inside block 1: candidates are blocks 0 and 1 only
+    pos, _ = oracle.block_candidates(v, "f32", 2, 3, pos_end=np.array([4], np.int32))
+    assert pos[0].tolist() == [0, 1, 2, 3, -1, -1]
+    # no valid position / end past the last block
+    pos, _ = oracle.block_candidates(v, "f32", 1, 3, pos_end=np.array([0], np.int32))
+    assert pos[0].tolist() == [-1, -1, -1]
+    pos, _ = oracle.block_candidates(v, "f32", 1, 3, pos_end=np.array([99], np.int32))
+    assert pos[0].tolist() == [3, 4, 5]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_block_candidates_match_brute_force(dtype):
+    # chosen blocks by the O(n^2) rank definition; positions by numpy repeat / nonzero
+    rng = np.random.default_rng(41)
+    for trial in range(60):
+        n_blocks = int(rng.integers(1, 12))
+        bs = int(rng.integers(1, 6))
+        tb = int(rng.integers(1, n_blocks + 3))
+        kind = ["small_ints", "two_level", "normal"][trial % 3]
+        x = tiny_row(kind, n_blocks, rng, dtype)[None, :]
+        pe = int(rng.integers(0, n_blocks * bs + 3))
+        pos, _ = oracle.block_candidates(x, dtype, tb, bs, pos_end=np.array([pe], np.int32))
+        pe_c = min(pe, n_blocks * bs)
+        n_cand = -(-pe_c // bs)
+        chosen = np.zeros(n_blocks, bool)
+        chosen[oracle.brute_topk_row(oracle.bits_to_values(x[0], dtype), n_cand, tb)] = True
+        valid = np.repeat(chosen, bs) & (np.arange(n_blocks * bs) < pe_c)
+        want = np.nonzero(valid)[0].tolist()
+        assert pos[0].tolist() == want + [-1] * (tb * bs - len(want)), (trial, n_blocks, bs, tb, pe)
+
+
+def test_block_candidates_all_blocks_is_every_valid_position():
+    rng = np.random.default_rng(43)
+    x = tiny_row("normal", 20, rng, "bf16")
+    x = np.stack([x, x, x])
+    pe = np.array([0, 37, 500], np.int32)
+    pos, _ = oracle.block_candidates(x, "bf16", 20, 8, pos_end=pe)
+    for r in range(3):
+        n = min(int(pe[r]), 160)
+        assert pos[r].tolist() == list(range(n)) + [-1] * (160 - n)
+
+
+# --------------------------------------------------------------------------
 # hand-worked closed forms
 # --------------------------------------------------------------------------
 
