@@ -359,6 +359,7 @@ def gpu_arm(args):
         e2e_ms, h2d, d2h = e2e_measure(w, dev, max(2, min(args.steps, 10)), 2)
         per = per_workload(args, dev, flush, peak) if not args.no_per_workload else None
         pair = pair_gather_measure(dev, flush, peak) if not args.no_per_workload else None
+        blocks = block_measure(dev, flush, peak) if not args.no_per_workload else None
         cpu = cpu_baseline(args.workload)
         import gather_radix_select_gb300 as g
 
@@ -397,6 +398,7 @@ def gpu_arm(args):
             "device_err_flag": err_flag,
             "per_workload": per,
             "pair_gather": pair,
+            "block_candidates": blocks,
         }
     if dist:
         dist.barrier()
@@ -479,6 +481,34 @@ def pair_gather_measure(dev, flush, peak):
            "gbs": round(nbytes / (t1 * 1e-3) / 1e9, 2), "frac_of_peak": round(nbytes / (t1 * 1e-3) / 1e9 / peak, 4),
            "bytes": nbytes, "two_launches_ms": round(t2, 5)}
     del out, out2
+    torch.cuda.empty_cache()
+    return res
+
+
+def block_measure(dev, flush, peak):
+    """The block-level candidate chain: 1024 rows of 32 block scores (blocks of 64 over
+    compressed length 2048), 16 blocks -> 1024 positions a row, causal ends, and the gather
+    of the 128-wide key rows at those positions (one launch)."""
+    import torch
+
+    import gather_radix_select_gb300 as g
+
+    w = syn.block_candidates_workload()
+    scores = torch.from_numpy(w["scores"].view(np.int16)).view(torch.bfloat16).to(dev)
+    key = torch.from_numpy(w["key"].view(np.int16)).view(torch.bfloat16).to(dev)
+    pe = torch.from_numpy(w["pos_end"]).to(dev)
+    R, tb, bs, d = w["rows"], w["topk_blocks"], w["block_size"], w["d"]
+    npos = tb * bs
+    pos = torch.empty((R, npos), dtype=torch.int32, device=dev)
+    out = torch.empty((R, npos, d), dtype=torch.bfloat16, device=dev)
+    t = statistics.median(time_steps(_Call(lambda: g.block_topk_gather(scores, tb, bs, pos_end=pe, key=key,
+                                                                      out_pos=pos, gather_out=out)), 10, 3, flush))
+    # algorithmic bytes: block scores + positions + the key rows at least once + the gathered rows
+    nbytes = R * w["n_blocks"] * 2 + R * npos * 4 + w["comp_len"] * d * 2 + R * npos * d * 2
+    res = {"workload": "block_candidates_bf16_1024x32_top16x64_gather_d128", "ms": round(t, 5),
+           "gbs": round(nbytes / (t * 1e-3) / 1e9, 2), "frac_of_peak": round(nbytes / (t * 1e-3) / 1e9 / peak, 4),
+           "bytes": nbytes, "launches": 1}
+    del out, pos
     torch.cuda.empty_cache()
     return res
 

@@ -20,7 +20,7 @@ import torch
 from . import _native
 from ._native import SelError, SEL_MAX_K
 
-__all__ = ["topk", "gather_rows", "gather_rows_pair", "topk_gather", "stride_requirement", "max_cols", "workspace_size", "kernel_name",
+__all__ = ["topk", "gather_rows", "gather_rows_pair", "topk_gather", "block_topk_gather", "stride_requirement", "max_cols", "workspace_size", "kernel_name",
            "SelError",
            "SEL_MAX_K", "library_path"]
 
@@ -266,6 +266,55 @@ def gather_rows_pair(key: torch.Tensor, key2: torch.Tensor, idx: torch.Tensor, *
             _stream(key.device, stream))
     _native.check(st, "sel_gather_rows_pair")
     return outs[0], outs[1]
+
+
+def block_topk_gather(scores: torch.Tensor, topk_blocks: int, block_size: int, *,
+                      pos_end: torch.Tensor | None = None, key: torch.Tensor | None = None,
+                      out_pos: torch.Tensor | None = None, gather_out: torch.Tensor | None = None,
+                      nan_flag: torch.Tensor | None = None, err_flag: torch.Tensor | None = None, stream=None,
+                      workspace: torch.Tensor | None = None):
+    """Block-level candidate selection: the ``topk_blocks`` best blocks of each row of
+    ``scores`` [rows, n_blocks] (blocks of ``block_size`` positions; a block is a candidate
+    when it holds a position below ``pos_end[r]``), expanded to their valid positions in
+    ascending order then -1 (int32 [rows, topk_blocks * block_size]), and, with ``key``
+    (bf16 [b, comp_len, d]), the key rows gathered there.  Returns ``(positions, gathered)``,
+    ``gathered`` None without ``key``.
+    """
+    _check_x(scores)
+    rows, n_blocks = scores.shape
+    dev = scores.device
+    pos_end = _check_end(pos_end, rows, dev)
+    npos = int(topk_blocks) * int(block_size)
+    if out_pos is None:
+        pos = _padded_rows(rows, npos, torch.int32, dev)
+    else:
+        pos = out_pos
+        if pos.dtype != torch.int32 or pos.dim() != 2 or pos.shape[0] != rows or pos.shape[1] < npos \
+                or (rows > 1 and pos.stride(1) != 1) or pos.device != dev:
+            raise ValueError("out_pos must be an int32 [rows, >=topk_blocks*block_size] tensor on scores' device")
+    b = comp_len = d = kbs = krs = 0
+    if key is not None:
+        kbs, krs = _key_strides(key)
+        b, comp_len, d = key.shape
+        if key.device != dev:
+            raise ValueError("key must be on scores' device")
+        if gather_out is None:
+            gather_out = torch.empty((rows, npos, d), dtype=torch.bfloat16, device=dev)
+        elif gather_out.shape != (rows, npos, d) or not gather_out.is_contiguous():
+            raise ValueError("gather_out must be a contiguous bf16 [rows, topk_blocks*block_size, d] tensor")
+    else:
+        gather_out = None
+    with torch.cuda.device(dev):
+        lib = _native.load()
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        ws, ws_bytes = _ws_for(lib, workspace, scores.dtype, rows, n_blocks, topk_blocks, dev, s)
+        st = lib.sel_block_topk_gather(
+            _ptr(scores), _DTYPES[scores.dtype], rows, n_blocks, _row_stride(scores), _ptr(pos_end),
+            int(topk_blocks), int(block_size), _ptr(pos), pos.stride(0) if rows > 1 else max(pos.stride(0), npos),
+            _ptr(key), b, comp_len, d, kbs, krs, _ptr(gather_out),
+            _ptr(ws), ws_bytes, _ptr(nan_flag), _ptr(err_flag), ctypes.c_void_p(s.cuda_stream))
+    _native.check(st, "sel_block_topk_gather")
+    return (pos[:, :npos] if out_pos is not None else pos), gather_out
 
 
 def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, end: torch.Tensor | None = None,

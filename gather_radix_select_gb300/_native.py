@@ -29,6 +29,9 @@ SIGNATURES = {
                                _vp, _vp, _vp]),
     "sel_gather_rows_pair": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _int,
                                     _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "sel_block_topk_gather": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _int, _i64, _vp, _i64,
+                                     _vp, _i64, _i64, _i64, _i64, _i64, _vp,
+                                     _vp, ctypes.c_size_t, _vp, _vp, _vp]),
     "sel_topk_gather": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _int, _int, _int, _int,
                                _vp, _i64, _vp, _i64,
                                _vp, _i64, _i64, _i64, _i64, _i64, _i64, _vp,

@@ -505,7 +505,7 @@ int run_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
              int idx_dtype, int want_values, void *out_idx, int64_t out_idx_stride, void *out_val,
              int64_t out_val_stride, const void *key, int64_t b, int64_t comp_len, int64_t d,
              int64_t key_batch_stride, int64_t key_row_stride, int64_t n_gather, void *gather_out, void *workspace,
-             size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag, void *stream)
+             size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag, void *stream, int64_t row_end_div = 1)
 {
     Plan p;
     int st = cached_plan(dtype, rows, cols, k, n_gather > 0, n_gather, p);
@@ -520,6 +520,7 @@ int run_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
     a.cols = cols;
     a.stride = stride;
     a.row_end = row_end;
+    a.row_end_div = row_end_div;
     a.k = k;
     a.idx_i64 = idx_dtype == SEL_I64;
     a.want_values = want_values ? 1 : 0;
@@ -683,6 +684,59 @@ int sel_gather_rows_pair(const void *key, int64_t d, int64_t key_batch_stride, i
     a.out = static_cast<uint16_t *>(out);
     a.err_flag = err_flag;
     return status_of(sel::launch_gather(a, static_cast<cudaStream_t>(stream)));
+}
+
+int sel_block_topk_gather(const void *scores, int dtype, int64_t rows, int64_t n_blocks, int64_t stride,
+                          const int32_t *pos_end, int topk_blocks, int64_t block_size, int32_t *out_pos,
+                          int64_t out_pos_stride, const void *key, int64_t b, int64_t comp_len, int64_t d,
+                          int64_t key_batch_stride, int64_t key_row_stride, void *gather_out, void *workspace,
+                          size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag, void *stream)
+{
+    if (block_size < 1 || n_blocks < 0) return SEL_EINVAL;
+    if (n_blocks > 0 && n_blocks > 0x7fffffffLL / block_size) return SEL_EUNSUPPORTED;  // positions are int32
+    if (topk_blocks >= 1 && static_cast<int64_t>(topk_blocks) * block_size > 0x7fffffffLL) return SEL_EUNSUPPORTED;
+    int st = check_topk_args(scores, dtype, rows, n_blocks, stride, topk_blocks, SEL_I32, 0, out_pos,
+                             out_pos_stride, nullptr, 0, true);
+    if (st != SEL_OK) return st;
+    const int64_t npos = static_cast<int64_t>(topk_blocks) * block_size;
+    if (rows > 0 && out_pos_stride < npos) return SEL_EINVAL;
+    if (key || gather_out) {
+        st = check_gather_key(key, b, comp_len, d, key_batch_stride, key_row_stride, rows, gather_out);
+        if (st != SEL_OK) return st;
+    }
+    if (rows == 0) return SEL_OK;
+    sel::BlockArgs a{};
+    if (n_blocks <= sel::kBlockSelectMax) {
+        // few blocks a row: the expansion kernel selects them itself (one launch)
+        a.scores = scores;
+        a.scores_bf16 = dtype == SEL_BF16;
+        a.n_blocks = n_blocks;
+        a.scores_stride = stride;
+        a.nan_flag = nan_flag;
+    } else {
+        // the selected block ids land in the first topk_blocks columns of out_pos (ascending, fills
+        // last), to be expanded in place
+        st = run_topk(scores, dtype, rows, n_blocks, stride, pos_end, topk_blocks, SEL_I32, 0, out_pos,
+                      out_pos_stride, nullptr, 0, nullptr, 1, 0, 0, 0, 0, 0, nullptr, workspace, workspace_bytes,
+                      nan_flag, err_flag, stream, block_size);
+        if (st != SEL_OK) return st;
+    }
+    a.pos = out_pos;
+    a.pos_stride = out_pos_stride;
+    a.rows = rows;
+    a.topk_blocks = topk_blocks;
+    a.block_size = block_size;
+    a.pos_end = pos_end;
+    a.pos_limit = n_blocks * block_size;
+    a.key = static_cast<const uint16_t *>(key);
+    a.comp_len = comp_len;
+    a.d = d;
+    a.key_batch_stride = key_batch_stride;
+    a.key_row_stride = key_row_stride;
+    a.rows_per_batch = key ? rows / b : 1;
+    a.out = static_cast<uint16_t *>(gather_out);
+    a.err_flag = err_flag;
+    return status_of(sel::launch_block_expand(a, static_cast<cudaStream_t>(stream)));
 }
 
 int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride, const int32_t *row_end,

@@ -83,7 +83,138 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs
                   s_pos);
 }
 
+// Order-preserving key of a score (larger value => larger key; -0 and +0 equal).
+__device__ __forceinline__ uint32_t score_key(uint32_t u, bool bf16)
+{
+    if (bf16) {
+        u = (u == 0x8000u) ? 0u : u;
+        return (u & 0x8000u) ? (~u & 0xffffu) : (u | 0x8000u);
+    }
+    u = (u == 0x80000000u) ? 0u : u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ bool score_is_nan(uint32_t u, bool bf16)
+{
+    return bf16 ? (u & 0x7fffu) > 0x7f80u : (u & 0x7fffffffu) > 0x7f800000u;
+}
+
+// The row's block selection done in the CTA (n_blocks <= kBlockSelectMax): block c is chosen when
+// fewer than topk_blocks candidates beat it (a larger key, or an equal key and a smaller index);
+// the chosen ids are compacted in ascending order into s_blk, -1 after them.  A row with more
+// candidates than topk_blocks holding a NaN sets nan_flag (its selection is then unspecified).
+__device__ void select_blocks(const BlockArgs &a, int64_t row, int64_t n_cand, int32_t *s_blk)
+{
+    __shared__ uint32_t s_key[kBlockSelectMax];
+    __shared__ int s_warp_cnt[kBlockSelectMax / 32];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int nb = static_cast<int>(a.n_blocks), nc = static_cast<int>(n_cand), tb = a.topk_blocks;
+    const bool bf16 = a.scores_bf16 != 0;
+    bool nan = false;
+    if (t < nb) {
+        const uint32_t u = bf16 ? static_cast<const uint16_t *>(a.scores)[row * a.scores_stride + t]
+                                : static_cast<const uint32_t *>(a.scores)[row * a.scores_stride + t];
+        s_key[t] = score_key(u, bf16);
+        nan = t < nc && score_is_nan(u, bf16);
+    }
+    if (__syncthreads_or(nan) && nc > tb && t == 0 && a.nan_flag) atomicOr(a.nan_flag, 1);
+    bool chosen = false;
+    if (t < nc) {
+        const uint32_t kt = s_key[t];
+        int beaten = 0;
+        for (int i = 0; i < nc; ++i) {
+            const uint32_t ki = s_key[i];
+            beaten += (ki > kt) | ((ki == kt) & (i < t));
+        }
+        chosen = beaten < tb;
+    }
+    // ordered compaction; the first kBlockSelectMax threads are whole warps
+    unsigned m = 0;
+    if (t < kBlockSelectMax) {
+        m = __ballot_sync(0xffffffffu, chosen);
+        if (lane == 0) s_warp_cnt[warp] = __popc(m);
+    }
+    __syncthreads();
+    if (t < kBlockSelectMax) {
+        int base = 0, total = 0;
+        for (int w = 0; w < kBlockSelectMax / 32; ++w) {
+            base += w < warp ? s_warp_cnt[w] : 0;
+            total += s_warp_cnt[w];
+        }
+        if (chosen) s_blk[base + __popc(m & ((1u << lane) - 1u))] = t;
+        for (int j = total + t; j < tb; j += kBlockSelectMax) s_blk[j] = -1;
+    }
+}
+
+// One CTA per row: the row's selected block ids (ascending; -1 fills last) are read into shared
+// memory (or chosen here, see select_blocks), then every block expands to its positions blk * block_size + i, positions at or past the
+// row's end become -1, and the valid positions are written first (ascending), -1 after them; the
+// key rows of each chunk of positions are gathered as in gather_kernel (a -1 reads position 0).
+__global__ void __launch_bounds__(kGatherThreads) block_expand_kernel(const BlockArgs a)
+{
+    extern __shared__ int32_t s_blk[];  // topk_blocks ids
+    __shared__ int64_t s_pos[kPairsPerCta];
+    const int64_t row = blockIdx.x / a.ctas_per_row;
+    const int part = static_cast<int>(blockIdx.x - row * a.ctas_per_row);
+    int32_t *prow = a.pos + row * a.pos_stride;
+    const int tb = a.topk_blocks;
+    int64_t pe = a.pos_limit;
+    if (a.pos_end) {
+        const int64_t e = a.pos_end[row];
+        pe = e < 0 ? 0 : (e > a.pos_limit ? a.pos_limit : e);
+    }
+    if (a.scores)
+        select_blocks(a, row, (pe + a.block_size - 1) / a.block_size, s_blk);
+    else
+        for (int j = threadIdx.x; j < tb; j += kGatherThreads) s_blk[j] = prow[j];
+    __syncthreads();  // every id is read before the row is overwritten
+    // blocks are ascending and only the last valid block can reach past pe, so the valid positions
+    // of block j start at j * block_size and the row is: valid positions, then -1
+    const int64_t bs = a.block_size;
+    const int64_t npos = static_cast<int64_t>(tb) * bs;
+    const uint16_t *kb = a.key ? a.key + (row / a.rows_per_batch) * a.key_batch_stride : nullptr;
+    // this CTA's positions: all of them, or one chunk of kPairsPerCta when the row is split
+    const int64_t qb = a.ctas_per_row > 1 ? static_cast<int64_t>(part) * kPairsPerCta : 0;
+    const int64_t qe = a.ctas_per_row > 1 ? min(npos, qb + kPairsPerCta) : npos;
+    for (int64_t q0 = qb; q0 < qe; q0 += kPairsPerCta) {
+        const int np = static_cast<int>(qe - q0 < kPairsPerCta ? qe - q0 : kPairsPerCta);
+        for (int i = threadIdx.x; i < np; i += kGatherThreads) {
+            const int64_t q = q0 + i;
+            const int64_t j = q / bs;
+            const int32_t blk = s_blk[j];
+            int64_t p = blk < 0 ? -1 : static_cast<int64_t>(blk) * bs + (q - j * bs);
+            if (p >= pe) p = -1;
+            prow[q] = static_cast<int32_t>(p);
+            int64_t g = p < 0 ? 0 : p;  // safe position
+            if (g >= a.comp_len) {
+                g = -1;  // out of range: a zero row and an error flag
+                if (a.err_flag && kb) atomicCAS(a.err_flag, 0, kStatusInval);
+            }
+            s_pos[i] = g;
+        }
+        __syncthreads();
+        if (kb) copy_rows(kb, a.key_row_stride, a.d, a.out + (row * npos + q0) * a.d, np, s_pos);
+        __syncthreads();
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_block_expand(const BlockArgs &a_in, cudaStream_t stream)
+{
+    BlockArgs a = a_in;
+    if (a.rows <= 0) return cudaSuccess;
+    if (a.topk_blocks < 1) return cudaErrorInvalidValue;
+    // a row selected in the kernel is split into chunks of kPairsPerCta positions, one CTA each;
+    // block ids read from pos are expanded in place, so such a row stays with one CTA
+    const int64_t npos = static_cast<int64_t>(a.topk_blocks) * a.block_size;
+    a.ctas_per_row = a.scores ? static_cast<int32_t>((npos + kPairsPerCta - 1) / kPairsPerCta) : 1;
+    const int64_t grid = a.rows * a.ctas_per_row;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const size_t smem = static_cast<size_t>(a.topk_blocks) * sizeof(int32_t);
+    block_expand_kernel<<<static_cast<unsigned>(grid), kGatherThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gather(const GatherArgs &a_in, cudaStream_t stream)
 {

@@ -32,6 +32,7 @@ struct TopkArgs {
     const void *x;            // [rows, stride] elements (fp32 or bf16 bits)
     int64_t rows, cols, stride;
     const int32_t *row_end;   // nullable
+    int64_t row_end_div;      // > 1: a row has ceil(row_end / row_end_div) valid columns
     int32_t k;
     int32_t idx_i64;          // 0: int32 indices, 1: int64
     int32_t want_values;
@@ -84,6 +85,32 @@ struct GatherArgs {
     int64_t pairs_per_cta;    // (row, position) pairs handled by one CTA
     int32_t ctas_per_row;
 };
+
+// Expansion of selected blocks to positions, with the gather of their key rows (gather.cu).
+constexpr int kBlockSelectMax = 128;  // block_expand_kernel selects rows of at most this many blocks itself
+
+struct BlockArgs {
+    int32_t *pos;             // [rows, pos_stride]: selected block ids in [0, topk_blocks) on entry
+    int64_t pos_stride;       //   (unless scores is set), their valid positions ascending then -1 on exit
+    // set: the kernel selects the blocks itself from these scores (n_blocks <= kBlockSelectMax)
+    const void *scores;
+    int32_t scores_bf16;
+    int64_t n_blocks, scores_stride;
+    int32_t *nan_flag;
+    int64_t rows;
+    int32_t topk_blocks;
+    int64_t block_size;
+    const int32_t *pos_end;   // nullable: exclusive end of each row's valid positions
+    int64_t pos_limit;        // n_blocks * block_size (the end when pos_end is null)
+    // gather (key null = none), as GatherArgs
+    const uint16_t *key;
+    int64_t comp_len, d, key_batch_stride, key_row_stride, rows_per_batch;
+    uint16_t *out;            // [rows, topk_blocks * block_size, d]
+    int32_t *err_flag;
+    int32_t ctas_per_row;     // set by the launcher: several only when the kernel selects the blocks
+};
+
+cudaError_t launch_block_expand(const BlockArgs &a, cudaStream_t stream);
 
 // Re-ordering of finished output rows by value (order.cu).
 struct OrderArgs {

@@ -455,7 +455,10 @@ __device__ __forceinline__ int64_t valid_cols(const TopkArgs &a, int64_t row)
 {
     int64_t n = a.cols;
     if (a.row_end) {
-        const int64_t re = a.row_end[row];
+        int64_t re = a.row_end[row];
+        // row_end in units of row_end_div columns' worth (block selection: a row end in positions,
+        // a column per block; the blocks holding a valid position)
+        if (a.row_end_div > 1) re = re <= 0 ? 0 : (re + a.row_end_div - 1) / a.row_end_div;
         n = re < 0 ? 0 : (re > a.cols ? a.cols : re);
     }
     return n;

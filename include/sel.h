@@ -169,6 +169,38 @@ SEL_API int sel_gather_rows_pair(const void *key, int64_t d, int64_t key_batch_s
                                  int64_t b, int64_t comp_len, const void *idx, int idx_dtype, int64_t rows, int64_t n,
                                  int64_t idx_row_stride, void *out, void *out2, int32_t *err_flag, void *stream);
 
+/* Block-level candidate selection with its gather (MindSpore hyper-parallel
+ * pull request "perf/gather-index-select": the `compressed_candidate_topk`
+ * chain picks the top blocks of compressed positions, expands them to
+ * topk_blocks * block_size positions, sorts and masks the positions, and
+ * gathers the key rows there -- its Index, Sort and MaskedFill steps):
+ *   scores      [rows, stride] block scores of `dtype`, n_blocks columns; block
+ *               c covers positions [c * block_size, (c + 1) * block_size).
+ *   pos_end     int32 [rows]: exclusive end of each row's valid positions,
+ *               clamped on the device to [0, n_blocks * block_size]; NULL
+ *               means n_blocks * block_size.  A block is a candidate when it
+ *               holds a valid position.
+ *   topk_blocks 1..SEL_MAX_K blocks chosen per row by sel_topk's rule (largest
+ *               score, smaller block first on ties; fewer candidates than
+ *               topk_blocks: all of them).
+ *   out_pos     int32 [rows, out_pos_stride], out_pos_stride >= topk_blocks *
+ *               block_size (alignment as sel_topk's out_idx): the chosen
+ *               blocks' valid positions, ascending, then -1.
+ *   key .. key_row_stride, gather_out   as sel_gather_rows, gathering
+ *               out_pos (a -1 reads position 0); key and gather_out both
+ *               NULL: positions only.
+ *   workspace, nan_flag, err_flag       as sel_topk (shape rows x n_blocks,
+ *               k = topk_blocks).
+ * One launch for rows of at most 128 blocks (the expansion kernel ranks the
+ * blocks itself); wider rows take two (sel_topk's selection, then the
+ * expansion with the gather). */
+SEL_API int sel_block_topk_gather(const void *scores, int dtype, int64_t rows, int64_t n_blocks, int64_t stride,
+                                  const int32_t *pos_end, int topk_blocks, int64_t block_size, int32_t *out_pos,
+                                  int64_t out_pos_stride, const void *key, int64_t b, int64_t comp_len, int64_t d,
+                                  int64_t key_batch_stride, int64_t key_row_stride, void *gather_out,
+                                  void *workspace, size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag,
+                                  void *stream);
+
 /* sel_topk followed by sel_gather_rows of the first n_gather output columns
  * (n_gather <= k), in one launch.  The top-k arguments are those of
  * sel_topk (out_idx may be NULL when the indices themselves are not needed);

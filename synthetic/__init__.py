@@ -237,3 +237,23 @@ def kl_pair_gather(rows: int = 1024, n: int = 512, comp_len: int = 2048, d: int 
     pos = gather_positions(seed + 1, rows, n, comp_len, neg_frac=0.02)
     return {"key": key, "key2": key2, "pos": pos, "rows": rows, "n": n, "comp_len": comp_len, "d": d, "d2": d2,
             "b": b}
+
+
+def block_candidates_workload(rows: int = 1024, comp_len: int = 2048, block_size: int = 64, topk_blocks: int = 16,
+                              d: int = 128, seed: int = SEED_BASE + 7) -> dict:
+    """Inputs of the block-level candidate chain (MindSpore hyper-parallel pull request
+    "perf/gather-index-select": per query chunk of 1024 rows the chain gathers
+    topk_blocks * block_size = 1024 positions at compressed length 2048, head_dim 128).
+
+    Block scores bf16 N(0,1) [rows, comp_len / block_size]; causal position ends
+    pos_end[i] = min(comp_len, 2 (i + 1)) (the chunk's rows spread over the compressed
+    length, so early rows hold fewer candidate blocks than topk_blocks); key bf16 N(0,1)
+    [1, comp_len, d].
+    """
+    g = rng_for(seed)
+    n_blocks = comp_len // block_size
+    scores = f32_to_bf16_bits(g.standard_normal((rows, n_blocks), dtype=np.float32))
+    key = f32_to_bf16_bits(g.standard_normal((1, comp_len, d), dtype=np.float32))
+    pos_end = np.minimum(comp_len, 2 * (np.arange(rows) + 1)).astype(np.int32)
+    return {"scores": scores, "key": key, "pos_end": pos_end, "rows": rows, "n_blocks": n_blocks,
+            "block_size": block_size, "topk_blocks": topk_blocks, "comp_len": comp_len, "d": d}

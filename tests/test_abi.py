@@ -23,7 +23,8 @@ def declared_symbols():
 
 
 def test_header_declares_the_boundary():
-    assert declared_symbols() == sorted(["sel_gather_rows", "sel_gather_rows_pair", "sel_max_cols", "sel_stride_requirement",
+    assert declared_symbols() == sorted(["sel_block_topk_gather", "sel_gather_rows", "sel_gather_rows_pair",
+                                         "sel_max_cols", "sel_stride_requirement",
                                          "sel_strerror", "sel_topk", "sel_topk_gather", "sel_topk_kernel_name",
                                          "sel_topk_noalloc", "sel_topk_workspace_size"])
 
@@ -118,6 +119,25 @@ def test_gather_pair_rejections(lib):
     assert g(rows=5, b=2) == EINVAL
     assert g(idx_dtype=2) == EINVAL
     assert g(rows=0) == 0 and g(n=0) == 0
+
+
+def test_block_rejections(lib):
+    EINVAL, EALIGN, EUNSUP = 1, 2, 3
+    def g(scores=FAKE, rows=4, n_blocks=32, stride=32, tb=4, bs=64, out_pos=FAKE, ops=256, key=None, b=1,
+          comp_len=2048, d=128, kbs=2048 * 128, krs=128, gout=None):
+        return lib.sel_block_topk_gather(scores, 0, rows, n_blocks, stride, None, tb, bs, out_pos, ops, key, b,
+                                         comp_len, d, kbs, krs, gout, None, 0, None, None, None)
+    assert g(bs=0) == EINVAL
+    assert g(tb=0) == EINVAL
+    assert g(tb=4097) == EINVAL
+    assert g(ops=252) == EINVAL            # out_pos rows shorter than topk_blocks * block_size
+    assert g(ops=258) == EALIGN            # 1032-byte rows
+    assert g(out_pos=None) == EINVAL
+    assert g(key=FAKE) == EINVAL           # key without an output
+    assert g(gout=FAKE) == EINVAL          # output without a key
+    assert g(key=FAKE, gout=FAKE, d=12, krs=12, kbs=12 * 2048) == EALIGN
+    assert g(n_blocks=1 << 20, stride=1 << 20, bs=1 << 12) == EUNSUP   # positions past int32
+    assert g(rows=0) == 0
 
 
 def test_fused_rejections(lib):
