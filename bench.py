@@ -319,7 +319,7 @@ def gpu_arm(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = syn.workload(args.workload)
-    runner = Runner(w, dev)
+    runner = Runner(w, dev, sorted_value=args.sorted_value)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     peak, peak_kind = measured_peaks()
 
@@ -351,7 +351,8 @@ def gpu_arm(args):
 
     result = None
     if rank == 0 and args.profile:
-        result = {"profile_run": True, "workload": args.workload, "ms_per_step": round(ms_max, 5),
+        result = {"profile_run": True, "workload": args.workload, "sorted_value": args.sorted_value,
+                  "ms_per_step": round(ms_max, 5),
                   "value": round(value, 2), "unit": "GB/s", "steps": args.steps, "warmup": args.warmup}
     elif rank == 0:
         kernel_ms = statistics.median(times)
@@ -450,6 +451,38 @@ class _Call:
         import torch
 
         self.torch, self.step = torch, fn
+
+
+def profile_extra(args):
+    """--profile-extra pair|block: only the warm-up and timed calls of the double gather or the
+    block-level candidate chain (a short run for ncu); prints their median time."""
+    import torch
+
+    import gather_radix_select_gb300 as g
+
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    if args.profile_extra == "pair":
+        w = syn.kl_pair_gather()
+        key = torch.from_numpy(w["key"].view(np.int16)).view(torch.bfloat16).to(dev)
+        key2 = torch.from_numpy(w["key2"].view(np.int16)).view(torch.bfloat16).to(dev)
+        pos = torch.from_numpy(w["pos"]).to(dev)
+        out = torch.empty((w["rows"], w["n"], w["d"]), dtype=torch.bfloat16, device=dev)
+        out2 = torch.empty((w["rows"], w["n"], w["d2"]), dtype=torch.bfloat16, device=dev)
+        call = _Call(lambda: g.gather_rows_pair(key, key2, pos, out=out, out2=out2))
+    else:
+        w = syn.block_candidates_workload()
+        scores = torch.from_numpy(w["scores"].view(np.int16)).view(torch.bfloat16).to(dev)
+        key = torch.from_numpy(w["key"].view(np.int16)).view(torch.bfloat16).to(dev)
+        pe = torch.from_numpy(w["pos_end"]).to(dev)
+        npos = w["topk_blocks"] * w["block_size"]
+        pos = torch.empty((w["rows"], npos), dtype=torch.int32, device=dev)
+        out = torch.empty((w["rows"], npos, w["d"]), dtype=torch.bfloat16, device=dev)
+        call = _Call(lambda: g.block_topk_gather(scores, w["topk_blocks"], w["block_size"], pos_end=pe, key=key,
+                                                 out_pos=pos, gather_out=out))
+    times = time_steps(call, args.steps, args.warmup, flush)
+    return {"profile_run": True, "extra": args.profile_extra, "ms": round(statistics.median(times), 5),
+            "steps": args.steps, "warmup": args.warmup}
 
 
 def pair_gather_measure(dev, flush, peak):
@@ -606,9 +639,18 @@ def main():
     ap.add_argument("--no-per-workload", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="only the warm-up and timed steps of --workload (a short run for ncu)")
+    ap.add_argument("--sorted-value", action="store_true",
+                    help="with --profile: the workload's step with value-ordered output")
+    ap.add_argument("--profile-extra", choices=["pair", "block"],
+                    help="only the double gather or the block-level candidate chain (a short run for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.sorted_value and not args.profile:
+        ap.error("--sorted-value is a profiling mode; it needs --profile")
+    if args.profile_extra:
+        print(json.dumps(profile_extra(args)), flush=True)
+        return
     res = reference_arm(args) if args.impl == "reference" else gpu_arm(args)
     if res is not None:
         print(json.dumps(res), flush=True)
