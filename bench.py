@@ -306,6 +306,21 @@ def e2e_measure(w, dev, steps, warmup):
     return ms, h2d, d2h
 
 
+def combine_ranks(ms_step: float, nbytes: int, dist, device):
+    """Replicas: every rank runs the same per-GPU workload.  The step time is the slowest rank's;
+    the value is the bytes all ranks processed per second (GB/s).  dist None = one rank."""
+    import torch
+
+    ms_max = ms_step
+    world = 1
+    if dist is not None:
+        world = dist.get_world_size()
+        t = torch.tensor([ms_step], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    return ms_max, nbytes * world / (ms_max * 1e-3) / 1e9
+
+
 def gpu_arm(args):
     import torch
 
@@ -340,13 +355,8 @@ def gpu_arm(args):
     if dist:
         dist.barrier()
     ms_step = sum(times) / len(times)
-    ms_max = ms_step
-    if dist:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
     nbytes = step_bytes(w)
-    value = nbytes * world / (ms_max * 1e-3) / 1e9
+    ms_max, value = combine_ranks(ms_step, nbytes, dist, dev)
     err_flag = int(runner.err.item())
 
     result = None
