@@ -95,6 +95,21 @@ def test_noalloc_matches_on_fp32_split_rows_with_row_end_and_nan(monkeypatch):
     assert res[0][2] == 1
 
 
+def test_noalloc_value_order(monkeypatch):
+    # value-ordered output through the no-workspace entry point, on split rows
+    monkeypatch.setenv("SEL_PLAN", "split")
+    import oracle
+    w = syn.workload("indexer_bf16_4x204800_k1024")
+    x = torch.from_numpy(w["x"].view(np.int16)).view(torch.bfloat16).cuda()
+    need, res = run_both(x, 1, w["rows"], w["cols"], w["k"], 1, True, sorted_index=2)
+    assert need > 0
+    same(res[0], res[1])
+    same(res[0], res[2])
+    o_idx, o_bits, _ = oracle.topk(w["x"], "bf16", w["k"], sorted_value=True)
+    assert (res[1][0].numpy() == o_idx).all()
+    assert (res[1][1].view(torch.int16).numpy().view(np.uint16) == o_bits).all()
+
+
 def test_noalloc_without_scratch_and_oversize_rejection(monkeypatch):
     # a shape that needs no scratch runs too
     rng = np.random.default_rng(5)
