@@ -254,7 +254,6 @@ cudaError_t launch_value_order(int dtype, bool idx_i64, const OrderArgs &a_in, c
     int threads = 32;  // a power of two from 32 to 512 with threads * 8 >= k
     while (threads * kEpt < a.k) threads <<= 1;
     const int n_items = threads * kEpt;
-    a.p2 = n_items;
     const size_t ksz = dtype == 1 ? sizeof(uint32_t) : sizeof(uint64_t);
     const int counters = kDigits * threads;
     const size_t smem = static_cast<size_t>(n_items) * (ksz + sizeof(int32_t) + sizeof(uint32_t)) +

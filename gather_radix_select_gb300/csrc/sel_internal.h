@@ -118,7 +118,6 @@ struct OrderArgs {
     int64_t x_stride;         // elements
     int64_t rows;
     int32_t k;
-    int32_t p2;               // items sorted per row: k rounded up to 8 x a multiple of 32 threads (set by the launcher)
     void *out_idx;            // [rows, out_idx_stride] int32 or int64
     int64_t out_idx_stride;
     void *out_val;            // nullable: [rows, out_val_stride] value bits
