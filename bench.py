@@ -577,6 +577,18 @@ def oracle_step(w, rows_sel):
     return time.perf_counter() - t0
 
 
+def oracle_step_parallel(w, rows_sel, workers):
+    """oracle_step over the rows split into `workers` chunks on as many threads (the C oracle
+    runs without the interpreter lock)."""
+    import concurrent.futures
+
+    chunks = [c for c in np.array_split(rows_sel, workers) if len(c)]
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(chunks)) as ex:
+        list(ex.map(lambda c: oracle_step(w, c), chunks))
+    return time.perf_counter() - t0
+
+
 def sample_bytes(w, rows_sel):
     s = syn.row_subset(w, rows_sel)
     s["key"] = w.get("key")
@@ -602,11 +614,18 @@ def cpu_baseline(name, budget_s=10.0):
         reps += 1
     per = total / reps
     nb = sample_bytes(w, rows_sel)
+    # the same sample row-parallel over the host's cores (one thread per core, rows split evenly)
+    workers = max(1, os.cpu_count() or 1)
+    ptimes = [oracle_step_parallel(w, rows_sel, workers) for _ in range(3)]
+    pper = statistics.median(ptimes)
     return {"value": round(nb / per / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": "%d of %d rows (evenly spaced), %d passes, %.2f s per pass; single-threaded C full sort "
                       "per row%s" % (len(rows_sel), R, reps, per, " + triple-loop gather" if w.get("key") is not None
                                      else ""),
-            "rows_per_s": round(len(rows_sel) / per, 1)}
+            "rows_per_s": round(len(rows_sel) / per, 1),
+            "row_parallel": {"value": round(nb / pper / 1e9, 4), "unit": "GB/s", "cores": workers,
+                             "rows_per_s": round(len(rows_sel) / pper, 1),
+                             "sample": "the same rows split over %d threads, median of 3 passes" % workers}}
 
 
 def reference_arm(args):
