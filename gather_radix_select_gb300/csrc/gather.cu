@@ -35,6 +35,30 @@ __device__ __forceinline__ void copy_rows(const uint16_t *kb, int64_t row_stride
     const int vsh = (vpr & (vpr - 1)) == 0 ? __ffs(vpr) - 1 : -1;  // log2(vpr), or -1
     uint4 *ob = reinterpret_cast<uint4 *>(out);
     const int total = np * vpr;
+    if (vsh >= 0 && vpr <= kGatherThreads) {
+        // rows of a power-of-two number of vectors: thread t always copies vector (t mod vpr) of
+        // rows t / vpr, t / vpr + threads / vpr, ... -- no per-vector index division
+        const int c = static_cast<int>(threadIdx.x) & (vpr - 1);
+        const int rstep = kGatherThreads >> vsh;
+        for (int jb = static_cast<int>(threadIdx.x) >> vsh; jb < np; jb += kUnroll * rstep) {
+            uint4 v[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int jj = jb + u * rstep;
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (jj < np) {
+                    const int64_t p = s_pos[jj];
+                    if (p >= 0) v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * row_stride) + c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int jj = jb + u * rstep;
+                if (jj < np) __stcs(ob + (static_cast<int64_t>(jj) << vsh) + c, v[u]);
+            }
+        }
+        return;
+    }
     for (int t0 = threadIdx.x; t0 < total; t0 += kUnroll * kGatherThreads) {
         uint4 v[kUnroll];
 #pragma unroll

@@ -405,6 +405,36 @@ __device__ void gather_rows_of(const TopkArgs &a, int64_t row, int64_t j0, int64
     uint4 *ob = reinterpret_cast<uint4 *>(a.gather_out + (row * a.n_gather + j0) * a.d);
     const int total = static_cast<int>(j1 - j0) * vpr;
     constexpr int U = 4;
+    if (vsh >= 0 && vpr <= NT) {
+        // rows of a power-of-two number of vectors: thread t always copies vector (t mod vpr) of
+        // rows t / vpr, t / vpr + NT / vpr, ... -- one column read per row, no index division
+        const int nrows = static_cast<int>(j1 - j0);
+        const int c = static_cast<int>(threadIdx.x) & (vpr - 1);
+        const int rstep = NT >> vsh;
+        for (int jb = static_cast<int>(threadIdx.x) >> vsh; jb < nrows; jb += U * rstep) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int jj = jb + u * rstep;
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (jj < nrows) {
+                    const int64_t j = j0 + jj;
+                    int64_t p = glist ? static_cast<int64_t>(glist[jj]) : (j < n_short ? j : 0);
+                    if (p < 0) p = 0;
+                    if (p < a.comp_len)
+                        v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + c);
+                    else if (c == 0)
+                        set_err(a.err_flag, kStatusInval);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int jj = jb + u * rstep;
+                if (jj < nrows) __stcs(ob + (static_cast<int64_t>(jj) << vsh) + c, v[u]);
+            }
+        }
+        return;
+    }
     for (int t0 = threadIdx.x; t0 < total; t0 += U * NT) {
         uint4 v[U];
 #pragma unroll

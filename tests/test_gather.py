@@ -213,3 +213,24 @@ def test_gather_pair_full_size():
     want2, _ = oracle.gather_rows(w["key2"], w["pos"][rows], 1)
     assert (to_bits(out[torch.from_numpy(rows).cuda()]) == want).all()
     assert (to_bits(out2[torch.from_numpy(rows).cuda()]) == want2).all()
+
+
+@pytest.mark.parametrize("d", [48, 2560])
+def test_gather_general_row_widths(d):
+    # 6 and 320 16-byte vectors a row: not a power of two / wider than the CTA (the general loop)
+    rng = np.random.default_rng(d)
+    b, comp_len, rows_per_b, n = 2, 90, 3, 37
+    key = syn.f32_to_bf16_bits(rng.standard_normal((b, comp_len, d)).astype(np.float32)).reshape(b, comp_len, d)
+    key2 = syn.f32_to_bf16_bits(rng.standard_normal((b, comp_len, 16)).astype(np.float32)).reshape(b, comp_len, 16)
+    pos = syn.gather_positions(7, b * rows_per_b, n, comp_len, neg_frac=0.1)
+    pos[1, 3] = comp_len + 2  # out of range: zero row and error flag
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gsel().gather_rows(key_tensor(key), torch.from_numpy(pos).cuda(), err_flag=err)
+    err2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p1, p2 = gsel().gather_rows_pair(key_tensor(key), key_tensor(key2), torch.from_numpy(pos).cuda(), err_flag=err2)
+    torch.cuda.synchronize()
+    want, bad = oracle.gather_rows(key, pos, b)
+    want2, _ = oracle.gather_rows(key2, pos, b)
+    assert bad == 1 and int(err.item()) == 1 and int(err2.item()) == 1
+    assert (to_bits(out) == want).all()
+    assert (to_bits(p1) == want).all() and (to_bits(p2) == want2).all()

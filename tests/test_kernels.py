@@ -168,3 +168,32 @@ def test_forced_fused_gather(mode, monkeypatch):
     assert (fidx.cpu().numpy().astype(np.int64) == o_idx).all()
     want, bad = oracle.gather_rows(key_bits, o_idx[:, :ng], b)
     assert bad == 0 and (to_bits(fout) == want).all()
+
+
+@pytest.mark.parametrize("mode", ["reg", "row", "wide"])
+@pytest.mark.parametrize("d", [48, 200, 512, 2048])
+def test_fused_gather_row_widths(mode, d, monkeypatch):
+    # key rows of 6, 25, 64 and 256 16-byte vectors: the general copy loop (not a power of two, or
+    # wider than the CTA) and the per-column one; the last case has a key shorter than the scored
+    # row, so some selected positions are out of range (zero rows, error flag)
+    monkeypatch.setenv("SEL_PLAN", mode)
+    import gather_radix_select_gb300 as g
+    rng = np.random.default_rng(d)
+    b, rows, k, ng = 2, 6, 300, 200
+    cols = {"reg": 3000, "row": 20000, "wide": 140000}[mode]
+    comp_len = cols if d != 2048 else cols // 2
+    v = rng.standard_normal((rows, cols)).astype(np.float32)
+    x = to_torch(syn.f32_to_bf16_bits(v), "bf16")
+    key_bits = syn.f32_to_bf16_bits(rng.standard_normal((b, comp_len, d)).astype(np.float32)).reshape(b, comp_len, d)
+    key = to_torch(key_bits, "bf16")
+    end = torch.from_numpy(np.array([cols, 200, cols // 2, cols - 1, 299, 7], dtype=np.int32)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, fidx, fout = g.topk_gather(x, k, key, ng, end=end, err_flag=err)
+    torch.cuda.synchronize()
+    o_idx, _, _ = oracle.topk(syn.f32_to_bf16_bits(v), "bf16", k, row_end=end.cpu().numpy(), sorted_index=True,
+                              cols=cols)
+    assert (fidx.cpu().numpy().astype(np.int64) == o_idx).all()
+    want, bad = oracle.gather_rows(key_bits, o_idx[:, :ng], b)
+    assert (to_bits(fout) == want).all()
+    assert int(err.item()) == (1 if bad else 0)
+    assert (bad > 0) == (d == 2048)
