@@ -35,26 +35,38 @@ __device__ __forceinline__ void copy_rows(const uint16_t *kb, int64_t row_stride
     const int vsh = (vpr & (vpr - 1)) == 0 ? __ffs(vpr) - 1 : -1;  // log2(vpr), or -1
     uint4 *ob = reinterpret_cast<uint4 *>(out);
     const int total = np * vpr;
-    if (vsh >= 0 && vpr <= kGatherThreads) {
-        // rows of a power-of-two number of vectors: thread t always copies vector (t mod vpr) of
-        // rows t / vpr, t / vpr + threads / vpr, ... -- no per-vector index division
-        const int c = static_cast<int>(threadIdx.x) & (vpr - 1);
-        const int rstep = kGatherThreads >> vsh;
-        for (int jb = static_cast<int>(threadIdx.x) >> vsh; jb < np; jb += kUnroll * rstep) {
-            uint4 v[kUnroll];
+    if (vsh >= 1 && vpr <= 2 * kGatherThreads) {
+        // rows of a power-of-two number (>= 2) of vectors: lpr = vpr / 2 lanes share a row and
+        // thread t copies vectors c and c + lpr (c = t mod lpr) of rows t / lpr,
+        // t / lpr + threads / lpr, ... -- no per-vector index division, each instruction covers
+        // whole 128-byte pieces of the rows
+        const int lsh = vsh - 1, lpr = vpr >> 1;
+        const int c = static_cast<int>(threadIdx.x) & (lpr - 1);
+        const int rstep = kGatherThreads >> lsh;
+        constexpr int UR = kUnroll / 2;  // rows a thread has in flight (two vectors each)
+        for (int jb = static_cast<int>(threadIdx.x) >> lsh; jb < np; jb += UR * rstep) {
+            uint4 v[UR][2];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < UR; ++u) {
                 const int jj = jb + u * rstep;
-                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                v[u][0] = v[u][1] = make_uint4(0u, 0u, 0u, 0u);
                 if (jj < np) {
                     const int64_t p = s_pos[jj];
-                    if (p >= 0) v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * row_stride) + c);
+                    if (p >= 0) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(kb + p * row_stride) + c;
+                        v[u][0] = __ldg(src);
+                        v[u][1] = __ldg(src + lpr);
+                    }
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < UR; ++u) {
                 const int jj = jb + u * rstep;
-                if (jj < np) __stcs(ob + (static_cast<int64_t>(jj) << vsh) + c, v[u]);
+                if (jj < np) {
+                    uint4 *dst = ob + (static_cast<int64_t>(jj) << vsh) + c;
+                    __stcs(dst, v[u][0]);
+                    __stcs(dst + lpr, v[u][1]);
+                }
             }
         }
         return;

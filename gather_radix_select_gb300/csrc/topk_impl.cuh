@@ -405,32 +405,43 @@ __device__ void gather_rows_of(const TopkArgs &a, int64_t row, int64_t j0, int64
     uint4 *ob = reinterpret_cast<uint4 *>(a.gather_out + (row * a.n_gather + j0) * a.d);
     const int total = static_cast<int>(j1 - j0) * vpr;
     constexpr int U = 4;
-    if (vsh >= 0 && vpr <= NT) {
-        // rows of a power-of-two number of vectors: thread t always copies vector (t mod vpr) of
-        // rows t / vpr, t / vpr + NT / vpr, ... -- one column read per row, no index division
+    if (vsh >= 1 && vpr <= 2 * NT) {
+        // rows of a power-of-two number (>= 2) of vectors: lpr = vpr / 2 lanes share a row and
+        // thread t copies vectors c and c + lpr (c = t mod lpr) of rows t / lpr, t / lpr + NT / lpr,
+        // ... -- a row's column is read once for two vectors, no index division, and each load or
+        // store instruction covers whole 128-byte pieces of the rows
         const int nrows = static_cast<int>(j1 - j0);
-        const int c = static_cast<int>(threadIdx.x) & (vpr - 1);
-        const int rstep = NT >> vsh;
-        for (int jb = static_cast<int>(threadIdx.x) >> vsh; jb < nrows; jb += U * rstep) {
-            uint4 v[U];
+        const int lsh = vsh - 1, lpr = vpr >> 1;
+        const int c = static_cast<int>(threadIdx.x) & (lpr - 1);
+        const int rstep = NT >> lsh;
+        constexpr int UR = NT <= 128 ? U : U / 2;  // rows a thread has in flight (two vectors each)
+        for (int jb = static_cast<int>(threadIdx.x) >> lsh; jb < nrows; jb += UR * rstep) {
+            uint4 v[UR][2];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int u = 0; u < UR; ++u) {
                 const int jj = jb + u * rstep;
-                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                v[u][0] = v[u][1] = make_uint4(0u, 0u, 0u, 0u);
                 if (jj < nrows) {
                     const int64_t j = j0 + jj;
                     int64_t p = glist ? static_cast<int64_t>(glist[jj]) : (j < n_short ? j : 0);
                     if (p < 0) p = 0;
-                    if (p < a.comp_len)
-                        v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + c);
-                    else if (c == 0)
+                    if (p < a.comp_len) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + c;
+                        v[u][0] = __ldg(src);
+                        v[u][1] = __ldg(src + lpr);
+                    } else if (c == 0) {
                         set_err(a.err_flag, kStatusInval);
+                    }
                 }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int u = 0; u < UR; ++u) {
                 const int jj = jb + u * rstep;
-                if (jj < nrows) __stcs(ob + (static_cast<int64_t>(jj) << vsh) + c, v[u]);
+                if (jj < nrows) {
+                    uint4 *dst = ob + (static_cast<int64_t>(jj) << vsh) + c;
+                    __stcs(dst, v[u][0]);
+                    __stcs(dst + lpr, v[u][1]);
+                }
             }
         }
         return;
