@@ -268,19 +268,6 @@ __device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, int32
     }
 }
 
-// Shared-memory histogram increment.  `agg`: warp-aggregated (one atomicAdd per
-// distinct digit per warp, via __match_any_sync; all 32 lanes must call), else
-// one plain shared atomicAdd per valid lane.
-__device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t digit, bool valid, int lane, bool agg)
-{
-    if (agg) {
-        const unsigned peers = __match_any_sync(kFull, valid ? digit : 0xffffffffu);
-        if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
-    } else if (valid) {
-        atomicAdd(&hist[digit], 1u);
-    }
-}
-
 // Warp-aggregated shared histogram increment: lanes with equal digits are grouped with
 // __match_any_sync and only the group leader adds the group's size.  For digits that pile
 // up on few bins (candidates near the threshold, tie-heavy classes).  All 32 lanes must call.
@@ -538,13 +525,22 @@ __device__ void stage_and_histogram(const TopkArgs &a, const E *xrow, int64_t lo
         const uint32_t cb = min(kChunkBytes, bulk - static_cast<uint32_t>(c) * kChunkBytes);
         const int nv = static_cast<int>(cb >> 4);
         const uint4 *vb = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(c) * kChunkBytes);
-        for (int base = warp * 32; base * step < nv; base += NT) {
-            const int v = (base + lane) * step;
-            const bool ok = v < nv;
-            E el[V];
-            T::unpack(ok ? vb[v] : make_uint4(0u, 0u, 0u, 0u), el);
+        if (agg) {
+            for (int base = warp * 32; base * step < nv; base += NT) {
+                const int v = (base + lane) * step;
+                const bool ok = v < nv;
+                E el[V];
+                T::unpack(ok ? vb[v] : make_uint4(0u, 0u, 0u, 0u), el);
 #pragma unroll
-            for (int t = 0; t < V; ++t) hist_add(hist, T::key(el[t]) >> sh0, ok, lane, agg);
+                for (int t = 0; t < V; ++t) hist_add_grouped(hist, T::key(el[t]) >> sh0, ok, lane);
+            }
+        } else {
+            for (int v = tid * step; v < nv; v += NT * step) {
+                E el[V];
+                T::unpack(vb[v], el);
+#pragma unroll
+                for (int t = 0; t < V; ++t) atomicAdd(&hist[T::key(el[t]) >> sh0], 1u);
+            }
         }
     }
     const int tail0 = static_cast<int>(bulk / sizeof(E));
@@ -1016,7 +1012,7 @@ __global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(c
     using T = Elem<E>;
     constexpr int V = T::V;
     static_assert(NT * R * V <= 65536, "source columns are 16-bit");
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint32_t s_warp[NT / 32];
     __shared__ uint32_t s_res[4];
     const int tid = threadIdx.x, lane = tid & 31;
@@ -1067,16 +1063,32 @@ __global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(c
         const int nsh = shift - bl;
         const int nb = 1 << bl;
         const uint32_t mask = static_cast<uint32_t>(nb - 1);
+        if (a.agg) {
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
-            if (j < re) {
-                E el[V];
-                T::unpack(q[j], el);
+            for (int j = 0; j < R; ++j) {
+                if (j < re) {
+                    E el[V];
+                    T::unpack(q[j], el);
 #pragma unroll
-                for (int t = 0; t < V; ++t) {
-                    const uint32_t kk = T::key(el[t]);
-                    hist_add(hist, (kk >> nsh) & mask, j * V + t < cnt && (l == 0 || (kk >> shift) == prefix),
-                             lane, a.agg != 0);
+                    for (int t = 0; t < V; ++t) {
+                        const uint32_t kk = T::key(el[t]);
+                        hist_add_grouped(hist, (kk >> nsh) & mask,
+                                         j * V + t < cnt && (l == 0 || (kk >> shift) == prefix), lane);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                if (j < re) {
+                    E el[V];
+                    T::unpack(q[j], el);
+#pragma unroll
+                    for (int t = 0; t < V; ++t) {
+                        const uint32_t kk = T::key(el[t]);
+                        if (j * V + t < cnt && (l == 0 || (kk >> shift) == prefix))
+                            atomicAdd(&hist[(kk >> nsh) & mask], 1u);
+                    }
                 }
             }
         }
@@ -1455,7 +1467,6 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
     uint16_t *list = reinterpret_cast<uint16_t *>(smem + a.smem_list_off);
     int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
     const int sh0 = T::KB - a.bits[0];
-    const int nb0 = 1 << a.bits[0];
     const int64_t lo = static_cast<int64_t>(part) * a.slice;
     const int64_t hi = min(n, lo + a.slice);
     const int len = hi > lo ? static_cast<int>(hi - lo) : 0;
@@ -1683,13 +1694,25 @@ __device__ uint32_t estimate_threshold(const TopkArgs &a, const uint4 (&q)[kQ], 
     const int tid = threadIdx.x, lane = tid & 31;
     const int sh0 = T::KB - a.bits[0];
     const int nb0 = 1 << a.bits[0];
+    if (a.agg) {
 #pragma unroll
-    for (int j = 0; j < kSU; ++j) {
-        const bool okj = (ok >> j) & 1u;
-        E el[V];
-        T::unpack(q[j], el);
+        for (int j = 0; j < kSU; ++j) {
+            const bool okj = (ok >> j) & 1u;
+            E el[V];
+            T::unpack(q[j], el);
 #pragma unroll
-        for (int t = 0; t < V; ++t) hist_add(h, T::key(el[t]) >> sh0, okj, lane, a.agg != 0);
+            for (int t = 0; t < V; ++t) hist_add_grouped(h, T::key(el[t]) >> sh0, okj, lane);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kSU; ++j) {
+            if ((ok >> j) & 1u) {
+                E el[V];
+                T::unpack(q[j], el);
+#pragma unroll
+                for (int t = 0; t < V; ++t) atomicAdd(&h[T::key(el[t]) >> sh0], 1u);
+            }
+        }
     }
     __syncthreads();
     const float total = static_cast<float>(ns) * V;
@@ -1935,7 +1958,7 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
     constexpr int U = kWideUnroll;
     constexpr int kSU = kWideSampleVecsPerLane;
     static_assert(kSU <= U, "the sample comes from the first loads");
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint32_t s_warp[W];
     __shared__ uint32_t s_res[4];
     __shared__ uint32_t s_cnt[W];
