@@ -61,7 +61,9 @@ def topk_bytes(w) -> int:
 
 
 def gather_bytes(w, fused: bool) -> int:
-    """Unique key rows read at least once + gathered rows written (+ the index read when not fused)."""
+    """The key + gathered rows written (+ the index read when not fused).  The whole key stands in
+    for the unique key rows read: exact up to 2 rows on the 2048-key workload, an overcount of
+    9.4 MB (3.2 MB of 12.6 MB are read; 0.5% of the step's bytes) on the 64-level one."""
     if w.get("key") is None:
         return 0
     key_bytes = w["b"] * w["comp_len"] * w["d"] * 2
