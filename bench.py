@@ -1,6 +1,7 @@
 """Benchmark: batched row-wise top-k + flat row gather on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+                    [--no-per-workload] [--profile [--sorted-value]] [--profile-extra pair|block]
 
 One step = one pass of the whole path over one batch of the workload: the
 fused top-k + gather launch (sel_topk_gather) for the gather workloads, the
@@ -10,11 +11,22 @@ is flushed (a 256 MiB write) before every timed step and the flush is not
 timed.  Each step is timed with CUDA events on the launching stream.
 
 Prints ONE JSON line on rank 0.  The default workload is the bf16 indexer
-top-k + gather on scores[4096, 2048]; the line also carries per-workload
-numbers for all five named workloads (`per_workload`).
+top-k + gather on scores[4096, 2048].  Besides the contract's keys the line
+carries:
+  per_workload      all five named workloads: flushed and warm-L2 step times,
+                    the top-k alone for the gather workloads, and the step
+                    with value-ordered output;
+  pair_gather       the two-key gather (1024 x 512 positions, d 128 + 512);
+  block_candidates  the block-level candidate chain with its gather;
+  cpu_baseline      the oracle single-threaded, and row-parallel over the
+                    host's cores (`row_parallel`).
 
 --impl reference times the CPU oracle (the plain full-sort definition) on a
 bounded sample of the same workload, on the host cores.
+
+Profiling modes (short runs for ncu): --profile [--sorted-value] runs only the
+warm-up and timed steps of --workload; --profile-extra pair|block runs only
+the two-key gather or the block-level chain.
 """
 from __future__ import annotations
 
