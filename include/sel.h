@@ -22,6 +22,22 @@
  *                     with clamped ("safe") positions.
  *   sel_topk_gather   the two above in one launch: the selection's index list
  *                     feeds the gather without a round trip through memory.
+ *   sel_gather_rows_pair
+ *                     the same pull request: the Indexer KL loss gathers the
+ *                     index key and the attention key at one index list;
+ *                     both gathers in one launch.
+ *   sel_block_topk_gather
+ *                     the same pull request: the compressed_candidate_topk
+ *                     chain -- top blocks of compressed positions, expanded
+ *                     to topk_blocks * block_size positions, sorted, masked
+ *                     and gathered.
+ *   sel_topk_noalloc  sel_topk with its scratch in a built-in device array.
+ *   sel_topk_workspace_size, sel_max_cols, sel_topk_kernel_name, sel_strerror
+ *                     queries (no device work).
+ *
+ * Value order (sorted_index = SEL_SORT_VALUE; the tutorial's "Performance
+ * and advanced tips", item 3, names ordering by index or by value) is an
+ * extra launch after the selection.
  *
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller; the library
