@@ -120,6 +120,28 @@ def _check_end(end, rows, device):
     return end
 
 
+def _out_idx(output_idx, rows, k, indices_type, dev):
+    """The caller's [rows, >=k] index buffer, checked, or a new padded one."""
+    if indices_type not in _IDX:
+        raise TypeError("indices_type must be torch.int32 or torch.int64")
+    if output_idx is None:
+        return _padded_rows(rows, k, indices_type, dev)
+    if output_idx.dtype != indices_type or output_idx.dim() != 2 or output_idx.shape[0] != rows \
+            or output_idx.shape[1] < k or (rows > 1 and output_idx.stride(1) != 1) or output_idx.device != dev:
+        raise ValueError("output_idx must be a [rows, >=k] %s tensor on x's device" % indices_type)
+    return output_idx
+
+
+def _out_val(output_val, rows, k, dtype, dev):
+    """The caller's [rows, >=k] value buffer, checked, or a new padded one."""
+    if output_val is None:
+        return _padded_rows(rows, k, dtype, dev)
+    if output_val.dtype != dtype or output_val.dim() != 2 or output_val.shape[0] != rows \
+            or output_val.shape[1] < k or (rows > 1 and output_val.stride(1) != 1) or output_val.device != dev:
+        raise ValueError("output_val must be a [rows, >=k] tensor of x's dtype on x's device")
+    return output_val
+
+
 def _row_stride(x):
     return x.stride(0) if x.size(0) > 1 else max(x.stride(0), x.size(1))
 
@@ -155,24 +177,8 @@ def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_ind
     rows, cols = x.shape
     dev = x.device
     end = _check_end(end, rows, dev)
-    if indices_type not in _IDX:
-        raise TypeError("indices_type must be torch.int32 or torch.int64")
-    if output_idx is None:
-        idx = _padded_rows(rows, k, indices_type, dev)
-    else:
-        idx = output_idx
-        if idx.dtype != indices_type or idx.dim() != 2 or idx.shape[0] != rows or idx.shape[1] < k \
-                or (rows > 1 and idx.stride(1) != 1) or idx.device != dev:
-            raise ValueError("output_idx must be a [rows, >=k] %s tensor on x's device" % indices_type)
-    if not return_value:
-        val = None
-    elif output_val is None:
-        val = _padded_rows(rows, k, x.dtype, dev)
-    else:
-        val = output_val
-        if val.dtype != x.dtype or val.dim() != 2 or val.shape[0] != rows or val.shape[1] < k \
-                or (rows > 1 and val.stride(1) != 1) or val.device != dev:
-            raise ValueError("output_val must be a [rows, >=k] tensor of x's dtype on x's device")
+    idx = _out_idx(output_idx, rows, k, indices_type, dev)
+    val = _out_val(output_val, rows, k, x.dtype, dev) if return_value else None
     with torch.cuda.device(dev):
         lib = _native.load()
         s = stream if stream is not None else torch.cuda.current_stream(dev)
@@ -222,7 +228,8 @@ def gather_rows(key: torch.Tensor, idx: torch.Tensor, *, out: torch.Tensor | Non
     rows, n = idx.shape
     if out is None:
         out = torch.empty((rows, n, d), dtype=torch.bfloat16, device=key.device)
-    elif out.shape != (rows, n, d) or not out.is_contiguous() or out.dtype != torch.bfloat16:
+    elif out.shape != (rows, n, d) or not out.is_contiguous() or out.dtype != torch.bfloat16 \
+            or out.device != key.device:
         raise ValueError("out must be a contiguous bf16 [rows, n, d] tensor")
     with torch.cuda.device(key.device):
         st = _native.load().sel_gather_rows(
@@ -256,7 +263,8 @@ def gather_rows_pair(key: torch.Tensor, key2: torch.Tensor, idx: torch.Tensor, *
     for o, dd in ((out, d), (out2, d2)):
         if o is None:
             o = torch.empty((rows, n, dd), dtype=torch.bfloat16, device=key.device)
-        elif o.shape != (rows, n, dd) or not o.is_contiguous() or o.dtype != torch.bfloat16:
+        elif o.shape != (rows, n, dd) or not o.is_contiguous() or o.dtype != torch.bfloat16 \
+                or o.device != key.device:
             raise ValueError("outputs must be contiguous bf16 [rows, n, d] tensors")
         outs.append(o)
     with torch.cuda.device(key.device):
@@ -300,7 +308,8 @@ def block_topk_gather(scores: torch.Tensor, topk_blocks: int, block_size: int, *
             raise ValueError("key must be on scores' device")
         if gather_out is None:
             gather_out = torch.empty((rows, npos, d), dtype=torch.bfloat16, device=dev)
-        elif gather_out.shape != (rows, npos, d) or not gather_out.is_contiguous():
+        elif gather_out.shape != (rows, npos, d) or not gather_out.is_contiguous() \
+                or gather_out.dtype != torch.bfloat16 or gather_out.device != dev:
             raise ValueError("gather_out must be a contiguous bf16 [rows, topk_blocks*block_size, d] tensor")
     else:
         gather_out = None
@@ -343,15 +352,13 @@ def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, en
     if not return_indices and order != 2:
         idx = None
     else:  # value order gathers from the ordered index rows, so they are always written
-        idx = output_idx if output_idx is not None else _padded_rows(rows, k, indices_type, dev)
-    if not return_value:
-        val = None
-    else:
-        val = output_val if output_val is not None else _padded_rows(rows, k, x.dtype, dev)
+        idx = _out_idx(output_idx, rows, k, indices_type, dev)
+    val = _out_val(output_val, rows, k, x.dtype, dev) if return_value else None
     if gather_out is None:
         gather_out = torch.empty((rows, n_gather, d), dtype=torch.bfloat16, device=dev)
-    elif gather_out.shape != (rows, n_gather, d) or not gather_out.is_contiguous():
-        raise ValueError("gather_out must be a contiguous bf16 [rows, n_gather, d] tensor")
+    elif gather_out.shape != (rows, n_gather, d) or not gather_out.is_contiguous() \
+            or gather_out.dtype != torch.bfloat16 or gather_out.device != dev:
+        raise ValueError("gather_out must be a contiguous bf16 [rows, n_gather, d] tensor on x's device")
     with torch.cuda.device(dev):
         lib = _native.load()
         s = stream if stream is not None else torch.cuda.current_stream(dev)
