@@ -7,12 +7,18 @@
 // (ties: smaller column first), or, when n <= k, every valid column followed
 // by fills (index -1, value -inf).  Rows with n > k are checked for NaN.
 //
-// Four kernels, chosen per launch by the host plan:
+// Five kernels, chosen per launch by the host plan:
+//   reg_kernel    one CTA per row of at most 16 KB; the row is held in
+//                 registers (a contiguous run of vectors per thread) and the
+//                 radix levels run from there.
 //   row_kernel    one CTA per row; the row is staged whole in shared memory.
-//   wide_kernel   one CTA per row for rows too wide to stage: the row streams
-//                 through a ring of shared-memory chunks, is filtered on
-//                 arrival into a candidate list in shared memory, and the
-//                 selection runs on that list (the row is read once).
+//   wide_kernel   rows too wide to stage: each warp streams its share of the
+//                 row with 16-byte loads (read once), tests every vector
+//                 against a threshold estimated from the first loads, and
+//                 appends the passing keys to its own region of a candidate
+//                 list in shared memory; the selection runs on the regions.
+//                 Few wide rows are cut into parts whose candidates meet in a
+//                 caller workspace, merged by the last part to arrive.
 //   split_kernel  a wide row is cut into `parts` slices, one CTA each.  Every
 //                 CTA filters its slice down to an index-ordered candidate
 //                 list in a caller-provided workspace; the CTA that finishes
@@ -22,9 +28,10 @@
 //                 radix pass (the exact fallback of the others).
 //
 // Building blocks (GB300 design):
-//   * Slices are staged into shared memory with bulk async copies
-//     (cp.async.bulk, 16 KB chunks, one mbarrier each); waiting threads sleep
-//     in hardware (try_wait with a suspend hint), bounded by a ~2 s budget.
+//   * Staged slices (row_kernel, split_kernel) arrive in shared memory by bulk
+//     async copies (cp.async.bulk, 16 KB chunks, one mbarrier each); waiting
+//     threads sleep in hardware (try_wait with a suspend hint), bounded by a
+//     ~2 s budget.
 //   * Order-preserving key: fp32/bf16 bits -> unsigned key, larger float =>
 //     larger key, -0 folded onto +0.
 //   * Radix select over digits from the most significant end (11/11/10 bits
