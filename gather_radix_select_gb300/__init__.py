@@ -21,7 +21,7 @@ from . import _native
 from ._native import SelError, SEL_MAX_K
 
 __all__ = ["topk", "gather_rows", "gather_rows_pair", "topk_gather", "block_topk_gather", "stride_requirement", "max_cols", "workspace_size", "kernel_name",
-           "SelError",
+           "set_tuning", "get_tuning", "SelError",
            "SEL_MAX_K", "library_path"]
 
 _DTYPES = {torch.float32: _native.SEL_F32, torch.bfloat16: _native.SEL_BF16}
@@ -76,6 +76,36 @@ def kernel_name(dtype: torch.dtype, rows: int, cols: int, k: int, n_gather: int 
     if name is None:
         raise ValueError("invalid shape for kernel_name")
     return name.decode()
+
+
+_KNOBS = {"plan": _native.SEL_TUNE_PLAN, "parts": _native.SEL_TUNE_PARTS,
+          "row_sample": _native.SEL_TUNE_ROW_SAMPLE, "hist_agg": _native.SEL_TUNE_HIST_AGG}
+
+
+def set_tuning(plan: str | None = None, parts: int | None = None, row_sample: bool | None = None,
+               hist_agg: bool | None = None) -> None:
+    """Tuning and test hooks (include/sel_tuning.h); None leaves a knob as it is.
+
+    ``plan``: "auto" or the kernel to force where it can run a shape ("reg", "row", "wide",
+    "split", "stream", "flat").  ``parts``: parts per row of the streaming kernel's split mode
+    (0 = automatic).  Process-wide; takes effect on the next call."""
+    lib = _native.load()
+    vals = {"plan": None if plan is None else _native.SEL_PLANS[plan], "parts": parts,
+            "row_sample": None if row_sample is None else int(bool(row_sample)),
+            "hist_agg": None if hist_agg is None else int(bool(hist_agg))}
+    for name, v in vals.items():
+        if v is not None:
+            _native.check(lib.sel_set_tuning(_KNOBS[name], int(v)), "sel_set_tuning(%s)" % name)
+
+
+def get_tuning() -> dict:
+    """The knobs' current values, in the form set_tuning takes."""
+    lib = _native.load()
+    plans = {v: k for k, v in _native.SEL_PLANS.items()}
+    return {"plan": plans[lib.sel_get_tuning(_native.SEL_TUNE_PLAN)],
+            "parts": int(lib.sel_get_tuning(_native.SEL_TUNE_PARTS)),
+            "row_sample": bool(lib.sel_get_tuning(_native.SEL_TUNE_ROW_SAMPLE)),
+            "hist_agg": bool(lib.sel_get_tuning(_native.SEL_TUNE_HIST_AGG))}
 
 
 def _workspace(nbytes: int, device, stream):

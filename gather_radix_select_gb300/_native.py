@@ -16,6 +16,9 @@ SEL_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 SEL_F32, SEL_BF16 = 0, 1
 SEL_I32, SEL_I64 = 0, 1
 SEL_MAX_K = 4096
+# include/sel_tuning.h
+SEL_TUNE_PLAN, SEL_TUNE_PARTS, SEL_TUNE_ROW_SAMPLE, SEL_TUNE_HIST_AGG = range(4)
+SEL_PLANS = {"auto": -1, "reg": 0, "row": 1, "wide": 2, "split": 3, "stream": 4, "flat": 5}
 
 # every symbol include/sel.h declares, with its ctypes signature
 _vp, _i64, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
@@ -40,6 +43,8 @@ SIGNATURES = {
                                 _vp, _i64, _vp, _i64, _vp, _vp, _vp]),
     "sel_strerror": (ctypes.c_char_p, [_int]),
     "sel_topk_kernel_name": (ctypes.c_char_p, [_int, _i64, _i64, _int, _i64]),
+    "sel_set_tuning": (_int, [_int, _int]),
+    "sel_get_tuning": (_int, [_int]),
 }
 
 _lock = threading.Lock()

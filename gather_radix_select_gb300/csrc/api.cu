@@ -3,14 +3,16 @@
 // kernels of topk.cu and gather.cu.
 #include <cstdint>
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
-#include <string>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <tuple>
 
 #include "../../include/sel.h"
+#include "../../include/sel_tuning.h"
 #include "sel_internal.h"
 
 namespace {
@@ -25,6 +27,8 @@ constexpr int kWideHistBins = 2048;               // wide_kernel's range histogr
 constexpr int64_t kRegMaxRowBytes = 16 * 1024;    // longer rows take the staged row kernel by default
 constexpr int kWideSplitCtasPerSm = 6;            // wide rows: split them until this many CTAs per SM
 constexpr int64_t kWidePartMinBytes = 32 * 1024;  // ... but no part smaller than this
+constexpr int64_t kFlatChunkMaxVecs = 8192;       // flat_kernel: 128 KB chunks at most
+constexpr int64_t kFlatChunkMinVecs = 256;        // ... and 4 KB at least
 
 int elem_bytes(int dtype) { return dtype == SEL_F32 ? 4 : 2; }
 int idx_bytes(int idx_dtype) { return idx_dtype == SEL_I64 ? 8 : 4; }
@@ -132,6 +136,55 @@ size_t layout_workspace(int dtype, int64_t rows, int parts, int64_t cap, sel::To
     return static_cast<size_t>(a.ws_counter_bytes + rows * a.ws_row_bytes);
 }
 
+// Tuning knobs (include/sel_tuning.h): read from the environment once, when first needed, and
+// settable at any time through sel_set_tuning.  The plan cache is keyed on them.
+struct Tuning {
+    std::atomic<int> plan{SEL_PLAN_AUTO}, parts{0}, row_sample{0}, hist_agg{0};
+};
+
+int plan_from_name(const char *v)
+{
+    if (!v) return SEL_PLAN_AUTO;
+    if (!std::strcmp(v, "reg")) return SEL_PLAN_REG;
+    if (!std::strcmp(v, "row")) return SEL_PLAN_ROW;
+    if (!std::strcmp(v, "wide")) return SEL_PLAN_WIDE;
+    if (!std::strcmp(v, "split")) return SEL_PLAN_SPLIT;
+    if (!std::strcmp(v, "stream")) return SEL_PLAN_STREAM;
+    if (!std::strcmp(v, "flat")) return SEL_PLAN_FLAT;
+    return SEL_PLAN_AUTO;
+}
+
+Tuning &tuning()
+{
+    static Tuning *t = [] {
+        Tuning *n = new Tuning();
+        n->plan = plan_from_name(std::getenv("SEL_PLAN"));
+        const char *e = std::getenv("SEL_PARTS");
+        const int v = e ? std::atoi(e) : 0;
+        n->parts = v > 0 ? v : 0;
+        e = std::getenv("SEL_ROW_SAMPLE");
+        n->row_sample = (e && e[0] == '1') ? 1 : 0;
+        e = std::getenv("SEL_HIST_AGG");
+        n->hist_agg = (e && e[0] == '1') ? 1 : 0;
+        return n;
+    }();
+    return *t;
+}
+
+// SEL_PLAN_* -> the kernel mode it forces (-1: none)
+int forced_mode(int plan)
+{
+    switch (plan) {
+    case SEL_PLAN_REG: return sel::kModeReg8;
+    case SEL_PLAN_ROW: return sel::kModeRow;
+    case SEL_PLAN_WIDE: return sel::kModeWide;
+    case SEL_PLAN_SPLIT: return sel::kModeSplit;
+    case SEL_PLAN_STREAM: return sel::kModeStream;
+    case SEL_PLAN_FLAT: return sel::kModeFlat;
+    default: return -1;
+    }
+}
+
 int cached_blocks_per_sm(int dtype, int mode, int threads, bool gather, size_t smem)
 {
     static std::mutex mu;
@@ -148,14 +201,6 @@ int cached_blocks_per_sm(int dtype, int mode, int threads, bool gather, size_t s
     std::lock_guard<std::mutex> g(mu);
     cache[key] = n;
     return n;
-}
-
-// First-pass histogram flavour: SEL_HIST_AGG=1 selects warp-aggregated atomics
-// (__match_any_sync), anything else plain shared atomics (the default).  Read per call.
-int hist_agg()
-{
-    const char *e = std::getenv("SEL_HIST_AGG");
-    return (e && e[0] == '1') ? 1 : 0;
 }
 
 // Candidate capacity of wide_kernel for rows of `cols` elements.  The threshold is estimated
@@ -219,36 +264,61 @@ size_t layout_wide(int64_t cap, bool gather, int64_t n_gather, sel::TopkArgs &a)
     return off;
 }
 
-// Forced kernel choice for tuning and tests: SEL_PLAN=reg|row|split|wide|stream (when that kernel
-// can run the shape).  Unset: the automatic plan.
-// SEL_ROW_SAMPLE=1: the staged row kernel estimates the threshold from every 8th vector on long
-// rows instead of taking the exact first histogram while the row lands (tuning; measured slower
-// on the bf16 [12288, 16384] and fp32 [4, 8192] workloads, hence off by default).
-int row_sample()
+// Layout of a flat_kernel launch (topk_impl.cuh): each row's full 16-byte vectors cut into
+// `parts` chunks of `slice` vectors, chunk q on CTA q mod grid (one CTA per SM).  Capacities
+// follow the threshold estimate's margins: the estimate keeps about kept = mu*9/8 + 3 sqrt(mu) + 4
+// of the m sampled keys (mu = k * m / cols), so a share e of the row holds about e * kept / m
+// candidates; four standard deviations are added on top.
+bool plan_flat(int dtype, int64_t rows, int64_t cols, int k, int sms, size_t limit, Plan &fp)
 {
-    const char *e = std::getenv("SEL_ROW_SAMPLE");
-    return (e && e[0] == '1') ? 1 : 0;
-}
-
-// SEL_PARTS=n: streaming kernel parts per row (tuning).
-int parts_override()
-{
-    const char *e = std::getenv("SEL_PARTS");
-    const int v = e ? std::atoi(e) : 0;
-    return v > 0 ? v : 0;
-}
-
-int plan_override()
-{
-    const char *e = std::getenv("SEL_PLAN");
-    if (!e) return -1;
-    const std::string v(e);
-    if (v == "row") return sel::kModeRow;
-    if (v == "split") return sel::kModeSplit;
-    if (v == "stream") return sel::kModeStream;
-    if (v == "wide") return sel::kModeWide;
-    if (v == "reg") return sel::kModeReg8;
-    return -1;
+    sel::TopkArgs &a = fp.layout;
+    const int64_t e = elem_bytes(dtype);
+    const int64_t V = 16 / e;
+    const int64_t nvr = cols * e / 16;
+    if (nvr < 1 || sms < 1 || cols > 0x7fffffffLL) return false;
+    int64_t cv = std::min(kFlatChunkMaxVecs, std::max(kFlatChunkMinVecs, ceil_div(rows * nvr, sms)));
+    cv = std::max(cv, ceil_div(nvr, sel::kFlatMaxSlots / sel::kFlatStreamWarps));  // slots of a row bounded
+    const int64_t cpr = ceil_div(nvr, cv);
+    cv = ceil_div(nvr, cpr);
+    if (cpr * sel::kFlatStreamWarps > sel::kFlatMaxSlots) return false;
+    if (ceil_div(rows * cpr, sms) > sel::kFlatQueue) return false;
+    const double m = static_cast<double>(std::min<int64_t>(nvr, sel::kFlatSampleVecs) * V);
+    const double mu = static_cast<double>(k) * m / static_cast<double>(cols);
+    const double kept = mu * 1.125 + 3.0 * std::sqrt(mu) + 4.0;
+    const double frac = std::min(1.0, (kept + 4.0 * std::sqrt(kept)) / m);
+    const double ew = static_cast<double>(ceil_div(cv, sel::kFlatStreamWarps) * V);  // one warp's share of a chunk
+    const int64_t part_cap =
+        std::min<int64_t>(static_cast<int64_t>(ew) + 2 * V,
+                          static_cast<int64_t>(ew * frac + 4.0 * std::sqrt(ew * frac) + 16.0) + V);
+    const double cf = static_cast<double>(cols) * frac;
+    const int64_t total_cap = std::min<int64_t>(round_up(cols, 8), static_cast<int64_t>(cf + 4.0 * std::sqrt(cf)) + 64);
+    const int64_t capw = ceil_div(total_cap, sel::kFlatSelWarps) + 16;
+    a.hist_bins = std::max(a.hist_bins, kWideHistBins);
+    a.slice = cv;
+    a.parts = static_cast<int32_t>(cpr);
+    a.part_cap = static_cast<int32_t>(part_cap);
+    a.list_cap = static_cast<int32_t>(capw);
+    a.region_stride = static_cast<int32_t>(round_up(capw + 1, 2));
+    a.smem_buf_bytes = 0;
+    a.smem_hist_off = 0;
+    a.smem_mask_off = 0;
+    size_t off = static_cast<size_t>(a.hist_bins) * 4;
+    a.smem_list_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(sel::kFlatSelWarps) * static_cast<size_t>(a.region_stride) * 8;
+    off = static_cast<size_t>(round_up(static_cast<int64_t>(off), 16));
+    a.smem_glist_off = static_cast<uint32_t>(off);
+    a.smem_stage_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(sel::kFlatStreamWarps) * sel::kWideStage * (16 + 4);
+    if (off > limit || cached_blocks_per_sm(dtype, sel::kModeFlat, sel::kFlatThreads, false, off) < 1) return false;
+    a.ws_counter_bytes = round_up(3 * rows * 4, 256);
+    a.ws_part_bytes = round_up(16 + (part_cap + 1) * 8, 16);
+    a.ws_row_bytes = cpr * sel::kFlatStreamWarps * a.ws_part_bytes;
+    fp.mode = sel::kModeFlat;
+    fp.threads = sel::kFlatThreads;
+    fp.smem = off;
+    fp.grid = sms;
+    fp.ws_bytes = static_cast<size_t>(a.ws_counter_bytes + rows * a.ws_row_bytes);
+    return true;
 }
 
 // Chooses the kernel (row / split / wide / stream), its CTA shape, shared memory and workspace.
@@ -257,8 +327,8 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
 {
     sel::TopkArgs &a = p.layout;
     digit_plan(dtype, cols, a);
-    a.agg = hist_agg();
-    a.sample_step = row_sample() ? 8 : 1;
+    a.agg = tuning().hist_agg.load(std::memory_order_relaxed);
+    a.sample_step = tuning().row_sample.load(std::memory_order_relaxed) ? 8 : 1;
     a.sample_min_cols = 8192;
     const size_t limit = sel::topk_smem_limit();
     const int sms = sel::device_sm_count();
@@ -366,6 +436,14 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
         p = wide_plan;
         return SEL_OK;
     }
+    // rows cut into chunks dealt over a persistent grid (flat_kernel): forced only, for now
+    if (force == sel::kModeFlat) {
+        Plan fp = p;
+        if (!gather && plan_flat(dtype, rows, c1, k, sms, limit, fp)) {
+            p = fp;
+            return SEL_OK;
+        }
+    }
     // few wide rows (or rows that do not fit one CTA) leave the row plan
     const bool leave_row = !row_ok || (rows < 2 * sms && row_bytes >= kSplitMinRowBytes);
     if (!leave_row && force < 0) {
@@ -424,30 +502,47 @@ int make_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t
     return SEL_OK;
 }
 
-// make_plan behind a cache: the plan depends only on the device and the call's shape.
+// make_plan behind a cache: the plan depends only on the device, the call's shape and the tuning
+// knobs.  A thread's last plan is kept in a thread-local entry, so repeated calls of one shape
+// take no lock.
 int cached_plan(int dtype, int64_t rows, int64_t cols, int k, bool gather, int64_t n_gather, Plan &p)
 {
+    using Key = std::tuple<int, int, int64_t, int64_t, int, int64_t, int, int, int>;
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int64_t, int64_t, int, int64_t, int, int, int>, Plan> cache;
+    static std::map<Key, Plan> cache;
+    thread_local bool last_valid = false;
+    thread_local Key last_key;
+    thread_local Plan last_plan;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SEL_ECUDA;
-    const int force = plan_override(), force_parts = parts_override();
-    const auto key =
-        std::make_tuple(dev, dtype, rows, cols, k, gather ? n_gather : -1, force, hist_agg() + 2 * row_sample(),
-                        force_parts);
+    Tuning &t = tuning();
+    const int force = forced_mode(t.plan.load(std::memory_order_relaxed));
+    const int force_parts = t.parts.load(std::memory_order_relaxed);
+    const int flavour = t.hist_agg.load(std::memory_order_relaxed) + 2 * t.row_sample.load(std::memory_order_relaxed);
+    const Key key = std::make_tuple(dev, dtype, rows, cols, k, gather ? n_gather : -1, force, flavour, force_parts);
+    if (last_valid && key == last_key) {
+        p = last_plan;
+        return SEL_OK;
+    }
+    bool found = false;
     {
         std::lock_guard<std::mutex> g(mu);
         auto it = cache.find(key);
         if (it != cache.end()) {
             p = it->second;
-            return SEL_OK;
+            found = true;
         }
     }
-    const int st = make_plan(dtype, rows, cols, k, gather, n_gather, force, force_parts, p);
-    if (st != SEL_OK) return st;
-    std::lock_guard<std::mutex> g(mu);
-    if (cache.size() > 4096) cache.clear();
-    cache[key] = p;
+    if (!found) {
+        const int st = make_plan(dtype, rows, cols, k, gather, n_gather, force, force_parts, p);
+        if (st != SEL_OK) return st;
+        std::lock_guard<std::mutex> g(mu);
+        if (cache.size() > 4096) cache.clear();
+        cache[key] = p;
+    }
+    last_key = key;
+    last_plan = p;
+    last_valid = true;
     return SEL_OK;
 }
 
@@ -551,7 +646,54 @@ int run_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
 
 }  // namespace
 
+namespace sel {
+
+int check_topk_call(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride, int k, int sorted_index,
+                    int idx_dtype, int want_values, const void *out_idx, int64_t out_idx_stride, const void *out_val,
+                    int64_t out_val_stride)
+{
+    if (sorted_index < SEL_UNSORTED || sorted_index > SEL_SORT_VALUE) return SEL_EINVAL;
+    return check_topk_args(x, dtype, rows, cols, stride, k, idx_dtype, want_values, out_idx, out_idx_stride, out_val,
+                           out_val_stride, true);
+}
+
+}  // namespace sel
+
 extern "C" {
+
+int sel_set_tuning(int knob, int value)
+{
+    Tuning &t = tuning();
+    switch (knob) {
+    case SEL_TUNE_PLAN:
+        if (value < SEL_PLAN_AUTO || value > SEL_PLAN_FLAT) return SEL_EINVAL;
+        t.plan = value;
+        return SEL_OK;
+    case SEL_TUNE_PARTS:
+        if (value < 0) return SEL_EINVAL;
+        t.parts = value;
+        return SEL_OK;
+    case SEL_TUNE_ROW_SAMPLE:
+        t.row_sample = value ? 1 : 0;
+        return SEL_OK;
+    case SEL_TUNE_HIST_AGG:
+        t.hist_agg = value ? 1 : 0;
+        return SEL_OK;
+    default: return SEL_EINVAL;
+    }
+}
+
+int sel_get_tuning(int knob)
+{
+    Tuning &t = tuning();
+    switch (knob) {
+    case SEL_TUNE_PLAN: return t.plan.load();
+    case SEL_TUNE_PARTS: return t.parts.load();
+    case SEL_TUNE_ROW_SAMPLE: return t.row_sample.load();
+    case SEL_TUNE_HIST_AGG: return t.hist_agg.load();
+    default: return -1;
+    }
+}
 
 int sel_stride_requirement(int *in_align_bytes, int *out_align_bytes)
 {
@@ -602,6 +744,7 @@ const char *sel_topk_kernel_name(int dtype, int64_t rows, int64_t cols, int k, i
     case sel::kModeStream: return "stream_kernel";
     case sel::kModeReg2:
     case sel::kModeReg8: return "reg_kernel";
+    case sel::kModeFlat: return "flat_kernel";
     default: return nullptr;
     }
 }

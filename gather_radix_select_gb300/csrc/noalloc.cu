@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/sel.h"
+#include "sel_internal.h"
 
 namespace {
 
@@ -27,14 +28,19 @@ std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
 
 // In host code the array's name is only a host-side stand-in; the device address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current (the caller's).
-int scratch_address(void **out)
+// cudaGetSymbolAddress, with the device current (the caller's).  The address belongs to the
+// current context: a device reset (or another context made current) can move the array.  So it
+// is looked up again on every call whose stream is not capturing a graph; a capturing call uses
+// the address the last non-capturing call on this device found (or looks it up if there was none).
+int scratch_address(cudaStream_t stream, void **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SEL_ECUDA;
     if (dev < 0 || dev >= kMaxDevices) return SEL_EUNSUPPORTED;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return SEL_ECUDA;
     std::lock_guard<std::mutex> g(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (cs == cudaStreamCaptureStatusNone || !g_scratch_ptr[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SEL_ECUDA;
         g_scratch_ptr[dev] = p;
@@ -51,11 +57,15 @@ int sel_topk_noalloc(const void *x, int dtype, int64_t rows, int64_t cols, int64
                      int k, int sorted_index, int idx_dtype, int want_values, void *out_idx, int64_t out_idx_stride,
                      void *out_val, int64_t out_val_stride, int32_t *nan_flag, int32_t *err_flag, void *stream)
 {
-    const size_t need = rows > 0 ? sel_topk_workspace_size(dtype, rows, cols, k) : 0;
+    // sel_topk's own argument errors come first, then the scratch limit
+    const int chk = sel::check_topk_call(x, dtype, rows, cols, stride, k, sorted_index, idx_dtype, want_values, out_idx,
+                                         out_idx_stride, out_val, out_val_stride);
+    if (chk != SEL_OK || rows == 0) return chk;
+    const size_t need = sel_topk_workspace_size(dtype, rows, cols, k);
     if (need > static_cast<size_t>(SEL_NOALLOC_SCRATCH_BYTES)) return SEL_ESCRATCH;
     void *ws = nullptr;
     if (need > 0) {
-        const int st = scratch_address(&ws);
+        const int st = scratch_address(static_cast<cudaStream_t>(stream), &ws);
         if (st != SEL_OK) return st;
     }
     return sel_topk(x, dtype, rows, cols, stride, row_end, k, sorted_index, idx_dtype, want_values, out_idx,

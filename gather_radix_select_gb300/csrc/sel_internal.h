@@ -24,7 +24,15 @@ constexpr int kModeWide = 3;        // wide_kernel: one CTA per row, one streami
 constexpr int kModeReg2 = 4;        // reg_kernel: one CTA per row held in registers, 2 vectors a thread
 constexpr int kModeReg8 = 5;        // reg_kernel: 8 vectors a thread
 constexpr int kModeWideSplit = 6;   // wide_kernel over `parts` CTAs per row, last-arriver merge
-constexpr int kNumModes = 7;
+constexpr int kModeFlat = 7;        // flat_kernel: rows cut into chunks dealt over a persistent grid
+constexpr int kNumModes = 8;
+// flat_kernel: warps 0..15 stream, warps 16..23 estimate thresholds and select
+constexpr int kFlatStreamWarps = 16;
+constexpr int kFlatSelWarps = 8;
+constexpr int kFlatThreads = (kFlatStreamWarps + kFlatSelWarps) * 32;
+constexpr int kFlatQueue = 64;        // chunks of one CTA at most (each can queue one row)
+constexpr int kFlatMaxSlots = 1024;   // (chunk, streaming warp) slots of one row at most
+constexpr int kFlatSampleVecs = 1024; // row sample for the threshold estimate: 32 runs of 32 vectors
 constexpr int kGatherThreads = 256;
 
 // Everything one selection launch needs; passed by value (kernel parameter space).
@@ -42,8 +50,8 @@ struct TopkArgs {
     int64_t out_val_stride;
     int32_t *nan_flag;        // nullable
     int32_t *err_flag;        // nullable
-    int64_t slice;            // elements of a row per CTA (multiple of 64)
-    int32_t parts;            // CTAs per row (split_kernel)
+    int64_t slice;            // elements of a row per CTA (multiple of 64); flat_kernel: 16-byte vectors per chunk
+    int32_t parts;            // CTAs per row (split_kernel); chunks per row (flat_kernel)
     int32_t nlevels;          // digits from the most significant end
     int32_t bits[kMaxLevels];
     int32_t hist_bins;        // 1 << max(bits)
@@ -55,7 +63,8 @@ struct TopkArgs {
     uint32_t smem_stage_off;  // wide_kernel: staged candidate vectors
     int32_t list_cap;         // capacity of the candidate list
     int32_t region_stride;    // wide_kernel: candidate pairs per warp region (capacity list_cap + 1)
-    int32_t part_cap;         // wide_kernel over parts: candidate pairs a part may leave in the workspace
+    int32_t part_cap;         // wide_kernel over parts: candidate pairs a part may leave in the workspace;
+                              // flat_kernel: pairs one streaming warp may leave for one chunk
     int32_t agg;              // 1: first-pass histogram with warp-aggregated atomics
     int32_t sample_step;      // > 1: the first digit's threshold is estimated from every
                               //      sample_step-th 16-byte vector of the row
@@ -146,5 +155,10 @@ size_t topk_smem_limit();
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t stream);
 
 int device_sm_count();
+
+// sel_topk's host-side argument checks (api.cu), for entry points that wrap it.
+int check_topk_call(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride, int k, int sorted_index,
+                    int idx_dtype, int want_values, const void *out_idx, int64_t out_idx_stride, const void *out_val,
+                    int64_t out_val_stride);
 
 }  // namespace sel

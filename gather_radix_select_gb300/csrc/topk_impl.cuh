@@ -62,6 +62,41 @@ constexpr long long kWaitCycles = 4000000000LL;  // bound on any mbarrier wait (
 constexpr int32_t kStatusInval = 1;
 constexpr int32_t kStatusTimeout = 5;
 
+// A set of consecutive warps that synchronises on its own: the whole CTA (barrier 0, i.e.
+// __syncthreads), or warps [BASE/32, (BASE+NT)/32) on named barrier BAR.  Helpers that run on
+// a group use G::tid() (0..NT-1 within the group) and G::sync() instead of threadIdx.x and
+// __syncthreads().
+template <int NT_, int BAR = 0, int BASE = 0>
+struct Grp {
+    static constexpr int NT = NT_;
+    static constexpr int W = NT_ / 32;
+    static_assert(NT_ % 32 == 0 && BASE % 32 == 0, "whole warps");
+    static __device__ __forceinline__ int tid() { return static_cast<int>(threadIdx.x) - BASE; }
+    static __device__ __forceinline__ void sync()
+    {
+        if constexpr (BAR == 0)
+            __syncthreads();
+        else
+            asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NT_) : "memory");
+    }
+    // sync() that also returns whether `p` held on any thread of the group
+    static __device__ __forceinline__ bool sync_or(bool p)
+    {
+        if constexpr (BAR == 0) {
+            return __syncthreads_or(p) != 0;
+        } else {
+            uint32_t r;
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                : "=r"(r)
+                : "r"(static_cast<uint32_t>(p)), "n"(BAR), "n"(NT_)
+                : "memory");
+            return r != 0;
+        }
+    }
+};
+
 template <typename E>
 struct Elem;
 
@@ -303,12 +338,13 @@ __device__ __forceinline__ uint32_t take_from_ties(uint32_t need, uint32_t befor
     return count < left ? count : left;
 }
 
-// Exclusive prefix sum over the CTA (thread order); `total` gets the CTA sum.
-// Uses s_warp[NT/32]; contains two __syncthreads.
-template <int NT>
+// Exclusive prefix sum over the group (thread order); `total` gets the group's sum.
+// Uses s_warp[G::W]; contains two group barriers.
+template <typename G>
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s_warp, uint32_t &total)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int NT = G::NT;
+    const int lane = G::tid() & 31, warp = G::tid() >> 5;
     uint32_t inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -316,7 +352,7 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s
         if (lane >= o) inc += y;
     }
     if (lane == 31) s_warp[warp] = inc;
-    __syncthreads();
+    G::sync();
     uint32_t before = 0, tot = 0;
 #pragma unroll
     for (int w = 0; w < NT / 32; ++w) {
@@ -324,18 +360,19 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s
         before += (w < warp) ? t : 0u;
         tot += t;
     }
-    __syncthreads();
+    G::sync();
     total = tot;
     return before + inc - v;
 }
 
 // Threshold digit of a histogram h[0, nb): the digit d with
 //   sum_{e > d} h[e] < need <= sum_{e >= d} h[e].
-// Result in out[0] = d, out[1] = sum_{e > d} h[e], out[2] = h[d].  All threads call.
-template <int NT>
+// Result in out[0] = d, out[1] = sum_{e > d} h[e], out[2] = h[d].  Every thread of the group calls.
+template <typename G>
 __device__ void find_threshold(const uint32_t *h, int nb, uint32_t need, uint32_t *out, uint32_t *s_warp)
 {
-    const int tid = threadIdx.x;
+    constexpr int NT = G::NT;
+    const int tid = G::tid();
     const int per = nb > NT ? nb / NT : 1;
     const int lo = tid * per;
     uint32_t s = 0;
@@ -350,7 +387,7 @@ __device__ void find_threshold(const uint32_t *h, int nb, uint32_t need, uint32_
         if (lane + o < 32) inc += y;
     }
     if (lane == 0) s_warp[warp] = inc;
-    __syncthreads();
+    G::sync();
     uint32_t above = inc - s;
 #pragma unroll
     for (int w = 0; w < NT / 32; ++w) above += (w > warp) ? s_warp[w] : 0u;
@@ -367,7 +404,7 @@ __device__ void find_threshold(const uint32_t *h, int nb, uint32_t need, uint32_
             acc += c;
         }
     }
-    __syncthreads();
+    G::sync();
 }
 
 __device__ __forceinline__ void store_idx(const TopkArgs &a, int64_t row, int64_t pos, int64_t col)
@@ -388,10 +425,12 @@ __device__ __forceinline__ void store_val(const TopkArgs &a, int64_t row, int64_
 // Copies key rows for output positions [j0, j1) of `row`:
 //   gather_out[row, j, :] = key[row / rows_per_batch, max(col_j, 0), :]
 // col_j = glist[j - j0] when glist is given, else j for j < n_short and 0 beyond.
-template <int NT>
+template <typename G>
 __device__ void gather_rows_of(const TopkArgs &a, int64_t row, int64_t j0, int64_t j1, const int32_t *glist,
                                int64_t n_short)
 {
+    constexpr int NT = G::NT;
+    const int gt = G::tid();
     const int vpr = static_cast<int>(a.d >> 3);  // 16-byte vectors per key row
     const int vsh = (vpr & (vpr - 1)) == 0 ? __ffs(vpr) - 1 : -1;  // log2(vpr), or -1
     const int64_t bb = row / a.rows_per_batch;
@@ -406,10 +445,10 @@ __device__ void gather_rows_of(const TopkArgs &a, int64_t row, int64_t j0, int64
         // store instruction covers whole 128-byte pieces of the rows
         const int nrows = static_cast<int>(j1 - j0);
         const int lsh = vsh - 1, lpr = vpr >> 1;
-        const int c = static_cast<int>(threadIdx.x) & (lpr - 1);
+        const int c = gt & (lpr - 1);
         const int rstep = NT >> lsh;
         constexpr int UR = NT <= 128 ? U : U / 2;  // rows a thread has in flight (two vectors each)
-        for (int jb = static_cast<int>(threadIdx.x) >> lsh; jb < nrows; jb += UR * rstep) {
+        for (int jb = gt >> lsh; jb < nrows; jb += UR * rstep) {
             uint4 v[UR][2];
 #pragma unroll
             for (int u = 0; u < UR; ++u) {
@@ -440,7 +479,7 @@ __device__ void gather_rows_of(const TopkArgs &a, int64_t row, int64_t j0, int64
         }
         return;
     }
-    for (int t0 = threadIdx.x; t0 < total; t0 += U * NT) {
+    for (int t0 = gt; t0 < total; t0 += U * NT) {
         uint4 v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -471,18 +510,18 @@ struct MinBlocks {
 };
 
 // Short row (n <= k): columns 0..n-1 then fills; positions [j0, j1) of the output row.
-template <typename E, int NT, bool GATHER>
+template <typename E, typename G, bool GATHER>
 __device__ void short_row(const TopkArgs &a, int64_t row, int64_t n, int j0, int j1)
 {
     using T = Elem<E>;
     const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
-    for (int j = j0 + static_cast<int>(threadIdx.x); j < j1; j += NT) {
+    for (int j = j0 + G::tid(); j < j1; j += G::NT) {
         store_idx(a, row, j, j < n ? j : -1);
         if (a.want_values) store_val<E>(a, row, j, j < n ? xrow[j] : static_cast<E>(T::kFill));
     }
     if (GATHER) {
         const int64_t g1 = min(static_cast<int64_t>(j1), a.n_gather);
-        if (j0 < g1) gather_rows_of<NT>(a, row, j0, g1, nullptr, n);
+        if (j0 < g1) gather_rows_of<G>(a, row, j0, g1, nullptr, n);
     }
 }
 
@@ -602,7 +641,7 @@ __device__ int filter_to_list(const TopkArgs &a, const E *buf, int len, uint32_t
     uint32_t c = 0;
     for (int v = v0; v < v1; ++v) c += __popc(static_cast<uint32_t>(masks[v]));
     uint32_t tot;
-    uint32_t pos = block_exclusive_scan<NT>(c, s_warp, tot);
+    uint32_t pos = block_exclusive_scan<Grp<NT>>(c, s_warp, tot);
     if (tot <= static_cast<uint32_t>(cap)) {
         for (int v = v0; v < v1; ++v) {
             uint32_t m = masks[v];
@@ -618,19 +657,20 @@ __device__ int filter_to_list(const TopkArgs &a, const E *buf, int len, uint32_t
 }
 
 // Sum of a histogram over the CTA (all threads get it).  Two __syncthreads.
-template <int NT>
+template <typename G>
 __device__ __forceinline__ uint32_t hist_total(const uint32_t *h, int nb, uint32_t *s_warp)
 {
-    const int tid = threadIdx.x;
+    constexpr int NT = G::NT;
+    const int tid = G::tid();
     uint32_t s = 0;
     for (int i = tid; i < nb; i += NT) s += h[i];
     s = __reduce_add_sync(kFull, s);
     if ((tid & 31) == 0) s_warp[tid >> 5] = s;
-    __syncthreads();
+    G::sync();
     uint32_t total = 0;
 #pragma unroll
     for (int w = 0; w < NT / 32; ++w) total += s_warp[w];
-    __syncthreads();
+    G::sync();
     return total;
 }
 
@@ -649,7 +689,7 @@ __device__ uint32_t sample_threshold_key(const TopkArgs &a, const E *buf, int nv
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sh0 = T::KB - a.bits[0];
     const int nb0 = 1 << a.bits[0];
-    const uint32_t total = hist_total<NT>(h, nb0, s_warp);
+    const uint32_t total = hist_total<Grp<NT>>(h, nb0, s_warp);
     const float mu = share * static_cast<float>(total) / population;
     const float want = mu * 1.125f + 3.0f * sqrtf(mu) + 4.0f;
     if (want >= static_cast<float>(total)) {
@@ -657,7 +697,7 @@ __device__ uint32_t sample_threshold_key(const TopkArgs &a, const E *buf, int nv
         __syncthreads();
         return 0u;
     }
-    find_threshold<NT>(h, nb0, static_cast<uint32_t>(want), s_res, s_warp);
+    find_threshold<Grp<NT>>(h, nb0, static_cast<uint32_t>(want), s_res, s_warp);
     const uint32_t d = s_res[0];
     const uint32_t need2 = static_cast<uint32_t>(want) - s_res[1];
     for (int i = tid; i < nb0; i += NT) h[i] = 0u;
@@ -679,7 +719,7 @@ __device__ uint32_t sample_threshold_key(const TopkArgs &a, const E *buf, int nv
         }
     }
     __syncthreads();
-    find_threshold<NT>(h, 1 << b2, need2, s_res, s_warp);
+    find_threshold<Grp<NT>>(h, 1 << b2, need2, s_res, s_warp);
     const uint32_t key = (d << sh0) | (s_res[0] << sh1);
     for (int i = tid; i < (1 << b2); i += NT) h[i] = 0u;
     __syncthreads();
@@ -716,12 +756,13 @@ __device__ __forceinline__ int64_t seg_col(const Segments<E> &sg, int s, uint32_
     return sg.cols[s] ? static_cast<int64_t>(__ldcg(sg.cols[s] + i)) : sg.base[s] + i;
 }
 
-template <typename E, int NT, bool GATHER>
+template <typename E, typename G, bool GATHER>
 __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E> &sg, uint32_t max_tkey,
                                  uint32_t *hist, uint32_t *s_res, uint32_t *s_warp, int32_t *glist)
 {
     using T = Elem<E>;
-    const int tid = threadIdx.x;
+    constexpr int NT = G::NT;
+    const int tid = G::tid();
     const uint32_t total = sg.pre[sg.n];
     uint32_t prefix = 0, need = static_cast<uint32_t>(a.k), cnt = 0;
     int shift = T::KB;
@@ -740,11 +781,11 @@ __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E
                 hist_add_grouped(hist, (kk >> nsh) & mask, in && (l == 0 || (kk >> shift) == prefix), lane);
             }
         }
-        __syncthreads();
-        find_threshold<NT>(hist, nb, need, s_res, s_warp);
+        G::sync();
+        find_threshold<G>(hist, nb, need, s_res, s_warp);
         const uint32_t d = s_res[0];
         for (int i = tid; i < nb; i += NT) hist[i] = 0u;
-        __syncthreads();
+        G::sync();
         if (l == 0 && d < (max_tkey >> nsh)) return false;
         prefix = (l == 0) ? d : ((prefix << bl) | d);
         need -= s_res[1];
@@ -771,10 +812,10 @@ __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E
         }
     }
     uint32_t tq;
-    uint32_t r = block_exclusive_scan<NT>(q, s_warp, tq);
+    uint32_t r = block_exclusive_scan<G>(q, s_warp, tq);
     const uint32_t sel = g + take_from_ties(E_need, r, q);
     uint32_t ts;
-    uint32_t pos = block_exclusive_scan<NT>(sel, s_warp, ts);
+    uint32_t pos = block_exclusive_scan<G>(sel, s_warp, ts);
     // The histogram is free now.  When it can hold a 16-bit source index per output position,
     // record which entry lands where, then write the outputs position by position: the column
     // loads are independent (many in flight) and the stores coalesce.
@@ -803,7 +844,7 @@ __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E
         }
     }
     if (by_position) {
-        __syncthreads();
+        G::sync();
         constexpr int U = 4;
         for (int j0 = tid; j0 < a.k; j0 += U * NT) {
             int64_t col[U];
@@ -836,8 +877,8 @@ __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E
         }
     }
     if (GATHER) {
-        __syncthreads();
-        gather_rows_of<NT>(a, row, 0, a.n_gather, glist, 0);
+        G::sync();
+        gather_rows_of<G>(a, row, 0, a.n_gather, glist, 0);
     }
     return true;
 }
@@ -890,7 +931,7 @@ __device__ bool select_staged(const TopkArgs &a, int64_t row, const Segments<E> 
             }
         }
         __syncthreads();
-        find_threshold<NT>(hist, nb, need, s_res, s_warp);
+        find_threshold<Grp<NT>>(hist, nb, need, s_res, s_warp);
         const uint32_t d = s_res[0];
         for (int i = tid; i < nb; i += NT) hist[i] = 0u;
         __syncthreads();
@@ -923,10 +964,10 @@ __device__ bool select_staged(const TopkArgs &a, int64_t row, const Segments<E> 
         }
     }
     uint32_t tq;
-    uint32_t r = block_exclusive_scan<NT>(q, s_warp, tq);
+    uint32_t r = block_exclusive_scan<Grp<NT>>(q, s_warp, tq);
     const uint32_t sel = g + take_from_ties(E_need, r, q);
     uint32_t ts;
-    uint32_t pos = block_exclusive_scan<NT>(sel, s_warp, ts);
+    uint32_t pos = block_exclusive_scan<Grp<NT>>(sel, s_warp, ts);
     const uint32_t total = sg.pre[sg.n];
     const bool by_position = total <= 65535u && static_cast<uint32_t>(a.k) <= 2u * static_cast<uint32_t>(a.hist_bins);
     uint16_t *src = reinterpret_cast<uint16_t *>(hist);  // the histogram is free now
@@ -992,7 +1033,7 @@ __device__ bool select_staged(const TopkArgs &a, int64_t row, const Segments<E> 
     }
     if (GATHER) {
         __syncthreads();
-        gather_rows_of<NT>(a, row, 0, a.n_gather, glist, 0);
+        gather_rows_of<Grp<NT>>(a, row, 0, a.n_gather, glist, 0);
     }
     return true;
 }
@@ -1027,7 +1068,7 @@ __global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(c
     const int64_t n = valid_cols(a, row);
     const int k = a.k;
     if (n <= k) {
-        short_row<E, NT, GATHER>(a, row, n, 0, k);
+        short_row<E, Grp<NT>, GATHER>(a, row, n, 0, k);
         return;
     }
     const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
@@ -1100,7 +1141,7 @@ __global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(c
             }
         }
         __syncthreads();
-        find_threshold<NT>(hist, nb, need, s_res, s_warp);
+        find_threshold<Grp<NT>>(hist, nb, need, s_res, s_warp);
         for (int i = tid; i < nb; i += NT) hist[i] = 0u;
         __syncthreads();
         prefix = (l == 0) ? s_res[0] : ((prefix << bl) | s_res[0]);
@@ -1129,10 +1170,10 @@ __global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(c
         }
     }
     uint32_t tq;
-    uint32_t r = block_exclusive_scan<NT>(qq, s_warp, tq);
+    uint32_t r = block_exclusive_scan<Grp<NT>>(qq, s_warp, tq);
     const uint32_t sel = g + take_from_ties(E_need, r, qq);
     uint32_t ts;
-    uint32_t pos = block_exclusive_scan<NT>(sel, s_warp, ts);
+    uint32_t pos = block_exclusive_scan<Grp<NT>>(sel, s_warp, ts);
 #pragma unroll
     for (int j = 0; j < R; ++j) {
         if (j < re) {
@@ -1157,7 +1198,7 @@ __global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(c
     }
     if (GATHER) {
         __syncthreads();
-        gather_rows_of<NT>(a, row, 0, a.n_gather, glist, 0);
+        gather_rows_of<Grp<NT>>(a, row, 0, a.n_gather, glist, 0);
     }
 }
 
@@ -1182,7 +1223,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
     const int64_t n = valid_cols(a, row);
     const int k = a.k;
     if (n <= k) {
-        short_row<E, NT, GATHER>(a, row, n, 0, k);
+        short_row<E, Grp<NT>, GATHER>(a, row, n, 0, k);
         return;
     }
     const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
@@ -1231,7 +1272,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
             }
         }
         __syncthreads();
-        exact = hist_total<NT>(hist, nb0, s_warp) >= static_cast<uint32_t>(k);
+        exact = hist_total<Grp<NT>>(hist, nb0, s_warp) >= static_cast<uint32_t>(k);
         if (!exact) {  // the estimate was too high: exact histogram of the whole slice
             for (int i = tid; i < nb0; i += NT) hist[i] = 0u;
             __syncthreads();
@@ -1249,7 +1290,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
             __syncthreads();
         }
     }
-    find_threshold<NT>(hist, nb0, static_cast<uint32_t>(k), s_res, s_warp);
+    find_threshold<Grp<NT>>(hist, nb0, static_cast<uint32_t>(k), s_res, s_warp);
     for (int i = tid; i < nb0; i += NT) hist[i] = 0u;
     __syncthreads();
     if (!exact) {
@@ -1291,7 +1332,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
             }
         }
         __syncthreads();
-        find_threshold<NT>(hist, nb, need, s_res, s_warp);
+        find_threshold<Grp<NT>>(hist, nb, need, s_res, s_warp);
         for (int i = tid; i < nb; i += NT) hist[i] = 0u;
         __syncthreads();
         prefix = (prefix << bl) | s_res[0];
@@ -1314,10 +1355,10 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
             q += c == P;
         }
         uint32_t tq;
-        uint32_t r = block_exclusive_scan<NT>(q, s_warp, tq);
+        uint32_t r = block_exclusive_scan<Grp<NT>>(q, s_warp, tq);
         const uint32_t sel = g + take_from_ties(E_need, r, q);
         uint32_t ts;
-        uint32_t pos = block_exclusive_scan<NT>(sel, s_warp, ts);
+        uint32_t pos = block_exclusive_scan<Grp<NT>>(sel, s_warp, ts);
         // each output position's column goes to the (free) histogram first when it fits (16 bits
         // each); the outputs are then written in position order, coalesced
         const bool by_position = static_cast<uint32_t>(k) <= 2u * static_cast<uint32_t>(a.hist_bins);
@@ -1428,7 +1469,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
     }
     if (GATHER) {
         __syncthreads();
-        gather_rows_of<NT>(a, row, 0, a.n_gather, glist, 0);
+        gather_rows_of<Grp<NT>>(a, row, 0, a.n_gather, glist, 0);
     }
 }
 
@@ -1464,7 +1505,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
     const int64_t n = valid_cols(a, row);
     const int k = a.k;
     if (n <= k) {
-        if (part == 0) short_row<E, NT, GATHER>(a, row, n, 0, k);
+        if (part == 0) short_row<E, Grp<NT>, GATHER>(a, row, n, 0, k);
         return;
     }
     const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
@@ -1606,7 +1647,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
     if (cand_ok) {
         done = s_staged ? select_staged<E, NT, GATHER>(a, row, s_seg, s_stage_off, s_staged, smem, max_tkey, hist,
                                                        s_res, s_warp, glist)
-                        : select_segments<E, NT, GATHER>(a, row, s_seg, max_tkey, hist, s_res, s_warp, glist);
+                        : select_segments<E, Grp<NT>, GATHER>(a, row, s_seg, max_tkey, hist, s_res, s_warp, glist);
     }
     if (!done) {
         __syncthreads();
@@ -1619,7 +1660,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
             s_seg.pre[1] = static_cast<uint32_t>(n);
         }
         __syncthreads();
-        select_segments<E, NT, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
+        select_segments<E, Grp<NT>, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
     }
 }
 
@@ -1640,7 +1681,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) stream_kernel(const 
     const int64_t row = blockIdx.x;
     const int64_t n = valid_cols(a, row);
     if (n <= a.k) {
-        short_row<E, NT, GATHER>(a, row, n, 0, a.k);
+        short_row<E, Grp<NT>, GATHER>(a, row, n, 0, a.k);
         return;
     }
     const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
@@ -1659,7 +1700,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) stream_kernel(const 
         s_seg.pre[1] = static_cast<uint32_t>(n);
     }
     __syncthreads();
-    select_segments<E, NT, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
+    select_segments<E, Grp<NT>, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
 }
 
 // ---------------------------------------------------------------------------
@@ -1730,7 +1771,7 @@ __device__ uint32_t estimate_threshold(const TopkArgs &a, const uint4 (&q)[kQ], 
         __syncthreads();
         return 0u;
     }
-    find_threshold<NT>(h, nb0, static_cast<uint32_t>(want), s_res, s_warp);
+    find_threshold<Grp<NT>>(h, nb0, static_cast<uint32_t>(want), s_res, s_warp);
     const uint32_t d = s_res[0];
     const uint32_t need2 = static_cast<uint32_t>(want) - s_res[1];
     for (int i = tid; i < nb0; i += NT) h[i] = 0u;
@@ -1751,7 +1792,7 @@ __device__ uint32_t estimate_threshold(const TopkArgs &a, const uint4 (&q)[kQ], 
         }
     }
     __syncthreads();
-    find_threshold<NT>(h, 1 << b2, need2, s_res, s_warp);
+    find_threshold<Grp<NT>>(h, 1 << b2, need2, s_res, s_warp);
     const uint32_t key = (d << sh0) | (s_res[0] << sh1);
     for (int i = tid; i < (1 << b2); i += NT) h[i] = 0u;
     __syncthreads();
@@ -1788,16 +1829,17 @@ __device__ __forceinline__ void for_region(const uint2 *reg, uint32_t c, int lan
     for (uint32_t i = i0 + lane; i < c; i += 32) f(i, reg[i]);
 }
 
-template <typename E, int NT, bool GATHER>
+template <typename E, typename G, bool GATHER>
 __device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int rs, const uint32_t *cnt, uint32_t tlo,
                                uint32_t thi, uint32_t *hist, uint32_t *s_res, uint32_t *s_warp, uint32_t *s_gq,
                                int32_t *glist)
 {
     using T = Elem<E>;
-    constexpr int W = NT / 32;
+    constexpr int NT = G::NT;
+    constexpr int W = G::W;
     constexpr uint32_t kMark = 0x80000000u;
     __shared__ uint32_t s_nbin;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = G::tid(), lane = tid & 31, warp = tid >> 5;
     uint2 *reg = list + warp * rs;
     const uint32_t c = cnt[warp];
     const uint32_t lt = (1u << lane) - 1u;
@@ -1807,8 +1849,8 @@ __device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int 
     for_region(reg, c, lane, [&](uint32_t, uint2 e) { atomicAdd(&hist[(T::key(static_cast<E>(e.x)) - tlo) >> rsh], 1u); });
     if (tid == 0) s_nbin = 0u;
     if (tid < W) s_gq[2 * W + tid] = 0u;
-    __syncthreads();
-    find_threshold<NT>(hist, kRangeBins, static_cast<uint32_t>(a.k), s_res, s_warp);
+    G::sync();
+    find_threshold<G>(hist, kRangeBins, static_cast<uint32_t>(a.k), s_res, s_warp);
     const uint32_t dstar = s_res[0], above = s_res[1], inbin = s_res[2];
     const uint32_t bneed = static_cast<uint32_t>(a.k) - above;  // taken from the threshold bin
     const bool whole = inbin == bneed;
@@ -1842,7 +1884,7 @@ __device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int 
             s_gq[warp] = na;
             s_gq[W + warp] = nin;
         }
-        __syncthreads();  // bin members and counts complete
+        G::sync();  // bin members and counts complete
         if (!whole) {
             // rank of a member among the bin's (larger key first, then smaller column): one warp
             // per member, its lanes comparing against the other members
@@ -1855,11 +1897,11 @@ __device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int 
                     atomicAdd(&s_gq[2 * W + bi[m] / static_cast<uint32_t>(rs)], 1u);
                 }
             }
-            __syncthreads();
+            G::sync();
         }
     } else {
         for (int i = tid; i < kRangeBins; i += NT) hist[i] = 0u;
-        __syncthreads();
+        G::sync();
         uint32_t prefix = 0, need = static_cast<uint32_t>(a.k), cls = 0;
         int shift = T::KB;
         for (int l = 0; l < a.nlevels && (l == 0 || cls != need); ++l) {
@@ -1873,10 +1915,10 @@ __device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int 
                 const uint32_t kk = in ? T::key(static_cast<E>(reg[i].x)) : 0u;
                 hist_add_grouped(hist, (kk >> nsh) & mask, in && (l == 0 || (kk >> shift) == prefix), lane);
             }
-            __syncthreads();
-            find_threshold<NT>(hist, nb, need, s_res, s_warp);
+            G::sync();
+            find_threshold<G>(hist, nb, need, s_res, s_warp);
             for (int i = tid; i < nb; i += NT) hist[i] = 0u;
-            __syncthreads();
+            G::sync();
             prefix = (l == 0) ? s_res[0] : ((prefix << bl) | s_res[0]);
             need -= s_res[1];
             cls = s_res[2];
@@ -1897,7 +1939,7 @@ __device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int 
             s_gq[warp] = g;
             s_gq[W + warp] = q;
         }
-        __syncthreads();
+        G::sync();
     }
     // outputs of the regions before this warp's (and, for full-key classes, their ties)
     auto taken_of = [&](int w, uint32_t ties_before) {
@@ -1951,8 +1993,8 @@ __device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int 
         }
     }
     if (GATHER) {
-        __syncthreads();
-        gather_rows_of<NT>(a, row, 0, a.n_gather, glist, 0);
+        G::sync();
+        gather_rows_of<G>(a, row, 0, a.n_gather, glist, 0);
     }
 }
 
@@ -1980,7 +2022,7 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
     const int64_t n = valid_cols(a, row);
     const int k = a.k;
     if (n <= k) {
-        if (part == 0) short_row<E, NT, GATHER>(a, row, n, 0, k);
+        if (part == 0) short_row<E, Grp<NT>, GATHER>(a, row, n, 0, k);
         return;
     }
     const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
@@ -2215,7 +2257,7 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
         thi = max(thi, s_kmax[w]);
     }
     if (!over && L >= static_cast<uint32_t>(k)) {
-        select_regions<E, NT, GATHER>(a, row, list, rs, s_cnt, tlo, thi, hist, s_res, s_warp, s_gq, glist);
+        select_regions<E, Grp<NT>, GATHER>(a, row, list, rs, s_cnt, tlo, thi, hist, s_res, s_warp, s_gq, glist);
         return;
     }
     if (tid == 0) {
@@ -2227,7 +2269,546 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
         s_seg.pre[1] = static_cast<uint32_t>(n);
     }
     __syncthreads();
-    select_segments<E, NT, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
+    select_segments<E, Grp<NT>, GATHER>(a, row, s_seg, 0u, hist, s_res, s_warp, glist);
+}
+
+// ---------------------------------------------------------------------------
+// flat_kernel: wide rows spread evenly over a persistent grid of one CTA per
+// SM (a cooperative launch, so every CTA is resident and the bounded waits
+// below on other CTAs' flags always end).
+//
+// Work split.  Each row's 16-byte vectors are cut into `parts` chunks of at
+// most `slice` vectors; chunk q (row q / parts, index q % parts) belongs to
+// CTA q mod grid.  At any moment the whole GPU works on a band of
+// consecutive rows, so rows finish one after another over the launch
+// instead of all at its end, and every SM moves the same number of bytes.
+//
+// Streaming warps (0..15) never synchronise with one another.  For each of
+// its CTA's chunks, warp w reads its 1/16 of the chunk with two sets of
+// kFlatU 16-byte loads per lane in flight (the next set, possibly of the
+// next chunk, is issued before the current one is examined), keeps the keys
+// at or above the row's threshold estimate, and writes them as (key bits,
+// column) pairs, in column order, to its own slot of the workspace.  The
+// slot's header takes the count and the largest key.  Then it bumps the
+// row's arrival counter; the warp that arrives last queues the row for its
+// own CTA's selection warps.
+//
+// Selection warps (16..23, a group on named barrier 1) first compute the
+// threshold estimates of the rows this CTA is designated for (row r: CTA
+// r mod grid) from a sample of 32 runs of 32 vectors spread over the row,
+// and publish each through a flag in the workspace; the streaming warps of
+// every CTA wait for that flag (bounded) before examining a chunk of the
+// row.  Rows with n <= k get their fills here and are skipped by the
+// streaming warps.  Then the selection warps take the queued rows: the
+// row's slots are copied into shared-memory regions (one per selection
+// warp, in column order) and select_regions picks the k.  A slot that
+// overflowed, or fewer than k candidates, falls back to exact passes over
+// the row in global memory.
+//
+// Workspace (caller-owned, 256-byte aligned; the first ws_counter_bytes are
+// zeroed on the stream before every launch):
+//   uint32 arrival counter [rows], estimate-ready flag [rows], estimate [rows]
+//   per row r at ws_counter_bytes + r * ws_row_bytes, per chunk j and
+//   streaming warp w at ((j * 16 + w) * ws_part_bytes):
+//     uint4 {count (or kSlotOverflow), largest key, 0, 0}, uint2 pairs[part_cap + 1]
+// Shared memory: histogram (2048 words) | selection regions (8 x
+// region_stride pairs) | staging (16 x kStage vectors, then 16 x kStage
+// columns).
+// ---------------------------------------------------------------------------
+constexpr int kFlatU = 4;
+constexpr uint32_t kSlotOverflow = 0xffffffffu;
+using FlatSel = Grp<kFlatSelWarps * 32, 1, kFlatStreamWarps * 32>;
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Threshold estimate of one row from a fixed sample (32 runs of 32 consecutive vectors spread
+// evenly over the row's full vectors, or all of them when fewer): the key that
+// mu*(1+1/8) + 3*sqrt(mu) + 4 sampled keys reach, mu being the sample's expected share of the
+// k.  Top digit from a histogram, then a second digit from the sampled keys in that bin.  0
+// (keep everything) when that is the whole sample.  h: 2048 zeroed words, left zeroed.
+template <typename E, typename G>
+__device__ uint32_t flat_estimate(const TopkArgs &a, int64_t row, int64_t n, uint32_t *h, uint32_t *s_res,
+                                  uint32_t *s_warp)
+{
+    using T = Elem<E>;
+    constexpr int V = T::V;
+    constexpr int NT = G::NT;
+    constexpr int kRuns = kFlatSampleVecs / 32;
+    constexpr int PER = kFlatSampleVecs / NT;
+    static_assert(kFlatSampleVecs % NT == 0, "whole loads per thread");
+    const int tid = G::tid();
+    const uint4 *xv = reinterpret_cast<const uint4 *>(static_cast<const E *>(a.x) + row * a.stride);
+    const int64_t nv = (n * static_cast<int64_t>(sizeof(E))) >> 4;
+    const int64_t m = nv < kFlatSampleVecs ? nv : kFlatSampleVecs;
+    uint4 q[PER];
+#pragma unroll
+    for (int s = 0; s < PER; ++s) {
+        const int64_t i = tid + s * NT;
+        q[s] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < m) {
+            const int64_t pos = nv <= kFlatSampleVecs ? i : (i >> 5) * (nv - 32) / (kRuns - 1) + (i & 31);
+            q[s] = __ldcg(xv + pos);
+        }
+    }
+    const int sh0 = T::KB - a.bits[0];
+    const int nb0 = 1 << a.bits[0];
+#pragma unroll
+    for (int s = 0; s < PER; ++s) {
+        if (tid + s * NT < m) {
+            E el[V];
+            T::unpack(q[s], el);
+#pragma unroll
+            for (int t = 0; t < V; ++t) atomicAdd(&h[T::key(el[t]) >> sh0], 1u);
+        }
+    }
+    G::sync();
+    const float total = static_cast<float>(m) * V;
+    const float mu = static_cast<float>(a.k) * total / static_cast<float>(n);
+    const float want = mu * 1.125f + 3.0f * sqrtf(mu) + 4.0f;
+    if (want >= total) {
+        for (int i = tid; i < nb0; i += NT) h[i] = 0u;
+        G::sync();
+        return 0u;
+    }
+    find_threshold<G>(h, nb0, static_cast<uint32_t>(want), s_res, s_warp);
+    const uint32_t d = s_res[0];
+    const uint32_t need2 = static_cast<uint32_t>(want) - s_res[1];
+    for (int i = tid; i < nb0; i += NT) h[i] = 0u;
+    G::sync();
+    const int b2 = sh0 < 11 ? sh0 : 11;
+    const int sh1 = sh0 - b2;
+    const uint32_t m2 = (1u << b2) - 1u;
+#pragma unroll
+    for (int s = 0; s < PER; ++s) {
+        if (tid + s * NT < m) {
+            E el[V];
+            T::unpack(q[s], el);
+#pragma unroll
+            for (int t = 0; t < V; ++t) {
+                const uint32_t kk = T::key(el[t]);
+                if ((kk >> sh0) == d) atomicAdd(&h[(kk >> sh1) & m2], 1u);
+            }
+        }
+    }
+    G::sync();
+    find_threshold<G>(h, 1 << b2, need2, s_res, s_warp);
+    const uint32_t key = (d << sh0) | (s_res[0] << sh1);
+    for (int i = tid; i < (1 << b2); i += NT) h[i] = 0u;
+    G::sync();
+    return key;
+}
+
+// The streaming warps' side of flat_kernel (see above).  s_q / s_qtail: this CTA's queue of
+// rows to select; s_sdone: streaming warps finished.
+template <typename E>
+__device__ void flat_stream(const TopkArgs &a, unsigned char *smem, volatile uint32_t *s_q, uint32_t *s_qtail,
+                            uint32_t *s_sdone)
+{
+    using T = Elem<E>;
+    constexpr int V = T::V;
+    constexpr int U = kFlatU;
+    constexpr int SW = kFlatStreamWarps;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t lt = (1u << lane) - 1u;
+    const int64_t G = gridDim.x;
+    const int cpr = a.parts;
+    const int64_t nchunks = a.rows * cpr;
+    const int64_t nvr = (a.cols * static_cast<int64_t>(sizeof(E))) >> 4;  // full vectors of a whole row
+    uint32_t *ctr = reinterpret_cast<uint32_t *>(a.ws);
+    const uint32_t *flag = ctr + a.rows;
+    const uint32_t *tkeys = flag + a.rows;
+    const uint32_t capw = static_cast<uint32_t>(a.part_cap);
+    const uint32_t arrivals = static_cast<uint32_t>(cpr) * SW;
+    uint4 *stv = reinterpret_cast<uint4 *>(smem + a.smem_stage_off) + warp * kStage;
+    int32_t *stc = reinterpret_cast<int32_t *>(smem + a.smem_stage_off + SW * kStage * 16) + warp * kStage;
+
+    // this warp's vectors [vb, ve) of chunk q's row; n: the row's valid columns (short rows: empty)
+    auto range_of = [&](int64_t q, int64_t &row, int &j, int64_t &n, int64_t &vb, int64_t &ve) {
+        row = q / cpr;
+        j = static_cast<int>(q - row * cpr);
+        n = valid_cols(a, row);
+        const int64_t nv = n > a.k ? (n * static_cast<int64_t>(sizeof(E))) >> 4 : 0;
+        const int64_t c0 = min(static_cast<int64_t>(j) * a.slice, nv);
+        const int64_t c1 = min(min((static_cast<int64_t>(j) + 1) * a.slice, nvr), nv);
+        const int64_t len = c1 - c0, per = len / SW, rem = len % SW;
+        vb = c0 + warp * per + min(static_cast<int64_t>(warp), rem);
+        ve = vb + per + (warp < rem ? 1 : 0);
+    };
+    constexpr int64_t kIt = 32 * U;  // vectors of one iteration (one set of loads)
+
+    // ---- load cursor: two iterations ahead of the one being examined
+    int64_t lq = blockIdx.x, lvb = 0, lve = 0, lbase = 0;
+    const uint4 *lxv = nullptr;
+    bool lvalid = false;
+    auto seek = [&](int64_t q) {  // first chunk at or after q with vectors for this warp
+        for (; q < nchunks; q += G) {
+            int64_t row, n;
+            int j;
+            range_of(q, row, j, n, lvb, lve);
+            if (lve > lvb) {
+                lq = q;
+                lbase = lvb;
+                lxv = reinterpret_cast<const uint4 *>(static_cast<const E *>(a.x) + row * a.stride);
+                lvalid = true;
+                return;
+            }
+        }
+        lvalid = false;
+    };
+    auto load_next = [&](uint4 (&q)[U]) {
+        if (lvalid) {
+            if (lbase + kIt <= lve) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) q[u] = __ldcs(lxv + lbase + u * 32 + lane);
+            } else {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = lbase + u * 32 + lane;
+                    q[u] = v < lve ? __ldcs(lxv + v) : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            lbase += kIt;
+            if (lbase >= lve) seek(lq + G);
+        }
+    };
+    uint4 qa[U], qb[U];
+    seek(blockIdx.x);
+    load_next(qa);
+    load_next(qb);
+    bool use_a = true;  // buffer holding the next iteration to examine
+
+    // ---- chunk state of the iteration being examined
+    uint32_t tkey = 0, tsg = 0, off = 0, kmax = 0, smax = T::kSmaxInit, umax = T::kUmaxInit;
+    bool positive = false, pnan = false;
+    int sc = 0;
+    uint2 *pairs = nullptr;
+    auto expand = [&]() {
+        __syncwarp();
+        for (int r0 = 0; r0 < sc; r0 += 32) {
+            const int i = r0 + lane;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            int cb = 0;
+            uint32_t m = 0;
+            if (i < sc) {
+                v = stv[i];
+                cb = stc[i];
+                m = positive ? T::ge_mask_raw(v, tsg) : T::ge_mask_key(v, tkey);
+            }
+            uint32_t tot;
+            uint32_t p = off + warp_exclusive_scan(static_cast<uint32_t>(__popc(m)), lane, tot);
+            while (m) {
+                const int t = __ffs(m) - 1;
+                m &= m - 1u;
+                const E e = T::lane_of(v, t);
+                kmax = max(kmax, T::key(e));
+                pnan |= T::is_nan(e);
+                __stcg(pairs + (p < capw ? p : capw), make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(cb + t)));
+                ++p;
+            }
+            off += tot;
+        }
+        sc = 0;
+        __syncwarp();
+    };
+    // examines one iteration's vectors [base, base + kIt) ∩ [.., ve)
+    auto examine = [&](const uint4 (&q)[U], int64_t base, int64_t ve) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            bool any;
+            if (positive) {
+                T::nan_acc_neg(q[u], umax);  // zero vectors past the range pass nothing, hold no NaN
+                any = T::any_ge_raw(q[u], tsg);
+            } else {
+                T::nan_acc(q[u], smax, umax);
+                any = base + u * 32 + lane < ve && T::ge_mask_key(q[u], tkey) != 0u;
+            }
+            const uint32_t b = __ballot_sync(kFull, any);
+            if (b) {
+                const int nb = __popc(b);
+                if (sc + nb > kStage) expand();
+                if (any) {
+                    const int slot = sc + __popc(b & lt);
+                    stv[slot] = q[u];
+                    stc[slot] = static_cast<int32_t>((base + u * 32 + lane) * V);
+                }
+                sc += nb;
+            }
+        }
+    };
+
+    for (int64_t q = blockIdx.x; q < nchunks; q += G) {
+        int64_t row, n, vb, ve;
+        int j;
+        range_of(q, row, j, n, vb, ve);
+        if (n <= a.k) continue;  // short row: the designated CTA writes its fills
+        const bool tail = j == cpr - 1 && warp == SW - 1;  // this warp also takes the < 16-byte tail
+        const int64_t nv = (n * static_cast<int64_t>(sizeof(E))) >> 4;
+        const bool has_tail = tail && nv * V < n;
+        const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
+        unsigned char *slot = a.ws + a.ws_counter_bytes + row * a.ws_row_bytes +
+                              (static_cast<int64_t>(j) * SW + warp) * a.ws_part_bytes;
+        pairs = reinterpret_cast<uint2 *>(slot + 16);
+        off = 0;
+        kmax = 0;
+        smax = T::kSmaxInit;
+        umax = T::kUmaxInit;
+        if (ve > vb || has_tail) {
+            // the row's estimate (published once by its designated CTA)
+            uint32_t t = 0;
+            if (lane == 0) {
+                const long long t0 = clock64();
+                while (ld_acquire_gpu(flag + row) == 0u) {
+                    if (clock64() - t0 > kWaitCycles) {
+                        set_err(a.err_flag, kStatusTimeout);
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+                t = __ldcg(tkeys + row);
+            }
+            tkey = __shfl_sync(kFull, t, 0);
+            positive = tkey > T::kSignKey;
+            tsg = tkey ^ T::kSignKey;
+            pnan = tkey > T::key(static_cast<E>(T::kInfMagnitude));  // an estimate above +inf: a sampled NaN
+            for (int64_t base = vb; base < ve; base += kIt) {
+                if (use_a) {
+                    examine(qa, base, ve);
+                    load_next(qa);
+                } else {
+                    examine(qb, base, ve);
+                    load_next(qb);
+                }
+                use_a = !use_a;
+            }
+            if (sc) expand();
+            if (has_tail) {
+                const int64_t jt = nv * V + lane;
+                const bool in = jt < n;
+                const E e = in ? xrow[jt] : static_cast<E>(0);
+                if (in) T::nan_acc1(e, smax, umax);
+                const bool pass = in && T::key(e) >= tkey;
+                const uint32_t bp = __ballot_sync(kFull, pass);
+                if (pass) {
+                    kmax = max(kmax, T::key(e));
+                    const uint32_t p = off + __popc(bp & lt);
+                    __stcg(pairs + (p < capw ? p : capw), make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(jt)));
+                }
+                off += __popc(bp);
+            }
+        } else {
+            pnan = false;
+        }
+        // ---- the slot's header, then the arrival
+        kmax = __reduce_max_sync(kFull, kmax);
+        const bool nan = __any_sync(kFull, pnan || T::has_nan(smax, umax));
+        __threadfence();  // this lane's pairs, before the header and the arrival
+        __syncwarp();
+        if (lane == 0) {
+            if (nan && a.nan_flag) atomicOr(a.nan_flag, 1);
+            __stcg(reinterpret_cast<uint4 *>(slot), make_uint4(off > capw ? kSlotOverflow : off, kmax, 0u, 0u));
+            __threadfence();
+            if (atomicAdd(ctr + row, 1u) == arrivals - 1u) {
+                __threadfence();  // the other warps' slots, before the selection warps read them
+                const uint32_t s = atomicAdd(s_qtail, 1u);
+                if (s < static_cast<uint32_t>(kFlatQueue))
+                    s_q[s] = static_cast<uint32_t>(row) + 1u;
+                else
+                    set_err(a.err_flag, kStatusInval);
+                __threadfence_block();
+            }
+        }
+        __syncwarp();
+    }
+    if (lane == 0) {
+        __threadfence_block();
+        atomicAdd(s_sdone, 1u);
+    }
+}
+
+// One queued row: its slots into the selection regions, then select_regions (or the exact
+// fallback).  hist: 2048 words, zeroed on entry and on exit.
+template <typename E>
+__device__ void flat_select_row(const TopkArgs &a, int64_t row, unsigned char *smem, uint32_t *s_warp,
+                                uint32_t *s_res, uint32_t *s_cnt, uint32_t *s_gq, Segments<E> &s_seg)
+{
+    using S = FlatSel;
+    constexpr int SW = kFlatStreamWarps;
+    constexpr int NT = S::NT;
+    __shared__ uint32_t s_bad, s_thi;
+    const int gt = S::tid(), lane = gt & 31, gw = gt >> 5;
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
+    uint2 *list = reinterpret_cast<uint2 *>(smem + a.smem_list_off);
+    const int rs = a.region_stride;
+    const uint32_t capw = static_cast<uint32_t>(a.list_cap);
+    const uint32_t *tkeys = reinterpret_cast<const uint32_t *>(a.ws) + 2 * a.rows;
+    const unsigned char *wrow = a.ws + a.ws_counter_bytes + row * a.ws_row_bytes;
+    const int nsub = a.parts * SW;
+    const uint32_t tkey = __ldcg(tkeys + row);
+    // prefix of the slot counts (the histogram holds it: pre[s], s <= nsub)
+    uint32_t *pre = hist;
+    if (gt == 0) {
+        s_bad = 0u;
+        s_thi = 0u;
+    }
+    const int m = (nsub + NT - 1) / NT;
+    const int s0 = min(nsub, gt * m), s1 = min(nsub, s0 + m);
+    uint32_t c = 0, thi = 0;
+    bool bad = false;
+    for (int s = s0; s < s1; ++s) {
+        const uint4 h = __ldcg(reinterpret_cast<const uint4 *>(wrow + static_cast<int64_t>(s) * a.ws_part_bytes));
+        bad |= h.x == kSlotOverflow;
+        c += h.x == kSlotOverflow ? 0u : h.x;
+        thi = max(thi, h.y);
+    }
+    uint32_t total;
+    uint32_t p0 = block_exclusive_scan<S>(c, s_warp, total);
+    for (int s = s0; s < s1; ++s) {
+        pre[s] = p0;
+        const uint4 h = __ldcg(reinterpret_cast<const uint4 *>(wrow + static_cast<int64_t>(s) * a.ws_part_bytes));
+        p0 += h.x == kSlotOverflow ? 0u : h.x;
+    }
+    if (gt == 0) pre[nsub] = total;
+    thi = __reduce_max_sync(kFull, thi);
+    bad = __any_sync(kFull, bad);
+    if (lane == 0) {
+        atomicMax(&s_thi, thi);
+        if (bad) atomicOr(&s_bad, 1u);
+    }
+    S::sync();
+    const bool ok = s_bad == 0u && total >= static_cast<uint32_t>(a.k) && total <= static_cast<uint32_t>(S::W) * capw;
+    if (ok) {
+        // warp gw copies the flat range [f0, f1) of the slots (slots in column order) into its region
+        const uint32_t f0 = static_cast<uint32_t>(static_cast<uint64_t>(total) * gw / S::W);
+        const uint32_t f1 = static_cast<uint32_t>(static_cast<uint64_t>(total) * (gw + 1) / S::W);
+        uint2 *reg = list + gw * rs;
+        int lo = 0, hi = nsub - 1;  // the slot holding f0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pre[mid] <= f0) lo = mid;
+            else hi = mid - 1;
+        }
+        int s = lo;
+        for (uint32_t f = f0; f < f1;) {
+            while (s < nsub - 1 && pre[s + 1] <= f) ++s;
+            const uint32_t end = min(f1, pre[s + 1]);
+            const uint2 *sp = reinterpret_cast<const uint2 *>(wrow + static_cast<int64_t>(s) * a.ws_part_bytes + 16) - pre[s];
+            for (uint32_t i = f + lane; i < end; i += 32) reg[i - f0] = __ldcg(sp + i);
+            f = end;
+        }
+        if (lane == 0) s_cnt[gw] = f1 - f0;
+        S::sync();
+        const uint32_t thi_all = s_thi;
+        for (int i = gt; i < kRangeBins; i += NT) hist[i] = 0u;
+        S::sync();
+        select_regions<E, S, false>(a, row, list, rs, s_cnt, tkey, thi_all, hist, s_res, s_warp, s_gq, nullptr);
+    } else {
+        for (int i = gt; i < a.hist_bins; i += NT) hist[i] = 0u;
+        if (gt == 0) {
+            s_seg.n = 1;
+            s_seg.bits[0] = static_cast<const E *>(a.x) + row * a.stride;
+            s_seg.cols[0] = nullptr;
+            s_seg.base[0] = 0;
+            s_seg.pre[0] = 0;
+            s_seg.pre[1] = static_cast<uint32_t>(valid_cols(a, row));
+        }
+        S::sync();
+        select_segments<E, S, false>(a, row, s_seg, 0u, hist, s_res, s_warp, nullptr);
+    }
+    S::sync();
+    for (int i = gt; i < a.hist_bins; i += NT) hist[i] = 0u;
+    S::sync();
+}
+
+template <typename E>
+__device__ void flat_select(const TopkArgs &a, unsigned char *smem, volatile uint32_t *s_q, volatile uint32_t *s_qtail,
+                            volatile uint32_t *s_sdone)
+{
+    using S = FlatSel;
+    constexpr int NT = S::NT;
+    __shared__ uint32_t s_warp[S::W], s_res[4], s_cnt[S::W], s_gq[3 * S::W], s_item;
+    __shared__ Segments<E> s_seg;
+    const int gt = S::tid();
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
+    uint32_t *flag = reinterpret_cast<uint32_t *>(a.ws) + a.rows;
+    uint32_t *tkeys = flag + a.rows;
+    const int64_t G = gridDim.x;
+    for (int i = gt; i < a.hist_bins; i += NT) hist[i] = 0u;
+    S::sync();
+    // ---- 1. the rows this CTA is designated for: short-row fills, or the threshold estimate
+    for (int64_t r = blockIdx.x; r < a.rows; r += G) {
+        const int64_t n = valid_cols(a, r);
+        if (n <= a.k) {
+            short_row<E, S, false>(a, r, n, 0, a.k);
+            continue;
+        }
+        const uint32_t t = flat_estimate<E, S>(a, r, n, hist, s_res, s_warp);
+        if (gt == 0) {
+            tkeys[r] = t;
+            __threadfence();
+            st_release_gpu(flag + r, 1u);
+        }
+    }
+    // ---- 2. the rows queued by this CTA's streaming warps
+    uint32_t head = 0;
+    while (true) {
+        if (gt == 0) {
+            uint32_t item = 0;
+            const long long t0 = clock64();
+            while (true) {
+                if (head < static_cast<uint32_t>(kFlatQueue) && s_q[head] != 0u) {
+                    item = s_q[head];
+                    break;
+                }
+                if (*s_sdone == static_cast<uint32_t>(kFlatStreamWarps)) {
+                    __threadfence_block();
+                    if (head < static_cast<uint32_t>(kFlatQueue) && s_q[head] != 0u) continue;
+                    if (*s_qtail <= head) break;  // every streaming warp is done and nothing is left
+                }
+                if (clock64() - t0 > kWaitCycles) {
+                    set_err(a.err_flag, kStatusTimeout);
+                    break;
+                }
+                __nanosleep(128);
+            }
+            s_item = item;
+        }
+        S::sync();
+        const uint32_t item = s_item;
+        S::sync();
+        if (item == 0u) break;
+        ++head;
+        __threadfence();  // the streaming warps' slots (their arrivals are ordered before the queue entry)
+        flat_select_row<E>(a, static_cast<int64_t>(item) - 1, smem, s_warp, s_res, s_cnt, s_gq, s_seg);
+    }
+}
+
+template <typename E, bool GATHER>
+__global__ void __launch_bounds__(kFlatThreads, 1) flat_kernel(const TopkArgs a)
+{
+    static_assert(!GATHER, "flat_kernel has no fused gather");
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ uint32_t s_q[kFlatQueue];
+    __shared__ uint32_t s_qtail, s_sdone;
+    for (int i = threadIdx.x; i < kFlatQueue; i += blockDim.x) s_q[i] = 0u;
+    if (threadIdx.x == 0) {
+        s_qtail = 0u;
+        s_sdone = 0u;
+    }
+    __syncthreads();
+    if (static_cast<int>(threadIdx.x) < kFlatStreamWarps * 32)
+        flat_stream<E>(a, smem, s_q, &s_qtail, &s_sdone);
+    else
+        flat_select<E>(a, smem, s_q, &s_qtail, &s_sdone);
 }
 
 // Raises a kernel's dynamic shared-memory limit once per device; later calls that need no more
@@ -2267,6 +2848,9 @@ void (*kernel_of(int mode))(TopkArgs)
         if (mode == kModeWide) return wide_kernel<E, NT, G, false>;
         if (mode == kModeWideSplit) return wide_kernel<E, NT, G, true>;
     }
+    if constexpr (NT == kFlatThreads && !G) {
+        if (mode == kModeFlat) return flat_kernel<E, false>;
+    }
     return nullptr;
 }
 
@@ -2282,6 +2866,12 @@ cudaError_t launch_one(int mode, size_t smem, const TopkArgs &a, cudaStream_t st
     if (query) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kern, NT, smem);
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (mode == kModeFlat) {
+        // every CTA must be resident: the streaming warps wait on flags other CTAs publish
+        void *args[] = {const_cast<TopkArgs *>(&a)};
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(static_cast<unsigned>(grid)),
+                                           dim3(NT), args, smem, stream);
+    }
     kern<<<dim3(static_cast<unsigned>(grid)), dim3(NT), smem, stream>>>(a);
     return cudaGetLastError();
 }
@@ -2296,6 +2886,10 @@ cudaError_t launch_e(int mode, int threads, bool gather, size_t smem, const Topk
         if (threads != 256) return cudaErrorInvalidValue;
         return gather ? launch_one<E, 256, true>(mode, smem, a, s, grid, query, blocks_per_sm)
                       : launch_one<E, 256, false>(mode, smem, a, s, grid, query, blocks_per_sm);
+    }
+    if (mode == kModeFlat) {
+        if (threads != kFlatThreads || gather) return cudaErrorInvalidValue;
+        return launch_one<E, kFlatThreads, false>(mode, smem, a, s, grid, query, blocks_per_sm);
     }
     if (mode == kModeStream || mode == kModeWide || mode == kModeWideSplit) {
         if (threads != 512) return cudaErrorInvalidValue;

@@ -246,11 +246,14 @@ SEL_API int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols
  *   sel_topk_workspace_size exceeds SEL_NOALLOC_SCRATCH_BYTES are rejected
  *   with SEL_ESCRATCH before anything is launched; use sel_topk with a
  *   workspace for those.
+ *   Argument errors (SEL_EINVAL, SEL_EALIGN) are reported before SEL_ESCRATCH.
  *   The scratch is one file-scope device array per GPU, loaded with the
  *   library and held until the process exits; nothing is allocated by the
- *   call.  The first call on each device that needs scratch looks up the
- *   array's device address (with that device current); make that first call
- *   before any stream capture.
+ *   call.  The array's device address is looked up (with the device current)
+ *   on every call whose stream is not capturing a graph, so a device reset
+ *   or another current context is picked up; a call made while `stream`
+ *   captures reuses the address the last non-capturing call on that device
+ *   found.  So after a device reset make one ordinary call before capturing.
  *   Every call shares the array and it keeps the previous call's contents:
  *   the counters that must start at zero are cleared on `stream` by each call.
  *   Calls that overlap on the GPU (other streams, other host threads) race on

@@ -25,3 +25,13 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture
+def tuning():
+    """set_tuning for one test: forces a kernel plan (plan="wide", parts=7, ...) and puts every
+    knob back afterwards."""
+    import gather_radix_select_gb300 as g
+    saved = g.get_tuning()
+    yield g.set_tuning
+    g.set_tuning(**saved)

@@ -1,7 +1,8 @@
 """The C-ABI library without a GPU: it builds, loads, exports every symbol
-include/sel.h declares, and rejects bad arguments on the host before any
-CUDA call is made."""
+the headers under include/ declare, and rejects bad arguments on the host
+before any CUDA call is made."""
 import ctypes
+import glob
 import os
 import re
 
@@ -17,16 +18,40 @@ def lib():
 
 
 def declared_symbols():
-    text = open(os.path.join(ROOT, "include", "sel.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(sel_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(sel_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
     assert declared_symbols() == sorted(["sel_block_topk_gather", "sel_gather_rows", "sel_gather_rows_pair",
                                          "sel_max_cols", "sel_stride_requirement",
                                          "sel_strerror", "sel_topk", "sel_topk_gather", "sel_topk_kernel_name",
-                                         "sel_topk_noalloc", "sel_topk_workspace_size"])
+                                         "sel_topk_noalloc", "sel_topk_workspace_size", "sel_set_tuning",
+                                         "sel_get_tuning"])
+
+
+def test_tuning_knobs_round_trip_and_reject_bad_values(lib):
+    # host-only: the knobs are plain process state, no CUDA call is made
+    import gather_radix_select_gb300 as g
+    saved = g.get_tuning()
+    try:
+        for plan in ("reg", "row", "wide", "split", "stream", "flat", "auto"):
+            g.set_tuning(plan=plan)
+            assert g.get_tuning()["plan"] == plan
+        g.set_tuning(parts=7, row_sample=True, hist_agg=True)
+        assert g.get_tuning() == {"plan": "auto", "parts": 7, "row_sample": True, "hist_agg": True}
+        SEL_EINVAL = 1
+        assert lib.sel_set_tuning(0, 99) == SEL_EINVAL   # no such plan
+        assert lib.sel_set_tuning(0, -2) == SEL_EINVAL
+        assert lib.sel_set_tuning(1, -1) == SEL_EINVAL   # negative parts
+        assert lib.sel_set_tuning(42, 0) == SEL_EINVAL   # no such knob
+        assert lib.sel_get_tuning(42) == -1
+        assert g.get_tuning()["parts"] == 7              # a refused value changes nothing
+    finally:
+        g.set_tuning(**saved)
 
 
 def test_every_declared_symbol_is_exported(lib):

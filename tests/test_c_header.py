@@ -11,6 +11,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PROGRAM = r"""
 #include <stdio.h>
 #include "sel.h"
+#include "sel_tuning.h"
 
 int main(void)
 {
@@ -29,6 +30,13 @@ int main(void)
     if (sel_block_topk_gather(x, SEL_F32, 1, 16, 16, NULL, 4, 0, idx, 16, NULL, 1, 0, 0, 0, 0, NULL, NULL, 0,
                               NULL, NULL, NULL) != SEL_EINVAL) return 6;  /* block_size 0 */
     if (sel_max_cols(SEL_BF16) <= 0 || sel_topk_workspace_size(7, 1, 16, 4) != 0) return 7;
+    /* the tuning knobs: set, read back, restore */
+    {
+        const int plan = sel_get_tuning(SEL_TUNE_PLAN);
+        if (sel_set_tuning(SEL_TUNE_PLAN, SEL_PLAN_FLAT) != SEL_OK || sel_get_tuning(SEL_TUNE_PLAN) != SEL_PLAN_FLAT)
+            return 8;
+        if (sel_set_tuning(SEL_TUNE_PLAN, plan) != SEL_OK || sel_set_tuning(99, 0) != SEL_EINVAL) return 9;
+    }
     printf("%s\n", sel_strerror(SEL_EALIGN));
     return 0;
 }

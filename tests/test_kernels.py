@@ -32,7 +32,7 @@ CASES = [
     ("f32", 4, 131072, 4096, "normal"),
 ]
 
-MODES = ["wide", "split", "stream"]
+MODES = ["wide", "split", "stream", "flat"]
 
 # shapes the register-resident kernel holds (bf16 up to 32768 columns, fp32 up to 16384): every
 # tile size, ragged tails ending inside a vector, ties, infinities and near-full selections
@@ -50,8 +50,8 @@ REG_CASES = [
 
 
 @pytest.mark.parametrize("case", REG_CASES, ids=lambda c: "-".join(map(str, c)))
-def test_reg_kernel(case, monkeypatch):
-    monkeypatch.setenv("SEL_PLAN", "reg")
+def test_reg_kernel(case, tuning):
+    tuning(plan="reg")
     import gather_radix_select_gb300 as g
     dtype, rows, cols, k, kind = case
     assert g.kernel_name(torch.float32 if dtype == "f32" else torch.bfloat16, rows, cols, k) == "reg_kernel"
@@ -73,8 +73,8 @@ def padded(dtype, rows, cols, k, kind, row_end=None):
 
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
-def test_forced_kernel(mode, case, monkeypatch):
-    monkeypatch.setenv("SEL_PLAN", mode)
+def test_forced_kernel(mode, case, tuning):
+    tuning(plan=mode)
     dtype, rows, cols, k, kind = case
     w = padded(*case)
     x, end, vals, idx, nan, err = run(w)
@@ -86,11 +86,11 @@ def test_forced_kernel(mode, case, monkeypatch):
 
 
 @pytest.mark.parametrize("parts", ["1", "2", "7", "64"])
-def test_wide_parts(parts, monkeypatch):
+def test_wide_parts(parts, tuning):
     # the streaming kernel on one CTA per row, and with rows split over CTAs whose candidate lists
     # meet in the workspace (the last part to arrive merges)
-    monkeypatch.setenv("SEL_PLAN", "wide")
-    monkeypatch.setenv("SEL_PARTS", parts)
+    tuning(plan="wide")
+    tuning(parts=int(parts))
     for case in (("f32", 3, 131075, 4096, "normal"), ("bf16", 2, 204803, 1024, "levels"),
                  ("f32", 2, 70001, 100, "descending"), ("bf16", 3, 100000, 3000, "zeros_inf")):
         w = padded(*case)
@@ -115,8 +115,8 @@ WIDE_CASES = [
 
 
 @pytest.mark.parametrize("case", WIDE_CASES, ids=lambda c: "-".join(map(str, c)))
-def test_wide_kernel_paths(case, monkeypatch):
-    monkeypatch.setenv("SEL_PLAN", "wide")
+def test_wide_kernel_paths(case, tuning):
+    tuning(plan="wide")
     w = padded(*case)
     x, end, vals, idx, nan, err = run(w)
     assert err == 0 and nan == 0
@@ -127,8 +127,8 @@ def test_wide_kernel_paths(case, monkeypatch):
 
 
 @pytest.mark.parametrize("mode", MODES + ["reg"])
-def test_forced_row_end_and_nan(mode, monkeypatch):
-    monkeypatch.setenv("SEL_PLAN", mode)
+def test_forced_row_end_and_nan(mode, tuning):
+    tuning(plan=mode)
     rows, cols, k = 6, (12000 if mode == "reg" else 90000), 2000
     row_end = np.array([0, 1999, 2000, 2001, cols // 2, 200000], dtype=np.int32)
     w = padded("f32", rows, cols, k, "normal", row_end=row_end)
@@ -149,8 +149,8 @@ def test_forced_row_end_and_nan(mode, monkeypatch):
 
 
 @pytest.mark.parametrize("mode", MODES + ["reg"])
-def test_forced_fused_gather(mode, monkeypatch):
-    monkeypatch.setenv("SEL_PLAN", mode)
+def test_forced_fused_gather(mode, tuning):
+    tuning(plan=mode)
     import gather_radix_select_gb300 as g
     rng = np.random.default_rng(5)
     b, rows, cols, k, ng, d = 2, 4, (30000 if mode == "reg" else 150000), 1024, 700, 64
@@ -172,11 +172,11 @@ def test_forced_fused_gather(mode, monkeypatch):
 
 @pytest.mark.parametrize("mode", ["reg", "row", "wide"])
 @pytest.mark.parametrize("d", [48, 200, 512, 2048])
-def test_fused_gather_row_widths(mode, d, monkeypatch):
+def test_fused_gather_row_widths(mode, d, tuning):
     # key rows of 6, 25, 64 and 256 16-byte vectors: the general copy loop (not a power of two, or
     # wider than the CTA) and the per-column one; the last case has a key shorter than the scored
     # row, so some selected positions are out of range (zero rows, error flag)
-    monkeypatch.setenv("SEL_PLAN", mode)
+    tuning(plan=mode)
     import gather_radix_select_gb300 as g
     rng = np.random.default_rng(d)
     b, rows, k, ng = 2, 6, 300, 200

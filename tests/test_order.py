@@ -71,9 +71,9 @@ KERNEL_CASES = [
 
 
 @pytest.mark.parametrize("c", KERNEL_CASES, ids=lambda c: "-".join(map(str, c)))
-def test_value_order_each_kernel(c, monkeypatch):
+def test_value_order_each_kernel(c, tuning):
     plan, dtype, rows, cols, k, kind = c
-    monkeypatch.setenv("SEL_PLAN", plan)
+    tuning(plan=plan)
     w = case(dtype, rows, cols, k, kind)
     for idx_dtype, want_values in (("i32", True), ("i64", False)):
         x, vals, idx, nan, err = run_value_order(w, idx_dtype, want_values)

@@ -34,19 +34,25 @@ def padded(rows, k, dtype):
 
 
 def run_both(x, dtype_code, rows, cols, k, idx_dtype, want_values, row_end=None, sorted_index=1):
-    """sel_topk with a fresh workspace, then sel_topk_noalloc twice; returns the three results."""
+    """sel_topk with a fresh workspace, then sel_topk_noalloc twice, with a no-alloc call on other
+    data (the rows negated) in between, so that the second compared call finds the array holding
+    another input's candidates.  Returns the scratch size and the three compared results."""
+    from gather_radix_select_gb300 import _native
     L = lib()
     itype = torch.int64 if idx_dtype == 1 else torch.int32
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     need = L.sel_topk_workspace_size(dtype_code, rows, cols, k)
+    assert need <= _native.SEL_NOALLOC_SCRATCH_BYTES
     ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
+    other = -x
     results = []
-    for mode in ("workspace", "noalloc", "noalloc"):
+    for mode in ("workspace", "noalloc", "noalloc-other", "noalloc"):
+        src = other if mode == "noalloc-other" else x
         idx = padded(rows, k, itype)
         val = padded(rows, k, x.dtype) if want_values else None
         nan = torch.zeros(1, dtype=torch.int32, device="cuda")
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        common = (ptr(x), dtype_code, rows, cols, x.stride(0), ptr(row_end), k, sorted_index, idx_dtype,
+        common = (ptr(src), dtype_code, rows, cols, src.stride(0), ptr(row_end), k, sorted_index, idx_dtype,
                   int(want_values), ptr(idx), idx.stride(0), ptr(val), 0 if val is None else val.stride(0))
         if mode == "workspace":
             st = L.sel_topk(*common, ptr(ws), ws.numel(), ptr(nan), ptr(err), stream)
@@ -54,8 +60,9 @@ def run_both(x, dtype_code, rows, cols, k, idx_dtype, want_values, row_end=None,
             st = L.sel_topk_noalloc(*common, ptr(nan), ptr(err), stream)
         assert st == 0, L.sel_strerror(st)
         torch.cuda.synchronize()
-        results.append((idx[:, :k].cpu(), None if val is None else val[:, :k].cpu(), int(nan.item()),
-                        int(err.item())))
+        if mode != "noalloc-other":
+            results.append((idx[:, :k].cpu(), None if val is None else val[:, :k].cpu(), int(nan.item()),
+                            int(err.item())))
     return need, results
 
 
@@ -69,19 +76,37 @@ def same(a, b):
     assert na == nb and ea == eb == 0
 
 
-def test_noalloc_matches_workspace_entry_point_on_split_rows(monkeypatch):
+def test_noalloc_matches_workspace_entry_point_on_split_rows(tuning):
     # four 204800-wide bf16 rows split over many CTAs (forced), so the scratch is really used
-    monkeypatch.setenv("SEL_PLAN", "split")
+    tuning(plan="split")
     w = syn.workload("indexer_bf16_4x204800_k1024")
     x = torch.from_numpy(w["x"].view(np.int16)).view(torch.bfloat16).cuda()
     need, res = run_both(x, 1, w["rows"], w["cols"], w["k"], 0, True)
-    assert 0 < need <= lib().sel_topk_workspace_size(1, w["rows"], w["cols"], w["k"])
+    assert need > 0
     same(res[0], res[1])
     same(res[0], res[2])
 
 
-def test_noalloc_matches_on_fp32_split_rows_with_row_end_and_nan(monkeypatch):
-    monkeypatch.setenv("SEL_PLAN", "split")
+def test_noalloc_on_the_default_plan_of_few_wide_rows():
+    # no forced plan: four 204800-wide bf16 rows are split over many CTAs whose candidate lists
+    # meet in the scratch
+    import oracle
+    import gather_radix_select_gb300 as g
+    w = syn.workload("indexer_bf16_4x204800_k1024")
+    assert g.kernel_name(torch.bfloat16, w["rows"], w["cols"], w["k"]) in ("wide_kernel", "flat_kernel")
+    x = torch.from_numpy(w["x"].view(np.int16)).view(torch.bfloat16).cuda()
+    need, res = run_both(x, 1, w["rows"], w["cols"], w["k"], 0, True)
+    assert need > 0
+    same(res[0], res[1])
+    same(res[0], res[2])
+    o_idx, o_bits, _ = oracle.topk(w["x"], "bf16", w["k"], sorted_index=True)
+    assert (res[1][0].numpy() == o_idx).all()
+    assert (res[1][1].view(torch.int16).numpy().view(np.uint16) == o_bits).all()
+
+
+@pytest.mark.parametrize("plan", ["split", "flat"])
+def test_noalloc_matches_on_fp32_split_rows_with_row_end_and_nan(plan, tuning):
+    tuning(plan=plan)
     rng = np.random.default_rng(31)
     rows, cols, k = 6, 131072, 4096
     v = (rng.standard_normal((rows, cols)) * 2).astype(np.float32)
@@ -95,9 +120,9 @@ def test_noalloc_matches_on_fp32_split_rows_with_row_end_and_nan(monkeypatch):
     assert res[0][2] == 1
 
 
-def test_noalloc_value_order(monkeypatch):
+def test_noalloc_value_order(tuning):
     # value-ordered output through the no-workspace entry point, on split rows
-    monkeypatch.setenv("SEL_PLAN", "split")
+    tuning(plan="split")
     import oracle
     w = syn.workload("indexer_bf16_4x204800_k1024")
     x = torch.from_numpy(w["x"].view(np.int16)).view(torch.bfloat16).cuda()
@@ -110,7 +135,7 @@ def test_noalloc_value_order(monkeypatch):
     assert (res[1][1].view(torch.int16).numpy().view(np.uint16) == o_bits).all()
 
 
-def test_noalloc_without_scratch_and_oversize_rejection(monkeypatch):
+def test_noalloc_without_scratch_and_oversize_rejection(tuning):
     # a shape that needs no scratch runs too
     rng = np.random.default_rng(5)
     x = torch.from_numpy(rng.standard_normal((300, 2048)).astype(np.float32)).cuda()
@@ -119,7 +144,7 @@ def test_noalloc_without_scratch_and_oversize_rejection(monkeypatch):
     same(res[0], res[1])
     same(res[0], res[2])
     # a shape whose scratch exceeds the built-in array is refused before any launch
-    monkeypatch.setenv("SEL_PLAN", "split")
+    tuning(plan="split")
     L = lib()
     from gather_radix_select_gb300 import _native
     rows, cols = 300, 2_000_000
