@@ -272,47 +272,51 @@ size_t layout_wide(int64_t cap, bool gather, int64_t n_gather, sel::TopkArgs &a)
 bool plan_flat(int dtype, int64_t rows, int64_t cols, int k, int sms, size_t limit, Plan &fp)
 {
     sel::TopkArgs &a = fp.layout;
+    constexpr int SW = sel::kFlatStreamWarps;
     const int64_t e = elem_bytes(dtype);
     const int64_t V = 16 / e;
     const int64_t nvr = cols * e / 16;
     if (nvr < 1 || sms < 1 || cols > 0x7fffffffLL) return false;
     int64_t cv = std::min(kFlatChunkMaxVecs, std::max(kFlatChunkMinVecs, ceil_div(rows * nvr, sms)));
-    cv = std::max(cv, ceil_div(nvr, sel::kFlatMaxSlots / sel::kFlatStreamWarps));  // slots of a row bounded
+    cv = std::max(cv, ceil_div(nvr, sel::kFlatMaxParts));  // chunks of a row bounded
     const int64_t cpr = ceil_div(nvr, cv);
     cv = ceil_div(nvr, cpr);
-    if (cpr * sel::kFlatStreamWarps > sel::kFlatMaxSlots) return false;
-    if (ceil_div(rows * cpr, sms) > sel::kFlatQueue) return false;
+    if (cpr > sel::kFlatMaxParts || ceil_div(rows * cpr, sms) > sel::kFlatQueue) return false;
     const double m = static_cast<double>(std::min<int64_t>(nvr, sel::kFlatSampleVecs) * V);
     const double mu = static_cast<double>(k) * m / static_cast<double>(cols);
     const double kept = mu * 1.125 + 3.0 * std::sqrt(mu) + 4.0;
     const double frac = std::min(1.0, (kept + 4.0 * std::sqrt(kept)) / m);
-    const double ew = static_cast<double>(ceil_div(cv, sel::kFlatStreamWarps) * V);  // one warp's share of a chunk
-    const int64_t part_cap =
-        std::min<int64_t>(static_cast<int64_t>(ew) + 2 * V,
-                          static_cast<int64_t>(ew * frac + 4.0 * std::sqrt(ew * frac) + 16.0) + V);
+    const double ew = static_cast<double>(ceil_div(cv, SW) * V);  // one streaming warp's share of a chunk
+    const int64_t wcap = std::min<int64_t>(static_cast<int64_t>(ew) + 2 * V,
+                                           static_cast<int64_t>(ew * frac + 4.0 * std::sqrt(ew * frac) + 16.0) + V);
     const double cf = static_cast<double>(cols) * frac;
     const int64_t total_cap = std::min<int64_t>(round_up(cols, 8), static_cast<int64_t>(cf + 4.0 * std::sqrt(cf)) + 64);
-    const int64_t capw = ceil_div(total_cap, sel::kFlatSelWarps) + 16;
+    const int64_t rs8 = round_up(ceil_div(total_cap, sel::kFlatSelWarps) + 17, 2);  // a region and its spare pair
     a.hist_bins = std::max(a.hist_bins, kWideHistBins);
     a.slice = cv;
     a.parts = static_cast<int32_t>(cpr);
-    a.part_cap = static_cast<int32_t>(part_cap);
-    a.list_cap = static_cast<int32_t>(capw);
-    a.region_stride = static_cast<int32_t>(round_up(capw + 1, 2));
+    a.flat_wcap = static_cast<int32_t>(wcap);
+    a.part_cap = static_cast<int32_t>(SW * wcap);  // a chunk's slot: every warp's region, concatenated
+    a.flat_sel_pairs = static_cast<int32_t>(sel::kFlatSelWarps * rs8);
+    a.list_cap = 0;
+    a.region_stride = 0;
     a.smem_buf_bytes = 0;
-    a.smem_hist_off = 0;
     a.smem_mask_off = 0;
+    a.smem_hist_off = 0;
     size_t off = static_cast<size_t>(a.hist_bins) * 4;
     a.smem_list_off = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(sel::kFlatSelWarps) * static_cast<size_t>(a.region_stride) * 8;
+    off += static_cast<size_t>(a.flat_sel_pairs) * 8;
     off = static_cast<size_t>(round_up(static_cast<int64_t>(off), 16));
     a.smem_glist_off = static_cast<uint32_t>(off);
     a.smem_stage_off = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(sel::kFlatStreamWarps) * sel::kWideStage * (16 + 4);
+    off += static_cast<size_t>(SW) * sel::kWideStage * (16 + 4);
+    off = static_cast<size_t>(round_up(static_cast<int64_t>(off), 16));
+    a.smem_cbuf_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(sel::kFlatBufs) * SW * static_cast<size_t>(wcap + 1) * 8;
     if (off > limit || cached_blocks_per_sm(dtype, sel::kModeFlat, sel::kFlatThreads, false, off) < 1) return false;
     a.ws_counter_bytes = round_up(3 * rows * 4, 256);
-    a.ws_part_bytes = round_up(16 + (part_cap + 1) * 8, 16);
-    a.ws_row_bytes = cpr * sel::kFlatStreamWarps * a.ws_part_bytes;
+    a.ws_part_bytes = round_up(16 + SW * wcap * 8, 16);
+    a.ws_row_bytes = cpr * a.ws_part_bytes;
     fp.mode = sel::kModeFlat;
     fp.threads = sel::kFlatThreads;
     fp.smem = off;

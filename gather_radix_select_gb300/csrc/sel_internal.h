@@ -26,12 +26,13 @@ constexpr int kModeReg8 = 5;        // reg_kernel: 8 vectors a thread
 constexpr int kModeWideSplit = 6;   // wide_kernel over `parts` CTAs per row, last-arriver merge
 constexpr int kModeFlat = 7;        // flat_kernel: rows cut into chunks dealt over a persistent grid
 constexpr int kNumModes = 8;
-// flat_kernel: warps 0..15 stream, warps 16..23 estimate thresholds and select
-constexpr int kFlatStreamWarps = 16;
+// flat_kernel: warps 0..23 stream, warps 24..31 estimate thresholds, flush chunks and select
+constexpr int kFlatStreamWarps = 24;
 constexpr int kFlatSelWarps = 8;
 constexpr int kFlatThreads = (kFlatStreamWarps + kFlatSelWarps) * 32;
-constexpr int kFlatQueue = 64;        // chunks of one CTA at most (each can queue one row)
-constexpr int kFlatMaxSlots = 1024;   // (chunk, streaming warp) slots of one row at most
+constexpr int kFlatQueue = 64;        // chunks of one CTA at most
+constexpr int kFlatMaxParts = 64;     // chunks of one row at most
+constexpr int kFlatBufs = 3;          // chunk buffers in shared memory, in rotation
 constexpr int kFlatSampleVecs = 1024; // row sample for the threshold estimate: 32 runs of 32 vectors
 constexpr int kGatherThreads = 256;
 
@@ -60,7 +61,10 @@ struct TopkArgs {
     uint32_t smem_mask_off;   // offset of the per-vector candidate masks (one byte per 16-byte vector)
     uint32_t smem_list_off;   // offset of the candidate list (16-bit offsets within the slice)
     uint32_t smem_glist_off;  // offset of the gather position list (fused only)
-    uint32_t smem_stage_off;  // wide_kernel: staged candidate vectors
+    uint32_t smem_stage_off;  // wide_kernel, flat_kernel: staged candidate vectors
+    uint32_t smem_cbuf_off;   // flat_kernel: chunk buffers
+    int32_t flat_wcap;        // flat_kernel: pairs one streaming warp may keep of one chunk
+    int32_t flat_sel_pairs;   // flat_kernel: pairs the selection regions hold in all
     int32_t list_cap;         // capacity of the candidate list
     int32_t region_stride;    // wide_kernel: candidate pairs per warp region (capacity list_cap + 1)
     int32_t part_cap;         // wide_kernel over parts: candidate pairs a part may leave in the workspace;

@@ -7,7 +7,7 @@
 // (ties: smaller column first), or, when n <= k, every valid column followed
 // by fills (index -1, value -inf).  Rows with n > k are checked for NaN.
 //
-// Five kernels, chosen per launch by the host plan:
+// Six kernels, chosen per launch by the host plan:
 //   reg_kernel    one CTA per row of at most 16 KB; the row is held in
 //                 registers (a contiguous run of vectors per thread) and the
 //                 radix levels run from there.
@@ -26,6 +26,10 @@
 //                 the k from the merged candidates.
 //   stream_kernel one CTA per row, the row read from global memory on every
 //                 radix pass (the exact fallback of the others).
+//   flat_kernel   rows cut into chunks dealt over one resident CTA per SM;
+//                 streaming warps filter, helper warps estimate, flush and
+//                 select (reached only when forced: measured slower, see the
+//                 kernel's comment).
 //
 // Building blocks (GB300 design):
 //   * Staged slices (row_kernel, split_kernel) arrive in shared memory by bulk
@@ -133,12 +137,6 @@ struct Elem<uint32_t> {  // fp32 bit patterns
         smax = static_cast<uint32_t>(max(static_cast<int>(smax), m));
         umax = max(umax, max(max(q.x, q.y), max(q.z, q.w)));
     }
-    // Only the negative-NaN half of nan_acc: enough where every positive NaN passes the filter
-    // (a positive threshold) and is checked among the candidates.
-    static __device__ __forceinline__ void nan_acc_neg(const uint4 &q, uint32_t &umax)
-    {
-        umax = max(umax, max(max(q.x, q.y), max(q.z, q.w)));
-    }
     static __device__ __forceinline__ void nan_acc1(uint32_t u, uint32_t &smax, uint32_t &umax)
     {
         smax = static_cast<uint32_t>(max(static_cast<int>(smax), static_cast<int>(u)));
@@ -147,12 +145,6 @@ struct Elem<uint32_t> {  // fp32 bit patterns
     static __device__ __forceinline__ bool has_nan(uint32_t smax, uint32_t umax)
     {
         return static_cast<int>(smax) > 0x7f800000 || umax > 0xff800000u;
-    }
-    // Whether some element's key is >= tkey, for a threshold above +/-0 (ts = tkey ^ kSignKey).
-    static __device__ __forceinline__ bool any_ge_raw(const uint4 &q, uint32_t ts)
-    {
-        return max(max(static_cast<int>(q.x), static_cast<int>(q.y)), max(static_cast<int>(q.z), static_cast<int>(q.w))) >=
-               static_cast<int>(ts);
     }
     // As ge_mask_positive, without the magnitude.
     static __device__ __forceinline__ uint32_t ge_mask_raw(const uint4 &q, uint32_t ts)
@@ -182,6 +174,25 @@ struct Elem<uint32_t> {  // fp32 bit patterns
         e[3] = q.w;
     }
     static __device__ __forceinline__ uint4 pack(const uint32_t (&e)[4]) { return make_uint4(e[0], e[1], e[2], e[3]); }
+    // Streaming test with running maxima: smax_vec = signed maximum of a vector's raw words; a
+    // vector holds a key >= tkey (threshold above +/-0, ts = tkey ^ kSignKey) iff ge_raw(smax_vec,
+    // ts).  smax_fold / umax_fold keep the running signed / unsigned maxima that has_nan reads;
+    // smax_key is the key of the largest element folded into a running signed maximum.
+    static __device__ __forceinline__ uint32_t smax_vec(const uint4 &q)
+    {
+        return static_cast<uint32_t>(max(__vimax3_s32(static_cast<int>(q.x), static_cast<int>(q.y), static_cast<int>(q.z)),
+                                         static_cast<int>(q.w)));
+    }
+    static __device__ __forceinline__ uint32_t smax_fold(uint32_t s, uint32_t ms)
+    {
+        return static_cast<uint32_t>(max(static_cast<int>(s), static_cast<int>(ms)));
+    }
+    static __device__ __forceinline__ uint32_t umax_fold(uint32_t u, const uint4 &q)
+    {
+        return __vimax3_u32(u, __vimax3_u32(q.x, q.y, q.z), q.w);
+    }
+    static __device__ __forceinline__ bool ge_raw(uint32_t ms, uint32_t ts) { return static_cast<int>(ms) >= static_cast<int>(ts); }
+    static __device__ __forceinline__ uint32_t smax_key(uint32_t s) { return key(s); }
 };
 
 template <>
@@ -222,10 +233,6 @@ struct Elem<uint16_t> {  // bf16 bit patterns
         smax = __vmaxs2(smax, __vmaxs2(__vmaxs2(q.x, q.y), __vmaxs2(q.z, q.w)));
         umax = __vmaxu2(umax, __vmaxu2(__vmaxu2(q.x, q.y), __vmaxu2(q.z, q.w)));
     }
-    static __device__ __forceinline__ void nan_acc_neg(const uint4 &q, uint32_t &umax)
-    {
-        umax = __vmaxu2(umax, __vmaxu2(__vmaxu2(q.x, q.y), __vmaxu2(q.z, q.w)));
-    }
     static __device__ __forceinline__ void nan_acc1(uint16_t h, uint32_t &smax, uint32_t &umax)
     {
         smax = __vmaxs2(smax, static_cast<uint32_t>(h) | 0x80000000u);  // other half: the signed minimum
@@ -235,12 +242,6 @@ struct Elem<uint16_t> {  // bf16 bit patterns
     {
         return static_cast<int16_t>(smax & 0xffffu) > 0x7f80 || static_cast<int16_t>(smax >> 16) > 0x7f80 ||
                (umax & 0xffffu) > 0xff80u || (umax >> 16) > 0xff80u;
-    }
-    static __device__ __forceinline__ bool any_ge_raw(const uint4 &q, uint32_t ts)
-    {
-        const uint32_t m = __vmaxs2(__vmaxs2(q.x, q.y), __vmaxs2(q.z, q.w));
-        const int t = static_cast<int>(ts << 16);
-        return static_cast<int>(m << 16) >= t || static_cast<int>(m & 0xffff0000u) >= t;
     }
     static __device__ __forceinline__ uint32_t ge_mask_raw(const uint4 &q, uint32_t ts)
     {
@@ -288,6 +289,23 @@ struct Elem<uint16_t> {  // bf16 bit patterns
         return make_uint4(e[0] | (static_cast<uint32_t>(e[1]) << 16), e[2] | (static_cast<uint32_t>(e[3]) << 16),
                           e[4] | (static_cast<uint32_t>(e[5]) << 16), e[6] | (static_cast<uint32_t>(e[7]) << 16));
     }
+    // As for fp32, on the two 16-bit halves of each word (packed per-half maxima).
+    static __device__ __forceinline__ uint32_t smax_vec(const uint4 &q) { return __vmaxs2(__vimax3_s16x2(q.x, q.y, q.z), q.w); }
+    static __device__ __forceinline__ uint32_t smax_fold(uint32_t s, uint32_t ms) { return __vmaxs2(s, ms); }
+    static __device__ __forceinline__ uint32_t umax_fold(uint32_t u, const uint4 &q)
+    {
+        return __vimax3_u16x2(u, __vimax3_u16x2(q.x, q.y, q.z), q.w);
+    }
+    static __device__ __forceinline__ bool ge_raw(uint32_t ms, uint32_t ts)
+    {
+        const int t = static_cast<int>(ts << 16);
+        return static_cast<int>(ms << 16) >= t || static_cast<int>(ms & 0xffff0000u) >= t;
+    }
+    static __device__ __forceinline__ uint32_t smax_key(uint32_t s)
+    {
+        const int16_t lo = static_cast<int16_t>(s & 0xffffu), hi = static_cast<int16_t>(s >> 16);
+        return key(static_cast<uint16_t>(lo > hi ? lo : hi));
+    }
 };
 
 __device__ __forceinline__ void set_err(int32_t *flag, int32_t code)
@@ -308,6 +326,12 @@ __device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, int32
             return;
         }
     }
+}
+
+// Prefetches [p, p + bytes) into L2 (p and bytes multiples of 16); no registers held, nothing waited for.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Warp-aggregated shared histogram increment: lanes with equal digits are grouped with
@@ -1715,7 +1739,10 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) stream_kernel(const 
 //     range of the row's vectors with kWideUnroll coalesced 128-bit loads in
 //     flight per lane and appends the (key bits, column) pairs at or above
 //     the estimate to its own region of the candidate list, in column order.
-//     No block-wide synchronisation while streaming.
+//     Each vector costs two three-way maxima and one ballot on the usual
+//     (positive threshold) path; the running maxima also give the largest
+//     candidate key and the NaN check.  No block-wide synchronisation while
+//     streaming.
 //  3. Exact selection on the regions (select_regions), using the largest
 //     candidate key, tracked while streaming, to scale its digits.
 //  Too few candidates, or a region overflowing, falls back to exact passes
@@ -2068,8 +2095,8 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
     const uint32_t tsg = tkey ^ T::kSignKey;
     uint32_t smax = T::kSmaxInit, umax = T::kUmaxInit;
     uint32_t off = 0;   // pairs appended to this warp's region (warp-uniform)
-    uint32_t kmax = 0;  // largest candidate key seen by this lane
-    // a positive NaN among the candidates; an estimate above the +inf key came from a sampled NaN
+    uint32_t kmax = 0;  // largest candidate key seen by this lane (kept per key off the raw-compare path)
+    // an estimate above the +inf key came from a sampled NaN
     bool pnan = tkey > T::key(static_cast<E>(T::kInfMagnitude));
     // Vectors holding a candidate are staged (16-byte vector + its first column, in column order)
     // in the warp's buffer of kStage entries, and expanded into (key, column) pairs a full
@@ -2095,8 +2122,10 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
                 const int t = __ffs(m) - 1;
                 m &= m - 1u;
                 const E e = T::lane_of(v, t);
-                kmax = max(kmax, T::key(e));
-                pnan |= T::is_nan(e);
+                if (!positive) {
+                    kmax = max(kmax, T::key(e));
+                    pnan |= T::is_nan(e);
+                }
                 reg[p < capw ? p : capw] = make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(cb + t));
                 ++p;
             }
@@ -2122,10 +2151,12 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
         for (int u = 0; u < U; ++u) {
             bool any;
             if (positive) {
-                // zero vectors past the range select nothing and are NaN-free; a positive NaN
-                // always passes, so only negative NaNs need the running maximum
-                T::nan_acc_neg(q[u], umax);
-                any = T::any_ge_raw(q[u], tsg);
+                // zero vectors past the range select nothing and are NaN-free; the running signed /
+                // unsigned maxima give the largest key and the NaN check at the end
+                const uint32_t ms = T::smax_vec(q[u]);
+                smax = T::smax_fold(smax, ms);
+                umax = T::umax_fold(umax, q[u]);
+                any = T::ge_raw(ms, tsg);
             } else {
                 T::nan_acc(q[u], smax, umax);
                 any = base + u * 32 + lane < ve && T::ge_mask_key(q[u], tkey) != 0u;
@@ -2157,6 +2188,10 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
             reg[p < capw ? p : capw] = make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(j));
         }
         off += __popc(bp);
+    }
+    if (positive) {  // the largest element, when it passes, is the largest candidate
+        const uint32_t lk = T::smax_key(smax);
+        kmax = max(kmax, lk >= tkey ? lk : 0u);
     }
     kmax = __reduce_max_sync(kFull, kmax);
     if (lane == 0) {
@@ -2275,49 +2310,64 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
 // ---------------------------------------------------------------------------
 // flat_kernel: wide rows spread evenly over a persistent grid of one CTA per
 // SM (a cooperative launch, so every CTA is resident and the bounded waits
-// below on other CTAs' flags always end).
+// below on flags other CTAs publish always end).
 //
 // Work split.  Each row's 16-byte vectors are cut into `parts` chunks of at
 // most `slice` vectors; chunk q (row q / parts, index q % parts) belongs to
-// CTA q mod grid.  At any moment the whole GPU works on a band of
-// consecutive rows, so rows finish one after another over the launch
-// instead of all at its end, and every SM moves the same number of bytes.
+// CTA q mod grid, which takes its chunks in order.  At any moment the whole
+// GPU works on a band of consecutive rows, so rows finish one after another
+// over the launch instead of all at its end, and every SM moves the same
+// number of bytes.
 //
-// Streaming warps (0..15) never synchronise with one another.  For each of
-// its CTA's chunks, warp w reads its 1/16 of the chunk with two sets of
-// kFlatU 16-byte loads per lane in flight (the next set, possibly of the
-// next chunk, is issued before the current one is examined), keeps the keys
-// at or above the row's threshold estimate, and writes them as (key bits,
-// column) pairs, in column order, to its own slot of the workspace.  The
-// slot's header takes the count and the largest key.  Then it bumps the
-// row's arrival counter; the warp that arrives last queues the row for its
-// own CTA's selection warps.
+// Streaming warps (0..23) do nothing but read and filter.  For each chunk of
+// its CTA, warp w reads its 1/24 of the chunk (four coalesced 16-byte loads a
+// lane in flight), tests every vector against the row's threshold estimate
+// with two three-way maxima and one ballot, stages the passing vectors, and
+// expands them (one ballot per element position gives every key its place)
+// into its region of one of kFlatBufs chunk buffers in shared memory, in
+// column order.  It then posts its count and largest key and bumps the
+// buffer's completion counter.  It waits (in shared memory, bounded) only
+// for the chunk's threshold and for a free buffer.
 //
-// Selection warps (16..23, a group on named barrier 1) first compute the
-// threshold estimates of the rows this CTA is designated for (row r: CTA
-// r mod grid) from a sample of 32 runs of 32 vectors spread over the row,
-// and publish each through a flag in the workspace; the streaming warps of
-// every CTA wait for that flag (bounded) before examining a chunk of the
-// row.  Rows with n <= k get their fills here and are skipped by the
-// streaming warps.  Then the selection warps take the queued rows: the
-// row's slots are copied into shared-memory regions (one per selection
-// warp, in column order) and select_regions picks the k.  A slot that
-// overflowed, or fewer than k candidates, falls back to exact passes over
-// the row in global memory.
+// Helper warps (24..31, a group on named barrier 1):
+//   1. compute the threshold estimates of the rows this CTA is designated for
+//      (row r: CTA r mod grid; rows needed in the first round first) from a
+//      sample of 32 runs of 32 vectors spread over the row, and publish each
+//      through a flag in the workspace; rows with n <= k get their fills here
+//      (the streaming warps skip them);
+//   2. copy each chunk's threshold from the workspace into shared memory
+//      ahead of the streaming warps;
+//   3. flush each finished chunk: the 24 regions, concatenated in column
+//      order, go to the chunk's slot in the workspace with a header (count,
+//      largest key, NaN seen), then one arrival on the row's counter; the
+//      buffer is free again;
+//   4. select the rows whose last chunk arrived here (select_regions over the
+//      row's slots copied into shared-memory regions; a slot that overflowed,
+//      or fewer than k candidates, falls back to exact passes over the row).
+// A row whose last chunk is this CTA's final one is selected by all 32 warps
+// together once the streaming is over, which shortens the launch's tail.
+//
+// Measured on fp32 [256, 131072], k = 4096: 0.15 ms against 0.055 ms for
+// wide_kernel, so the automatic plan does not pick it.  The 24 streaming warps
+// filter about 30 GB/s per SM (the 32 warps of two wide_kernel CTAs about 40),
+// and one row's selection on the 8 helper warps takes ~16 us: copying the
+// slots in from L2 and writing the outputs queue behind the streaming loads.
+// The helpers fall behind and the streaming warps wait for free buffers.
 //
 // Workspace (caller-owned, 256-byte aligned; the first ws_counter_bytes are
 // zeroed on the stream before every launch):
 //   uint32 arrival counter [rows], estimate-ready flag [rows], estimate [rows]
-//   per row r at ws_counter_bytes + r * ws_row_bytes, per chunk j and
-//   streaming warp w at ((j * 16 + w) * ws_part_bytes):
-//     uint4 {count (or kSlotOverflow), largest key, 0, 0}, uint2 pairs[part_cap + 1]
-// Shared memory: histogram (2048 words) | selection regions (8 x
-// region_stride pairs) | staging (16 x kStage vectors, then 16 x kStage
-// columns).
+//   per row r at ws_counter_bytes + r * ws_row_bytes, per chunk j at
+//   j * ws_part_bytes: uint4 {count (or kSlotOverflow), largest key, NaN, 0},
+//   uint2 pairs[part_cap]
+// Shared memory: histogram (2048 words) | selection regions (flat_sel_pairs
+// pairs) | staging (24 x kStage vectors, then 24 x kStage columns) | chunk
+// buffers (kFlatBufs x 24 x (flat_wcap + 1) pairs).
 // ---------------------------------------------------------------------------
-constexpr int kFlatU = 4;
 constexpr uint32_t kSlotOverflow = 0xffffffffu;
-using FlatSel = Grp<kFlatSelWarps * 32, 1, kFlatStreamWarps * 32>;
+constexpr int kFlatSW = kFlatStreamWarps;
+using FlatHelp = Grp<kFlatSelWarps * 32, 1, kFlatStreamWarps * 32>;
+using FlatAll = Grp<kFlatThreads, 2, 0>;
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
 {
@@ -2329,6 +2379,18 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
 __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
 {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Spins (bounded, ~2 s) until *p >= v; false on timeout.
+__device__ __forceinline__ bool wait_at_least(const volatile uint32_t *p, uint32_t v)
+{
+    if (*p >= v) return true;
+    const long long t0 = clock64();
+    while (*p < v) {
+        if (clock64() - t0 > kWaitCycles) return false;
+        __nanosleep(64);
+    }
+    return true;
 }
 
 // Threshold estimate of one row from a fixed sample (32 runs of 32 consecutive vectors spread
@@ -2408,311 +2470,249 @@ __device__ uint32_t flat_estimate(const TopkArgs &a, int64_t row, int64_t n, uin
     return key;
 }
 
-// The streaming warps' side of flat_kernel (see above).  s_q / s_qtail: this CTA's queue of
-// rows to select; s_sdone: streaming warps finished.
+// Shared state of one flat_kernel CTA.
+struct FlatShared {
+    uint32_t tk[kFlatQueue];          // threshold of each chunk ordinal (valid once tkseq > ordinal)
+    uint32_t tkseq;                   // thresholds published for ordinals [0, tkseq)
+    uint32_t bufgen[kFlatBufs];       // buffer b is free for ordinals <= bufgen[b]
+    uint32_t done[kFlatBufs];         // streaming warps finished with buffer b (cumulative)
+    uint32_t wcnt[kFlatBufs][kFlatStreamWarps];  // per buffer and warp: pairs kept (or kSlotOverflow)
+    uint32_t wmax[kFlatBufs][kFlatStreamWarps];  // largest key kept
+    uint32_t wnan[kFlatBufs][kFlatStreamWarps];  // NaN seen
+    uint32_t defer;                   // row + 1 left for the whole CTA to select (0: none)
+    uint32_t item;                    // broadcast within the helper group
+    uint32_t s_warp[32], s_res[4], s_cnt[32], s_gq[96], s_pre[kFlatMaxParts + 2];
+};
+
+// The streaming warps' side (see above).
 template <typename E>
-__device__ void flat_stream(const TopkArgs &a, unsigned char *smem, volatile uint32_t *s_q, uint32_t *s_qtail,
-                            uint32_t *s_sdone)
+__device__ void flat_stream(const TopkArgs &a, unsigned char *smem, FlatShared &fs)
 {
     using T = Elem<E>;
     constexpr int V = T::V;
-    constexpr int U = kFlatU;
-    constexpr int SW = kFlatStreamWarps;
+    constexpr int U = kWideUnroll;
+    constexpr int SW = kFlatSW;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t lt = (1u << lane) - 1u;
     const int64_t G = gridDim.x;
     const int cpr = a.parts;
     const int64_t nchunks = a.rows * cpr;
     const int64_t nvr = (a.cols * static_cast<int64_t>(sizeof(E))) >> 4;  // full vectors of a whole row
-    uint32_t *ctr = reinterpret_cast<uint32_t *>(a.ws);
-    const uint32_t *flag = ctr + a.rows;
-    const uint32_t *tkeys = flag + a.rows;
-    const uint32_t capw = static_cast<uint32_t>(a.part_cap);
-    const uint32_t arrivals = static_cast<uint32_t>(cpr) * SW;
+    const uint32_t wcap = static_cast<uint32_t>(a.flat_wcap);
     uint4 *stv = reinterpret_cast<uint4 *>(smem + a.smem_stage_off) + warp * kStage;
     int32_t *stc = reinterpret_cast<int32_t *>(smem + a.smem_stage_off + SW * kStage * 16) + warp * kStage;
-
-    // this warp's vectors [vb, ve) of chunk q's row; n: the row's valid columns (short rows: empty)
-    auto range_of = [&](int64_t q, int64_t &row, int &j, int64_t &n, int64_t &vb, int64_t &ve) {
-        row = q / cpr;
-        j = static_cast<int>(q - row * cpr);
-        n = valid_cols(a, row);
-        const int64_t nv = n > a.k ? (n * static_cast<int64_t>(sizeof(E))) >> 4 : 0;
+    volatile uint32_t *vtkseq = &fs.tkseq;
+    int ci = 0;
+    for (int64_t q = blockIdx.x; q < nchunks; q += G, ++ci) {
+        const int64_t row = q / cpr;
+        const int j = static_cast<int>(q - row * cpr);
+        const int64_t n = valid_cols(a, row);
+        if (n <= a.k) continue;  // short row: its designated CTA writes the fills
+        const int64_t nv = (n * static_cast<int64_t>(sizeof(E))) >> 4;
         const int64_t c0 = min(static_cast<int64_t>(j) * a.slice, nv);
         const int64_t c1 = min(min((static_cast<int64_t>(j) + 1) * a.slice, nvr), nv);
         const int64_t len = c1 - c0, per = len / SW, rem = len % SW;
-        vb = c0 + warp * per + min(static_cast<int64_t>(warp), rem);
-        ve = vb + per + (warp < rem ? 1 : 0);
-    };
-    constexpr int64_t kIt = 32 * U;  // vectors of one iteration (one set of loads)
-
-    // ---- load cursor: two iterations ahead of the one being examined
-    int64_t lq = blockIdx.x, lvb = 0, lve = 0, lbase = 0;
-    const uint4 *lxv = nullptr;
-    bool lvalid = false;
-    auto seek = [&](int64_t q) {  // first chunk at or after q with vectors for this warp
-        for (; q < nchunks; q += G) {
-            int64_t row, n;
-            int j;
-            range_of(q, row, j, n, lvb, lve);
-            if (lve > lvb) {
-                lq = q;
-                lbase = lvb;
-                lxv = reinterpret_cast<const uint4 *>(static_cast<const E *>(a.x) + row * a.stride);
-                lvalid = true;
-                return;
-            }
-        }
-        lvalid = false;
-    };
-    auto load_next = [&](uint4 (&q)[U]) {
-        if (lvalid) {
-            if (lbase + kIt <= lve) {
-#pragma unroll
-                for (int u = 0; u < U; ++u) q[u] = __ldcs(lxv + lbase + u * 32 + lane);
-            } else {
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int64_t v = lbase + u * 32 + lane;
-                    q[u] = v < lve ? __ldcs(lxv + v) : make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-            lbase += kIt;
-            if (lbase >= lve) seek(lq + G);
-        }
-    };
-    uint4 qa[U], qb[U];
-    seek(blockIdx.x);
-    load_next(qa);
-    load_next(qb);
-    bool use_a = true;  // buffer holding the next iteration to examine
-
-    // ---- chunk state of the iteration being examined
-    uint32_t tkey = 0, tsg = 0, off = 0, kmax = 0, smax = T::kSmaxInit, umax = T::kUmaxInit;
-    bool positive = false, pnan = false;
-    int sc = 0;
-    uint2 *pairs = nullptr;
-    auto expand = [&]() {
-        __syncwarp();
-        for (int r0 = 0; r0 < sc; r0 += 32) {
-            const int i = r0 + lane;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            int cb = 0;
-            uint32_t m = 0;
-            if (i < sc) {
-                v = stv[i];
-                cb = stc[i];
-                m = positive ? T::ge_mask_raw(v, tsg) : T::ge_mask_key(v, tkey);
-            }
-            uint32_t tot;
-            uint32_t p = off + warp_exclusive_scan(static_cast<uint32_t>(__popc(m)), lane, tot);
-            while (m) {
-                const int t = __ffs(m) - 1;
-                m &= m - 1u;
-                const E e = T::lane_of(v, t);
-                kmax = max(kmax, T::key(e));
-                pnan |= T::is_nan(e);
-                __stcg(pairs + (p < capw ? p : capw), make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(cb + t)));
-                ++p;
-            }
-            off += tot;
-        }
-        sc = 0;
-        __syncwarp();
-    };
-    // examines one iteration's vectors [base, base + kIt) ∩ [.., ve)
-    auto examine = [&](const uint4 (&q)[U], int64_t base, int64_t ve) {
+        const int64_t vb = c0 + warp * per + min(static_cast<int64_t>(warp), rem);
+        const int64_t ve = vb + per + (warp < rem ? 1 : 0);
+        const bool has_tail = j == cpr - 1 && warp == SW - 1 && nv * V < n;
+        const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
+        const uint4 *xv = reinterpret_cast<const uint4 *>(xrow);
+        const int b = ci % kFlatBufs;
+        uint2 *reg = reinterpret_cast<uint2 *>(smem + a.smem_cbuf_off) + (b * SW + warp) * (wcap + 1);
+        // the first loads go out before the waits
+        uint4 q4[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            bool any;
-            if (positive) {
-                T::nan_acc_neg(q[u], umax);  // zero vectors past the range pass nothing, hold no NaN
-                any = T::any_ge_raw(q[u], tsg);
-            } else {
-                T::nan_acc(q[u], smax, umax);
-                any = base + u * 32 + lane < ve && T::ge_mask_key(q[u], tkey) != 0u;
-            }
-            const uint32_t b = __ballot_sync(kFull, any);
-            if (b) {
-                const int nb = __popc(b);
-                if (sc + nb > kStage) expand();
-                if (any) {
-                    const int slot = sc + __popc(b & lt);
-                    stv[slot] = q[u];
-                    stc[slot] = static_cast<int32_t>((base + u * 32 + lane) * V);
-                }
-                sc += nb;
-            }
+            const int64_t v = vb + u * 32 + lane;
+            q4[u] = v < ve ? __ldcs(xv + v) : make_uint4(0u, 0u, 0u, 0u);
         }
-    };
-
-    for (int64_t q = blockIdx.x; q < nchunks; q += G) {
-        int64_t row, n, vb, ve;
-        int j;
-        range_of(q, row, j, n, vb, ve);
-        if (n <= a.k) continue;  // short row: the designated CTA writes its fills
-        const bool tail = j == cpr - 1 && warp == SW - 1;  // this warp also takes the < 16-byte tail
-        const int64_t nv = (n * static_cast<int64_t>(sizeof(E))) >> 4;
-        const bool has_tail = tail && nv * V < n;
-        const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
-        unsigned char *slot = a.ws + a.ws_counter_bytes + row * a.ws_row_bytes +
-                              (static_cast<int64_t>(j) * SW + warp) * a.ws_part_bytes;
-        pairs = reinterpret_cast<uint2 *>(slot + 16);
-        off = 0;
-        kmax = 0;
-        smax = T::kSmaxInit;
-        umax = T::kUmaxInit;
-        if (ve > vb || has_tail) {
-            // the row's estimate (published once by its designated CTA)
-            uint32_t t = 0;
-            if (lane == 0) {
-                const long long t0 = clock64();
-                while (ld_acquire_gpu(flag + row) == 0u) {
-                    if (clock64() - t0 > kWaitCycles) {
-                        set_err(a.err_flag, kStatusTimeout);
-                        break;
+        bool ok = wait_at_least(vtkseq, static_cast<uint32_t>(ci) + 1u);
+        ok = wait_at_least(&fs.bufgen[b], static_cast<uint32_t>(ci)) && ok;
+        if (!ok) set_err(a.err_flag, kStatusTimeout);
+        const uint32_t tkey = static_cast<volatile uint32_t *>(fs.tk)[ci];
+        const bool positive = tkey > T::kSignKey;  // raw-bit compares suffice above +/-0
+        const uint32_t tsg = tkey ^ T::kSignKey;
+        uint32_t smax = T::kSmaxInit, umax = T::kUmaxInit, kmax = 0, off = 0;
+        int sc = 0;
+        auto expand = [&]() {
+            __syncwarp();
+            for (int r0 = 0; r0 < sc; r0 += 32) {
+                const int i = r0 + lane;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                int cb = 0;
+                uint32_t m = 0;
+                if (i < sc) {
+                    v = stv[i];
+                    cb = stc[i];
+                    m = positive ? T::ge_mask_raw(v, tsg) : T::ge_mask_key(v, tkey);
+                }
+                uint32_t before = 0, tot = 0;
+#pragma unroll
+                for (int t = 0; t < V; ++t) {
+                    const uint32_t bt = __ballot_sync(kFull, (m >> t) & 1u);
+                    before += __popc(bt & lt);
+                    tot += __popc(bt);
+                }
+                uint32_t p = off + before;
+#pragma unroll
+                for (int t = 0; t < V; ++t) {
+                    if ((m >> t) & 1u) {
+                        const E e = T::lane_of(v, t);
+                        if (!positive) kmax = max(kmax, T::key(e));
+                        reg[p < wcap ? p : wcap] = make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(cb + t));
+                        ++p;
                     }
-                    __nanosleep(256);
                 }
-                t = __ldcg(tkeys + row);
+                off += tot;
             }
-            tkey = __shfl_sync(kFull, t, 0);
-            positive = tkey > T::kSignKey;
-            tsg = tkey ^ T::kSignKey;
-            pnan = tkey > T::key(static_cast<E>(T::kInfMagnitude));  // an estimate above +inf: a sampled NaN
-            for (int64_t base = vb; base < ve; base += kIt) {
-                if (use_a) {
-                    examine(qa, base, ve);
-                    load_next(qa);
+            sc = 0;
+            __syncwarp();
+        };
+        for (int64_t base = vb; base < ve; base += 32 * U) {
+            if (base != vb) {
+                if (base + 32 * U <= ve) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) q4[u] = __ldcs(xv + base + u * 32 + lane);
                 } else {
-                    examine(qb, base, ve);
-                    load_next(qb);
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int64_t v = base + u * 32 + lane;
+                        q4[u] = v < ve ? __ldcs(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
-                use_a = !use_a;
             }
-            if (sc) expand();
-            if (has_tail) {
-                const int64_t jt = nv * V + lane;
-                const bool in = jt < n;
-                const E e = in ? xrow[jt] : static_cast<E>(0);
-                if (in) T::nan_acc1(e, smax, umax);
-                const bool pass = in && T::key(e) >= tkey;
-                const uint32_t bp = __ballot_sync(kFull, pass);
-                if (pass) {
-                    kmax = max(kmax, T::key(e));
-                    const uint32_t p = off + __popc(bp & lt);
-                    __stcg(pairs + (p < capw ? p : capw), make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(jt)));
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                bool any;
+                if (positive) {
+                    // zero vectors past the range pass nothing and hold no NaN
+                    const uint32_t ms = T::smax_vec(q4[u]);
+                    smax = T::smax_fold(smax, ms);
+                    umax = T::umax_fold(umax, q4[u]);
+                    any = T::ge_raw(ms, tsg);
+                } else {
+                    T::nan_acc(q4[u], smax, umax);
+                    any = base + u * 32 + lane < ve && T::ge_mask_key(q4[u], tkey) != 0u;
                 }
-                off += __popc(bp);
+                const uint32_t bb = __ballot_sync(kFull, any);
+                if (bb) {
+                    const int nb = __popc(bb);
+                    if (sc + nb > kStage) expand();
+                    if (any) {
+                        const int slot = sc + __popc(bb & lt);
+                        stv[slot] = q4[u];
+                        stc[slot] = static_cast<int32_t>((base + u * 32 + lane) * V);
+                    }
+                    sc += nb;
+                }
             }
-        } else {
-            pnan = false;
         }
-        // ---- the slot's header, then the arrival
+        if (sc) expand();
+        if (has_tail) {
+            const int64_t jt = nv * V + lane;
+            const bool in = jt < n;
+            const E e = in ? xrow[jt] : static_cast<E>(0);
+            if (in) T::nan_acc1(e, smax, umax);
+            const bool pass = in && T::key(e) >= tkey;
+            const uint32_t bp = __ballot_sync(kFull, pass);
+            if (pass) {
+                kmax = max(kmax, T::key(e));
+                const uint32_t p = off + __popc(bp & lt);
+                reg[p < wcap ? p : wcap] = make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(jt));
+            }
+            off += __popc(bp);
+        }
+        // on the raw-compare path the largest candidate is the largest element when it passes
+        if (positive) {
+            const uint32_t lk = T::smax_key(smax);
+            kmax = max(kmax, lk >= tkey ? lk : 0u);
+        }
         kmax = __reduce_max_sync(kFull, kmax);
-        const bool nan = __any_sync(kFull, pnan || T::has_nan(smax, umax));
-        __threadfence();  // this lane's pairs, before the header and the arrival
-        __syncwarp();
+        const bool nan = __any_sync(kFull, T::has_nan(smax, umax));
         if (lane == 0) {
-            if (nan && a.nan_flag) atomicOr(a.nan_flag, 1);
-            __stcg(reinterpret_cast<uint4 *>(slot), make_uint4(off > capw ? kSlotOverflow : off, kmax, 0u, 0u));
-            __threadfence();
-            if (atomicAdd(ctr + row, 1u) == arrivals - 1u) {
-                __threadfence();  // the other warps' slots, before the selection warps read them
-                const uint32_t s = atomicAdd(s_qtail, 1u);
-                if (s < static_cast<uint32_t>(kFlatQueue))
-                    s_q[s] = static_cast<uint32_t>(row) + 1u;
-                else
-                    set_err(a.err_flag, kStatusInval);
-                __threadfence_block();
-            }
+            fs.wcnt[b][warp] = off > wcap ? kSlotOverflow : off;
+            fs.wmax[b][warp] = kmax;
+            fs.wnan[b][warp] = nan ? 1u : 0u;
+            __threadfence_block();
+            atomicAdd(&fs.done[b], 1u);
         }
         __syncwarp();
-    }
-    if (lane == 0) {
-        __threadfence_block();
-        atomicAdd(s_sdone, 1u);
     }
 }
 
-// One queued row: its slots into the selection regions, then select_regions (or the exact
-// fallback).  hist: 2048 words, zeroed on entry and on exit.
-template <typename E>
-__device__ void flat_select_row(const TopkArgs &a, int64_t row, unsigned char *smem, uint32_t *s_warp,
-                                uint32_t *s_res, uint32_t *s_cnt, uint32_t *s_gq, Segments<E> &s_seg)
+// Selection of one row whose chunk slots are all in the workspace, by the warp group G
+// (select_regions over the slots copied into shared-memory regions, or the exact fallback).
+// hist: 2048 words, zeroed on entry and on exit.
+template <typename E, typename G>
+__device__ void flat_select_row(const TopkArgs &a, int64_t row, unsigned char *smem, FlatShared &fs,
+                                Segments<E> &s_seg)
 {
-    using S = FlatSel;
-    constexpr int SW = kFlatStreamWarps;
-    constexpr int NT = S::NT;
-    __shared__ uint32_t s_bad, s_thi;
-    const int gt = S::tid(), lane = gt & 31, gw = gt >> 5;
+    constexpr int NT = G::NT, W = G::W;
+    __shared__ uint32_t s_ok, s_thi;
+    const int gt = G::tid(), lane = gt & 31, gw = gt >> 5;
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
     uint2 *list = reinterpret_cast<uint2 *>(smem + a.smem_list_off);
-    const int rs = a.region_stride;
-    const uint32_t capw = static_cast<uint32_t>(a.list_cap);
+    const int rs = (a.flat_sel_pairs / W) & ~1;
+    const uint32_t capw = static_cast<uint32_t>(rs - 1);
     const uint32_t *tkeys = reinterpret_cast<const uint32_t *>(a.ws) + 2 * a.rows;
     const unsigned char *wrow = a.ws + a.ws_counter_bytes + row * a.ws_row_bytes;
-    const int nsub = a.parts * SW;
-    const uint32_t tkey = __ldcg(tkeys + row);
-    // prefix of the slot counts (the histogram holds it: pre[s], s <= nsub)
-    uint32_t *pre = hist;
-    if (gt == 0) {
-        s_bad = 0u;
-        s_thi = 0u;
-    }
-    const int m = (nsub + NT - 1) / NT;
-    const int s0 = min(nsub, gt * m), s1 = min(nsub, s0 + m);
-    uint32_t c = 0, thi = 0;
-    bool bad = false;
-    for (int s = s0; s < s1; ++s) {
-        const uint4 h = __ldcg(reinterpret_cast<const uint4 *>(wrow + static_cast<int64_t>(s) * a.ws_part_bytes));
-        bad |= h.x == kSlotOverflow;
-        c += h.x == kSlotOverflow ? 0u : h.x;
-        thi = max(thi, h.y);
-    }
-    uint32_t total;
-    uint32_t p0 = block_exclusive_scan<S>(c, s_warp, total);
-    for (int s = s0; s < s1; ++s) {
-        pre[s] = p0;
-        const uint4 h = __ldcg(reinterpret_cast<const uint4 *>(wrow + static_cast<int64_t>(s) * a.ws_part_bytes));
-        p0 += h.x == kSlotOverflow ? 0u : h.x;
-    }
-    if (gt == 0) pre[nsub] = total;
-    thi = __reduce_max_sync(kFull, thi);
-    bad = __any_sync(kFull, bad);
-    if (lane == 0) {
-        atomicMax(&s_thi, thi);
-        if (bad) atomicOr(&s_bad, 1u);
-    }
-    S::sync();
-    const bool ok = s_bad == 0u && total >= static_cast<uint32_t>(a.k) && total <= static_cast<uint32_t>(S::W) * capw;
-    if (ok) {
-        // warp gw copies the flat range [f0, f1) of the slots (slots in column order) into its region
-        const uint32_t f0 = static_cast<uint32_t>(static_cast<uint64_t>(total) * gw / S::W);
-        const uint32_t f1 = static_cast<uint32_t>(static_cast<uint64_t>(total) * (gw + 1) / S::W);
-        uint2 *reg = list + gw * rs;
-        int lo = 0, hi = nsub - 1;  // the slot holding f0
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (pre[mid] <= f0) lo = mid;
-            else hi = mid - 1;
+    const int cpr = a.parts;
+    // the slots' counts (one per chunk) -> prefix in s_pre
+    if (gt < 32) {
+        uint32_t c = 0, thi = 0;
+        bool bad = false;
+        uint32_t run = 0;
+        for (int s0 = 0; s0 < cpr; s0 += 32) {
+            const int s = s0 + gt;
+            uint4 h = make_uint4(0u, 0u, 0u, 0u);
+            if (s < cpr) h = __ldcg(reinterpret_cast<const uint4 *>(wrow + static_cast<int64_t>(s) * a.ws_part_bytes));
+            bad |= h.x == kSlotOverflow;
+            c = h.x == kSlotOverflow ? 0u : h.x;
+            thi = max(thi, h.y);
+            uint32_t tot;
+            const uint32_t ex = warp_exclusive_scan(c, lane, tot);
+            if (s < cpr) fs.s_pre[s] = run + ex;
+            run += tot;
         }
-        int s = lo;
+        thi = __reduce_max_sync(kFull, thi);
+        bad = __any_sync(kFull, bad);
+        if (gt == 0) {
+            fs.s_pre[cpr] = run;
+            s_thi = thi;
+            s_ok = (!bad && run >= static_cast<uint32_t>(a.k) && run <= static_cast<uint32_t>(W) * capw) ? 1u : 0u;
+        }
+    }
+    G::sync();
+    const uint32_t total = fs.s_pre[cpr];
+    if (s_ok) {
+        // warp gw copies the flat range [f0, f1) of the slots (in column order) into its region
+        const uint32_t f0 = static_cast<uint32_t>(static_cast<uint64_t>(total) * gw / W);
+        const uint32_t f1 = static_cast<uint32_t>(static_cast<uint64_t>(total) * (gw + 1) / W);
+        uint2 *reg = list + gw * rs;
+        int s = 0;
+        while (s < cpr - 1 && fs.s_pre[s + 1] <= f0) ++s;
         for (uint32_t f = f0; f < f1;) {
-            while (s < nsub - 1 && pre[s + 1] <= f) ++s;
-            const uint32_t end = min(f1, pre[s + 1]);
-            const uint2 *sp = reinterpret_cast<const uint2 *>(wrow + static_cast<int64_t>(s) * a.ws_part_bytes + 16) - pre[s];
-            for (uint32_t i = f + lane; i < end; i += 32) reg[i - f0] = __ldcg(sp + i);
+            while (s < cpr - 1 && fs.s_pre[s + 1] <= f) ++s;
+            const uint32_t end = min(f1, fs.s_pre[s + 1]);
+            const uint2 *sp =
+                reinterpret_cast<const uint2 *>(wrow + static_cast<int64_t>(s) * a.ws_part_bytes + 16) - fs.s_pre[s];
+            uint32_t i = f + lane;
+            for (; i + 96 < end; i += 128) {
+                const uint2 e0 = __ldcg(sp + i), e1 = __ldcg(sp + i + 32), e2 = __ldcg(sp + i + 64),
+                            e3 = __ldcg(sp + i + 96);
+                reg[i - f0] = e0;
+                reg[i + 32 - f0] = e1;
+                reg[i + 64 - f0] = e2;
+                reg[i + 96 - f0] = e3;
+            }
+            for (; i < end; i += 32) reg[i - f0] = __ldcg(sp + i);
             f = end;
         }
-        if (lane == 0) s_cnt[gw] = f1 - f0;
-        S::sync();
-        const uint32_t thi_all = s_thi;
-        for (int i = gt; i < kRangeBins; i += NT) hist[i] = 0u;
-        S::sync();
-        select_regions<E, S, false>(a, row, list, rs, s_cnt, tkey, thi_all, hist, s_res, s_warp, s_gq, nullptr);
+        if (lane == 0) fs.s_cnt[gw] = f1 - f0;
+        G::sync();
+        select_regions<E, G, false>(a, row, list, rs, fs.s_cnt, __ldcg(tkeys + row), s_thi, hist, fs.s_res,
+                                    fs.s_warp, fs.s_gq, nullptr);
     } else {
-        for (int i = gt; i < a.hist_bins; i += NT) hist[i] = 0u;
         if (gt == 0) {
             s_seg.n = 1;
             s_seg.bits[0] = static_cast<const E *>(a.x) + row * a.stride;
@@ -2721,75 +2721,165 @@ __device__ void flat_select_row(const TopkArgs &a, int64_t row, unsigned char *s
             s_seg.pre[0] = 0;
             s_seg.pre[1] = static_cast<uint32_t>(valid_cols(a, row));
         }
-        S::sync();
-        select_segments<E, S, false>(a, row, s_seg, 0u, hist, s_res, s_warp, nullptr);
+        G::sync();
+        select_segments<E, G, false>(a, row, s_seg, 0u, hist, fs.s_res, fs.s_warp, nullptr);
     }
-    S::sync();
+    G::sync();
     for (int i = gt; i < a.hist_bins; i += NT) hist[i] = 0u;
-    S::sync();
+    G::sync();
 }
 
+// The helper warps' side (see above).  Leaves in fs.defer the row (+ 1) for the whole CTA.
 template <typename E>
-__device__ void flat_select(const TopkArgs &a, unsigned char *smem, volatile uint32_t *s_q, volatile uint32_t *s_qtail,
-                            volatile uint32_t *s_sdone)
+__device__ void flat_help(const TopkArgs &a, unsigned char *smem, FlatShared &fs, Segments<E> &s_seg)
 {
-    using S = FlatSel;
-    constexpr int NT = S::NT;
-    __shared__ uint32_t s_warp[S::W], s_res[4], s_cnt[S::W], s_gq[3 * S::W], s_item;
-    __shared__ Segments<E> s_seg;
-    const int gt = S::tid();
+    using S = FlatHelp;
+    constexpr int NT = S::NT, SW = kFlatSW;
+    const int gt = S::tid(), lane = gt & 31;
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
-    uint32_t *flag = reinterpret_cast<uint32_t *>(a.ws) + a.rows;
+    uint32_t *ctr = reinterpret_cast<uint32_t *>(a.ws);
+    uint32_t *flag = ctr + a.rows;
     uint32_t *tkeys = flag + a.rows;
     const int64_t G = gridDim.x;
+    const int cpr = a.parts;
+    const int64_t nchunks = a.rows * cpr;
+    const int nci = blockIdx.x < nchunks ? static_cast<int>((nchunks - 1 - blockIdx.x) / G) + 1 : 0;
+    const uint32_t wcap = static_cast<uint32_t>(a.flat_wcap);
+    volatile uint32_t *vtkseq = &fs.tkseq;
     for (int i = gt; i < a.hist_bins; i += NT) hist[i] = 0u;
+    // the first chunk's rows are prefetched into L2 while the estimates are worked out
+    if (nci > 0) {
+        const int64_t row = blockIdx.x / cpr;
+        const int j = static_cast<int>(blockIdx.x - row * cpr);
+        const int64_t n = valid_cols(a, row);
+        const int64_t nv = n > a.k ? (n * static_cast<int64_t>(sizeof(E))) >> 4 : 0;  // inside [0, n) only
+        const int64_t c0 = static_cast<int64_t>(j) * a.slice, c1 = min(c0 + a.slice, nv);
+        const unsigned char *base = reinterpret_cast<const unsigned char *>(static_cast<const E *>(a.x) + row * a.stride);
+        for (int64_t v = c0 + static_cast<int64_t>(gt) * 64; v < c1; v += static_cast<int64_t>(NT) * 64)
+            prefetch_l2(base + v * 16, static_cast<uint32_t>(min(static_cast<int64_t>(64), c1 - v) * 16));
+    }
     S::sync();
-    // ---- 1. the rows this CTA is designated for: short-row fills, or the threshold estimate
-    for (int64_t r = blockIdx.x; r < a.rows; r += G) {
-        const int64_t n = valid_cols(a, r);
-        if (n <= a.k) {
-            short_row<E, S, false>(a, r, n, 0, a.k);
+    // ---- 1. designated rows: short-row fills or the threshold estimate; rows needed in the
+    //         first round (r * cpr < grid) first
+    auto designated = [&](bool first_round) {
+        for (int64_t r = blockIdx.x; r < a.rows; r += G) {
+            if ((r * cpr < G) != first_round) continue;
+            const int64_t n = valid_cols(a, r);
+            if (n <= a.k) {
+                short_row<E, S, false>(a, r, n, 0, a.k);
+                continue;
+            }
+            const uint32_t t = flat_estimate<E, S>(a, r, n, hist, fs.s_res, fs.s_warp);
+            if (gt == 0) {
+                tkeys[r] = t;
+                __threadfence();
+                st_release_gpu(flag + r, 1u);
+            }
+        }
+    };
+    // copies the thresholds of this CTA's chunks whose row estimate is out, in order; `block`:
+    // wait (bounded) for the next one
+    auto publish = [&](bool block) {
+        if (gt == 0) {
+            uint32_t s = *vtkseq;
+            while (static_cast<int>(s) < nci) {
+                const int64_t row = (blockIdx.x + static_cast<int64_t>(s) * G) / cpr;
+                uint32_t t = 0;
+                if (valid_cols(a, row) > a.k) {
+                    if (ld_acquire_gpu(flag + row) == 0u) {
+                        if (!block) break;
+                        const long long t0 = clock64();
+                        bool ok = true;
+                        while (ld_acquire_gpu(flag + row) == 0u) {
+                            if (clock64() - t0 > kWaitCycles) {
+                                ok = false;
+                                break;
+                            }
+                            __nanosleep(128);
+                        }
+                        if (!ok) {
+                            set_err(a.err_flag, kStatusTimeout);  // the streaming warps go on with key 0
+                        }
+                    }
+                    t = __ldcg(tkeys + row);
+                }
+                fs.tk[s] = t;
+                __threadfence_block();
+                *vtkseq = ++s;
+                block = false;
+            }
+        }
+    };
+    designated(true);
+    publish(true);
+    designated(false);
+    // ---- 2./3./4. the chunk loop
+    uint32_t expect[kFlatBufs] = {};
+    int64_t defer = -1;
+    for (int ci = 0; ci < nci; ++ci) {
+        publish(static_cast<int>(*vtkseq) <= ci + 1);  // keep two thresholds ahead
+        const int64_t q = blockIdx.x + static_cast<int64_t>(ci) * G;
+        const int64_t row = q / cpr;
+        const int j = static_cast<int>(q - row * cpr);
+        const int b = ci % kFlatBufs;
+        if (valid_cols(a, row) <= a.k) {  // short row: nothing streamed, nothing flushed
+            if (gt == 0) {
+                __threadfence_block();
+                atomicMax(&fs.bufgen[b], static_cast<uint32_t>(ci + kFlatBufs));
+            }
             continue;
         }
-        const uint32_t t = flat_estimate<E, S>(a, r, n, hist, s_res, s_warp);
-        if (gt == 0) {
-            tkeys[r] = t;
-            __threadfence();
-            st_release_gpu(flag + r, 1u);
-        }
-    }
-    // ---- 2. the rows queued by this CTA's streaming warps
-    uint32_t head = 0;
-    while (true) {
-        if (gt == 0) {
-            uint32_t item = 0;
-            const long long t0 = clock64();
-            while (true) {
-                if (head < static_cast<uint32_t>(kFlatQueue) && s_q[head] != 0u) {
-                    item = s_q[head];
-                    break;
-                }
-                if (*s_sdone == static_cast<uint32_t>(kFlatStreamWarps)) {
-                    __threadfence_block();
-                    if (head < static_cast<uint32_t>(kFlatQueue) && s_q[head] != 0u) continue;
-                    if (*s_qtail <= head) break;  // every streaming warp is done and nothing is left
-                }
-                if (clock64() - t0 > kWaitCycles) {
-                    set_err(a.err_flag, kStatusTimeout);
-                    break;
-                }
-                __nanosleep(128);
+        expect[b] += SW;
+        if (gt == 0 && !wait_at_least(&fs.done[b], expect[b])) set_err(a.err_flag, kStatusTimeout);
+        S::sync();
+        // flush: the 24 regions, concatenated, into the chunk's slot
+        unsigned char *slot = a.ws + a.ws_counter_bytes + row * a.ws_row_bytes + static_cast<int64_t>(j) * a.ws_part_bytes;
+        uint2 *dst = reinterpret_cast<uint2 *>(slot + 16);
+        const uint2 *src = reinterpret_cast<const uint2 *>(smem + a.smem_cbuf_off) + b * SW * (wcap + 1);
+        if (gt < 32) {
+            const volatile uint32_t *vcnt = fs.wcnt[b], *vmax = fs.wmax[b], *vnan = fs.wnan[b];
+            const uint32_t c = lane < SW ? vcnt[lane] : 0u;
+            const bool ovf = __any_sync(kFull, c == kSlotOverflow);
+            uint32_t tot;
+            const uint32_t ex = warp_exclusive_scan(ovf ? 0u : c, lane, tot);
+            if (lane < SW) fs.s_pre[lane] = ex;
+            const uint32_t km = __reduce_max_sync(kFull, lane < SW ? vmax[lane] : 0u);
+            const bool nan = __any_sync(kFull, lane < SW && vnan[lane] != 0u);
+            if (lane == 0) {
+                fs.s_pre[SW] = ovf ? 0u : tot;
+                __stcg(reinterpret_cast<uint4 *>(slot), make_uint4(ovf ? kSlotOverflow : tot, km, nan ? 1u : 0u, 0u));
+                if (nan && a.nan_flag) atomicOr(a.nan_flag, 1);
             }
-            s_item = item;
         }
         S::sync();
-        const uint32_t item = s_item;
+        {
+            // warp w' of the group copies regions w', w' + 8, ... (each a contiguous run of the slot)
+            for (int w = gt >> 5; w < SW; w += S::W) {
+                const uint32_t p0 = fs.s_pre[w], cnt = fs.s_pre[w + 1] - p0;
+                const uint2 *srcw = src + w * (wcap + 1);
+                for (uint32_t i = lane; i < cnt; i += 32) __stcg(dst + p0 + i, srcw[i]);
+            }
+        }
         S::sync();
-        if (item == 0u) break;
-        ++head;
-        __threadfence();  // the streaming warps' slots (their arrivals are ordered before the queue entry)
-        flat_select_row<E>(a, static_cast<int64_t>(item) - 1, smem, s_warp, s_res, s_cnt, s_gq, s_seg);
+        if (gt == 0) {
+            __threadfence();  // the slot, before the arrival
+            const bool last = atomicAdd(ctr + row, 1u) == static_cast<uint32_t>(cpr - 1);
+            fs.item = last ? static_cast<uint32_t>(row) + 1u : 0u;
+            __threadfence_block();
+            atomicMax(&fs.bufgen[b], static_cast<uint32_t>(ci + kFlatBufs));  // the buffer is free
+        }
+        S::sync();
+        const uint32_t item = fs.item;
+        S::sync();
+        if (item) {
+            __threadfence();  // the other chunks' slots (their arrivals came before ours)
+            if (ci == nci - 1)
+                defer = static_cast<int64_t>(item) - 1;  // this CTA's last chunk: all warps select it
+            else
+                flat_select_row<E, S>(a, static_cast<int64_t>(item) - 1, smem, fs, s_seg);
+        }
     }
+    if (gt == 0) fs.defer = static_cast<uint32_t>(defer + 1);
 }
 
 template <typename E, bool GATHER>
@@ -2797,18 +2887,26 @@ __global__ void __launch_bounds__(kFlatThreads, 1) flat_kernel(const TopkArgs a)
 {
     static_assert(!GATHER, "flat_kernel has no fused gather");
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint32_t s_q[kFlatQueue];
-    __shared__ uint32_t s_qtail, s_sdone;
-    for (int i = threadIdx.x; i < kFlatQueue; i += blockDim.x) s_q[i] = 0u;
+    __shared__ FlatShared fs;
+    __shared__ Segments<E> s_seg;
+    for (int i = threadIdx.x; i < kFlatQueue; i += blockDim.x) fs.tk[i] = 0u;
+    if (threadIdx.x < kFlatBufs) {
+        fs.bufgen[threadIdx.x] = threadIdx.x;
+        fs.done[threadIdx.x] = 0u;
+    }
     if (threadIdx.x == 0) {
-        s_qtail = 0u;
-        s_sdone = 0u;
+        fs.tkseq = 0u;
+        fs.defer = 0u;
     }
     __syncthreads();
-    if (static_cast<int>(threadIdx.x) < kFlatStreamWarps * 32)
-        flat_stream<E>(a, smem, s_q, &s_qtail, &s_sdone);
+    if (static_cast<int>(threadIdx.x) < kFlatSW * 32)
+        flat_stream<E>(a, smem, fs);
     else
-        flat_select<E>(a, smem, s_q, &s_qtail, &s_sdone);
+        flat_help<E>(a, smem, fs, s_seg);
+    // the row (if any) whose last chunk was this CTA's final one: selected by every warp
+    FlatAll::sync();
+    const uint32_t d = fs.defer;
+    if (d) flat_select_row<E, FlatAll>(a, static_cast<int64_t>(d) - 1, smem, fs, s_seg);
 }
 
 // Raises a kernel's dynamic shared-memory limit once per device; later calls that need no more
