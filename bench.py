@@ -10,12 +10,13 @@ the workload's shape (no dataset), resident in HBM before timing starts; L2
 is flushed (a 256 MiB write) before every timed step and the flush is not
 timed.  Each step is timed with CUDA events on the launching stream.
 
-Prints ONE JSON line on rank 0.  The default workload is the bf16 indexer
-top-k + gather on scores[4096, 2048].  Besides the contract's keys the line
-carries:
+Prints ONE JSON line on rank 0.  The default workload is the fp32 sampling
+top-k on logits[256, 131072], k = 4096: the 128K-wide rows the top-k's
+bandwidth target is quoted on.  Besides the contract's keys the line carries:
   per_workload      all five named workloads: flushed and warm-L2 step times,
-                    the top-k alone for the gather workloads, and the step
-                    with value-ordered output;
+                    the top-k alone (topk_only_*: for the gather workloads the
+                    same selection without the fused gather, its own bytes and
+                    fraction of peak), and the step with value-ordered output;
   pair_gather       the two-key gather (1024 x 512 positions, d 128 + 512);
   block_candidates  the block-level candidate chain with its gather;
   cpu_baseline      the oracle single-threaded, and row-parallel over the
@@ -48,7 +49,7 @@ if ROOT not in sys.path:
 import synthetic as syn  # noqa: E402
 
 METRIC = "top-k effective HBM GB/s (fraction of GB300 peak) and rows/s per config, 1 GPU"
-DEFAULT_WORKLOAD = "indexer_bf16_4096x2048_causal_k512_gather"
+DEFAULT_WORKLOAD = "sampling_f32_256x131072_k4096_nan"
 FLUSH_BYTES = 256 << 20
 
 
@@ -153,35 +154,59 @@ class ClockSampler:
 # GPU arm
 # ----------------------------------------------------------------------------
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.tsv")
+
+
 def kernel_source_hash() -> str:
-    """Short hash of the selection kernels' source: a stored DRAM traffic figure is used only while it
-    still describes the kernels that run."""
+    """Short hash of the selection and gather kernels' source: a stored DRAM traffic figure is used only
+    while it still describes the kernels that run."""
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("topk_impl.cuh", "sel_internal.h", "ptx.cuh"):
+    for f in ("topk_impl.cuh", "sel_internal.h", "ptx.cuh", "gather.cu"):
         with open(os.path.join(ROOT, "gather_radix_select_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
 
 
 def stored_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of `kernel` on `workload`
-    from profiles/traffic.md, or None when absent or taken on other kernel source."""
-    path = os.path.join(ROOT, "profiles", "traffic.md")
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture) of `kernel`
+    on `workload` from the tab-separated table TRAFFIC_FILE (workload, kernel, bytes, source hash), or
+    None when absent or taken on other kernel source."""
     try:
-        lines = open(path).read().splitlines()
+        lines = open(TRAFFIC_FILE).read().splitlines()
     except OSError:
         return None
     src = kernel_source_hash()
     for ln in lines:
-        cells = [c.strip() for c in ln.strip().strip("|").split("|")]
-        if len(cells) >= 4 and cells[0] == workload and cells[1] == kernel and cells[3] == src:
+        cells = ln.split("\t")
+        if len(cells) >= 4 and cells[0] == workload and cells[1] == kernel and cells[3].strip() == src:
             try:
                 return int(cells[2])
             except ValueError:
                 return None
     return None
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (as the kernel reports it), or "" when it cannot be read."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                k, _, v = ln.partition(":")
+                if k.strip().lower() in ("model name", "cpu model") and v.strip():
+                    return v.strip()
+    except OSError:
+        pass
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for ln in r.stdout.splitlines():
+            k, _, v = ln.partition(":")
+            if k.strip() == "Model name" and v.strip():
+                return v.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return ""
 
 
 def measured_peaks():
@@ -456,15 +481,18 @@ def per_workload(args, dev, flush, peak):
                      "ms": round(ms, 5), "warm_l2_ms": round(warm, 5), "rows_per_s": round(w["rows"] / (ms * 1e-3), 1),
                      "gbs": round(nb / (ms * 1e-3) / 1e9, 2), "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
                      "bytes": nb, "topk_bytes": tb, "fused_gather": w.get("key") is not None}
+        t2 = ms
         if w.get("key") is not None:
-            # the top-k alone on the same workload
+            # the top-k alone on the same workload (the step above adds the fused gather's bytes)
             w2 = dict(w)
             w2["key"] = None
             r2 = Runner(w2, dev)
             t2 = statistics.median(time_steps(r2, 10, 3, flush))
-            out[name]["topk_only_ms"] = round(t2, 5)
-            out[name]["topk_only_gbs"] = round(tb / (t2 * 1e-3) / 1e9, 2)
+            out[name]["topk_only_kernel"] = r2.g.kernel_name(r2.x.dtype, w["rows"], w["cols"], w["k"], 0)
             del r2
+        out[name]["topk_only_ms"] = round(t2, 5)
+        out[name]["topk_only_gbs"] = round(tb / (t2 * 1e-3) / 1e9, 2)
+        out[name]["topk_only_frac"] = round(tb / (t2 * 1e-3) / 1e9 / peak, 4)
         # the same step with value-ordered output (selection + ordering launch; same algorithmic bytes)
         r3 = Runner(w, dev, sorted_value=True)
         t3 = statistics.median(time_steps(r3, 10, 3, flush))
@@ -640,7 +668,7 @@ def cpu_baseline(name, budget_s=10.0):
     workers = max(1, os.cpu_count() or 1)
     ptimes = [oracle_step_parallel(w, rows_sel, workers) for _ in range(3)]
     pper = statistics.median(ptimes)
-    return {"value": round(nb / per / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(nb / per / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu_model": cpu_model(),
             "sample": "%d of %d rows (evenly spaced), %d passes, %.2f s per pass; single-threaded C full sort "
                       "per row%s" % (len(rows_sel), R, reps, per, " + triple-loop gather" if w.get("key") is not None
                                      else ""),
@@ -676,7 +704,7 @@ def reference_arm(args):
             "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic (seeded)",
             "config": {"workload": args.workload, "rows": w["rows"], "cols": w["cols"], "k": w["k"]},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -11,7 +11,7 @@ import threading
 
 from . import build as _build
 
-SEL_OK, SEL_EINVAL, SEL_EALIGN, SEL_EUNSUPPORTED, SEL_ECUDA, SEL_ETIMEOUT, SEL_ESCRATCH = range(7)
+SEL_OK, SEL_EINVAL, SEL_EALIGN, SEL_EUNSUPPORTED, SEL_ECUDA, SEL_ETIMEOUT, SEL_ESCRATCH, SEL_EBOUNDS = range(8)
 SEL_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 SEL_F32, SEL_BF16 = 0, 1
 SEL_I32, SEL_I64 = 0, 1
@@ -45,6 +45,8 @@ SIGNATURES = {
     "sel_topk_kernel_name": (ctypes.c_char_p, [_int, _i64, _i64, _int, _i64]),
     "sel_set_tuning": (_int, [_int, _int]),
     "sel_get_tuning": (_int, [_int]),
+    "sel_selftest_wait_timeout": (_int, [_vp, ctypes.c_longlong, _vp]),
+    "sel_debug_build": (_int, []),
 }
 
 _lock = threading.Lock()
@@ -52,7 +54,9 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.SO
+    """libsel.so, or the bounds-checked libsel_debug.so when SEL_LIBRARY=debug is set (read when the
+    library is first loaded)."""
+    return _build.DEBUG_SO if os.environ.get("SEL_LIBRARY", "") == "debug" else _build.SO
 
 
 def load(build_if_missing: bool = False):
@@ -66,7 +70,7 @@ def load(build_if_missing: bool = False):
             if not build_if_missing:
                 raise RuntimeError(
                     "libsel.so is not built (%s); run `python -m gather_radix_select_gb300.build`" % path)
-            _build.build()
+            _build.build(debug=path == _build.DEBUG_SO)
         lib = ctypes.CDLL(path)
         for name, (res, args) in SIGNATURES.items():
             fn = getattr(lib, name)

@@ -584,6 +584,12 @@ int check_gather_key(const void *key, int64_t b, int64_t comp_len, int64_t d, in
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? SEL_OK : SEL_ECUDA; }
 
+// Elements from key[0] to the end of the key's last row (b batches of comp_len rows of d).
+int64_t key_span(int64_t b, int64_t comp_len, int64_t d, int64_t batch_stride, int64_t row_stride)
+{
+    return comp_len > 0 && b > 0 ? (b - 1) * batch_stride + (comp_len - 1) * row_stride + d : 0;
+}
+
 // Re-orders finished output rows by value (SEL_SORT_VALUE).
 int value_order(const void *x, int dtype, int64_t rows, int64_t stride, int k, int idx_dtype, int want_values,
                 void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride, void *stream)
@@ -630,12 +636,14 @@ int run_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
     a.nan_flag = nan_flag;
     a.err_flag = err_flag;
     a.ws = static_cast<unsigned char *>(workspace);
+    a.ws_bytes = workspace ? workspace_bytes : 0;
     a.key = static_cast<const uint16_t *>(key);
     a.comp_len = comp_len;
     a.d = d;
     a.key_batch_stride = key_batch_stride;
     a.key_row_stride = key_row_stride;
     a.rows_per_batch = n_gather > 0 ? rows / b : 1;
+    a.key_span = n_gather > 0 ? key_span(b, comp_len, d, key_batch_stride, key_row_stride) : 0;
     a.n_gather = n_gather;
     a.gather_out = static_cast<uint16_t *>(gather_out);
     if (p.ws_bytes > 0) {
@@ -699,6 +707,21 @@ int sel_get_tuning(int knob)
     }
 }
 
+int sel_debug_build(void)
+{
+#ifdef SEL_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+int sel_selftest_wait_timeout(int32_t *err_flag, long long cycles, void *stream)
+{
+    if (!err_flag || cycles < 0) return SEL_EINVAL;
+    return status_of(sel::launch_wait_selftest(err_flag, cycles, static_cast<cudaStream_t>(stream)));
+}
+
 int sel_stride_requirement(int *in_align_bytes, int *out_align_bytes)
 {
     if (in_align_bytes) *in_align_bytes = kInAlign;
@@ -716,6 +739,7 @@ const char *sel_strerror(int status)
     case SEL_ECUDA: return "CUDA runtime error";
     case SEL_ETIMEOUT: return "a bounded device wait timed out";
     case SEL_ESCRATCH: return "shape needs more scratch than sel_topk_noalloc's built-in array (use sel_topk with a workspace)";
+    case SEL_EBOUNDS: return "an out-of-bounds access was caught and skipped (debug build)";
     default: return "unknown status";
     }
 }
@@ -787,6 +811,7 @@ int sel_gather_rows(const void *key, int64_t b, int64_t comp_len, int64_t d, int
     a.d = d;
     a.key_batch_stride = key_batch_stride;
     a.key_row_stride = key_row_stride;
+    a.key_span = key_span(b, comp_len, d, key_batch_stride, key_row_stride);
     a.idx = idx;
     a.idx_i64 = idx_dtype == SEL_I64;
     a.rows = rows;
@@ -821,6 +846,8 @@ int sel_gather_rows_pair(const void *key, int64_t d, int64_t key_batch_stride, i
     a.d2 = d2;
     a.key2_batch_stride = key2_batch_stride;
     a.key2_row_stride = key2_row_stride;
+    a.key_span = key_span(b, comp_len, d, key_batch_stride, key_row_stride);
+    a.key2_span = key_span(b, comp_len, d2, key2_batch_stride, key2_row_stride);
     a.out2 = static_cast<uint16_t *>(out2);
     a.idx = idx;
     a.idx_i64 = idx_dtype == SEL_I64;
@@ -881,6 +908,7 @@ int sel_block_topk_gather(const void *scores, int dtype, int64_t rows, int64_t n
     a.key_batch_stride = key_batch_stride;
     a.key_row_stride = key_row_stride;
     a.rows_per_batch = key ? rows / b : 1;
+    a.key_span = key ? key_span(b, comp_len, d, key_batch_stride, key_row_stride) : 0;
     a.out = static_cast<uint16_t *>(gather_out);
     a.err_flag = err_flag;
     return status_of(sel::launch_block_expand(a, static_cast<cudaStream_t>(stream)));

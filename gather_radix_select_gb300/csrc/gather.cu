@@ -28,8 +28,10 @@ constexpr int32_t kStatusInval = 1;
 
 // Copies the key rows at positions s_pos[0, np) (batch base kb, rows of d elements) to the
 // contiguous output rows at ob; a position of -1 yields a zero row.
+// Debug builds check every key row read against kspan (elements from the batch base kb to the end
+// of the key) and record SEL_EBOUNDS in err_flag instead of reading outside.
 __device__ __forceinline__ void copy_rows(const uint16_t *kb, int64_t row_stride, int64_t d, uint16_t *out, int np,
-                                          const int64_t *s_pos)
+                                          const int64_t *s_pos, int64_t kspan, int32_t *err_flag)
 {
     const int vpr = static_cast<int>(d >> 3);  // 16-byte vectors per key row
     const int vsh = (vpr & (vpr - 1)) == 0 ? __ffs(vpr) - 1 : -1;  // log2(vpr), or -1
@@ -52,7 +54,7 @@ __device__ __forceinline__ void copy_rows(const uint16_t *kb, int64_t row_stride
                 v[u][0] = v[u][1] = make_uint4(0u, 0u, 0u, 0u);
                 if (jj < np) {
                     const int64_t p = s_pos[jj];
-                    if (p >= 0) {
+                    if (p >= 0 && SEL_IN_BOUNDS(p * row_stride + d <= kspan, err_flag)) {
                         const uint4 *src = reinterpret_cast<const uint4 *>(kb + p * row_stride) + c;
                         v[u][0] = __ldg(src);
                         v[u][1] = __ldg(src + lpr);
@@ -80,7 +82,8 @@ __device__ __forceinline__ void copy_rows(const uint16_t *kb, int64_t row_stride
             if (t < total) {
                 const int jj = vsh >= 0 ? (t >> vsh) : t / vpr;
                 const int64_t p = s_pos[jj];
-                if (p >= 0) v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * row_stride) + (t - jj * vpr));
+                if (p >= 0 && SEL_IN_BOUNDS(p * row_stride + d <= kspan, err_flag))
+                    v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * row_stride) + (t - jj * vpr));
             }
         }
 #pragma unroll
@@ -113,10 +116,11 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs
     }
     __syncthreads();
     const int64_t batch = row / a.rows_per_batch;
-    copy_rows(a.key + batch * a.key_batch_stride, a.key_row_stride, a.d, a.out + (row * a.n + j0) * a.d, np, s_pos);
+    copy_rows(a.key + batch * a.key_batch_stride, a.key_row_stride, a.d, a.out + (row * a.n + j0) * a.d, np, s_pos,
+              a.key_span - batch * a.key_batch_stride, a.err_flag);
     if (a.out2)
         copy_rows(a.key2 + batch * a.key2_batch_stride, a.key2_row_stride, a.d2, a.out2 + (row * a.n + j0) * a.d2, np,
-                  s_pos);
+                  s_pos, a.key2_span - batch * a.key2_batch_stride, a.err_flag);
 }
 
 // Order-preserving key of a score (larger value => larger key; -0 and +0 equal).
@@ -229,7 +233,9 @@ __global__ void __launch_bounds__(kGatherThreads) block_expand_kernel(const Bloc
             s_pos[i] = g;
         }
         __syncthreads();
-        if (kb) copy_rows(kb, a.key_row_stride, a.d, a.out + (row * npos + q0) * a.d, np, s_pos);
+        if (kb)
+            copy_rows(kb, a.key_row_stride, a.d, a.out + (row * npos + q0) * a.d, np, s_pos,
+                      a.key_span - (row / a.rows_per_batch) * a.key_batch_stride, a.err_flag);
         __syncthreads();
     }
 }

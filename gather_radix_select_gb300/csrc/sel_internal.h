@@ -9,6 +9,23 @@
 
 namespace sel {
 
+// Debug builds (-DSEL_DEBUG: the library libsel_debug.so) check selected accesses before they are
+// made -- staged-list and region offsets, workspace slots, output positions, gathered key rows.
+// SEL_IN_BOUNDS(cond, flag) is true when the access may go ahead; otherwise the access is skipped
+// and kStatusBounds (SEL_EBOUNDS) goes to *flag (the first nonzero status wins).  Normal builds
+// compile every check away (cond is not evaluated).
+constexpr int32_t kStatusBounds = 7;
+#if defined(__CUDACC__) && defined(SEL_DEBUG)
+__device__ __forceinline__ bool bounds_ok(bool ok, int32_t *flag)
+{
+    if (!ok && flag) atomicCAS(flag, 0, kStatusBounds);
+    return ok;
+}
+#define SEL_IN_BOUNDS(cond, flag) (::sel::bounds_ok((cond), (flag)))
+#else
+#define SEL_IN_BOUNDS(cond, flag) true
+#endif
+
 constexpr int kMaxLevels = 4;       // radix passes (digits) at most
 constexpr int kMaxSlice = 65536;    // elements of a row staged by one CTA (list offsets are 16-bit)
 constexpr int kMaxChunks = 16;      // bulk-copy chunks per CTA slice
@@ -75,10 +92,12 @@ struct TopkArgs {
     int32_t sample_min_cols;  // rows shorter than this use the exact first histogram
     // split_kernel workspace (see topk_impl.cuh for the layout)
     unsigned char *ws;
+    size_t ws_bytes;          // the workspace's size (debug-build checks)
     int64_t ws_counter_bytes, ws_row_bytes, ws_head_bytes, ws_part_bytes, ws_bits_bytes;
     // fused gather (ignored unless the gather variant is launched)
     const uint16_t *key;
     int64_t comp_len, d, key_batch_stride, key_row_stride, rows_per_batch;
+    int64_t key_span;         // elements from key[0] to the end of its last row (debug-build checks)
     int64_t n_gather;
     uint16_t *gather_out;     // [rows, n_gather, d]
 };
@@ -86,6 +105,7 @@ struct TopkArgs {
 struct GatherArgs {
     const uint16_t *key;
     int64_t comp_len, d, key_batch_stride, key_row_stride;
+    int64_t key_span, key2_span;  // elements from key[0] (key2[0]) to the end of its last row (debug checks)
     const void *idx;
     int32_t idx_i64;
     int64_t rows, n, idx_row_stride, rows_per_batch;
@@ -118,6 +138,7 @@ struct BlockArgs {
     // gather (key null = none), as GatherArgs
     const uint16_t *key;
     int64_t comp_len, d, key_batch_stride, key_row_stride, rows_per_batch;
+    int64_t key_span;
     uint16_t *out;            // [rows, topk_blocks * block_size, d]
     int32_t *err_flag;
     int32_t ctas_per_row;     // set by the launcher: several only when the kernel selects the blocks
@@ -152,6 +173,9 @@ cudaError_t launch_topk_f32(int mode, int threads, bool gather, size_t smem, con
                             int64_t grid, bool query, int *blocks_per_sm);
 cudaError_t launch_topk_bf16(int mode, int threads, bool gather, size_t smem, const TopkArgs &a, cudaStream_t s,
                              int64_t grid, bool query, int *blocks_per_sm);
+
+// One CTA whose bounded mbarrier wait runs out after `cycles` (test of the timeout path).
+cudaError_t launch_wait_selftest(int32_t *err_flag, long long cycles, cudaStream_t s);
 
 // Max dynamic shared memory a selection CTA may use on the current device.
 size_t topk_smem_limit();

@@ -313,15 +313,16 @@ __device__ __forceinline__ void set_err(int32_t *flag, int32_t code)
     if (flag) atomicCAS(flag, 0, code);
 }
 
-// Bounded wait on an mbarrier phase: after ~2 s the wait gives up, records
-// a timeout in err_flag and lets the CTA run on (its results are then unspecified).
-__device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, int32_t *err)
+// Bounded wait on an mbarrier phase: after `budget` clock cycles (~2 s by default) the wait gives
+// up, records a timeout in err_flag and lets the CTA run on (its results are then unspecified).
+__device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, int32_t *err,
+                                           long long budget = kWaitCycles)
 {
     constexpr uint32_t kSuspendNs = 100000;  // each try sleeps in hardware for up to 0.1 ms
     if (mbar_try_wait(bar, parity, kSuspendNs)) return;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity, kSuspendNs)) {
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > budget) {
             set_err(err, kStatusTimeout);
             return;
         }
@@ -434,6 +435,7 @@ __device__ void find_threshold(const uint32_t *h, int nb, uint32_t need, uint32_
 __device__ __forceinline__ void store_idx(const TopkArgs &a, int64_t row, int64_t pos, int64_t col)
 {
     if (!a.out_idx) return;
+    if (!SEL_IN_BOUNDS(row >= 0 && row < a.rows && pos >= 0 && pos < a.k, a.err_flag)) return;
     if (a.idx_i64)
         static_cast<int64_t *>(a.out_idx)[row * a.out_idx_stride + pos] = col;
     else
@@ -443,6 +445,7 @@ __device__ __forceinline__ void store_idx(const TopkArgs &a, int64_t row, int64_
 template <typename E>
 __device__ __forceinline__ void store_val(const TopkArgs &a, int64_t row, int64_t pos, E v)
 {
+    if (!SEL_IN_BOUNDS(row >= 0 && row < a.rows && pos >= 0 && pos < a.k, a.err_flag)) return;
     static_cast<E *>(a.out_val)[row * a.out_val_stride + pos] = v;
 }
 
@@ -484,8 +487,10 @@ __device__ void gather_rows_of(const TopkArgs &a, int64_t row, int64_t j0, int64
                     if (p < 0) p = 0;
                     if (p < a.comp_len) {
                         const uint4 *src = reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + c;
-                        v[u][0] = __ldg(src);
-                        v[u][1] = __ldg(src + lpr);
+                        if (SEL_IN_BOUNDS(bb * a.key_batch_stride + p * a.key_row_stride + a.d <= a.key_span, a.err_flag)) {
+                            v[u][0] = __ldg(src);
+                            v[u][1] = __ldg(src + lpr);
+                        }
                     } else if (c == 0) {
                         set_err(a.err_flag, kStatusInval);
                     }
@@ -494,7 +499,7 @@ __device__ void gather_rows_of(const TopkArgs &a, int64_t row, int64_t j0, int64
 #pragma unroll
             for (int u = 0; u < UR; ++u) {
                 const int jj = jb + u * rstep;
-                if (jj < nrows) {
+                if (jj < nrows && SEL_IN_BOUNDS(row < a.rows && j0 + jj < a.n_gather, a.err_flag)) {
                     uint4 *dst = ob + (static_cast<int64_t>(jj) << vsh) + c;
                     __stcs(dst, v[u][0]);
                     __stcs(dst + lpr, v[u][1]);
@@ -514,16 +519,17 @@ __device__ void gather_rows_of(const TopkArgs &a, int64_t row, int64_t j0, int64
                 const int64_t j = j0 + jj;
                 int64_t p = glist ? static_cast<int64_t>(glist[jj]) : (j < n_short ? j : 0);
                 if (p < 0) p = 0;
-                if (p < a.comp_len)
-                    v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + (t - jj * vpr));
-                else if (t - jj * vpr == 0)
+                if (p < a.comp_len) {
+                    if (SEL_IN_BOUNDS(bb * a.key_batch_stride + p * a.key_row_stride + a.d <= a.key_span, a.err_flag))
+                        v[u] = __ldg(reinterpret_cast<const uint4 *>(kb + p * a.key_row_stride) + (t - jj * vpr));
+                } else if (t - jj * vpr == 0)
                     set_err(a.err_flag, kStatusInval);
             }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int t = t0 + u * NT;
-            if (t < total) __stcs(ob + t, v[u]);
+            if (t < total && SEL_IN_BOUNDS(row < a.rows && j0 + t / vpr < a.n_gather, a.err_flag)) __stcs(ob + t, v[u]);
         }
     }
 }
@@ -671,7 +677,9 @@ __device__ int filter_to_list(const TopkArgs &a, const E *buf, int len, uint32_t
             uint32_t m = masks[v];
             while (m) {
                 const int b = __ffs(m) - 1;
-                list[pos++] = static_cast<uint16_t>(v * V + b);
+                if (SEL_IN_BOUNDS(v * V + b < len && pos < static_cast<uint32_t>(cap), a.err_flag))
+                    list[pos] = static_cast<uint16_t>(v * V + b);
+                ++pos;
                 m &= m - 1u;
             }
         }
@@ -856,7 +864,7 @@ __device__ bool select_segments(const TopkArgs &a, int64_t row, const Segments<E
             if (c == P) take = (r++ < E_need);
             if (take) {
                 if (by_position) {
-                    src[pos] = static_cast<uint16_t>(f);
+                    if (SEL_IN_BOUNDS(pos < static_cast<uint32_t>(a.k), a.err_flag)) src[pos] = static_cast<uint16_t>(f);
                 } else {
                     const int64_t col = seg_col(sg, s, i);
                     store_idx(a, row, pos, col);
@@ -1009,7 +1017,8 @@ __device__ bool select_staged(const TopkArgs &a, int64_t row, const Segments<E> 
                 if (take) {
                     const uint32_t i = static_cast<uint32_t>(first + t);
                     if (by_position) {
-                        src[pos] = static_cast<uint16_t>(sg.pre[seg] + i);
+                        if (SEL_IN_BOUNDS(pos < static_cast<uint32_t>(a.k), a.err_flag))
+                            src[pos] = static_cast<uint16_t>(sg.pre[seg] + i);
                     } else {
                         const int64_t col = seg_col(sg, seg, i);
                         store_idx(a, row, pos, col);
@@ -1209,7 +1218,11 @@ __global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(c
                 const bool in = j * V + t < cnt;
                 bool take = in && c > P;
                 if (in && c == P) take = r++ < E_need;
-                if (take) src[pos++] = static_cast<uint16_t>(e0 + j * V + t);
+                if (take) {
+                    if (SEL_IN_BOUNDS(pos < static_cast<uint32_t>(k) && e0 + j * V + t < n, a.err_flag))
+                        src[pos] = static_cast<uint16_t>(e0 + j * V + t);
+                    ++pos;
+                }
             }
         }
     }
@@ -1395,7 +1408,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
             if (c == P) take = (r++ < E_need);
             if (take) {
                 if (by_position) {
-                    src[pos] = static_cast<uint16_t>(o);
+                    if (SEL_IN_BOUNDS(pos < static_cast<uint32_t>(k) && o < len, a.err_flag)) src[pos] = static_cast<uint16_t>(o);
                 } else {
                     store_idx(a, row, pos, o);
                     if (a.want_values) store_val<E>(a, row, pos, e);
@@ -1544,6 +1557,8 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
     const int len = hi > lo ? static_cast<int>(hi - lo) : 0;
 
     unsigned char *wrow = a.ws + a.ws_counter_bytes + row * a.ws_row_bytes;
+    if (!SEL_IN_BOUNDS(static_cast<size_t>(a.ws_counter_bytes + (row + 1) * a.ws_row_bytes) <= a.ws_bytes, a.err_flag))
+        return;
     uint32_t *w_count = reinterpret_cast<uint32_t *>(wrow);
     uint32_t *w_tkey = w_count + P;
     unsigned char *wpart = wrow + a.ws_head_bytes + static_cast<int64_t>(part) * a.ws_part_bytes;
@@ -1568,6 +1583,7 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) split_kernel(const T
         if (fits) {
             for (int i = tid; i < L; i += NT) {
                 const int o = list[i];
+                if (!SEL_IN_BOUNDS(i < a.list_cap && o < len, a.err_flag)) continue;
                 w_bits[i] = buf[o];
                 w_cols[i] = static_cast<int32_t>(lo + o);
             }
@@ -2007,7 +2023,7 @@ __device__ void select_regions(const TopkArgs &a, int64_t row, uint2 *list, int 
             const uint32_t be = __ballot_sync(kFull, eq);
             const bool take = gt || (eq && ties + __popc(be & lt) < E_need);
             const uint32_t bt = __ballot_sync(kFull, take);
-            if (take) {
+            if (take && SEL_IN_BOUNDS(pos + __popc(bt & lt) < static_cast<uint32_t>(a.k), a.err_flag)) {
                 const uint32_t p = pos + __popc(bt & lt);
                 const int32_t col = static_cast<int32_t>(e.y & ~kMark);
                 if (oi64) oi64[p] = col;
@@ -2218,6 +2234,9 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
         }
         povf |= tp > static_cast<uint32_t>(a.part_cap);
         unsigned char *prow = a.ws + a.ws_counter_bytes + row * a.ws_row_bytes;
+        povf |= !SEL_IN_BOUNDS(static_cast<size_t>(a.ws_counter_bytes + (row + 1) * a.ws_row_bytes) <= a.ws_bytes &&
+                                   static_cast<int64_t>(P) * a.ws_part_bytes <= a.ws_row_bytes,
+                               a.err_flag);
         if (!povf) {
             uint2 *dst = reinterpret_cast<uint2 *>(prow + part * a.ws_part_bytes + 16) + pre;
             const uint32_t c = s_cnt[warp];
@@ -2665,7 +2684,14 @@ __device__ void flat_select_row(const TopkArgs &a, int64_t row, unsigned char *s
         for (int s0 = 0; s0 < cpr; s0 += 32) {
             const int s = s0 + gt;
             uint4 h = make_uint4(0u, 0u, 0u, 0u);
-            if (s < cpr) h = __ldcg(reinterpret_cast<const uint4 *>(wrow + static_cast<int64_t>(s) * a.ws_part_bytes));
+            if (s < cpr) {
+                if (SEL_IN_BOUNDS(static_cast<size_t>(a.ws_counter_bytes + row * a.ws_row_bytes + (s + 1) * a.ws_part_bytes) <=
+                                      a.ws_bytes,
+                                  a.err_flag))
+                    h = __ldcg(reinterpret_cast<const uint4 *>(wrow + static_cast<int64_t>(s) * a.ws_part_bytes));
+                else
+                    h.x = kSlotOverflow;
+            }
             bad |= h.x == kSlotOverflow;
             c = h.x == kSlotOverflow ? 0u : h.x;
             thi = max(thi, h.y);
@@ -2834,6 +2860,11 @@ __device__ void flat_help(const TopkArgs &a, unsigned char *smem, FlatShared &fs
         S::sync();
         // flush: the 24 regions, concatenated, into the chunk's slot
         unsigned char *slot = a.ws + a.ws_counter_bytes + row * a.ws_row_bytes + static_cast<int64_t>(j) * a.ws_part_bytes;
+        const bool slot_ok =
+            SEL_IN_BOUNDS(static_cast<size_t>(a.ws_counter_bytes + row * a.ws_row_bytes + (j + 1) * a.ws_part_bytes) <=
+                              a.ws_bytes &&
+                              16 + static_cast<int64_t>(SW) * wcap * 8 <= a.ws_part_bytes,
+                          a.err_flag);
         uint2 *dst = reinterpret_cast<uint2 *>(slot + 16);
         const uint2 *src = reinterpret_cast<const uint2 *>(smem + a.smem_cbuf_off) + b * SW * (wcap + 1);
         if (gt < 32) {
@@ -2842,12 +2873,13 @@ __device__ void flat_help(const TopkArgs &a, unsigned char *smem, FlatShared &fs
             const bool ovf = __any_sync(kFull, c == kSlotOverflow);
             uint32_t tot;
             const uint32_t ex = warp_exclusive_scan(ovf ? 0u : c, lane, tot);
-            if (lane < SW) fs.s_pre[lane] = ex;
+            if (lane < SW) fs.s_pre[lane] = slot_ok ? ex : 0u;
             const uint32_t km = __reduce_max_sync(kFull, lane < SW ? vmax[lane] : 0u);
             const bool nan = __any_sync(kFull, lane < SW && vnan[lane] != 0u);
             if (lane == 0) {
-                fs.s_pre[SW] = ovf ? 0u : tot;
-                __stcg(reinterpret_cast<uint4 *>(slot), make_uint4(ovf ? kSlotOverflow : tot, km, nan ? 1u : 0u, 0u));
+                fs.s_pre[SW] = ovf || !slot_ok ? 0u : tot;
+                if (slot_ok)
+                    __stcg(reinterpret_cast<uint4 *>(slot), make_uint4(ovf ? kSlotOverflow : tot, km, nan ? 1u : 0u, 0u));
                 if (nan && a.nan_flag) atomicOr(a.nan_flag, 1);
             }
         }
@@ -2907,6 +2939,21 @@ __global__ void __launch_bounds__(kFlatThreads, 1) flat_kernel(const TopkArgs a)
     FlatAll::sync();
     const uint32_t d = fs.defer;
     if (d) flat_select_row<E, FlatAll>(a, static_cast<int64_t>(d) - 1, smem, fs, s_seg);
+}
+
+// Self-test of the bounded wait above: one thread arms an mbarrier for 16 bytes that no copy will
+// ever deliver (none is issued), and every thread waits on it with a budget of `cycles`.  The
+// wait runs out, records SEL_ETIMEOUT in err_flag, and the CTA returns with nothing in flight.
+__global__ void wait_selftest_kernel(int32_t *err_flag, long long cycles)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&bar, 16);
+    }
+    __syncthreads();
+    wait_phase(&bar, 0u, err_flag, cycles);
 }
 
 // Raises a kernel's dynamic shared-memory limit once per device; later calls that need no more

@@ -91,7 +91,8 @@ typedef enum {
     SEL_EUNSUPPORTED = 3, /* dtype / width outside what the kernels handle */
     SEL_ECUDA = 4,        /* a CUDA runtime call failed (launch, attribute query) */
     SEL_ETIMEOUT = 5,     /* (device flag only) a bounded device wait ran out */
-    SEL_ESCRATCH = 6      /* sel_topk_noalloc: the shape needs more scratch than the built-in array */
+    SEL_ESCRATCH = 6,     /* sel_topk_noalloc: the shape needs more scratch than the built-in array */
+    SEL_EBOUNDS = 7       /* (device flag, debug build only) an out-of-bounds access was caught and skipped */
 } sel_status;
 
 enum { SEL_F32 = 0, SEL_BF16 = 1 };  /* input element type */

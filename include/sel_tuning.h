@@ -47,6 +47,26 @@ SEL_API int sel_set_tuning(int knob, int value);
 /* A knob's current value, or -1 for an unknown knob. */
 SEL_API int sel_get_tuning(int knob);
 
+/* 1 when this library is the debug build (libsel_debug.so, compiled with
+ * SEL_DEBUG): its kernels check their staged-list and region offsets,
+ * workspace slots, output positions and gathered key rows before each
+ * access, skip an access that would fall outside its buffer and write
+ * SEL_EBOUNDS to err_flag.  0 for the normal build, where those checks are
+ * compiled away. */
+SEL_API int sel_debug_build(void);
+
+/* Test of the failure path of the kernels' bounded waits (the tutorial's
+ * kernel traps on a NaN; this library never traps, and every wait on a
+ * barrier gives up after a bound and reports SEL_ETIMEOUT instead).  Launches
+ * on `stream` one CTA that waits, with a budget of `cycles` GPU clock cycles,
+ * on a barrier armed for 16 bytes that no copy ever delivers (none is issued,
+ * so nothing lands after the wait gives up).  The wait runs out, writes
+ * SEL_ETIMEOUT to the caller-owned, zeroed *err_flag and the CTA returns;
+ * the stream and the context stay usable.  Returns SEL_EINVAL for a NULL
+ * err_flag or negative cycles, SEL_ECUDA if the launch fails, else SEL_OK
+ * (asynchronous: read err_flag after synchronising). */
+SEL_API int sel_selftest_wait_timeout(int32_t *err_flag, long long cycles, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
                                          "sel_max_cols", "sel_stride_requirement",
                                          "sel_strerror", "sel_topk", "sel_topk_gather", "sel_topk_kernel_name",
                                          "sel_topk_noalloc", "sel_topk_workspace_size", "sel_set_tuning",
-                                         "sel_get_tuning"])
+                                         "sel_get_tuning", "sel_selftest_wait_timeout", "sel_debug_build"])
 
 
 def test_tuning_knobs_round_trip_and_reject_bad_values(lib):
@@ -54,6 +54,13 @@ def test_tuning_knobs_round_trip_and_reject_bad_values(lib):
         g.set_tuning(**saved)
 
 
+def test_wait_selftest_rejects_bad_arguments_on_the_host(lib):
+    SEL_EINVAL = 1
+    assert lib.sel_selftest_wait_timeout(None, 1000, None) == SEL_EINVAL
+    flag = ctypes.c_int32(0)
+    assert lib.sel_selftest_wait_timeout(ctypes.byref(flag), -1, None) == SEL_EINVAL
+
+
 def test_every_declared_symbol_is_exported(lib):
     from gather_radix_select_gb300 import _native
     for name in declared_symbols():
@@ -66,8 +73,8 @@ def test_stride_requirement_and_messages(lib):
     assert lib.sel_stride_requirement(ctypes.byref(a), ctypes.byref(b)) == 0
     assert (a.value, b.value) == (16, 16)
     assert lib.sel_stride_requirement(None, None) == 0
-    for st in range(7):
-        assert lib.sel_strerror(st)
+    for st in range(8):
+        assert lib.sel_strerror(st) != b"unknown status"
     assert lib.sel_strerror(99) == b"unknown status"
 
 
