@@ -218,10 +218,34 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-class Runner:
-    """Device-resident inputs/outputs of one workload and the call that is timed."""
+def shard_plan(w, rank: int, world: int):
+    """This rank's share of `world` copies of workload w laid end to end along rows (weak scaling):
+    rows partitioned with gather_radix_select_gb300.shard (dual chunks when rows have ends, blocks
+    otherwise).  Returns (global rows of this rank, pieces), a piece being (local start, local stop,
+    first key batch, stop key batch) of one library call; key batches index `world` copies of the
+    workload's key.  One rank: the whole workload in one call."""
+    from gather_radix_select_gb300 import shard
 
-    def __init__(self, w, dev, sorted_value=False):
+    R = w["rows"]
+    mode = "dual_chunk" if w["row_end"] is not None else "blocks"
+    ranges = shard.partition_rows(R * world, world, mode)[rank]
+    grows = shard.rows_of(ranges)
+    if w.get("key") is not None:
+        glob = shard.call_pieces(ranges, w["rows_per_batch"])
+    else:
+        glob = [(s, e, 0, 0) for s, e in ranges]
+    pieces, at = [], 0
+    for s, e, b0, b1 in glob:
+        pieces.append((at, at + (e - s), b0, b1))
+        at += e - s
+    return grows, pieces, mode
+
+
+class Runner:
+    """Device-resident inputs/outputs of one rank's share of a workload and the calls that are timed
+    (one rank: the whole workload, one call)."""
+
+    def __init__(self, w, dev, sorted_value=False, rank=0, world=1):
         import torch
 
         import gather_radix_select_gb300 as g
@@ -230,43 +254,60 @@ class Runner:
         # value-ordered output instead of the workload's own order (a second launch per step)
         self.sorted_value = sorted_value
         self.sorted_index = w["sorted_index"] and not sorted_value
+        self.grows, self.pieces, self.mode = shard_plan(w, rank, world)
+        local = self.grows % w["rows"]  # the workload row behind each of this rank's rows
+        whole = world == 1
+        xb = w["x"] if whole else np.ascontiguousarray(w["x"][local])
         if w["dtype"] == "f32":
-            self.x = torch.from_numpy(w["x"].view(np.int32)).view(torch.float32).to(dev)
+            self.x = torch.from_numpy(xb.view(np.int32)).view(torch.float32).to(dev)
         else:
-            self.x = torch.from_numpy(w["x"].view(np.int16)).view(torch.bfloat16).to(dev)
+            self.x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
         self.x = self.x[:, :w["cols"]]
-        self.end = None if w["row_end"] is None else torch.from_numpy(w["row_end"]).to(dev)
+        self.rows = len(self.grows)
+        self.end = None if w["row_end"] is None else torch.from_numpy(
+            w["row_end"] if whole else np.ascontiguousarray(w["row_end"][local])).to(dev)
         self.idx_t = torch.int64 if w["idx_dtype"] == "i64" else torch.int32
         self.key = None
         if w.get("key") is not None:
-            self.key = torch.from_numpy(w["key"].view(np.int16)).view(torch.bfloat16).to(dev)
-            self.gout = torch.empty((w["rows"], w["n_gather"], w["d"]), dtype=torch.bfloat16, device=dev)
+            key = torch.from_numpy(w["key"].view(np.int16)).view(torch.bfloat16).to(dev)
+            self.key = key if whole else torch.cat([key] * world)
+            self.gout = torch.empty((self.rows, w["n_gather"], w["d"]), dtype=torch.bfloat16, device=dev)
         self.nan = torch.zeros(1, dtype=torch.int32, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        # outputs allocated once (rows padded to 16 bytes), so a step is the library call alone
+        # outputs allocated once (rows padded to 16 bytes), so a step is the library calls alone
         k = w["k"]
         ipad = (k + 3) // 4 * 4 if self.idx_t == torch.int32 else (k + 1) // 2 * 2
-        self.out_idx = torch.empty((w["rows"], ipad), dtype=self.idx_t, device=dev)
+        self.out_idx = torch.empty((self.rows, ipad), dtype=self.idx_t, device=dev)
         self.out_val = None
         if w["want_values"]:
             vpad = (k + 3) // 4 * 4 if w["dtype"] == "f32" else (k + 7) // 8 * 8
-            self.out_val = torch.empty((w["rows"], vpad), dtype=self.x.dtype, device=dev)
-        # one fused launch; value order adds the ordering launch (and then a separate gather)
-        self.launches_per_step = 1 if not sorted_value else (3 if self.key is not None else 2)
+            self.out_val = torch.empty((self.rows, vpad), dtype=self.x.dtype, device=dev)
+        # one fused launch per piece; value order adds the ordering launch (and then a separate gather)
+        per = 1 if not sorted_value else (3 if self.key is not None else 2)
+        self.launches_per_step = per * len(self.pieces)
+
+    def local_workload(self):
+        """The workload's rows of this rank (for byte counts)."""
+        return self.w if len(self.grows) == self.w["rows"] and (self.grows == np.arange(self.rows)).all() \
+            else syn.row_subset(self.w, self.grows % self.w["rows"])
 
     def step(self):
         w = self.w
-        if self.key is not None:
-            return self.g.topk_gather(self.x, w["k"], self.key, w["n_gather"], end=self.end,
-                                      sorted_index=self.sorted_index, sorted_value=self.sorted_value,
-                                      indices_type=self.idx_t,
-                                      return_value=w["want_values"], gather_out=self.gout,
-                                      output_idx=self.out_idx, output_val=self.out_val,
-                                      nan_flag=self.nan, err_flag=self.err)
-        return self.g.topk(self.x, w["k"], end=self.end, sorted_index=self.sorted_index,
-                           sorted_value=self.sorted_value, indices_type=self.idx_t,
-                           return_value=w["want_values"], output_idx=self.out_idx, output_val=self.out_val,
-                           nan_flag=self.nan, err_flag=self.err)
+        for lo, hi, b0, b1 in self.pieces:
+            end = None if self.end is None else self.end[lo:hi]
+            ov = None if self.out_val is None else self.out_val[lo:hi]
+            if self.key is not None:
+                self.g.topk_gather(self.x[lo:hi], w["k"], self.key[b0:b1], w["n_gather"], end=end,
+                                   sorted_index=self.sorted_index, sorted_value=self.sorted_value,
+                                   indices_type=self.idx_t,
+                                   return_value=w["want_values"], gather_out=self.gout[lo:hi],
+                                   output_idx=self.out_idx[lo:hi], output_val=ov,
+                                   nan_flag=self.nan, err_flag=self.err)
+            else:
+                self.g.topk(self.x[lo:hi], w["k"], end=end, sorted_index=self.sorted_index,
+                            sorted_value=self.sorted_value, indices_type=self.idx_t,
+                            return_value=w["want_values"], output_idx=self.out_idx[lo:hi], output_val=ov,
+                            nan_flag=self.nan, err_flag=self.err)
 
 
 def time_steps(runner, steps, warmup, flush):
@@ -294,9 +335,24 @@ def time_steps(runner, steps, warmup, flush):
     return [a.elapsed_time(b) for a, b in evs]
 
 
-def e2e_measure(w, dev, steps, warmup):
-    """Same step through the public API with host buffers: pinned H2D of the inputs,
-    the call, D2H of every output, all inside the timed region."""
+def e2e_pieces(w, chunks: int):
+    """Row pieces of the end-to-end pipeline: `chunks` blocks of rows, cut where a fused call needs it
+    (one key batch per piece unless the piece holds whole batches).  (start, stop, first key batch,
+    stop key batch)."""
+    from gather_radix_select_gb300 import shard
+
+    blocks = [r for rs in shard.partition_rows(w["rows"], chunks, "blocks") for r in rs]
+    if w.get("key") is None:
+        return [(s, e, 0, 0) for s, e in blocks]
+    return [p for b in blocks for p in shard.call_pieces([b], w["rows_per_batch"])]
+
+
+def e2e_measure(w, dev, steps, warmup, chunks=4):
+    """The step through the public API with host buffers, every copy inside the timed region: the
+    inputs go host -> device in row chunks from pinned memory on one stream, each chunk's call runs
+    on a second stream as soon as its rows have landed, and its outputs go back to pinned host
+    memory on a third, so the copy of chunk j+1, the call on chunk j and the copy back of chunk
+    j-1 overlap.  Returns (ms per step, host->device bytes, device->host bytes)."""
     import torch
 
     import gather_radix_select_gb300 as g
@@ -308,63 +364,92 @@ def e2e_measure(w, dev, steps, warmup):
     if w.get("key") is not None:
         host_key = torch.from_numpy(w["key"].view(np.int16)).view(torch.bfloat16).pin_memory()
     idx_t = torch.int64 if w["idx_dtype"] == "i64" else torch.int32
+    R, k = w["rows"], w["k"]
     x = torch.empty(host_x.shape, dtype=tdt, device=dev)
     end = None if host_end is None else torch.empty(host_end.shape, dtype=torch.int32, device=dev)
     key = None if host_key is None else torch.empty(host_key.shape, dtype=torch.bfloat16, device=dev)
-    outs_host = None
+    # outputs: device buffers written by the calls, pinned host buffers they are read back into
+    ipad = (k + 3) // 4 * 4 if idx_t == torch.int32 else (k + 1) // 2 * 2
+    out_idx = torch.empty((R, ipad), dtype=idx_t, device=dev)
+    out_val = None
+    if w["want_values"]:
+        vpad = (k + 3) // 4 * 4 if w["dtype"] == "f32" else (k + 7) // 8 * 8
+        out_val = torch.empty((R, vpad), dtype=tdt, device=dev)
+    gout = None if key is None else torch.empty((R, w["n_gather"], w["d"]), dtype=torch.bfloat16, device=dev)
+    h_idx = torch.empty((R, k), dtype=idx_t, pin_memory=True)
+    h_val = None if out_val is None else torch.empty((R, k), dtype=tdt, pin_memory=True)
+    h_g = None if gout is None else torch.empty(tuple(gout.shape), dtype=torch.bfloat16, pin_memory=True)
+    pieces = e2e_pieces(w, chunks)
+    s_in, s_run, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    main = torch.cuda.current_stream(dev)
     h2d = host_x.numel() * host_x.element_size() + (0 if host_end is None else host_end.numel() * 4) + \
         (0 if host_key is None else host_key.numel() * 2)
+    d2h = h_idx.numel() * h_idx.element_size() + (0 if h_val is None else h_val.numel() * h_val.element_size()) + \
+        (0 if h_g is None else h_g.numel() * 2)
 
     def one():
-        nonlocal outs_host
-        x.copy_(host_x, non_blocking=True)
-        if end is not None:
-            end.copy_(host_end, non_blocking=True)
-        if key is not None:
-            key.copy_(host_key, non_blocking=True)
-        xv = x[:, :w["cols"]]
-        if key is not None:
-            vals, idx, gout = g.topk_gather(xv, w["k"], key, w["n_gather"], end=end, sorted_index=w["sorted_index"],
-                                            indices_type=idx_t, return_value=w["want_values"])
-            outs = [t for t in (vals, idx, gout) if t is not None]
-        else:
-            vals, idx = g.topk(xv, w["k"], end=end, sorted_index=w["sorted_index"], indices_type=idx_t,
-                               return_value=w["want_values"])
-            outs = [t for t in (vals, idx) if t is not None]
-        if outs_host is None:
-            outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-        for hdst, t in zip(outs_host, outs):
-            hdst.copy_(t, non_blocking=True)
-        return outs
+        start = torch.cuda.Event()
+        start.record(main)
+        for st in (s_in, s_run, s_out):
+            st.wait_event(start)
+        with torch.cuda.stream(s_in):
+            if key is not None:
+                key.copy_(host_key, non_blocking=True)
+        for lo, hi, b0, b1 in pieces:
+            landed, done = torch.cuda.Event(), torch.cuda.Event()
+            with torch.cuda.stream(s_in):
+                x[lo:hi].copy_(host_x[lo:hi], non_blocking=True)
+                if end is not None:
+                    end[lo:hi].copy_(host_end[lo:hi], non_blocking=True)
+                landed.record(s_in)
+            s_run.wait_event(landed)
+            xv = x[lo:hi, :w["cols"]]
+            ev = None if end is None else end[lo:hi]
+            ov = None if out_val is None else out_val[lo:hi]
+            if key is not None:
+                g.topk_gather(xv, k, key[b0:b1], w["n_gather"], end=ev, sorted_index=w["sorted_index"],
+                              indices_type=idx_t, return_value=w["want_values"], output_idx=out_idx[lo:hi],
+                              output_val=ov, gather_out=gout[lo:hi], stream=s_run)
+            else:
+                g.topk(xv, k, end=ev, sorted_index=w["sorted_index"], indices_type=idx_t,
+                       return_value=w["want_values"], output_idx=out_idx[lo:hi], output_val=ov, stream=s_run)
+            done.record(s_run)
+            s_out.wait_event(done)
+            with torch.cuda.stream(s_out):
+                h_idx[lo:hi].copy_(out_idx[lo:hi, :k], non_blocking=True)
+                if h_val is not None:
+                    h_val[lo:hi].copy_(out_val[lo:hi, :k], non_blocking=True)
+                if h_g is not None:
+                    h_g[lo:hi].copy_(gout[lo:hi], non_blocking=True)
+        for st in (s_in, s_run, s_out):
+            main.wait_stream(st)
 
     for _ in range(warmup):
         one()
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a.record(main)
     for _ in range(steps):
-        outs = one()
-    b.record(stream)
+        one()
+    b.record(main)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
-    d2h = sum(t.numel() * t.element_size() for t in outs)
-    return ms, h2d, d2h
+    return a.elapsed_time(b) / steps, h2d, d2h
 
 
 def combine_ranks(ms_step: float, nbytes: int, dist, device):
-    """Replicas: every rank runs the same per-GPU workload.  The step time is the slowest rank's;
-    the value is the bytes all ranks processed per second (GB/s).  dist None = one rank."""
+    """Every rank times its own share.  The step time is the slowest rank's; the value is the bytes all
+    ranks processed (each rank's own count, summed) per second (GB/s).  dist None = one rank."""
     import torch
 
-    ms_max = ms_step
-    world = 1
+    ms_max, total = ms_step, float(nbytes)
     if dist is not None:
-        world = dist.get_world_size()
         t = torch.tensor([ms_step], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_max = float(t.item())
-    return ms_max, nbytes * world / (ms_max * 1e-3) / 1e9
+        b = torch.tensor([float(nbytes)], dtype=torch.float64, device=device)
+        dist.all_reduce(b, op=dist.ReduceOp.SUM)
+        total = float(b.item())
+    return ms_max, total / (ms_max * 1e-3) / 1e9
 
 
 def gpu_arm(args):
@@ -380,7 +465,7 @@ def gpu_arm(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = syn.workload(args.workload)
-    runner = Runner(w, dev, sorted_value=args.sorted_value)
+    runner = Runner(w, dev, sorted_value=args.sorted_value, rank=rank, world=world)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     peak, peak_kind = measured_peaks()
 
@@ -401,8 +486,9 @@ def gpu_arm(args):
     if dist:
         dist.barrier()
     ms_step = sum(times) / len(times)
-    nbytes = step_bytes(w)
+    nbytes = step_bytes(runner.local_workload())  # this rank's rows
     ms_max, value = combine_ranks(ms_step, nbytes, dist, dev)
+    nbytes = step_bytes(w)  # per workload copy (one GPU's share)
     err_flag = int(runner.err.item())
 
     result = None
@@ -440,14 +526,16 @@ def gpu_arm(args):
                        "cols": w["cols"], "k": w["k"], "algorithmic_bytes_per_step": nbytes,
                        "rows_per_s": round(w["rows"] * world / (ms_max * 1e-3), 1),
                        "l2": "flushed before every timed step (256 MiB write, untimed)",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+                       "parallelism": ("rows of %d workload copies sharded over %d GPUs (%s)" % (world, world, runner.mode))
+                       if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "kernel": kname + ("<%s,gather>" % w["dtype"] if fused else "<%s>" % w["dtype"]),
                          "algorithmic_bytes": nbytes, "peak_kind": peak_kind},
             "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                    "ms_per_step": round(e2e_ms, 4)},
+                    "ms_per_step": round(e2e_ms, 4),
+                    "pipeline": "inputs copied in, selected and copied out in 4 row chunks on three streams"},
             "gpu_launches": args.steps * runner.launches_per_step,
             "cpu_baseline": cpu,
             "clocks": clocks,

@@ -79,20 +79,23 @@ def kernel_name(dtype: torch.dtype, rows: int, cols: int, k: int, n_gather: int 
 
 
 _KNOBS = {"plan": _native.SEL_TUNE_PLAN, "parts": _native.SEL_TUNE_PARTS,
-          "row_sample": _native.SEL_TUNE_ROW_SAMPLE, "hist_agg": _native.SEL_TUNE_HIST_AGG}
+          "row_sample": _native.SEL_TUNE_ROW_SAMPLE, "hist_agg": _native.SEL_TUNE_HIST_AGG,
+          "row_order": _native.SEL_TUNE_ROW_ORDER}
 
 
 def set_tuning(plan: str | None = None, parts: int | None = None, row_sample: bool | None = None,
-               hist_agg: bool | None = None) -> None:
+               hist_agg: bool | None = None, row_order: bool | None = None) -> None:
     """Tuning and test hooks (include/sel_tuning.h); None leaves a knob as it is.
 
     ``plan``: "auto" or the kernel to force where it can run a shape ("reg", "row", "wide",
     "split", "stream", "flat").  ``parts``: parts per row of the streaming kernel's split mode
-    (0 = automatic).  Process-wide; takes effect on the next call."""
+    (0 = automatic).  ``row_order``: with per-row ends, CTAs take rows from both ends of the batch
+    alternately (default False: in order, measured faster).  Process-wide; takes effect on the next call."""
     lib = _native.load()
     vals = {"plan": None if plan is None else _native.SEL_PLANS[plan], "parts": parts,
             "row_sample": None if row_sample is None else int(bool(row_sample)),
-            "hist_agg": None if hist_agg is None else int(bool(hist_agg))}
+            "hist_agg": None if hist_agg is None else int(bool(hist_agg)),
+            "row_order": None if row_order is None else int(bool(row_order))}
     for name, v in vals.items():
         if v is not None:
             _native.check(lib.sel_set_tuning(_KNOBS[name], int(v)), "sel_set_tuning(%s)" % name)
@@ -105,7 +108,8 @@ def get_tuning() -> dict:
     return {"plan": plans[lib.sel_get_tuning(_native.SEL_TUNE_PLAN)],
             "parts": int(lib.sel_get_tuning(_native.SEL_TUNE_PARTS)),
             "row_sample": bool(lib.sel_get_tuning(_native.SEL_TUNE_ROW_SAMPLE)),
-            "hist_agg": bool(lib.sel_get_tuning(_native.SEL_TUNE_HIST_AGG))}
+            "hist_agg": bool(lib.sel_get_tuning(_native.SEL_TUNE_HIST_AGG)),
+            "row_order": bool(lib.sel_get_tuning(_native.SEL_TUNE_ROW_ORDER))}
 
 
 def _workspace(nbytes: int, device, stream):

@@ -17,7 +17,7 @@ SEL_F32, SEL_BF16 = 0, 1
 SEL_I32, SEL_I64 = 0, 1
 SEL_MAX_K = 4096
 # include/sel_tuning.h
-SEL_TUNE_PLAN, SEL_TUNE_PARTS, SEL_TUNE_ROW_SAMPLE, SEL_TUNE_HIST_AGG = range(4)
+SEL_TUNE_PLAN, SEL_TUNE_PARTS, SEL_TUNE_ROW_SAMPLE, SEL_TUNE_HIST_AGG, SEL_TUNE_ROW_ORDER = range(5)
 SEL_PLANS = {"auto": -1, "reg": 0, "row": 1, "wide": 2, "split": 3, "stream": 4, "flat": 5}
 
 # every symbol include/sel.h declares, with its ctypes signature

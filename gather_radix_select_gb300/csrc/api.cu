@@ -139,7 +139,7 @@ size_t layout_workspace(int dtype, int64_t rows, int parts, int64_t cap, sel::To
 // Tuning knobs (include/sel_tuning.h): read from the environment once, when first needed, and
 // settable at any time through sel_set_tuning.  The plan cache is keyed on them.
 struct Tuning {
-    std::atomic<int> plan{SEL_PLAN_AUTO}, parts{0}, row_sample{0}, hist_agg{0};
+    std::atomic<int> plan{SEL_PLAN_AUTO}, parts{0}, row_sample{0}, hist_agg{0}, row_order{0};
 };
 
 int plan_from_name(const char *v)
@@ -166,6 +166,8 @@ Tuning &tuning()
         n->row_sample = (e && e[0] == '1') ? 1 : 0;
         e = std::getenv("SEL_HIST_AGG");
         n->hist_agg = (e && e[0] == '1') ? 1 : 0;
+        e = std::getenv("SEL_ROW_ORDER");
+        n->row_order = (e && e[0] == '1') ? 1 : 0;
         return n;
     }();
     return *t;
@@ -626,6 +628,7 @@ int run_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
     a.stride = stride;
     a.row_end = row_end;
     a.row_end_div = row_end_div;
+    a.row_order = row_end && tuning().row_order.load(std::memory_order_relaxed) ? 1 : 0;
     a.k = k;
     a.idx_i64 = idx_dtype == SEL_I64;
     a.want_values = want_values ? 1 : 0;
@@ -691,6 +694,9 @@ int sel_set_tuning(int knob, int value)
     case SEL_TUNE_HIST_AGG:
         t.hist_agg = value ? 1 : 0;
         return SEL_OK;
+    case SEL_TUNE_ROW_ORDER:
+        t.row_order = value ? 1 : 0;
+        return SEL_OK;
     default: return SEL_EINVAL;
     }
 }
@@ -703,6 +709,7 @@ int sel_get_tuning(int knob)
     case SEL_TUNE_PARTS: return t.parts.load();
     case SEL_TUNE_ROW_SAMPLE: return t.row_sample.load();
     case SEL_TUNE_HIST_AGG: return t.hist_agg.load();
+    case SEL_TUNE_ROW_ORDER: return t.row_order.load();
     default: return -1;
     }
 }

@@ -59,6 +59,7 @@ struct TopkArgs {
     int64_t rows, cols, stride;
     const int32_t *row_end;   // nullable
     int64_t row_end_div;      // > 1: a row has ceil(row_end / row_end_div) valid columns
+    int32_t row_order;        // 1: CTA (or CTA group) b takes row b/2 (b even) or rows - 1 - b/2 (b odd)
     int32_t k;
     int32_t idx_i64;          // 0: int32 indices, 1: int64
     int32_t want_values;

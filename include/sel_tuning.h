@@ -8,7 +8,7 @@
  *
  * The knobs start from the environment, read once when the library first
  * plans a call: SEL_PLAN=reg|row|wide|split|stream|flat, SEL_PARTS=n,
- * SEL_ROW_SAMPLE=1, SEL_HIST_AGG=1.  sel_set_tuning changes them at any time
+ * SEL_ROW_SAMPLE=1, SEL_HIST_AGG=1, SEL_ROW_ORDER=1.  sel_set_tuning changes them at any time
  * after that; plans are cached per knob setting, so a change takes effect on
  * the next call.  They are process-wide (not per thread).
  */
@@ -26,7 +26,10 @@ enum {
     SEL_TUNE_PLAN = 0,       /* a SEL_PLAN_* value: force one kernel where it can run the shape */
     SEL_TUNE_PARTS = 1,      /* > 0: parts per row of the streaming kernel's split mode; 0 = automatic */
     SEL_TUNE_ROW_SAMPLE = 2, /* 1: the staged row kernel estimates its first digit from a sample */
-    SEL_TUNE_HIST_AGG = 3    /* 1: first-pass histograms with warp-aggregated atomics */
+    SEL_TUNE_HIST_AGG = 3,   /* 1: first-pass histograms with warp-aggregated atomics */
+    SEL_TUNE_ROW_ORDER = 4   /* 1: with per-row ends, CTAs take rows from both ends of the batch
+                                alternately; 0 (default): in order -- measured faster on causal
+                                row ends, where neighbouring rows share memory traffic */
 };
 
 /* Values of SEL_TUNE_PLAN.  A forced kernel that cannot run a shape leaves

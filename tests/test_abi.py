@@ -42,7 +42,9 @@ def test_tuning_knobs_round_trip_and_reject_bad_values(lib):
             g.set_tuning(plan=plan)
             assert g.get_tuning()["plan"] == plan
         g.set_tuning(parts=7, row_sample=True, hist_agg=True)
-        assert g.get_tuning() == {"plan": "auto", "parts": 7, "row_sample": True, "hist_agg": True}
+        g.set_tuning(row_order=False)
+        assert g.get_tuning() == {"plan": "auto", "parts": 7, "row_sample": True, "hist_agg": True,
+                                  "row_order": False}
         SEL_EINVAL = 1
         assert lib.sel_set_tuning(0, 99) == SEL_EINVAL   # no such plan
         assert lib.sel_set_tuning(0, -2) == SEL_EINVAL

@@ -3,6 +3,7 @@ import os
 import sys
 
 import numpy as np
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
@@ -36,3 +37,19 @@ def test_gather_and_step_bytes():
     assert bench.gather_bytes(w, fused=False) == key + out + 3 * 2 * 4
     assert bench.step_bytes(w) == bench.topk_bytes(w) + key + out
     assert bench.gather_bytes(tiny(key=False), fused=True) == 0
+
+
+@pytest.mark.parametrize("name", ["indexer_bf16_4096x2048_causal_k512_gather", "sampling_f32_256x131072_k4096_nan",
+                                  "indexer_bf16_3x4096x16384_levels64_k2048_gather", "sampling_f32_4x8192_k64"])
+def test_e2e_pieces_cover_the_rows_and_respect_key_batches(name):
+    import bench
+    import synthetic as syn
+    w = syn.workload(name)
+    pieces = bench.e2e_pieces(w, 4)
+    assert pieces[0][0] == 0 and pieces[-1][1] == w["rows"]
+    assert all(pieces[i][1] == pieces[i + 1][0] for i in range(len(pieces) - 1))
+    if w.get("key") is not None:
+        rpb = w["rows_per_batch"]
+        for s, e, b0, b1 in pieces:
+            assert b0 * rpb <= s < e <= b1 * rpb
+            assert b1 - b0 == 1 or (s == b0 * rpb and e == b1 * rpb)

@@ -197,3 +197,23 @@ def test_fused_gather_row_widths(mode, d, tuning):
     assert (to_bits(fout) == want).all()
     assert int(err.item()) == (1 if bad else 0)
     assert (bad > 0) == (d == 2048)
+
+
+@pytest.mark.parametrize("mode", ["reg", "row", "wide", "split", "stream"])
+def test_row_order_interleaved_and_in_order_agree(mode, tuning):
+    # with per-row ends CTAs take rows from both ends of the batch alternately; the result must be
+    # the same, bit for bit, as taking them in order, and equal to the oracle
+    import gather_radix_select_gb300 as g
+    rows, cols, k = 37, (4000 if mode == "reg" else 70000), 300
+    row_end = np.minimum(cols, (np.arange(rows) * (cols // rows)) + 7).astype(np.int32)
+    row_end[5] = 0
+    w = padded("f32", rows, cols, k, "normal", row_end=row_end)
+    res = []
+    for order in (True, False):
+        tuning(plan=mode, row_order=order)
+        x, end, vals, idx, nan, err = run(w)
+        assert err == 0 and nan == 0
+        res.append((idx.cpu().numpy(), to_bits(vals)))
+    assert (res[0][0] == res[1][0]).all() and (res[0][1] == res[1][1]).all()
+    compare_with_oracle(w, np.arange(rows), res[0][0], res[0][1], True)
+    assert g.get_tuning()["row_order"] is False
