@@ -282,8 +282,8 @@ class Runner:
         if w["want_values"]:
             vpad = (k + 3) // 4 * 4 if w["dtype"] == "f32" else (k + 7) // 8 * 8
             self.out_val = torch.empty((self.rows, vpad), dtype=self.x.dtype, device=dev)
-        # one fused launch per piece; value order adds the ordering launch (and then a separate gather)
-        per = 1 if not sorted_value else (3 if self.key is not None else 2)
+        # one fused launch per piece; value order adds the ordering launch (which also gathers)
+        per = 1 if not sorted_value else 2
         self.launches_per_step = per * len(self.pieces)
 
     def local_workload(self):

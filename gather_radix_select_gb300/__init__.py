@@ -372,7 +372,7 @@ def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, en
     Returns ``(values, indices, gathered)`` with ``gathered`` bf16
     [rows, n_gather, d]; values / indices are None when not requested.  With
     ``sorted_value`` the gathered columns are the n_gather largest values, in
-    value order (selection, ordering and gather run as three launches).
+    value order (the selection, then one launch that orders and gathers).
     """
     _check_x(x)
     order = _order(sorted_index, sorted_value)

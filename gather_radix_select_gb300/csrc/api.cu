@@ -592,11 +592,33 @@ int64_t key_span(int64_t b, int64_t comp_len, int64_t d, int64_t batch_stride, i
     return comp_len > 0 && b > 0 ? (b - 1) * batch_stride + (comp_len - 1) * row_stride + d : 0;
 }
 
-// Re-orders finished output rows by value (SEL_SORT_VALUE).
+// The key rows to gather after ordering (n_gather 0: none).
+struct OrderGather {
+    const void *key = nullptr;
+    int64_t b = 1, comp_len = 0, d = 0, key_batch_stride = 0, key_row_stride = 0, n_gather = 0;
+    void *gather_out = nullptr;
+    int32_t *err_flag = nullptr;
+};
+
+// Re-orders finished output rows by value (SEL_SORT_VALUE), then gathers the first n_gather
+// ordered positions' key rows in the same launch.
 int value_order(const void *x, int dtype, int64_t rows, int64_t stride, int k, int idx_dtype, int want_values,
-                void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride, void *stream)
+                void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride, void *stream,
+                const OrderGather &g = OrderGather())
 {
     sel::OrderArgs a{};
+    if (g.n_gather > 0) {
+        a.key = static_cast<const uint16_t *>(g.key);
+        a.comp_len = g.comp_len;
+        a.d = g.d;
+        a.key_batch_stride = g.key_batch_stride;
+        a.key_row_stride = g.key_row_stride;
+        a.rows_per_batch = rows / g.b;
+        a.key_span = key_span(g.b, g.comp_len, g.d, g.key_batch_stride, g.key_row_stride);
+        a.n_gather = g.n_gather;
+        a.gather_out = static_cast<uint16_t *>(g.gather_out);
+        a.err_flag = g.err_flag;
+    }
     a.x = x;
     a.x_stride = stride;
     a.rows = rows;
@@ -939,12 +961,26 @@ int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_
         if (st != SEL_OK) return st;
     }
     if (by_value) {
-        // selection, then ordering, then the gather of the first n_gather ordered columns
-        st = sel_topk(x, dtype, rows, cols, stride, row_end, k, sorted_index, idx_dtype, want_values, out_idx,
-                      out_idx_stride, out_val, out_val_stride, workspace, workspace_bytes, nan_flag, err_flag, stream);
-        if (st != SEL_OK || n_gather == 0) return st;
-        return sel_gather_rows(key, b, comp_len, d, key_batch_stride, key_row_stride, out_idx, idx_dtype, rows,
-                               n_gather, out_idx_stride, gather_out, err_flag, stream);
+        // selection, then one launch that orders the rows and gathers the first n_gather ordered
+        // columns' key rows
+        st = run_topk(x, dtype, rows, cols, stride, row_end, k, idx_dtype, want_values, out_idx, out_idx_stride,
+                      out_val, out_val_stride, nullptr, 1, 0, 0, 0, 0, 0, nullptr, workspace, workspace_bytes,
+                      nan_flag, err_flag, stream);
+        if (st != SEL_OK) return st;
+        OrderGather g;
+        if (n_gather > 0) {
+            g.key = key;
+            g.b = b;
+            g.comp_len = comp_len;
+            g.d = d;
+            g.key_batch_stride = key_batch_stride;
+            g.key_row_stride = key_row_stride;
+            g.n_gather = n_gather;
+            g.gather_out = gather_out;
+            g.err_flag = err_flag;
+        }
+        return value_order(x, dtype, rows, stride, k, idx_dtype, want_values, out_idx, out_idx_stride, out_val,
+                           out_val_stride, stream, g);
     }
     return run_topk(x, dtype, rows, cols, stride, row_end, k, idx_dtype, want_values, out_idx, out_idx_stride, out_val,
                     out_val_stride, key, n_gather > 0 ? b : 1, comp_len, d, key_batch_stride, key_row_stride, n_gather,

@@ -157,9 +157,17 @@ struct OrderArgs {
     int64_t out_idx_stride;
     void *out_val;            // nullable: [rows, out_val_stride] value bits
     int64_t out_val_stride;
+    // optional gather of the first n_gather ordered positions (n_gather 0: none), as gather_kernel:
+    // gather_out[r, j, :] = key[r / rows_per_batch, max(idx[r, j], 0), :]
+    const uint16_t *key;
+    int64_t comp_len, d, key_batch_stride, key_row_stride, rows_per_batch, key_span;
+    int64_t n_gather;
+    uint16_t *gather_out;     // [rows, n_gather, d]
+    int32_t *err_flag;        // nullable: SEL_EINVAL for a position past comp_len (zero row written)
 };
 
-// dtype: 0 fp32, 1 bf16.  Sorts each output row by value descending (ties: column ascending).
+// dtype: 0 fp32, 1 bf16.  Sorts each output row by value descending (ties: column ascending), then
+// gathers the first n_gather ordered positions' key rows when n_gather > 0.
 cudaError_t launch_value_order(int dtype, bool idx_i64, const OrderArgs &a, cudaStream_t stream);
 
 // dtype: 0 fp32, 1 bf16.  mode: one of the kMode* values.  grid: CTAs to launch.

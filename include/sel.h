@@ -225,8 +225,9 @@ SEL_API int sel_block_topk_gather(const void *scores, int dtype, int64_t rows, i
  * selection.  Fill positions (-1) of short rows gather position 0, as in
  * sel_gather_rows.  The workspace rule is that of sel_topk.  With
  * SEL_SORT_VALUE the gathered columns are those of the value-ordered output
- * (the n_gather largest values); that takes three launches (selection,
- * ordering, gather) and out_idx must not be NULL. */
+ * (the n_gather largest values); that takes two launches (the selection,
+ * then one launch that orders each row and gathers its first n_gather
+ * ordered positions) and out_idx must not be NULL. */
 SEL_API int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride,
                     const int32_t *row_end, int k, int sorted_index, int idx_dtype, int want_values,
                     void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride,

@@ -174,6 +174,64 @@ def test_value_order_gather_takes_the_largest():
         assert (to_bits(out) == want).all()
 
 
+@pytest.mark.parametrize("dtype,k,n_gather,d,b,idx_dtype,want_values", [
+    ("bf16", 512, 512, 24, 3, "i32", False),    # every ordered position, 3-vector key rows
+    ("bf16", 2048, 37, 128, 1, "i64", False),
+    ("f32", 4096, 1000, 64, 2, "i64", True),
+    ("f32", 100, 1, 8, 2, "i32", False),        # one-vector key rows, 32-thread ordering CTAs
+])
+def test_value_order_gather_in_the_ordering_launch(dtype, k, n_gather, d, b, idx_dtype, want_values):
+    # the ordering launch gathers the first n_gather ordered positions' key rows: equal to
+    # torch.index_select over the batch-flattened key at the ordered indices (fills read row 0), and
+    # the order itself equals the oracle's
+    import gather_radix_select_gb300 as g
+    rows_per_batch, cols = 40, 4500
+    rows = b * rows_per_batch
+    end = np.where(np.arange(rows) % 5 == 0, k // 2 + 1, cols - (np.arange(rows) * 97) % 300).astype(np.int32)
+    w = case(dtype, rows, cols, k, "levels" if dtype == "bf16" else "normal", row_end=end)
+    x = to_torch(w["x"], dtype)[:, :cols]
+    key_bits = syn.f32_to_bf16_bits(np.random.default_rng(k + d).standard_normal((b, cols, d)).astype(np.float32))
+    key = to_torch(key_bits.reshape(b * cols, d), "bf16").view(b, cols, d)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    vals, idx, out = g.topk_gather(x, k, key, n_gather, end=torch.from_numpy(end).cuda(), sorted_value=True,
+                                   return_value=want_values, indices_type=IDX_DTYPE[idx_dtype], err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o_idx, o_bits, _ = oracle.topk(w["x"], dtype, k, row_end=end, cols=cols, sorted_value=True)
+    assert (idx.cpu().numpy().astype(np.int64) == o_idx).all()
+    if want_values:
+        assert (to_bits(vals).astype(np.uint32) == o_bits).all()
+    sel = idx[:, :n_gather].to(torch.int64).clamp(min=0)
+    batch = torch.arange(rows, device="cuda")[:, None] // rows_per_batch
+    ref = torch.index_select(key.reshape(-1, d), 0, (batch * cols + sel).reshape(-1)).reshape(out.shape)
+    assert torch.equal(ref.view(torch.int16), out.view(torch.int16))
+    for bb in range(b):  # and the oracle's gather on sampled rows of every batch
+        rr = np.array([bb * rows_per_batch, bb * rows_per_batch + 7, (bb + 1) * rows_per_batch - 1])
+        want, bad = oracle.gather_rows(np.ascontiguousarray(key_bits[bb:bb + 1]), o_idx[rr][:, :n_gather], 1)
+        assert bad == 0 and (to_bits(out[torch.from_numpy(rr).cuda()]) == want).all()
+
+
+def test_value_order_gather_flags_positions_past_the_key():
+    # a key shorter than the rows: ordered positions at or past comp_len gather a zero row and raise
+    # SEL_EINVAL, as the fused and the separate gather do
+    import gather_radix_select_gb300 as g
+    rows, cols, k, n_gather, comp_len, d = 16, 1000, 64, 64, 600, 16
+    w = case("bf16", rows, cols, k, "normal")
+    x = to_torch(w["x"], "bf16")[:, :cols]
+    key_bits = syn.f32_to_bf16_bits(np.random.default_rng(5).standard_normal((1, comp_len, d)).astype(np.float32))
+    key = to_torch(key_bits.reshape(comp_len, d), "bf16").view(1, comp_len, d)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, idx, out = g.topk_gather(x, k, key, n_gather, sorted_value=True, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1
+    past = (idx >= comp_len).cpu()
+    assert past.any()
+    o = out.cpu().view(torch.int16)
+    assert (o[past] == 0).all()
+    ref = torch.index_select(key.reshape(-1, d), 0, idx.to(torch.int64).clamp(0, comp_len - 1).reshape(-1)).reshape(out.shape)
+    assert torch.equal(o[~past], ref.cpu().view(torch.int16)[~past])
+
+
 def test_value_order_rejects_both_orders():
     import gather_radix_select_gb300 as g
     x = torch.zeros((2, 64), device="cuda")
