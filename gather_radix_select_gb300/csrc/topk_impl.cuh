@@ -401,8 +401,12 @@ __device__ void find_threshold(const uint32_t *h, int nb, uint32_t need, uint32_
     const int per = nb > NT ? nb / NT : 1;
     const int lo = tid * per;
     uint32_t s = 0;
-    if (lo < nb)
-        for (int i = 0; i < per; ++i) s += h[lo + i];
+    if (lo < nb) {
+        // each thread sums its `per` consecutive bins starting at a rotated bin, so that the
+        // threads of a warp read distinct banks (per is a power of two)
+        const int rot = (tid * per / 32) & (per - 1);
+        for (int i = 0; i < per; ++i) s += h[lo + ((i + rot) & (per - 1))];
+    }
     // exclusive scan in reversed thread order gives the count above this thread's bins
     const int lane = tid & 31, warp = tid >> 5;
     uint32_t inc = s;
@@ -1782,6 +1786,9 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) stream_kernel(const 
 // staging (W x kStage 16-byte vectors, then W x kStage first columns).
 // ---------------------------------------------------------------------------
 constexpr int kWideUnroll = 4;
+// wide_kernel: every iteration, lane 0 of a warp prefetches into L2 the warp's vectors this many
+// iterations ahead (0: none), so that more of the row is on its way than the registers hold
+constexpr int kWidePrefetch = 2;
 constexpr int kStage = kWideStage;
 
 // Threshold key estimated from sample vectors held in registers: q[0, kSU) of each thread, those
@@ -2164,7 +2171,17 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
         sc = 0;
         __syncwarp();
     };
+    if (kWidePrefetch > 0 && lane == 0) {  // the first iterations' prefetches
+        for (int d = 1; d < kWidePrefetch; ++d) {
+            const int64_t pb = vb + static_cast<int64_t>(d) * 32 * U;
+            if (pb < ve) prefetch_l2(xv + pb, static_cast<uint32_t>(min(static_cast<int64_t>(32 * U), ve - pb)) * 16u);
+        }
+    }
     for (int64_t base = vb; base < ve; base += 32 * U) {
+        if (kWidePrefetch > 0 && lane == 0) {
+            const int64_t pb = base + static_cast<int64_t>(kWidePrefetch) * 32 * U;
+            if (pb < ve) prefetch_l2(xv + pb, static_cast<uint32_t>(min(static_cast<int64_t>(32 * U), ve - pb)) * 16u);
+        }
         if (base != vb) {
             if (base + 32 * U <= ve) {  // a full iteration (warp-uniform): no bounds checks
 #pragma unroll
