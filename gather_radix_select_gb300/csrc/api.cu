@@ -13,6 +13,7 @@
 
 #include "../../include/sel.h"
 #include "../../include/sel_tuning.h"
+#include "order_core.cuh"
 #include "sel_internal.h"
 
 namespace {
@@ -630,15 +631,51 @@ int value_order(const void *x, int dtype, int64_t rows, int64_t stride, int k, i
     return status_of(sel::launch_value_order(dtype, idx_dtype == SEL_I64, a, static_cast<cudaStream_t>(stream)));
 }
 
+// The staged row kernel's value-ordered variant for a row plan: the ranking's items and counters
+// take the (then free) masks and candidate list and, where those are too small, push the
+// histogram and gather list back.  False when the plan is not the row kernel or the ranking does
+// not fit (k above 8 entries a thread, or above the 16-bit position slots of the histogram).
+bool ordered_row_plan(int dtype, int k, bool gather, const Plan &p, Plan &op)
+{
+    if (p.mode != sel::kModeRow || k > sel::order::kEpt * p.threads || k > 2 * p.layout.hist_bins ||
+        k > (1 << sel::order::kSlotBits))
+        return false;
+    op = p;
+    sel::TopkArgs &l = op.layout;
+    const size_t rank = dtype == SEL_BF16 ? sel::order::rank_smem_bytes<true>(p.threads)
+                                          : sel::order::rank_smem_bytes<false>(p.threads);
+    l.smem_order_off = l.smem_mask_off;
+    const size_t hist = static_cast<size_t>(
+        round_up(static_cast<int64_t>(std::max<size_t>(l.smem_hist_off, l.smem_order_off + rank)), 16));
+    const size_t delta = hist - l.smem_hist_off;
+    l.smem_hist_off = static_cast<uint32_t>(hist);
+    l.smem_glist_off = static_cast<uint32_t>(l.smem_glist_off + delta);
+    op.smem = p.smem + delta;
+    op.mode = sel::kModeRowOrdered;
+    return op.smem <= sel::topk_smem_limit() &&
+           cached_blocks_per_sm(dtype, sel::kModeRowOrdered, op.threads, gather, op.smem) > 0;
+}
+
+// One selection launch.  ordered (nullable): on entry, whether the outputs should come out in value
+// order from this launch; when the plan cannot, nothing is launched and *ordered becomes false.
 int run_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride, const int32_t *row_end, int k,
              int idx_dtype, int want_values, void *out_idx, int64_t out_idx_stride, void *out_val,
              int64_t out_val_stride, const void *key, int64_t b, int64_t comp_len, int64_t d,
              int64_t key_batch_stride, int64_t key_row_stride, int64_t n_gather, void *gather_out, void *workspace,
-             size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag, void *stream, int64_t row_end_div = 1)
+             size_t workspace_bytes, int32_t *nan_flag, int32_t *err_flag, void *stream, int64_t row_end_div = 1,
+             bool *ordered = nullptr)
 {
     Plan p;
     int st = cached_plan(dtype, rows, cols, k, n_gather > 0, n_gather, p);
     if (st != SEL_OK) return st;
+    if (ordered && *ordered) {
+        Plan op;
+        if (!ordered_row_plan(dtype, k, n_gather > 0, p, op)) {
+            *ordered = false;
+            return SEL_OK;
+        }
+        p = op;
+    }
     if (p.ws_bytes > 0) {
         if (!workspace || workspace_bytes < p.ws_bytes) return SEL_EINVAL;
         if (!aligned(workspace, 256)) return SEL_EALIGN;
@@ -794,7 +831,8 @@ const char *sel_topk_kernel_name(int dtype, int64_t rows, int64_t cols, int k, i
     Plan p;
     if (cached_plan(dtype, rows, cols, k, n_gather > 0, n_gather, p) != SEL_OK) return nullptr;
     switch (p.mode) {
-    case sel::kModeRow: return "row_kernel";
+    case sel::kModeRow:
+    case sel::kModeRowOrdered: return "row_kernel";
     case sel::kModeSplit: return "split_kernel";
     case sel::kModeWide:
     case sel::kModeWideSplit: return "wide_kernel";
@@ -816,6 +854,14 @@ int sel_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
     const int st = check_topk_args(x, dtype, rows, cols, stride, k, idx_dtype, want_values, out_idx, out_idx_stride,
                                    out_val, out_val_stride, true);
     if (st != SEL_OK || rows == 0) return st;
+    // value order: ranked inside the staged row kernel where it can, else a second launch
+    bool fused = sorted_index == SEL_SORT_VALUE;
+    if (fused) {
+        const int rc = run_topk(x, dtype, rows, cols, stride, row_end, k, idx_dtype, want_values, out_idx,
+                                out_idx_stride, out_val, out_val_stride, nullptr, 1, 0, 0, 0, 0, 0, nullptr, workspace,
+                                workspace_bytes, nan_flag, err_flag, stream, 1, &fused);
+        if (rc != SEL_OK || fused) return rc;
+    }
     const int rc = run_topk(x, dtype, rows, cols, stride, row_end, k, idx_dtype, want_values, out_idx, out_idx_stride,
                             out_val, out_val_stride, nullptr, 1, 0, 0, 0, 0, 0, nullptr, workspace, workspace_bytes,
                             nan_flag, err_flag, stream);
@@ -961,8 +1007,15 @@ int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_
         if (st != SEL_OK) return st;
     }
     if (by_value) {
+        // the staged row kernel ranks, writes and gathers in one launch where it can; else the
         // selection, then one launch that orders the rows and gathers the first n_gather ordered
         // columns' key rows
+        bool fused = true;
+        st = run_topk(x, dtype, rows, cols, stride, row_end, k, idx_dtype, want_values, out_idx, out_idx_stride,
+                      out_val, out_val_stride, key, n_gather > 0 ? b : 1, comp_len, d, key_batch_stride,
+                      key_row_stride, n_gather, gather_out, workspace, workspace_bytes, nan_flag, err_flag, stream, 1,
+                      &fused);
+        if (st != SEL_OK || fused) return st;
         st = run_topk(x, dtype, rows, cols, stride, row_end, k, idx_dtype, want_values, out_idx, out_idx_stride,
                       out_val, out_val_stride, nullptr, 1, 0, 0, 0, 0, 0, nullptr, workspace, workspace_bytes,
                       nan_flag, err_flag, stream);

@@ -6,61 +6,21 @@
 // this kernel re-orders one row per CTA by value, largest first, equal values
 // by column ascending, fills (index -1) last.  A NaN counts as larger than
 // every number (NaNs among themselves by column); only short rows, which are
-// not checked for NaN, can hold one in a defined selection.
-//
-// Because the row arrives in ascending column order, a STABLE sort by value
-// alone yields the column tie-break.  The sort is a least-significant-digit
-// radix sort on the inverted order-preserving key of each value (-0 folded
-// onto +0, any NaN above every number), rebased to the row's smallest
-// inverted key: the k values of a top-k row span a narrow range, so only the
-// bits that differ are sorted (8-bit digits; at most 3 passes for a bf16
-// row, about 4 for fp32 normal scores).  Fills take the key one
-// above the range and so stay last.  Each item carries its slot (12 bits)
-// beside the key; the column and value bits are looked up by slot at the end.
-//
-// Each pass ranks 8-bit digits: every warp ranks its 256 items with warp
-// match (items of equal digit in a warp find one another, the lowest lane of
-// each group advances that warp's counter for the digit), one block-wide
-// exclusive scan turns the per-warp counts into digit-major, warp-minor bases
-// (stable), and each item is scattered to its rank.  Items sit warp-striped:
-// item e of lane l in warp w is position 256 w + 32 e + l, so positions and
-// the ranking order agree.
+// not checked for NaN, can hold one in a defined selection.  The ranking is
+// order_core.cuh's stable radix sort; the staged row kernel ranks its rows
+// itself and needs no second launch.
 #include <cstdint>
 #include <type_traits>
 
+#include "order_core.cuh"
 #include "sel_internal.h"
 
 namespace sel {
 namespace {
 
-constexpr int kEpt = 8;         // items a thread holds
-constexpr int kSlotBits = 12;   // k <= 4096
-constexpr int kRadixBits = 8;
-constexpr int kDigits = 1 << kRadixBits;
-constexpr int kWarpItems = 32 * kEpt;
+using order::kEpt;
+using order::kWarpItems;
 constexpr int32_t kStatusInval = 1;  // SEL_EINVAL
-
-// inverted order-preserving keys: larger value => smaller key; NaN smallest
-__device__ __forceinline__ uint32_t inv_key_f32(uint32_t u)
-{
-    if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;
-    u = (u == 0x80000000u) ? 0u : u;
-    return (u & 0x80000000u) ? u : ~(u | 0x80000000u);
-}
-
-__device__ __forceinline__ uint32_t inv_key_bf16(uint32_t h)
-{
-    if ((h & 0x7fffu) > 0x7f80u) return 0u;
-    h = (h == 0x8000u) ? 0u : h;
-    return ((h & 0x8000u) ? h : ~(h | 0x8000u)) & 0xffffu;
-}
-
-__device__ __forceinline__ uint32_t lanemask_lt()
-{
-    uint32_t m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
 
 // Copies the key rows of the ordered positions s_pos[0, ng) of one row to gather_out[row], NT threads,
 // 16-byte loads (key rows are re-read across rows and stay in L2) and streaming stores (the output
@@ -103,22 +63,17 @@ __device__ void gather_ordered(const OrderArgs &a, int64_t row, const int32_t *s
 }
 
 // One CTA per row of NT threads (32..512, NT * 8 >= k; a compile-time count keeps every
-// shared-memory address a base plus an immediate).  Shared memory: NT*8 items (K), NT*8 columns,
-// NT*8 value words, the per-warp digit counters [NT/32][256], then the digit bases [256].
-// The s_red words hold the warps' key minima and maxima, then each pass's warp totals.
+// shared-memory address a base plus an immediate).  Shared memory: NT*8 columns, NT*8 value words,
+// then value_rank's items and counters.
 template <bool BF16, bool I64, int NT>
 __global__ void __launch_bounds__(NT) value_order_kernel(const OrderArgs a)
 {
-    using K = typename std::conditional<BF16, uint32_t, uint64_t>::type;
     extern __shared__ __align__(16) unsigned char s_raw[];
-    __shared__ uint32_t s_red[64];
-    constexpr int nt = NT, n_items = NT * kEpt, nw = NT / 32;
+    constexpr int nt = NT, n_items = NT * kEpt;
     const int k = a.k;
-    K *s_item = reinterpret_cast<K *>(s_raw);
-    int32_t *s_col = reinterpret_cast<int32_t *>(s_item + n_items);
+    int32_t *s_col = reinterpret_cast<int32_t *>(s_raw);
     uint32_t *s_val = reinterpret_cast<uint32_t *>(s_col + n_items);
-    uint32_t *s_cnt = s_val + n_items;       // [nw][kDigits]: per-warp counts, then per-warp bases
-    uint32_t *s_base = s_cnt + nw * kDigits;  // [kDigits]: digit totals, then exclusive digit bases
+    unsigned char *s_rank = reinterpret_cast<unsigned char *>(s_val + n_items);
     const int64_t row = blockIdx.x;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const char *xr = static_cast<const char *>(a.x) + row * a.x_stride * (BF16 ? 2 : 4);
@@ -148,154 +103,45 @@ __global__ void __launch_bounds__(NT) value_order_kernel(const OrderArgs a)
             if (col[e] >= 0)
                 v[e] = BF16 ? reinterpret_cast<const uint16_t *>(xr)[col[e]] : reinterpret_cast<const uint32_t *>(xr)[col[e]];
     }
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    bool valid[kEpt];
 #pragma unroll
     for (int e = 0; e < kEpt; ++e) {
         const int p = wbase + e * 32 + lane;
-        if (col[e] < 0) v[e] = fill_bits;  // an entry with no column (a fill) keeps the fill value
+        valid[e] = col[e] >= 0;
+        if (!valid[e]) v[e] = fill_bits;  // an entry with no column (a fill) keeps the fill value
         s_col[p] = col[e];
         s_val[p] = v[e];
-        if (col[e] >= 0) {
-            const uint32_t kp = BF16 ? inv_key_bf16(v[e]) : inv_key_f32(v[e]);
-            kmin = min(kmin, kp);
-            kmax = max(kmax, kp);
-        }
     }
-    kmin = __reduce_min_sync(0xffffffffu, kmin);
-    kmax = __reduce_max_sync(0xffffffffu, kmax);
-    if (lane == 0) {
-        s_red[warp] = kmin;
-        s_red[32 + warp] = kmax;
-    }
-    __syncthreads();
-    kmin = 0xffffffffu;
-    kmax = 0u;
-#pragma unroll
-    for (int w = 0; w < nw; ++w) {
-        kmin = min(kmin, s_red[w]);
-        kmax = max(kmax, s_red[32 + w]);
-    }
-    // keys rebased to the row's range; fills one above it (no valid entry: everything is a fill)
-    const uint64_t range = kmin <= kmax ? static_cast<uint64_t>(kmax - kmin) : 0ull;
-    const uint64_t fill_key = range + 1;
-    const int bits = 64 - __clzll(static_cast<long long>(fill_key));
-    K item[kEpt];
-#pragma unroll
-    for (int e = 0; e < kEpt; ++e) {
-        const uint32_t kp = BF16 ? inv_key_bf16(v[e]) : inv_key_f32(v[e]);
-        const uint64_t kk = col[e] >= 0 ? static_cast<uint64_t>(kp - kmin) : fill_key;
-        item[e] = (static_cast<K>(kk) << kSlotBits) | static_cast<K>(wbase + e * 32 + lane);
-    }
-    const uint32_t lt = lanemask_lt();
-    uint32_t *wcnt = s_cnt + warp * kDigits;
-    constexpr int dpt = kDigits >= nt ? kDigits / nt : 1;  // digits a thread scans
+    order::value_rank<BF16, NT>(v, valid, s_rank);
 
-    for (int shift = kSlotBits; shift < kSlotBits + bits; shift += kRadixBits) {
-        const int nb = min(kRadixBits, kSlotBits + bits - shift);  // digit bits that can be nonzero
-        // this warp's counters (the previous pass read them before its closing barrier)
-#pragma unroll
-        for (int i = lane; i < kDigits; i += 32) wcnt[i] = 0u;
-        // the lanes holding the same digit in each of the warp's 8 item rows: one ballot per bit
-        uint32_t dg[kEpt], peers[kEpt];
-#pragma unroll
-        for (int e = 0; e < kEpt; ++e) {
-            dg[e] = static_cast<uint32_t>(item[e] >> shift) & (kDigits - 1);
-            peers[e] = 0xffffffffu;
-        }
-#pragma unroll
-        for (int b = 0; b < kRadixBits; ++b) {
-            if (b < nb) {
-#pragma unroll
-                for (int e = 0; e < kEpt; ++e) {
-                    const bool one = (dg[e] >> b) & 1u;
-                    const uint32_t m = __ballot_sync(0xffffffffu, one);
-                    peers[e] &= one ? m : ~m;
-                }
-            }
-        }
-        __syncwarp();
-        // rank among the warp's earlier items of the digit: row e's lowest lane of each digit
-        // advances the warp's counter
-        uint32_t rk[kEpt];
-#pragma unroll
-        for (int e = 0; e < kEpt; ++e) {
-            const int leader = __ffs(peers[e]) - 1;
-            uint32_t base = 0u;
-            if (lane == leader) {
-                base = wcnt[dg[e]];
-                wcnt[dg[e]] = base + __popc(peers[e]);
-            }
-            __syncwarp();
-            rk[e] = __shfl_sync(0xffffffffu, base, leader) + __popc(peers[e] & lt);
-        }
-        __syncthreads();  // every warp's counts are in; every read of s_item in this pass is done
-        // digits [dpt t, dpt t + dpt) (threads past the digits hold none): exclusive over the warps
-        // in place, then an exclusive scan of the digit totals over the block
-        uint32_t tot[dpt], sum = 0u;
-#pragma unroll
-        for (int i = 0; i < dpt; ++i) {
-            const int d = t * dpt + i;
-            uint32_t run = 0u;
-            if (d < kDigits) {
-#pragma unroll
-                for (int w = 0; w < nw; ++w) {
-                    const uint32_t c = s_cnt[w * kDigits + d];
-                    s_cnt[w * kDigits + d] = run;
-                    run += c;
-                }
-            }
-            tot[i] = run;
-            sum += run;
-        }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) s_red[warp] = incl;
-        __syncthreads();
-        uint32_t run = incl - sum;
-#pragma unroll
-        for (int w = 0; w < nw - 1; ++w)
-            if (w < warp) run += s_red[w];
-#pragma unroll
-        for (int i = 0; i < dpt; ++i) {
-            const int d = t * dpt + i;
-            if (d < kDigits) s_base[d] = run;
-            run += tot[i];
-        }
-        __syncthreads();
-        // rank = the digit's base + this warp's base within the digit + the rank within the warp
-#pragma unroll
-        for (int e = 0; e < kEpt; ++e) s_item[s_base[dg[e]] + wcnt[dg[e]] + rk[e]] = item[e];
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < kEpt; ++e) item[e] = s_item[wbase + e * 32 + lane];
-    }
-
-    // write (coalesced): rank j's column and value, looked up by slot (s_item is in rank order:
-    // every call makes at least one pass, fill_key >= 1); the first n_gather columns also go to
-    // s_pos (the counters' words: n_items of them, free after the last pass)
-    int32_t *s_pos = reinterpret_cast<int32_t *>(s_cnt);
+    // write (coalesced): rank j's column and value, looked up by position; the first n_gather
+    // columns also go to s_pos (value_rank's item words: free once every position is read)
     const int ng = static_cast<int>(a.n_gather);
+    int32_t c_out[kEpt];
+    uint32_t v_out[kEpt];
+#pragma unroll
+    for (int u = 0; u < kEpt; ++u) {
+        const int j = t + u * nt;
+        const int slot = j < k ? order::ranked_position<BF16>(s_rank, j) : 0;
+        c_out[u] = s_col[slot];
+        v_out[u] = s_val[slot];
+    }
+    int32_t *s_pos = reinterpret_cast<int32_t *>(s_rank);
+    if (ng > 0) __syncthreads();  // every rank read before s_pos overwrites the items
 #pragma unroll
     for (int u = 0; u < kEpt; ++u) {
         const int j = t + u * nt;
         if (j >= k) break;
-        const int slot = static_cast<int>(s_item[j] & ((K(1) << kSlotBits) - 1));
-        const int32_t c_out = s_col[slot];
-        const uint32_t v_out = s_val[slot];
-        if (j < ng) s_pos[j] = c_out;
+        if (j < ng) s_pos[j] = c_out[u];
         if (I64)
-            static_cast<int64_t *>(a.out_idx)[row * a.out_idx_stride + j] = c_out;
+            static_cast<int64_t *>(a.out_idx)[row * a.out_idx_stride + j] = c_out[u];
         else
-            static_cast<int32_t *>(a.out_idx)[row * a.out_idx_stride + j] = c_out;
+            static_cast<int32_t *>(a.out_idx)[row * a.out_idx_stride + j] = c_out[u];
         if (a.out_val) {
             if (BF16)
-                static_cast<uint16_t *>(a.out_val)[row * a.out_val_stride + j] = static_cast<uint16_t>(v_out);
+                static_cast<uint16_t *>(a.out_val)[row * a.out_val_stride + j] = static_cast<uint16_t>(v_out[u]);
             else
-                static_cast<uint32_t *>(a.out_val)[row * a.out_val_stride + j] = v_out;
+                static_cast<uint32_t *>(a.out_val)[row * a.out_val_stride + j] = v_out[u];
         }
     }
     if (ng > 0) {
@@ -336,14 +182,12 @@ cudaError_t launch_value_order(int dtype, bool idx_i64, const OrderArgs &a_in, c
 {
     OrderArgs a = a_in;
     if (a.rows <= 0) return cudaSuccess;
-    if (a.rows > 0x7fffffffLL || a.k < 1 || a.k > (1 << kSlotBits)) return cudaErrorInvalidValue;
+    if (a.rows > 0x7fffffffLL || a.k < 1 || a.k > (1 << order::kSlotBits)) return cudaErrorInvalidValue;
     int threads = 32;  // a power of two from 32 to 512 with threads * 8 >= k
     while (threads * kEpt < a.k) threads <<= 1;
     const int n_items = threads * kEpt;
-    const size_t ksz = dtype == 1 ? sizeof(uint32_t) : sizeof(uint64_t);
-    const int counters = kDigits * (threads / 32) + kDigits;
-    const size_t smem = static_cast<size_t>(n_items) * (ksz + sizeof(int32_t) + sizeof(uint32_t)) +
-                        static_cast<size_t>(counters) * sizeof(uint32_t);
+    const size_t smem = static_cast<size_t>(n_items) * (sizeof(int32_t) + sizeof(uint32_t)) +
+                        (dtype == 1 ? order::rank_smem_bytes<true>(threads) : order::rank_smem_bytes<false>(threads));
     return dtype == 1 ? (idx_i64 ? launch_nt<true, true>(threads, a, smem, stream)
                                  : launch_nt<true, false>(threads, a, smem, stream))
                       : (idx_i64 ? launch_nt<false, true>(threads, a, smem, stream)

@@ -56,6 +56,7 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "order_core.cuh"
 #include "sel_internal.h"
 
 namespace sel {
@@ -1257,10 +1258,47 @@ __global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(c
     }
 }
 
+// Value-ordered outputs of one row (SEL_SORT_VALUE in the staged row kernel): the row's n_valid
+// selected columns, in ascending column order, are src[0, n_valid) (src null: columns 0 ..
+// n_valid-1 themselves), their values buf[col] (buf null: the row in global memory, xrow).  They
+// are ranked by value (order_core.cuh; NT * 8 >= k), and output j < k gets the column of rank j
+// (index -1 and the fill value past n_valid); with GATHER the first n_gather columns also go to
+// glist.  `rank` is order::rank_smem_bytes of shared memory that nothing else still reads.
+template <typename E, int NT, bool GATHER>
+__device__ void ordered_write(const TopkArgs &a, int64_t row, int n_valid, const uint16_t *src, const E *buf,
+                              const E *xrow, unsigned char *rank, int32_t *glist)
+{
+    using T = Elem<E>;
+    constexpr bool kBf16 = sizeof(E) == 2;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int k = a.k;
+    auto col_of = [&](int p) { return src ? static_cast<int>(src[p]) : p; };
+    auto val_of = [&](int c) { return buf ? buf[c] : xrow[c]; };
+    uint32_t v[order::kEpt];
+    bool valid[order::kEpt];
+#pragma unroll
+    for (int e = 0; e < order::kEpt; ++e) {
+        const int p = warp * order::kWarpItems + e * 32 + lane;
+        valid[e] = p < n_valid;
+        v[e] = valid[e] ? static_cast<uint32_t>(val_of(col_of(p))) : static_cast<uint32_t>(T::kFill);
+    }
+    order::value_rank<kBf16, NT>(v, valid, rank);
+#pragma unroll
+    for (int u = 0; u < order::kEpt; ++u) {
+        const int j = t + u * NT;
+        if (j >= k) break;
+        const int slot = order::ranked_position<kBf16>(rank, j);
+        const int c = slot < n_valid ? col_of(slot) : -1;
+        store_idx(a, row, j, c);
+        if (a.want_values) store_val<E>(a, row, j, c >= 0 ? val_of(c) : static_cast<E>(T::kFill));
+        if (GATHER && j < a.n_gather) glist[j] = c;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // row_kernel: one CTA per row, the row staged whole in shared memory.
 // ---------------------------------------------------------------------------
-template <typename E, int NT, bool GATHER>
+template <typename E, int NT, bool GATHER, bool ORDER>
 __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const TopkArgs a)
 {
     using T = Elem<E>;
@@ -1277,11 +1315,20 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
     const int64_t row = row_of_block(a, blockIdx.x);
     const int64_t n = valid_cols(a, row);
     const int k = a.k;
+    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
     if (n <= k) {
-        short_row<E, Grp<NT>, GATHER>(a, row, n, 0, k);
+        if constexpr (ORDER) {
+            int32_t *gl = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
+            ordered_write<E, NT, GATHER>(a, row, static_cast<int>(n), nullptr, nullptr, xrow, smem + a.smem_order_off, gl);
+            if (GATHER) {
+                __syncthreads();
+                gather_rows_of<Grp<NT>>(a, row, 0, a.n_gather, gl, 0);
+            }
+        } else {
+            short_row<E, Grp<NT>, GATHER>(a, row, n, 0, k);
+        }
         return;
     }
-    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
     E *buf = reinterpret_cast<E *>(smem);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
     uint8_t *masks = smem + a.smem_mask_off;
@@ -1416,7 +1463,8 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
         uint32_t pos = block_exclusive_scan<Grp<NT>>(sel, s_warp, ts);
         // each output position's column goes to the (free) histogram first when it fits (16 bits
         // each); the outputs are then written in position order, coalesced
-        const bool by_position = static_cast<uint32_t>(k) <= 2u * static_cast<uint32_t>(a.hist_bins);
+        // (value-ordered launches always fit: the plan checks k <= 2 * hist_bins)
+        const bool by_position = ORDER || static_cast<uint32_t>(k) <= 2u * static_cast<uint32_t>(a.hist_bins);
         uint16_t *src = reinterpret_cast<uint16_t *>(hist);
         for (int i = i0; i < i1; ++i) {
             const int o = list[i];
@@ -1426,7 +1474,10 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
             if (c == P) take = (r++ < E_need);
             if (take) {
                 if (by_position) {
-                    if (SEL_IN_BOUNDS(pos < static_cast<uint32_t>(k) && o < len, a.err_flag)) src[pos] = static_cast<uint16_t>(o);
+                    if (SEL_IN_BOUNDS(pos < static_cast<uint32_t>(k) && pos < 2u * static_cast<uint32_t>(a.hist_bins) &&
+                                          o < len,
+                                      a.err_flag))
+                        src[pos] = static_cast<uint16_t>(o);
                 } else {
                     store_idx(a, row, pos, o);
                     if (a.want_values) store_val<E>(a, row, pos, e);
@@ -1437,11 +1488,15 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
         }
         if (by_position) {
             __syncthreads();
-            for (int p = tid; p < k; p += NT) {
-                const int o = src[p];
-                store_idx(a, row, p, o);
-                if (a.want_values) store_val<E>(a, row, p, buf[o]);
-                if (GATHER && p < a.n_gather) glist[p] = o;
+            if constexpr (ORDER) {
+                ordered_write<E, NT, GATHER>(a, row, k, src, buf, xrow, smem + a.smem_order_off, glist);
+            } else {
+                for (int p = tid; p < k; p += NT) {
+                    const int o = src[p];
+                    store_idx(a, row, p, o);
+                    if (a.want_values) store_val<E>(a, row, p, buf[o]);
+                    if (GATHER && p < a.n_gather) glist[p] = o;
+                }
             }
         }
     } else {
@@ -1512,14 +1567,25 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
 #pragma unroll
             for (int t = 0; t < V; ++t) {
                 if ((sm >> t) & 1u) {
-                    store_idx(a, row, pos, o + t);
-                    if (a.want_values) store_val<E>(a, row, pos, el[t]);
-                    if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = o + t;
+                    if constexpr (ORDER) {  // the column goes to its position; ranked below
+                        if (SEL_IN_BOUNDS(pos < static_cast<uint32_t>(k) && pos < 2u * static_cast<uint32_t>(a.hist_bins),
+                                          a.err_flag))
+                            reinterpret_cast<uint16_t *>(hist)[pos] = static_cast<uint16_t>(o + t);
+                    } else {
+                        store_idx(a, row, pos, o + t);
+                        if (a.want_values) store_val<E>(a, row, pos, el[t]);
+                        if (GATHER && static_cast<int64_t>(pos) < a.n_gather) glist[pos] = o + t;
+                    }
                     ++pos;
                 }
             }
             eq_run += tq;
             sel_run += ts;
+        }
+        if constexpr (ORDER) {
+            __syncthreads();
+            ordered_write<E, NT, GATHER>(a, row, k, reinterpret_cast<const uint16_t *>(hist), buf, xrow,
+                                         smem + a.smem_order_off, glist);
         }
     }
     if (GATHER) {
@@ -3006,13 +3072,17 @@ cudaError_t raise_smem_limit(K kern, int *set_smem, size_t smem)
 }
 
 // Kernel of a mode for one element type, CTA size and gather flag; null where that combination
-// is never launched (row_kernel and reg_kernel with 8 vectors a thread: 128/256/512 threads;
+// is never launched (row_kernel, its value-ordered variant and reg_kernel with 8 vectors a
+// thread: 128/256/512 threads;
 // reg_kernel with 2 vectors a thread: 128; split_kernel: 256; stream and wide: 512).
 template <typename E, int NT, bool G>
 void (*kernel_of(int mode))(TopkArgs)
 {
-    if (mode == kModeRow) return row_kernel<E, NT, G>;
-    if (mode == kModeReg8) return reg_kernel<E, NT, 8, G>;
+    if constexpr (NT <= 512) {
+        if (mode == kModeRow) return row_kernel<E, NT, G, false>;
+        if (mode == kModeRowOrdered) return row_kernel<E, NT, G, true>;
+        if (mode == kModeReg8) return reg_kernel<E, NT, 8, G>;
+    }
     if constexpr (NT == 128) {
         if (mode == kModeReg2) return reg_kernel<E, NT, 2, G>;
     }

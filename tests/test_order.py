@@ -61,6 +61,12 @@ KERNEL_CASES = [
     ("row", "bf16", 5, 16384, 2048, "levels"),
     ("row", "f32", 4, 8192, 64, "normal"),
     ("row", "f32", 3, 12000, 4096, "zeros_inf"),
+    # ranked inside the row kernel: the list overflows on equal rows (full-slice path), 128-thread
+    # CTAs, and short bf16 rows on 256 histogram bins just inside and past the 2 * bins slot limit
+    ("row", "bf16", 3, 6000, 1000, "equal"),
+    ("row", "f32", 4, 4000, 1000, "two_level"),
+    ("row", "bf16", 3, 4000, 512, "levels"),
+    ("row", "bf16", 3, 4000, 600, "levels"),
     ("wide", "f32", 3, 131075, 4096, "normal"),
     ("wide", "bf16", 2, 204803, 1024, "levels"),
     ("split", "bf16", 3, 100000, 3000, "zeros_inf"),
@@ -82,9 +88,12 @@ def test_value_order_each_kernel(c, tuning):
         assert check_rows(w, np.arange(rows), idx.cpu().numpy(), gb) == rows
 
 
-def test_value_order_short_rows_nan_and_signed_zero():
+@pytest.mark.parametrize("plan", [None, "row"])
+def test_value_order_short_rows_nan_and_signed_zero(plan, tuning):
     # rows shorter than k are ordered by value too; they are not checked for NaN, and a NaN there
-    # ranks above every number; -0 and +0 tie and go by index
+    # ranks above every number; -0 and +0 tie and go by index (plan "row": ranked in the row kernel)
+    if plan:
+        tuning(plan=plan)
     rows, cols, k = 6, 300, 512
     g = np.random.default_rng(5)
     v = g.choice(np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, 0.5], np.float32), size=(rows, cols))
@@ -174,17 +183,21 @@ def test_value_order_gather_takes_the_largest():
         assert (to_bits(out) == want).all()
 
 
+@pytest.mark.parametrize("plan", [None, "row"])
 @pytest.mark.parametrize("dtype,k,n_gather,d,b,idx_dtype,want_values", [
     ("bf16", 512, 512, 24, 3, "i32", False),    # every ordered position, 3-vector key rows
     ("bf16", 2048, 37, 128, 1, "i64", False),
     ("f32", 4096, 1000, 64, 2, "i64", True),
     ("f32", 100, 1, 8, 2, "i32", False),        # one-vector key rows, 32-thread ordering CTAs
 ])
-def test_value_order_gather_in_the_ordering_launch(dtype, k, n_gather, d, b, idx_dtype, want_values):
-    # the ordering launch gathers the first n_gather ordered positions' key rows: equal to
+def test_value_order_gather_in_the_ordering_launch(dtype, k, n_gather, d, b, idx_dtype, want_values, plan, tuning):
+    # the first n_gather ordered positions' key rows are gathered (by the ordering launch, or with
+    # plan "row" by the row kernel that ranks its own outputs where it can): equal to
     # torch.index_select over the batch-flattened key at the ordered indices (fills read row 0), and
     # the order itself equals the oracle's
     import gather_radix_select_gb300 as g
+    if plan:
+        tuning(plan=plan)
     rows_per_batch, cols = 40, 4500
     rows = b * rows_per_batch
     end = np.where(np.arange(rows) % 5 == 0, k // 2 + 1, cols - (np.arange(rows) * 97) % 300).astype(np.int32)
