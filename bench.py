@@ -163,7 +163,7 @@ def kernel_source_hash() -> str:
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("topk_impl.cuh", "sel_internal.h", "ptx.cuh", "gather.cu"):
+    for f in ("topk_impl.cuh", "order_core.cuh", "sel_internal.h", "ptx.cuh", "gather.cu"):
         with open(os.path.join(ROOT, "gather_radix_select_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
@@ -464,7 +464,9 @@ def gpu_arm(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = syn.workload(args.workload)
+    w = syn.workload(args.workload, rows=args.rows)
+    if args.topk_only:
+        w["key"] = None
     runner = Runner(w, dev, sorted_value=args.sorted_value, rank=rank, world=world)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     peak, peak_kind = measured_peaks()
@@ -810,11 +812,15 @@ def main():
                     help="with --profile: the workload's step with value-ordered output")
     ap.add_argument("--profile-extra", choices=["pair", "block"],
                     help="only the double gather or the block-level candidate chain (a short run for ncu)")
+    ap.add_argument("--topk-only", action="store_true",
+                    help="with --profile: the workload's top-k without its fused gather")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="with --profile: only the workload's first ROWS rows")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.sorted_value and not args.profile:
-        ap.error("--sorted-value is a profiling mode; it needs --profile")
+    if (args.sorted_value or args.topk_only or args.rows is not None) and not args.profile:
+        ap.error("--sorted-value, --topk-only and --rows are profiling modes; they need --profile")
     if args.profile_extra:
         print(json.dumps(profile_extra(args)), flush=True)
         return
