@@ -69,6 +69,10 @@ KERNEL_CASES = [
     ("row", "bf16", 3, 4000, 600, "levels"),
     ("wide", "f32", 3, 131075, 4096, "normal"),
     ("wide", "bf16", 2, 204803, 1024, "levels"),
+    # one CTA per row (rows >= half the SMs), ranked by the ordering launch
+    ("wide", "f32", 80, 9000, 1000, "two_level"),
+    ("wide", "bf16", 80, 20000, 4096, "levels"),
+    ("wide", "f32", 78, 12000, 4096, "equal"),
     ("split", "bf16", 3, 100000, 3000, "zeros_inf"),
     ("split", "f32", 2, 70001, 1000, "equal"),
     ("stream", "f32", 2, 100003, 4096, "two_level"),
@@ -112,6 +116,22 @@ def test_value_order_short_rows_nan_and_signed_zero(plan, tuning):
         x, vals, idx, nan, err = run_value_order(w)
         assert err == 0 and nan == 0
         assert check_rows(w, np.arange(rows), idx.cpu().numpy(), to_bits(vals)) == rows
+
+
+@pytest.mark.parametrize("plan", ["wide", "row", None])
+def test_value_order_rows_with_ends(plan, tuning):
+    # rows shorter than k (fills last), rows just longer, full rows, under each plan's own ranking
+    if plan:
+        tuning(plan=plan)
+    rows, cols, k = 96, 6000, 700
+    end = np.array([[0, 1, 699, 700, 701, 2500, 6000, 123][i % 8] for i in range(rows)], np.int32)
+    for dtype in ("f32", "bf16"):
+        w = case(dtype, rows, cols, k, "two_level", row_end=end)
+        for idx_dtype, want_values in (("i32", True), ("i64", False)):
+            x, vals, idx, nan, err = run_value_order(w, idx_dtype, want_values)
+            assert err == 0 and nan == 0
+            gb = None if vals is None else to_bits(vals)
+            assert check_rows(w, np.arange(rows), idx.cpu().numpy(), gb) == rows
 
 
 def test_value_order_k_one_and_k_equal_cols():
