@@ -314,7 +314,8 @@ def time_steps(runner, steps, warmup, flush):
     """Per-step CUDA-event times (ms) with an untimed L2 flush before each step.  flush None: warm
     L2 (the previous step's data may still be cached); a ~0.1 ms GPU sleep (a fixed clock count)
     stands in for the flush so that the host queues the step meanwhile and the events time the step
-    alone, not the host's launch latency."""
+    alone, not the host's launch latency.  With a flush, one GPU sleep before the first step gives
+    the host the same head start."""
     torch = runner.torch
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -323,6 +324,11 @@ def time_steps(runner, steps, warmup, flush):
         runner.step()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if flush is not None:
+        # the GPU sleeps (a fixed clock count, ~0.1 ms a step) while the host queues the steps, so no
+        # step's events time the host's launch latency (after the synchronize above the first step's
+        # flush would otherwise finish before the host has issued its call)
+        torch.cuda._sleep(200_000 * steps)
     for a, b in evs:
         if flush is not None:
             flush.zero_()
