@@ -155,6 +155,7 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.tsv")
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth; fractions of it are reported beside the measured peak
 
 
 def kernel_source_hash() -> str:
@@ -538,6 +539,7 @@ def gpu_arm(args):
                        if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                          "kernel": kname + ("<%s,gather>" % w["dtype"] if fused else "<%s>" % w["dtype"]),
                          "algorithmic_bytes": nbytes, "peak_kind": peak_kind},
             "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
@@ -576,6 +578,7 @@ def per_workload(args, dev, flush, peak):
         out[name] = {"kernel": r.g.kernel_name(r.x.dtype, w["rows"], w["cols"], w["k"], w["n_gather"] if fused else 0),
                      "ms": round(ms, 5), "warm_l2_ms": round(warm, 5), "rows_per_s": round(w["rows"] / (ms * 1e-3), 1),
                      "gbs": round(nb / (ms * 1e-3) / 1e9, 2), "frac_of_peak": round(nb / (ms * 1e-3) / 1e9 / peak, 4),
+                     "frac_of_nominal": round(nb / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
                      "bytes": nb, "topk_bytes": tb, "fused_gather": w.get("key") is not None}
         t2 = ms
         if w.get("key") is not None:
