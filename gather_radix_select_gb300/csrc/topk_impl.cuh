@@ -2243,20 +2243,24 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
             if (pb < ve) prefetch_l2(xv + pb, static_cast<uint32_t>(min(static_cast<int64_t>(32 * U), ve - pb)) * 16u);
         }
     }
-    for (int64_t base = vb; base < ve; base += 32 * U) {
+    // 32-bit vector offsets from the warp's first vector (a row holds fewer than 2^29 vectors)
+    const uint4 *xw = xv + vb + lane;
+    const int nvw = static_cast<int>(ve - vb);
+    const int col0 = static_cast<int>(vb * V) + lane * V;  // column of this lane's vector at offset 0
+    for (int off0 = 0; off0 < nvw; off0 += 32 * U) {
         if (kWidePrefetch > 0 && lane == 0) {
-            const int64_t pb = base + static_cast<int64_t>(kWidePrefetch) * 32 * U;
-            if (pb < ve) prefetch_l2(xv + pb, static_cast<uint32_t>(min(static_cast<int64_t>(32 * U), ve - pb)) * 16u);
+            const int pb = off0 + kWidePrefetch * 32 * U;
+            if (pb < nvw) prefetch_l2(xw + pb, static_cast<uint32_t>(min(32 * U, nvw - pb)) * 16u);
         }
-        if (base != vb) {
-            if (base + 32 * U <= ve) {  // a full iteration (warp-uniform): no bounds checks
+        if (off0 != 0) {
+            if (off0 + 32 * U <= nvw) {  // a full iteration (warp-uniform): no bounds checks
 #pragma unroll
-                for (int u = 0; u < U; ++u) q[u] = __ldcs(xv + base + u * 32 + lane);
+                for (int u = 0; u < U; ++u) q[u] = __ldcs(xw + off0 + u * 32);
             } else {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const int64_t v = base + u * 32 + lane;
-                    q[u] = v < ve ? __ldcs(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+                    const int v = off0 + u * 32 + lane;
+                    q[u] = v < nvw ? __ldcs(xw + off0 + u * 32) : make_uint4(0u, 0u, 0u, 0u);
                 }
             }
         }
@@ -2272,7 +2276,7 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
                 any = T::ge_raw(ms, tsg);
             } else {
                 T::nan_acc(q[u], smax, umax);
-                any = base + u * 32 + lane < ve && T::ge_mask_key(q[u], tkey) != 0u;
+                any = off0 + u * 32 + lane < nvw && T::ge_mask_key(q[u], tkey) != 0u;
             }
             const uint32_t b = __ballot_sync(kFull, any);
             if (b) {
@@ -2281,7 +2285,7 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
                 if (any) {
                     const int slot = sc + __popc(b & ((1u << lane) - 1u));
                     stv[slot] = q[u];
-                    stc[slot] = static_cast<int32_t>((base + u * 32 + lane) * V);
+                    stc[slot] = col0 + (off0 + u * 32) * V;
                 }
                 sc += nb;
             }
