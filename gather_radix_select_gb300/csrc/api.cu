@@ -631,29 +631,41 @@ int value_order(const void *x, int dtype, int64_t rows, int64_t stride, int k, i
     return status_of(sel::launch_value_order(dtype, idx_dtype == SEL_I64, a, static_cast<cudaStream_t>(stream)));
 }
 
-// The staged row kernel's value-ordered variant for a row plan: the ranking's items and counters
-// take the (then free) masks and candidate list and, where those are too small, push the
-// histogram and gather list back.  False when the plan is not the row kernel or the ranking does
-// not fit (k above 8 entries a thread, or above the 16-bit position slots of the histogram).
-bool ordered_row_plan(int dtype, int k, bool gather, const Plan &p, Plan &op)
+// The value-ordered variant of a plan, where the selection kernel ranks its own outputs: the
+// staged row kernel, whose ranking takes the (then free) masks and candidate list and, where those
+// are too small, pushes the histogram and gather list back; or, for calls with a fused gather, the
+// register kernel, whose ranking goes after its histogram, position table and gather list.  k must
+// fit 8 entries a thread, and for the row kernel the 16-bit position slots of the histogram.  False
+// for every other plan, or when the ranking does not fit.
+bool ordered_plan(int dtype, int k, bool gather, const Plan &p, Plan &op)
 {
-    if (p.mode != sel::kModeRow || k > sel::order::kEpt * p.threads || k > 2 * p.layout.hist_bins ||
-        k > (1 << sel::order::kSlotBits))
-        return false;
-    op = p;
-    sel::TopkArgs &l = op.layout;
+    if (k > sel::order::kEpt * p.threads || k > (1 << sel::order::kSlotBits)) return false;
     const size_t rank = dtype == SEL_BF16 ? sel::order::rank_smem_bytes<true>(p.threads)
                                           : sel::order::rank_smem_bytes<false>(p.threads);
-    l.smem_order_off = l.smem_mask_off;
-    const size_t hist = static_cast<size_t>(
-        round_up(static_cast<int64_t>(std::max<size_t>(l.smem_hist_off, l.smem_order_off + rank)), 16));
-    const size_t delta = hist - l.smem_hist_off;
-    l.smem_hist_off = static_cast<uint32_t>(hist);
-    l.smem_glist_off = static_cast<uint32_t>(l.smem_glist_off + delta);
-    op.smem = p.smem + delta;
-    op.mode = sel::kModeRowOrdered;
-    return op.smem <= sel::topk_smem_limit() &&
-           cached_blocks_per_sm(dtype, sel::kModeRowOrdered, op.threads, gather, op.smem) > 0;
+    op = p;
+    sel::TopkArgs &l = op.layout;
+    if (p.mode == sel::kModeRow) {
+        if (k > 2 * p.layout.hist_bins) return false;
+        l.smem_order_off = l.smem_mask_off;
+        const size_t hist = static_cast<size_t>(
+            round_up(static_cast<int64_t>(std::max<size_t>(l.smem_hist_off, l.smem_order_off + rank)), 16));
+        const size_t delta = hist - l.smem_hist_off;
+        l.smem_hist_off = static_cast<uint32_t>(hist);
+        l.smem_glist_off = static_cast<uint32_t>(l.smem_glist_off + delta);
+        op.smem = p.smem + delta;
+        op.mode = sel::kModeRowOrdered;
+    } else if ((p.mode == sel::kModeReg2 || p.mode == sel::kModeReg8) && gather) {
+        // measured: with a fused gather, ranking in the register kernel saves the ordering launch's
+        // index round trip (bf16 [4096, 2048] causal k=512 + gather 512: 0.119 -> 0.103 ms); without
+        // one, the ordering launch ranks with more parallelism than the selection's epilogue
+        // (0.050 against 0.052-0.054 ms), so it keeps the second launch
+        l.smem_order_off = static_cast<uint32_t>(round_up(static_cast<int64_t>(p.smem), 16));
+        op.smem = l.smem_order_off + rank;
+        op.mode = p.mode == sel::kModeReg2 ? sel::kModeReg2Ordered : sel::kModeReg8Ordered;
+    } else {
+        return false;
+    }
+    return op.smem <= sel::topk_smem_limit() && cached_blocks_per_sm(dtype, op.mode, op.threads, gather, op.smem) > 0;
 }
 
 // One selection launch.  ordered (nullable): on entry, whether the outputs should come out in value
@@ -670,7 +682,7 @@ int run_topk(const void *x, int dtype, int64_t rows, int64_t cols, int64_t strid
     if (st != SEL_OK) return st;
     if (ordered && *ordered) {
         Plan op;
-        if (!ordered_row_plan(dtype, k, n_gather > 0, p, op)) {
+        if (!ordered_plan(dtype, k, n_gather > 0, p, op)) {
             *ordered = false;
             return SEL_OK;
         }
@@ -838,7 +850,9 @@ const char *sel_topk_kernel_name(int dtype, int64_t rows, int64_t cols, int k, i
     case sel::kModeWideSplit: return "wide_kernel";
     case sel::kModeStream: return "stream_kernel";
     case sel::kModeReg2:
-    case sel::kModeReg8: return "reg_kernel";
+    case sel::kModeReg8:
+    case sel::kModeReg2Ordered:
+    case sel::kModeReg8Ordered: return "reg_kernel";
     case sel::kModeFlat: return "flat_kernel";
     default: return nullptr;
     }

@@ -43,7 +43,9 @@ constexpr int kModeReg8 = 5;        // reg_kernel: 8 vectors a thread
 constexpr int kModeWideSplit = 6;   // wide_kernel over `parts` CTAs per row, last-arriver merge
 constexpr int kModeFlat = 7;        // flat_kernel: rows cut into chunks dealt over a persistent grid
 constexpr int kModeRowOrdered = 8;  // row_kernel that also ranks each row's outputs by value
-constexpr int kNumModes = 9;
+constexpr int kModeReg2Ordered = 9; // reg_kernel (2 vectors a thread) ranking its outputs by value
+constexpr int kModeReg8Ordered = 10; // reg_kernel (8 vectors a thread) ranking its outputs by value
+constexpr int kNumModes = 11;
 // flat_kernel: warps 0..23 stream, warps 24..31 estimate thresholds, flush chunks and select
 constexpr int kFlatStreamWarps = 24;
 constexpr int kFlatSelWarps = 8;
@@ -81,7 +83,7 @@ struct TopkArgs {
     uint32_t smem_list_off;   // offset of the candidate list (16-bit offsets within the slice)
     uint32_t smem_glist_off;  // offset of the gather position list (fused only)
     uint32_t smem_stage_off;  // wide_kernel, flat_kernel: staged candidate vectors
-    uint32_t smem_order_off;  // row_kernel ranked by value: the ranking's items and counters
+    uint32_t smem_order_off;  // row / reg kernel ranked by value: the ranking's items and counters
     uint32_t smem_cbuf_off;   // flat_kernel: chunk buffers
     int32_t flat_wcap;        // flat_kernel: pairs one streaming warp may keep of one chunk
     int32_t flat_sel_pairs;   // flat_kernel: pairs the selection regions hold in all

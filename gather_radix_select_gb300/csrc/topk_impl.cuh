@@ -1101,12 +1101,49 @@ __device__ bool select_staged(const TopkArgs &a, int64_t row, const Segments<E> 
 // and the outputs are then written in position order (coalesced).
 // Shared memory: histogram | source columns (k x 16 bits) | gather list.
 // ---------------------------------------------------------------------------
+// Value-ordered outputs of one row (SEL_SORT_VALUE in the register and staged row kernels): the row's n_valid
+// selected columns, in ascending column order, are src[0, n_valid) (src null: columns 0 ..
+// n_valid-1 themselves), their values buf[col] (buf null: the row in global memory, xrow).  They
+// are ranked by value (order_core.cuh; NT * 8 >= k), and output j < k gets the column of rank j
+// (index -1 and the fill value past n_valid); with GATHER the first n_gather columns also go to
+// glist.  `rank` is order::rank_smem_bytes of shared memory that nothing else still reads.
+template <typename E, int NT, bool GATHER>
+__device__ void ordered_write(const TopkArgs &a, int64_t row, int n_valid, const uint16_t *src, const E *buf,
+                              const E *xrow, unsigned char *rank, int32_t *glist)
+{
+    using T = Elem<E>;
+    constexpr bool kBf16 = sizeof(E) == 2;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int k = a.k;
+    auto col_of = [&](int p) { return src ? static_cast<int>(src[p]) : p; };
+    auto val_of = [&](int c) { return buf ? buf[c] : xrow[c]; };
+    uint32_t v[order::kEpt];
+    bool valid[order::kEpt];
+#pragma unroll
+    for (int e = 0; e < order::kEpt; ++e) {
+        const int p = warp * order::kWarpItems + e * 32 + lane;
+        valid[e] = p < n_valid;
+        v[e] = valid[e] ? static_cast<uint32_t>(val_of(col_of(p))) : static_cast<uint32_t>(T::kFill);
+    }
+    order::value_rank<kBf16, NT>(v, valid, rank);
+#pragma unroll
+    for (int u = 0; u < order::kEpt; ++u) {
+        const int j = t + u * NT;
+        if (j >= k) break;
+        const int slot = order::ranked_position<kBf16>(rank, j);
+        const int c = slot < n_valid ? col_of(slot) : -1;
+        store_idx(a, row, j, c);
+        if (a.want_values) store_val<E>(a, row, j, c >= 0 ? val_of(c) : static_cast<E>(T::kFill));
+        if (GATHER && j < a.n_gather) glist[j] = c;
+    }
+}
+
 template <int NT, int R>
 struct RegMinBlocks {  // a register budget that holds the run (R vectors) without spilling
     static constexpr int value = R <= 2 ? MinBlocks<NT>::value : (NT >= 512 ? 1 : (NT >= 256 ? 2 : 4));
 };
 
-template <typename E, int NT, int R, bool GATHER>
+template <typename E, int NT, int R, bool GATHER, bool ORDER>
 __global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(const TopkArgs a)
 {
     using T = Elem<E>;
@@ -1119,11 +1156,20 @@ __global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(c
     const int64_t row = row_of_block(a, blockIdx.x);
     const int64_t n = valid_cols(a, row);
     const int k = a.k;
+    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
     if (n <= k) {
-        short_row<E, Grp<NT>, GATHER>(a, row, n, 0, k);
+        if constexpr (ORDER) {
+            int32_t *gl = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
+            ordered_write<E, NT, GATHER>(a, row, static_cast<int>(n), nullptr, nullptr, xrow, smem + a.smem_order_off, gl);
+            if (GATHER) {
+                __syncthreads();
+                gather_rows_of<Grp<NT>>(a, row, 0, a.n_gather, gl, 0);
+            }
+        } else {
+            short_row<E, Grp<NT>, GATHER>(a, row, n, 0, k);
+        }
         return;
     }
-    const E *xrow = static_cast<const E *>(a.x) + row * a.stride;
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.smem_hist_off);
     uint16_t *src = reinterpret_cast<uint16_t *>(smem + a.smem_list_off);
     int32_t *glist = GATHER ? reinterpret_cast<int32_t *>(smem + a.smem_glist_off) : nullptr;
@@ -1246,52 +1292,19 @@ __global__ void __launch_bounds__(NT, (RegMinBlocks<NT, R>::value)) reg_kernel(c
         }
     }
     __syncthreads();
-    for (int p = tid; p < k; p += NT) {  // outputs in position order
-        const int col = src[p];
-        store_idx(a, row, p, col);
-        if (a.want_values) store_val<E>(a, row, p, xrow[col]);
-        if (GATHER && p < a.n_gather) glist[p] = col;
+    if constexpr (ORDER) {  // ranked by value (values re-read by column from L2)
+        ordered_write<E, NT, GATHER>(a, row, k, src, nullptr, xrow, smem + a.smem_order_off, glist);
+    } else {
+        for (int p = tid; p < k; p += NT) {  // outputs in position order
+            const int col = src[p];
+            store_idx(a, row, p, col);
+            if (a.want_values) store_val<E>(a, row, p, xrow[col]);
+            if (GATHER && p < a.n_gather) glist[p] = col;
+        }
     }
     if (GATHER) {
         __syncthreads();
         gather_rows_of<Grp<NT>>(a, row, 0, a.n_gather, glist, 0);
-    }
-}
-
-// Value-ordered outputs of one row (SEL_SORT_VALUE in the staged row kernel): the row's n_valid
-// selected columns, in ascending column order, are src[0, n_valid) (src null: columns 0 ..
-// n_valid-1 themselves), their values buf[col] (buf null: the row in global memory, xrow).  They
-// are ranked by value (order_core.cuh; NT * 8 >= k), and output j < k gets the column of rank j
-// (index -1 and the fill value past n_valid); with GATHER the first n_gather columns also go to
-// glist.  `rank` is order::rank_smem_bytes of shared memory that nothing else still reads.
-template <typename E, int NT, bool GATHER>
-__device__ void ordered_write(const TopkArgs &a, int64_t row, int n_valid, const uint16_t *src, const E *buf,
-                              const E *xrow, unsigned char *rank, int32_t *glist)
-{
-    using T = Elem<E>;
-    constexpr bool kBf16 = sizeof(E) == 2;
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int k = a.k;
-    auto col_of = [&](int p) { return src ? static_cast<int>(src[p]) : p; };
-    auto val_of = [&](int c) { return buf ? buf[c] : xrow[c]; };
-    uint32_t v[order::kEpt];
-    bool valid[order::kEpt];
-#pragma unroll
-    for (int e = 0; e < order::kEpt; ++e) {
-        const int p = warp * order::kWarpItems + e * 32 + lane;
-        valid[e] = p < n_valid;
-        v[e] = valid[e] ? static_cast<uint32_t>(val_of(col_of(p))) : static_cast<uint32_t>(T::kFill);
-    }
-    order::value_rank<kBf16, NT>(v, valid, rank);
-#pragma unroll
-    for (int u = 0; u < order::kEpt; ++u) {
-        const int j = t + u * NT;
-        if (j >= k) break;
-        const int slot = order::ranked_position<kBf16>(rank, j);
-        const int c = slot < n_valid ? col_of(slot) : -1;
-        store_idx(a, row, j, c);
-        if (a.want_values) store_val<E>(a, row, j, c >= 0 ? val_of(c) : static_cast<E>(T::kFill));
-        if (GATHER && j < a.n_gather) glist[j] = c;
     }
 }
 
@@ -3085,10 +3098,12 @@ void (*kernel_of(int mode))(TopkArgs)
     if constexpr (NT <= 512) {
         if (mode == kModeRow) return row_kernel<E, NT, G, false>;
         if (mode == kModeRowOrdered) return row_kernel<E, NT, G, true>;
-        if (mode == kModeReg8) return reg_kernel<E, NT, 8, G>;
+        if (mode == kModeReg8) return reg_kernel<E, NT, 8, G, false>;
+        if (mode == kModeReg8Ordered) return reg_kernel<E, NT, 8, G, true>;
     }
     if constexpr (NT == 128) {
-        if (mode == kModeReg2) return reg_kernel<E, NT, 2, G>;
+        if (mode == kModeReg2) return reg_kernel<E, NT, 2, G, false>;
+        if (mode == kModeReg2Ordered) return reg_kernel<E, NT, 2, G, true>;
     }
     if constexpr (NT == 256) {
         if (mode == kModeSplit) return split_kernel<E, NT, G>;

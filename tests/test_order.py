@@ -58,6 +58,10 @@ KERNEL_CASES = [
     ("reg", "bf16", 4, 8191, 2048, "levels"),
     ("reg", "f32", 3, 4093, 4000, "zeros_inf"),
     ("reg", "f32", 5, 1021, 64, "two_level"),
+    # register tiles of 2 and 8 vectors at k = 8 entries a thread (ranked inside the register
+    # kernel when the call also gathers)
+    ("reg", "bf16", 80, 2048, 512, "levels"),
+    ("reg", "f32", 40, 3000, 1024, "normal"),
     ("row", "bf16", 5, 16384, 2048, "levels"),
     ("row", "f32", 4, 8192, 64, "normal"),
     ("row", "f32", 3, 12000, 4096, "zeros_inf"),
@@ -203,7 +207,7 @@ def test_value_order_gather_takes_the_largest():
         assert (to_bits(out) == want).all()
 
 
-@pytest.mark.parametrize("plan", [None, "row"])
+@pytest.mark.parametrize("plan", [None, "row", "reg"])
 @pytest.mark.parametrize("dtype,k,n_gather,d,b,idx_dtype,want_values", [
     ("bf16", 512, 512, 24, 3, "i32", False),    # every ordered position, 3-vector key rows
     ("bf16", 2048, 37, 128, 1, "i64", False),
@@ -211,8 +215,8 @@ def test_value_order_gather_takes_the_largest():
     ("f32", 100, 1, 8, 2, "i32", False),        # one-vector key rows, 32-thread ordering CTAs
 ])
 def test_value_order_gather_in_the_ordering_launch(dtype, k, n_gather, d, b, idx_dtype, want_values, plan, tuning):
-    # the first n_gather ordered positions' key rows are gathered (by the ordering launch, or with
-    # plan "row" by the row kernel that ranks its own outputs where it can): equal to
+    # the first n_gather ordered positions' key rows are gathered (by the ordering launch, or by a
+    # row or register kernel that ranks its own outputs where it can): equal to
     # torch.index_select over the batch-flattened key at the ordered indices (fills read row 0), and
     # the order itself equals the oracle's
     import gather_radix_select_gb300 as g
