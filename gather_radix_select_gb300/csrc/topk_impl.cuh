@@ -1461,7 +1461,10 @@ __global__ void __launch_bounds__(NT, MinBlocks<NT>::value) row_kernel(const Top
 
     // --------------------------------------------- ordered write of the k
     if (list_ok) {
-        const int m = (L + NT - 1) / NT;
+        // thread t owns list entries [m t, m t + m); m is rounded up to 2 mod 4 so that the first
+        // entries of a warp's threads (16-bit, m/2 words apart, m/2 odd) fall in distinct banks
+        const int m0 = (L + NT - 1) / NT;
+        const int m = m0 <= 1 ? m0 : m0 + ((6 - (m0 & 3)) & 3);
         const int i0 = min(L, tid * m), i1 = min(L, i0 + m);
         uint32_t g = 0, q = 0;
         for (int i = i0; i < i1; ++i) {
