@@ -36,8 +36,10 @@
  *                     queries (no device work).
  *
  * Value order (sorted_index = SEL_SORT_VALUE; the tutorial's "Performance
- * and advanced tips", item 3, names ordering by index or by value) is an
- * extra launch after the selection.
+ * and advanced tips", item 3, names ordering by index or by value) is ranked
+ * inside the selection launch where the selection kernel holds the row's
+ * selected columns in shared memory (the staged row kernel; the register
+ * kernel when the call also gathers), else in one extra launch.
  *
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller; the library
@@ -121,7 +123,8 @@ SEL_API int sel_stride_requirement(int *in_align_bytes, int *out_align_bytes);
  *               ascending (values follow).  SEL_SORT_VALUE: values descending,
  *               equal values by index ascending, fills last; a NaN (possible
  *               only in a short row, which is not checked) counts above every
- *               number.  Value order is a second launch after the selection.
+ *               number.  Value order takes one launch where the plan is the
+ *               staged row kernel, else a second launch after the selection.
  *   idx_dtype   SEL_I32 | SEL_I64.
  *   out_idx     [rows, out_idx_stride] of idx_dtype; columns [0, k) written.
  *   out_val     [rows, out_val_stride] of `dtype`, or NULL when want_values == 0.
@@ -225,9 +228,10 @@ SEL_API int sel_block_topk_gather(const void *scores, int dtype, int64_t rows, i
  * selection.  Fill positions (-1) of short rows gather position 0, as in
  * sel_gather_rows.  The workspace rule is that of sel_topk.  With
  * SEL_SORT_VALUE the gathered columns are those of the value-ordered output
- * (the n_gather largest values); that takes two launches (the selection,
- * then one launch that orders each row and gathers its first n_gather
- * ordered positions) and out_idx must not be NULL. */
+ * (the n_gather largest values); that takes one launch where the plan is
+ * the staged row or register kernel, else two (the selection, then one
+ * launch that orders each row and gathers its first n_gather ordered
+ * positions), and out_idx must not be NULL. */
 SEL_API int sel_topk_gather(const void *x, int dtype, int64_t rows, int64_t cols, int64_t stride,
                     const int32_t *row_end, int k, int sorted_index, int idx_dtype, int want_values,
                     void *out_idx, int64_t out_idx_stride, void *out_val, int64_t out_val_stride,
