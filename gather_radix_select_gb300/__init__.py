@@ -197,7 +197,8 @@ def topk(x: torch.Tensor, k: int, *, end: torch.Tensor | None = None, sorted_ind
     Returns ``(values, indices)``; ``values`` is None when ``return_value``
     is False.  Rows shorter than k (per ``end``) are filled with index -1 and
     value -inf.  ``sorted_index``: each row by index ascending;
-    ``sorted_value``: by value descending, equal values by index (a second
+    ``sorted_value``: by value descending, equal values by index (ranked in the
+    selection launch when the plan is the staged row kernel, else a second
     launch).  Outputs may be non-contiguous (row strides padded to the
     output alignment).  ``nan_flag`` / ``err_flag`` are optional caller-zeroed
     int32 CUDA tensors the kernel ORs / writes into.  ``output_idx`` /
@@ -372,7 +373,8 @@ def topk_gather(x: torch.Tensor, k: int, key: torch.Tensor, n_gather: int, *, en
     Returns ``(values, indices, gathered)`` with ``gathered`` bf16
     [rows, n_gather, d]; values / indices are None when not requested.  With
     ``sorted_value`` the gathered columns are the n_gather largest values, in
-    value order (the selection, then one launch that orders and gathers).
+    value order (one launch when the plan is the staged row or register
+    kernel, else the selection, then one launch that orders and gathers).
     """
     _check_x(x)
     order = _order(sorted_index, sorted_value)
