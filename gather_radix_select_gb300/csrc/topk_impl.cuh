@@ -1873,6 +1873,64 @@ constexpr int kWideUnroll = 4;
 constexpr int kWidePrefetch = 2;
 constexpr int kStage = kWideStage;
 
+// State a warp carries through the expansion of its staged vectors.
+struct WideExpand {
+    uint32_t off;   // pairs appended to the warp's region
+    uint32_t kmax;  // largest candidate key seen by this lane (non-positive thresholds)
+    bool pnan;      // a NaN among this lane's candidates (non-positive thresholds)
+};
+
+// Expands a warp's sc staged vectors (stv, with their first columns stc; one vector a lane at a time,
+// in order) into (key bits, column) pairs appended to the warp's region reg at off (capacity capw;
+// writes past it land on the absorbing last pair).  All 32 lanes call.
+template <typename E>
+__device__ __forceinline__ WideExpand wide_expand(const uint4 *stv, const int32_t *stc, int sc, uint2 *reg,
+                                                  uint32_t capw, bool positive, uint32_t tsg, uint32_t tkey,
+                                                  uint32_t off, uint32_t kmax, bool pnan, int lane)
+{
+    using T = Elem<E>;
+    __syncwarp();
+    for (int r0 = 0; r0 < sc; r0 += 32) {
+        const int i = r0 + lane;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        int cb = 0;
+        uint32_t m = 0;
+        if (i < sc) {
+            v = stv[i];
+            cb = stc[i];
+            m = positive ? T::ge_mask_raw(v, tsg) : T::ge_mask_key(v, tkey);
+        }
+        uint32_t tot;
+        uint32_t p = off + warp_exclusive_scan(static_cast<uint32_t>(__popc(m)), lane, tot);
+        while (m) {
+            const int t = __ffs(m) - 1;
+            m &= m - 1u;
+            const E e = T::lane_of(v, t);
+            if (!positive) {
+                kmax = max(kmax, T::key(e));
+                pnan |= T::is_nan(e);
+            }
+            reg[p < capw ? p : capw] = make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(cb + t));
+            ++p;
+        }
+        off += tot;
+    }
+    __syncwarp();
+    return WideExpand{off, kmax, pnan};
+}
+
+// wide_expand as a call.  Measured: the split-row variant (a part streams a few iterations, then
+// merges) runs faster with the expansion out of line (bf16 [4, 204800] k=1024: 23.2 -> 21.2 us),
+// the one-row-per-CTA variant slower (fp32 [256, 131072] k=4096: 46.7 -> 48.8 us), so only the former
+// calls it.
+template <typename E>
+__device__ __noinline__ WideExpand wide_expand_call(const uint4 *stv, const int32_t *stc, int sc, uint2 *reg,
+                                                    uint32_t capw, bool positive, uint32_t tsg, uint32_t tkey,
+                                                    uint32_t off, uint32_t kmax, bool pnan, int lane)
+{
+    return wide_expand<E>(stv, stc, sc, reg, capw, positive, tsg, tkey, off, kmax, pnan, lane);
+}
+
 // Threshold key estimated from sample vectors held in registers: q[0, kSU) of each thread, those
 // with bit j of `ok` set valid, `ns` valid vectors over the CTA.  share / population: the k wanted
 // out of the row's n.  mu = the sample's expected share of the k; the estimate keeps
@@ -2224,34 +2282,12 @@ __global__ void __launch_bounds__(NT, 2) wide_kernel(const TopkArgs a)
     int32_t *stc = reinterpret_cast<int32_t *>(smem + a.smem_stage_off + W * kStage * 16) + warp * kStage;
     int sc = 0;  // staged vectors (warp-uniform)
     auto expand = [&]() {
-        __syncwarp();
-        for (int r0 = 0; r0 < sc; r0 += 32) {
-            const int i = r0 + lane;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            int cb = 0;
-            uint32_t m = 0;
-            if (i < sc) {
-                v = stv[i];
-                cb = stc[i];
-                m = positive ? T::ge_mask_raw(v, tsg) : T::ge_mask_key(v, tkey);
-            }
-            uint32_t tot;
-            uint32_t p = off + warp_exclusive_scan(static_cast<uint32_t>(__popc(m)), lane, tot);
-            while (m) {
-                const int t = __ffs(m) - 1;
-                m &= m - 1u;
-                const E e = T::lane_of(v, t);
-                if (!positive) {
-                    kmax = max(kmax, T::key(e));
-                    pnan |= T::is_nan(e);
-                }
-                reg[p < capw ? p : capw] = make_uint2(static_cast<uint32_t>(e), static_cast<uint32_t>(cb + t));
-                ++p;
-            }
-            off += tot;
-        }
+        const WideExpand st = SPLIT ? wide_expand_call<E>(stv, stc, sc, reg, capw, positive, tsg, tkey, off, kmax, pnan, lane)
+                                    : wide_expand<E>(stv, stc, sc, reg, capw, positive, tsg, tkey, off, kmax, pnan, lane);
+        off = st.off;
+        kmax = st.kmax;
+        pnan = st.pnan;
         sc = 0;
-        __syncwarp();
     };
     if (kWidePrefetch > 0 && lane == 0) {  // the first iterations' prefetches
         for (int d = 1; d < kWidePrefetch; ++d) {
