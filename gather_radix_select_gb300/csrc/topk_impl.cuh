@@ -1919,10 +1919,10 @@ __device__ __forceinline__ WideExpand wide_expand(const uint4 *stv, const int32_
     return WideExpand{off, kmax, pnan};
 }
 
-// wide_expand as a call.  Measured: the split-row variant (a part streams a few iterations, then
-// merges) runs faster with the expansion out of line (bf16 [4, 204800] k=1024: 23.2 -> 21.2 us),
-// the one-row-per-CTA variant slower (fp32 [256, 131072] k=4096: 46.7 -> 48.8 us), so only the former
-// calls it.
+// wide_expand as a call.  Measured with a memset L2 flush: the split-row variant (a part streams a
+// few iterations, then merges) runs faster with the expansion out of line (bf16 [4, 204800] k=1024:
+// 23.2 -> 21.2-22.8 us), the one-row-per-CTA variant slower (fp32 [256, 131072] k=4096: 46.7 ->
+// 48.8 us), so only the former calls it.
 template <typename E>
 __device__ __noinline__ WideExpand wide_expand_call(const uint4 *stv, const int32_t *stc, int sc, uint2 *reg,
                                                     uint32_t capw, bool positive, uint32_t tsg, uint32_t tkey,
